@@ -1,0 +1,442 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks one oracle function against a closed form, a brute force, an
+independent library routine, a hand-worked example or an invariant the
+pages state, so that a plausible slip (a dropped term, a wrong sign or index,
+a transposed operand) fails at least one of them.  No GPU is used.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mla_kv_fp8_gb300 import workload as wl
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _json(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+def test_e4m3_ocp_code_points():
+    for code, val in _json("e4m3_ocp_points.json")["points"]:
+        got = oracle.e4m3(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+
+
+def test_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        got = oracle.e4m3(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c], (c, got, ref[c])
+
+
+def test_bf16_matches_torch():
+    bits = torch.arange(0, 65536, 97, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    for i, b in enumerate(bits.numpy().astype(np.uint16)):
+        got = oracle.bf16(int(b))
+        if math.isnan(ref[i]):
+            assert math.isnan(got)
+        else:
+            assert got == ref[i]
+
+
+def test_dequant_row_e4m3_layout():
+    # codes i -> a known value per position, a distinct scale per 128-group
+    row = np.zeros(656, np.uint8)
+    codes = np.array([0x38, 0xB8, 0x40, 0x30] * 128, np.uint8)  # 1, -1, 2, 0.5
+    row[:512] = codes
+    scales = np.array([0.5, 2.0, 3.0, -1.25], np.float32)
+    row[512:528] = scales.view(np.uint8)
+    rope = torch.linspace(-3, 3, 64).to(torch.bfloat16)
+    row[528:656] = rope.view(torch.uint8).numpy()
+    got = oracle.dequant_rows(oracle.ROW_E4M3_656, row[None])[0]
+    base = np.array([1.0, -1.0, 2.0, 0.5] * 128)
+    want = np.concatenate([base * np.repeat(scales.astype(np.float64), 128),
+                           rope.to(torch.float64).numpy()])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_dequant_row_f32_layout():
+    x = np.random.default_rng(1).standard_normal(576).astype(np.float32)
+    got = oracle.dequant_rows(oracle.ROW_F32_2304, x.view(np.uint8)[None])[0]
+    np.testing.assert_array_equal(got, x.astype(np.float64))
+
+
+def test_generator_rows_roundtrip_within_e4m3_step():
+    """The FP8 rows the generator encodes decode to within half an E4M3 step of
+    the N(0,1) draw (sanity of the layout both sides read)."""
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn((5, 576), generator=g)
+    rows = wl.encode_rows(x, wl.ROW_E4M3_656).numpy()
+    y = oracle.dequant_rows(oracle.ROW_E4M3_656, rows)
+    nope_err = np.abs(y[:, :512] - x[:, :512].double().numpy())
+    amax = x[:, :512].abs().reshape(5, 4, 128).amax(-1).double().numpy()
+    # E4M3 relative step is 2^-3; half of it times the largest magnitude in range
+    bound = np.repeat(amax, 128, axis=1) * (2 ** -4) + 1e-12
+    assert (nope_err <= bound).all()
+    np.testing.assert_array_equal(y[:, 512:], x[:, 512:].to(torch.bfloat16).double().numpy())
+
+
+# --------------------------------------------------------------------------
+# indexer: exact integer recomputation
+# --------------------------------------------------------------------------
+def _int_recompute(qi, ki, wk, sig_e, N, nq):
+    """Closed form in integers.  q = qi/8, k = ki/8, w = 2^-wk, sigma = 2^sig_e:
+    s = sum_h 2^-wk * max(2^sig_e * (qi.ki)/64, 0), returned as an exact
+    rational via integers scaled by 2^(6+3+1)."""
+    dots = np.einsum("jhd,td->jht", qi.astype(np.int64), ki.astype(np.int64))  # units 2^-6
+    relu = np.maximum(dots, 0)
+    # term = 2^-wk * 2^sig_e * dot * 2^-6 ; scale everything by 2^10
+    scale = (2 ** (3 - wk))[:, :, None].astype(np.int64)           # 2^-wk * 2^3
+    sig = (2 ** (sig_e + 1))[None, None, :].astype(np.int64)      # 2^sig_e * 2^1
+    s_int = (relu * scale * sig).sum(1)                            # units 2^-(6+3+1)
+    s = s_int.astype(np.float64) / 2.0 ** 10
+    for j in range(nq):
+        s[j, N - nq + j + 1:] = -np.inf
+    return s
+
+
+@pytest.mark.parametrize("fmt,Hi,Di,bound,nq,N,sig", [
+    (oracle.IDX_E4M3, 8, 32, 8, 1, 50, False),
+    (oracle.IDX_E4M3, 4, 16, 8, 4, 37, True),
+    (oracle.IDX_F32, 4, 32, 64, 1, 64, False),
+    (oracle.IDX_F32, 3, 8, 64, 2, 21, True),
+])
+def test_indexer_scores_exact_int64(fmt, Hi, Di, bound, nq, N, sig):
+    rng = np.random.default_rng(7)
+    qi = rng.integers(-bound, bound + 1, (nq, Hi, Di))
+    ki = rng.integers(-bound, bound + 1, (N, Di))
+    wk = rng.integers(0, 4, (nq, Hi))
+    sig_e = rng.integers(-1, 2, N) if sig else np.zeros(N, np.int64)
+    w = (2.0 ** -wk).astype(np.float32)
+    sigma = (2.0 ** sig_e).astype(np.float32)
+    if fmt == oracle.IDX_E4M3:
+        q = torch.from_numpy(qi / 8.0).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        k = torch.from_numpy(ki / 8.0).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    else:
+        q = (qi / 8.0).astype(np.float32)
+        k = (ki / 8.0).astype(np.float32)
+    got = oracle.indexer_scores(fmt, q, w, k, sigma, N)
+    want = _int_recompute(qi, ki, wk, sig_e, N, nq)
+    np.testing.assert_array_equal(got.astype(np.float64), want)
+
+
+def test_indexer_generator_values_are_exact_grid():
+    """The generator's E4M3 indexer values are exactly m/8, |m| <= 8."""
+    v = wl.idx_values((4096,), wl.IDX_E4M3, 11).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    m = v * 8
+    assert np.array_equal(m, np.round(m)) and np.abs(m).max() <= 8
+    f = wl.idx_values((4096,), wl.IDX_F32, 11).double().numpy() * 8
+    assert np.array_equal(f, np.round(f)) and np.abs(f).max() <= 64
+
+
+# --------------------------------------------------------------------------
+# top-K
+# --------------------------------------------------------------------------
+def _brute_topk(s, vis, K):
+    """Enumerate every subset of size min(K, vis); keep the one where each
+    chosen score beats each unchosen one, ties going to the lower index."""
+    m = min(K, vis)
+    found = []
+    for sub in itertools.combinations(range(vis), m):
+        ss = set(sub)
+        ok = True
+        for a in sub:
+            for b in range(vis):
+                if b in ss:
+                    continue
+                if s[a] < s[b] or (s[a] == s[b] and a > b):
+                    ok = False
+                    break
+            if not ok:
+                break
+        if ok:
+            found.append(sub)
+    assert len(found) == 1
+    out = np.full(K, -1, np.int32)
+    out[:m] = sorted(found[0])
+    return out
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_brute_force_tiny(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 11))
+    vis = int(rng.integers(0, n + 1))
+    K = int(rng.integers(1, 6))
+    s = rng.integers(0, 4, n).astype(np.float32)  # many ties
+    if seed % 3 == 0:
+        s = rng.standard_normal(n).astype(np.float32)
+    got = oracle.topk(s, vis, K)
+    np.testing.assert_array_equal(got, _brute_topk(s, vis, K))
+
+
+def test_topk_invariants_large_with_ties():
+    rng = np.random.default_rng(5)
+    N, K = 5000, 777
+    s = rng.integers(0, 50, N).astype(np.float32)
+    got = oracle.topk(s, N, K)
+    assert (np.diff(got) > 0).all() and len(got) == K
+    sel = np.zeros(N, bool)
+    sel[got] = True
+    thr = s[sel].min()
+    assert (s[~sel] <= thr).all()
+    # ties at the threshold: chosen ones have lower indices than unchosen ones
+    tie_in = np.nonzero(sel & (s == thr))[0]
+    tie_out = np.nonzero(~sel & (s == thr))[0]
+    if len(tie_out):
+        assert tie_in.max() < tie_out.min()
+
+
+def test_topk_k_at_least_visible_selects_all():
+    s = np.random.default_rng(0).standard_normal(30).astype(np.float32)
+    got = oracle.topk(s, 20, 32)
+    np.testing.assert_array_equal(got[:20], np.arange(20))
+    assert (got[20:] == -1).all()
+
+
+# --------------------------------------------------------------------------
+# resolve / LRU
+# --------------------------------------------------------------------------
+def test_resolve_hand_worked_example():
+    ex = _json("resolve_hand_example.json")
+    P, N, C = ex["P"], ex["N"], ex["C"]
+    resident = np.zeros((N + P - 1) // P, np.uint8)
+    resident[ex["resident_pages"]] = 1
+    np.testing.assert_array_equal(resident, oracle.page_resident(oracle.MIXED, N, ex["T"], P))
+    st = oracle.HotState(C, N)
+    for i, step in enumerate(ex["steps"]):
+        r = st.resolve(resident, P, N, np.array([step["idx"]], np.int32))
+        assert r["status"] == 0
+        assert r["loc_kind"][0].tolist() == step["kind"], i
+        assert r["loc_val"][0].tolist() == step["val"], i
+        assert [[int(a), int(b)] for a, b in zip(r["miss_tok"], r["miss_slot"])] == step["misses"], i
+        assert st.slot_token.tolist() == step["slot_token"], i
+        assert st.stamp.tolist() == step["stamp"], i
+        assert int(st.step[0]) == i + 1
+    bad = ex["then_out_of_range"]
+    r = st.resolve(resident, P, N, np.array([bad["idx"]], np.int32))
+    assert r["status"] == bad["status"]
+
+
+class HistoryLRU:
+    """Independent formulation of the same policy: no stamps are kept; the
+    last use of a slot is found by scanning a full access log."""
+
+    def __init__(self, C):
+        self.C = C
+        self.log = []  # (step, slot)
+        self.token_of = {}  # slot -> token
+        self.step = 0
+
+    def last_use(self, c):
+        t = 0
+        for s, cc in self.log:
+            if cc == c:
+                t = max(t, s)
+        return t
+
+    def resolve(self, resident, P, idx):
+        self.step += 1
+        U = sorted(set(int(x) for x in idx.ravel() if x >= 0))
+        slot_of_tok = {t: c for c, t in self.token_of.items()}
+        where = {}
+        misses = []
+        for u in U:
+            if resident[u // P]:
+                where[u] = (1, u)
+            elif u in slot_of_tok:
+                self.log.append((self.step, slot_of_tok[u]))
+                where[u] = (2, slot_of_tok[u])
+            else:
+                misses.append(u)
+        free = [c for c in range(self.C) if self.last_use(c) < self.step]
+        free.sort(key=lambda c: (self.last_use(c), c))
+        victims = sorted(free[:len(misses)])
+        assert len(victims) == len(misses)
+        for u, c in zip(misses, victims):
+            self.token_of[c] = u
+            self.log.append((self.step, c))
+            where[u] = (2, c)
+        return where, list(zip(misses, victims))
+
+
+@pytest.mark.parametrize("nq,K,C,mode", [(1, 8, 16, oracle.MIXED), (2, 6, 18, oracle.MIXED),
+                                         (4, 4, 20, oracle.ZERO), (1, 8, 8, oracle.MIXED)])
+def test_resolve_matches_history_replay(nq, K, C, mode):
+    rng = np.random.default_rng(nq * 100 + K)
+    P, N, T = 4, 64, 12
+    resident = oracle.page_resident(mode, N, T, P)
+    st = oracle.HotState(C, N)
+    ref = HistoryLRU(C)
+    hot_before = set()
+    for step in range(40):
+        # skewed draws so that hits, misses and evictions all happen
+        idx = np.full((nq, K), -1, np.int32)
+        for j in range(nq):
+            pool = rng.choice(N, size=K, replace=False, p=None if step % 5 else None)
+            idx[j] = np.sort(pool)
+        r = st.resolve(resident, P, N, idx)
+        assert r["status"] == 0
+        where, pairs = ref.resolve(resident, P, idx)
+        for j in range(nq):
+            for k in range(K):
+                u = idx[j, k]
+                assert (r["loc_kind"][j, k], r["loc_val"][j, k]) == where[int(u)]
+        assert list(zip(r["miss_tok"].tolist(), r["miss_slot"].tolist())) == pairs
+        # invariants: tail tokens never enter the hot buffer; occupancy <= C;
+        # misses = |U \ (resident u hot before)|; hot_map and slot_token agree
+        U = set(int(x) for x in idx.ravel())
+        nonres = {u for u in U if not resident[u // P]}
+        assert r["misses"] == len(nonres - hot_before)
+        held = [t for t in st.slot_token.tolist() if t >= 0]
+        assert len(held) <= C and len(set(held)) == len(held)
+        assert all(not resident[t // P] for t in held)
+        for c, t in enumerate(st.slot_token.tolist()):
+            if t >= 0:
+                assert st.hot_map[t] == c
+        assert (st.hot_map >= 0).sum() == len(held)
+        hot_before = set(held)
+
+
+def test_resolve_full_residency_never_misses():
+    P, N = 8, 200
+    st = oracle.HotState(16, N)
+    res = oracle.page_resident(oracle.FULL, N, 0, P)
+    rng = np.random.default_rng(2)
+    for _ in range(10):
+        idx = np.sort(rng.choice(N, 8, replace=False)).astype(np.int32)[None]
+        r = st.resolve(res, P, N, idx)
+        assert r["misses"] == 0 and r["hits"] == 0 and r["resident"] == 8
+        assert (r["loc_kind"] == 1).all() and (r["loc_val"] == idx).all()
+
+
+def test_resolve_capacity_error_when_buffer_too_small():
+    P, N = 4, 64
+    st = oracle.HotState(3, N)
+    res = oracle.page_resident(oracle.ZERO, N, 0, P)
+    r = st.resolve(res, P, N, np.array([[1, 5, 9, 13]], np.int32))
+    assert r["status"] == oracle.ERR_CAPACITY
+
+
+def test_resolve_capacity_rule_always_has_victims():
+    """With C = (num_spec+2)*K the victims always exist (union <= nq*K = C-K)."""
+    rng = np.random.default_rng(9)
+    P, N = 4, 400
+    for nq in (1, 2, 4):
+        K = 16
+        C = (nq + 1) * K
+        st = oracle.HotState(C, N)
+        res = oracle.page_resident(oracle.ZERO, N, 0, P)
+        for _ in range(30):
+            idx = np.stack([np.sort(rng.choice(N, K, replace=False)) for _ in range(nq)]).astype(np.int32)
+            assert st.resolve(res, P, N, idx)["status"] == 0
+
+
+def test_page_resident_tail_window():
+    P, T = 64, 4096
+    for N in (4096, 4097, 5000, 142000):
+        r = oracle.page_resident(oracle.MIXED, N, T, P)
+        npages = (N + P - 1) // P
+        for p in range(npages):
+            assert bool(r[p]) == ((p + 1) * P > N - T)
+        # the tail covers at least the last T tokens
+        assert all(r[t // P] for t in range(max(N - T, 0), N))
+    assert oracle.page_resident(oracle.ZERO, 1000, T, P).sum() == 0
+    assert oracle.page_resident(oracle.FULL, 1000, T, P).sum() == (1000 + 63) // 64
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+def _rows_and_dense(fmt, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((n, 576), generator=g)
+    rows = wl.encode_rows(x, fmt)
+    if fmt == oracle.ROW_E4M3_656:
+        codes = rows[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        sc = rows[:, 512:528].contiguous().view(torch.float32).to(torch.float64)
+        rope = rows[:, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
+        kv = torch.cat([codes * sc.repeat_interleave(128, 1), rope], 1)
+    else:
+        kv = rows.contiguous().view(torch.float32).to(torch.float64)
+    return rows.numpy(), kv
+
+
+@pytest.mark.parametrize("fmt", [oracle.ROW_E4M3_656, oracle.ROW_F32_2304])
+def test_attention_k_ge_n_equals_dense_sdpa(fmt):
+    """When the selection covers every token (K >= N) sparse attention is
+    dense attention ("Comment s'y prendre": prompts inside the 2048 selected
+    tokens take the dense path).  Reference: torch SDPA in fp64."""
+    n, H = 37, 6
+    rows, kv = _rows_and_dense(fmt, n, 4)
+    q = torch.randn((H, 576), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    tau = 1.0 / math.sqrt(576)
+    o, lse = oracle.attention(fmt, q.view(torch.int16).numpy().view(np.uint16), rows, tau)
+    qd = q.to(torch.float64)[None, :, None, :].expand(1, H, 1, 576)
+    kd = kv[None, None].expand(1, H, n, 576)
+    vd = kv[:, :512][None, None].expand(1, H, n, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, scale=tau)[0, :, 0]
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+    ref_lse = torch.logsumexp(tau * (q.to(torch.float64) @ kv.T), 1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_masked_equals_gathered():
+    n, H = 50, 4
+    rows, _ = _rows_and_dense(oracle.ROW_E4M3_656, n, 8)
+    q = torch.randn((H, 576), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    mask = np.zeros(n, np.uint8)
+    sel = [0, 3, 4, 17, 30, 49]
+    mask[sel] = 1
+    o1, l1 = oracle.attention(oracle.ROW_E4M3_656, qb, rows, 0.05, mask)
+    o2, l2 = oracle.attention(oracle.ROW_E4M3_656, qb, rows[sel], 0.05)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-13, atol=1e-14)
+
+
+def test_attention_closed_forms():
+    rows, kv = _rows_and_dense(oracle.ROW_F32_2304, 5, 10)
+    kv = kv.numpy()
+    q = torch.randn((3, 576), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    # one row: output is that row's value part, lse is its score
+    o, lse = oracle.attention(oracle.ROW_F32_2304, qb, rows[2:3], 0.1)
+    np.testing.assert_allclose(o, np.repeat(kv[2:3, :512], 3, 0), rtol=0, atol=0)
+    np.testing.assert_allclose(lse, 0.1 * (q.double().numpy() @ kv[2]), rtol=1e-14)
+    # equal scores (q = 0): output is the mean of the rows, lse = log(n)
+    z = np.zeros((2, 576), np.uint16)
+    o, lse = oracle.attention(oracle.ROW_F32_2304, z, rows, 0.1)
+    np.testing.assert_allclose(o, np.repeat(kv[:, :512].mean(0, keepdims=True), 2, 0), rtol=1e-14)
+    np.testing.assert_allclose(lse, np.log(5), rtol=1e-15)
+    # nothing selected
+    o, lse = oracle.attention(oracle.ROW_F32_2304, qb, rows, 0.1, np.zeros(5, np.uint8))
+    assert (o == 0).all() and np.isneginf(lse).all()
+
+
+def test_page_constants_fixture_matches_capacity_rule():
+    pc = _json("page_constants.json")
+    K = pc["top_k"]["value"]
+    assert pc["hot_rows_per_topk_default"]["value"] * K == (0 + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K
+    ns = pc["mtp_speculative_tokens"]["value"]
+    assert (ns + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K == 10240
