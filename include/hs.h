@@ -1,0 +1,304 @@
+/*
+ * hs.h — C ABI of the Hybrid HiSparse sparse-MLA decode step on GB300 (sm_103a).
+ *
+ * What the library computes (sources are vLLM's Hybrid HiSparse write-ups):
+ *   "Un contexte d'un million sur huit H200", section "Ce qui se passe":
+ *     an indexer scores every cached token, the top-K are selected, and
+ *     sparse MLA attention reads only those K latent rows; one indexer layer
+ *     serves four sparse-MLA layers (IndexShare); the indexer cache stays
+ *     resident on the GPU.
+ *   same page, section "Les trois états de résidence":
+ *     full residency (all rows on the GPU), mixed residency (the tail stays on
+ *     the GPU and is never evicted, older pages live in pinned host memory,
+ *     selected rows of them go to hot buffers), zero residency (nothing on the
+ *     GPU; rows arrive as the indexer asks for them).  One fused resolve reads
+ *     resident rows in place, refreshes the LRU entry of a hot row, and on a
+ *     miss copies exactly one row from pinned host memory.  No CPU decision on
+ *     the decode path, so the step can be captured in a CUDA graph.  Hot
+ *     buffers are ordinary blocks of the same pool.
+ *   same page, section "Ce qu'il faut en retenir":
+ *     hot buffers hold 2 x top-K rows per request; with MTP,
+ *     (num_speculative_tokens + 2) x top-K.
+ *   "vLLM sert GLM-5.3 en contexte 1M sur 16 H200", section "Comment s'y
+ *     prendre": top-K = 2048 selected tokens.
+ *
+ * Conventions for every function below:
+ *   - Return value: HS_OK or an error status.  Argument errors are detected on
+ *     the host before anything is enqueued; nothing is enqueued then.
+ *   - Errors found on the device (an index outside the request, a hot buffer
+ *     too small, a bounded wait that ran out) set a sticky device error word
+ *     (read it with hs_pool_get_error); the affected kernel skips the work it
+ *     cannot do and never traps.
+ *   - "dev" pointers are CUDA device pointers owned by the caller; "host"
+ *     pointers are host memory owned by the caller.  The library keeps no
+ *     pointer to caller buffers beyond the call, except the two arenas given
+ *     to hs_pool_create.
+ *   - Hot-path calls (hs_indexer_score, hs_topk, hs_indexer_topk, hs_resolve,
+ *     hs_sparse_mla_decode, hs_step) only enqueue work on `stream`: no host
+ *     synchronisation, no allocation, no branch on device data.  They may be
+ *     captured in a CUDA graph and replayed.
+ *   - A pool is not thread-safe; use it from one host thread and one stream
+ *     at a time.
+ *   - Batch index b of a hot-path call is request id b (0 <= b < B).
+ */
+#ifndef HS_H
+#define HS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HS_OK = 0,
+    HS_ERR_INVALID_ARG = 1,     /* bad argument, unknown request, wrong mode   */
+    HS_ERR_ARENA_TOO_SMALL = 2, /* an arena is smaller than required           */
+    HS_ERR_CAPACITY = 3,        /* no free GPU block / hot buffer too small     */
+    HS_ERR_HOST_POOL_FULL = 4,  /* no free block in the pinned host pool        */
+    HS_ERR_INDEX_RANGE = 5,     /* a selected index outside [0, seq_len)        */
+    HS_ERR_TIMEOUT = 6,         /* a bounded device wait ran out                */
+    HS_ERR_CUDA = 7             /* a CUDA runtime call failed                   */
+} hs_status;
+
+/* Storage format of one MLA latent row (576 values = 512 nope + 64 rope). */
+typedef enum {
+    /* 656 bytes: [0,512) E4M3 codes of the nope dims, [512,528) four fp32
+     * scales (one per 128 nope dims), [528,656) 64 bf16 rope dims. */
+    HS_ROW_E4M3_656 = 0,
+    /* 2304 bytes: 576 fp32 values. */
+    HS_ROW_F32_2304 = 1
+} hs_row_format;
+
+/* Element format of indexer queries and keys. */
+typedef enum { HS_IDX_E4M3 = 0, HS_IDX_F32 = 1 } hs_idx_format;
+
+/* Residency of one request ("Les trois états de résidence"). */
+typedef enum {
+    HS_FULL = 0,  /* every page on the GPU                                   */
+    HS_MIXED = 1, /* tail window on the GPU, older pages host-only, hot buffer */
+    HS_ZERO = 2   /* nothing on the GPU, hot buffer filled on demand          */
+} hs_mode;
+
+typedef struct hs_pool hs_pool;
+
+typedef struct {
+    int32_t max_requests;   /* request ids are 0 .. max_requests-1              */
+    int32_t max_tokens;     /* context capacity of one request                  */
+    int32_t page_tokens;    /* P: tokens per page/block (64)                    */
+    int32_t top_k;          /* K                                                */
+    int32_t num_spec;       /* speculative tokens; nq = num_spec + 1 queries    */
+    int32_t tail_tokens;    /* T: tail window kept on the GPU in mixed mode     */
+    int32_t num_mla_layers; /* L: sparse-MLA layers served by one indexer layer */
+    int32_t mla_heads;      /* H: attention heads of one MLA layer              */
+    int32_t idx_heads;      /* Hi: indexer heads                                */
+    int32_t idx_dim;        /* Di: indexer head dim                             */
+    int32_t row_fmt;        /* hs_row_format                                    */
+    int32_t idx_fmt;        /* hs_idx_format                                    */
+    int32_t hot_rows;       /* C: hot-buffer rows per request; 0 selects the
+                               pages' rule (num_spec + 2) * top_k.  Must be a
+                               multiple of page_tokens and >= nq * top_k.      */
+    int32_t reserved;
+    int64_t gpu_blocks;     /* blocks in the device pool (each P tokens x L rows) */
+    int64_t host_blocks;    /* blocks in the pinned host pool (same shape); 0 =
+                               no host copies (full residency only)            */
+} hs_pool_config;
+
+typedef struct {
+    uint64_t resident; /* selected rows read in place (unique per request-step) */
+    uint64_t hits;     /* hot-buffer hits                                      */
+    uint64_t misses;   /* rows copied from pinned host (per request-step)      */
+    uint64_t bytes_copied; /* misses x L x row bytes                           */
+} hs_stats;
+
+/* Byte offsets of the regions the pool carved from the device arena, for
+ * inspection by tests and tools.  All offsets are from the arena base. */
+typedef struct {
+    size_t rows;             /* MLA block pool [gpu_blocks][L][P][R] bytes        */
+    size_t idx_keys;         /* indexer keys [max_requests][max_tokens][Di] elems */
+    size_t idx_scale;        /* indexer key scale [max_requests][max_tokens] fp32 */
+    size_t block_table;      /* [max_requests][max_pages] int32, -1 = not on GPU  */
+    size_t host_block_table; /* [max_requests][max_pages] int32, -1 = no host copy */
+    size_t hot_map;          /* [max_requests][max_tokens] int32 slot or -1       */
+    size_t slot_token;       /* [max_requests][C] int32 token or -1               */
+    size_t stamp;            /* [max_requests][C] uint32 last-use step, 0 = never */
+    size_t hot_blocks;       /* [max_requests][C/P] int32 pool block of each hot page */
+    size_t seq_len;          /* [max_requests] int32                              */
+    size_t req_step;         /* [max_requests] uint32 last resolved step          */
+    size_t row_bytes;        /* R                                                 */
+    size_t max_pages;        /* ceil(max_tokens / P)                              */
+    size_t hot_rows;         /* C                                                 */
+    size_t total;            /* bytes used of the arena                           */
+} hs_layout;
+
+/* ------------------------------------------------------------------------ */
+/* Pool creation (host, off the decode path)                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device and pinned-host arena a pool with this config needs.
+ * Pure host arithmetic; needs no GPU.  HS_ERR_INVALID_ARG for a bad config. */
+hs_status hs_pool_required_bytes(const hs_pool_config *cfg, size_t *dev_bytes,
+                                 size_t *host_bytes);
+
+/* Carve a pool out of caller-owned memory.  dev_arena: device memory of at
+ * least *dev_bytes (16-byte aligned, 256 recommended).  host_arena: pinned
+ * host memory (cudaHostAlloc / torch pin_memory) of at least *host_bytes, or
+ * NULL when cfg->host_blocks == 0; it must be reachable from the device
+ * (unified addressing).  Both must outlive the pool; the pool never allocates
+ * device or pinned memory after this call.  Initialises the arena's tables
+ * (synchronously on the default stream). */
+hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena,
+                         size_t dev_bytes, void *host_arena, size_t host_bytes,
+                         hs_pool **out);
+void hs_pool_destroy(hs_pool *pool);
+hs_status hs_pool_get_layout(const hs_pool *pool, hs_layout *out);
+
+/* ------------------------------------------------------------------------ */
+/* Request lifecycle (host, between decode steps)                            */
+/* ------------------------------------------------------------------------ */
+
+/* Open request `req` (empty, length 0) in residency `mode`.  Mixed and zero
+ * modes lease C/P hot-buffer blocks from the device pool and start with every
+ * slot empty ("Les trois états de résidence": zero residency starts with empty
+ * slots).  HS_ERR_CAPACITY when the pool lacks the blocks. */
+hs_status hs_request_open(hs_pool *pool, int32_t req, hs_mode mode);
+
+/* Append n tokens to request `req`.  mla_rows: [n][L][R] bytes; idx_keys:
+ * [n][Di] elements of the indexer format; idx_scale: [n] fp32 (NULL = 1.0).
+ * Each pointer may be host or device memory.  The rows are written to the GPU
+ * pool when their page is resident (full mode: every page; mixed: the tail
+ * window) and to the pinned host pool when it exists (a full-residency page
+ * thus already has its host copy, which later lets it leave the GPU without a
+ * copy: "Les trois états de résidence").  In mixed mode pages that slide out
+ * of the tail window give their GPU block back.  Synchronises `stream` before
+ * returning (off the decode path).  HS_ERR_CAPACITY: no GPU block;
+ * HS_ERR_HOST_POOL_FULL: no host block; HS_ERR_INVALID_ARG: past max_tokens. */
+hs_status hs_append(hs_pool *pool, int32_t req, const void *mla_rows,
+                    const void *idx_keys, const float *idx_scale, int32_t n,
+                    cudaStream_t stream);
+
+/* Change the residency of a request between steps.  full -> mixed: pages
+ * outside the tail window release their GPU blocks (their host copies exist),
+ * hot-buffer blocks are leased, every slot starts empty.  Needs a host pool.
+ * Other transitions: HS_ERR_INVALID_ARG.  Synchronises `stream`. */
+hs_status hs_request_set_mode(hs_pool *pool, int32_t req, hs_mode mode,
+                              cudaStream_t stream);
+
+/* Release every GPU and host block of the request. */
+hs_status hs_request_close(hs_pool *pool, int32_t req);
+
+/* Number of free blocks left in the device pool. */
+int64_t hs_pool_free_gpu_blocks(const hs_pool *pool);
+
+/* ------------------------------------------------------------------------ */
+/* Decode-step calls (async on `stream`, graph-capturable)                   */
+/* ------------------------------------------------------------------------ */
+
+/* Indexer score ("Ce qui se passe"): for b < B, query j < nq, token t <
+ * seq_len[b]:
+ *   scores[(b*nq + j)*score_stride + t] =
+ *       sum_h w[b][j][h] * ReLU(sigma[b][t] * (q[b][j][h][:] . k[b][t][:]))
+ * with ReLU(x) = x > 0 ? x : +0 (fp32).  q: dev [B][nq][Hi][Di] in the pool's
+ * indexer format (E4M3 bytes or fp32); w: dev [B][nq][Hi] fp32; scores: dev
+ * fp32, score_stride >= max_tokens.  Entries t >= seq_len[b] are untouched. */
+hs_status hs_indexer_score(hs_pool *pool, const void *q, const float *w,
+                           int32_t B, int32_t nq, float *scores,
+                           int64_t score_stride, cudaStream_t stream);
+
+/* Top-K: for each (b, j) the K largest scores[(b*nq+j)*score_stride + t] over
+ * t < seq_len[b] - nq + j + 1 (query j sees up to its own position); equal
+ * scores go to the lower t; written ascending to topk[(b*nq+j)*K ..] and
+ * padded with -1 when fewer than K tokens are visible.  Deterministic. */
+hs_status hs_topk(hs_pool *pool, const float *scores, int64_t score_stride,
+                  int32_t B, int32_t nq, int32_t *topk, cudaStream_t stream);
+
+/* hs_indexer_score + hs_topk with the scores kept in the pool's workspace. */
+hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
+                          int32_t B, int32_t nq, int32_t *topk,
+                          cudaStream_t stream);
+
+/* Fused resolve ("Les trois états de résidence") of one step for requests
+ * b < B.  topk: dev [B][nq][K] (ascending per (b,j), -1 padded).  Per request:
+ * the union U of its nq lists; each u in U is resident (its page is on the
+ * GPU: read in place), a hit (in the hot buffer: its stamp becomes this step,
+ * i.e. the LRU entry is refreshed) or a miss.  Misses take the least recently
+ * used slots not touched in this step (order (stamp, slot)); the i-th miss in
+ * ascending token order takes the i-th such victim in ascending slot order;
+ * then exactly one row per layer is copied from pinned host memory into the
+ * slot.  row_id: dev [B][nq][K] int32, the pool row (block * P + offset) each
+ * entry reads, -1 for padding.  The step number is a per-request device
+ * counter incremented by this call (so graph replays keep counting). */
+hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
+                     int32_t *row_id, cudaStream_t stream);
+
+/* Sparse MLA decode of one layer over the resolved rows ("Ce qui se passe"):
+ *   z[b][j][h][k] = softmax_scale * q[b][j][h][:576] . row(row_id[b][j][k])[:576]
+ *   out[b][j][h][:512] = sum_k softmax_k(z) * row[:512]   (rows with id -1 skipped)
+ *   lse[b][j][h] = ln(sum_k exp(z))                        (if lse != NULL)
+ * q: dev [B][nq][H][576] bf16; out: dev [B][nq][H][512] bf16; lse: dev fp32
+ * or NULL.  A query with no row gets out = 0, lse = -inf. */
+hs_status hs_sparse_mla_decode(hs_pool *pool, int32_t layer, const void *q,
+                               const int32_t *row_id, int32_t B, int32_t nq,
+                               float softmax_scale, void *out, float *lse,
+                               cudaStream_t stream);
+
+typedef struct {
+    int32_t B, nq;
+    const void *q_idx;    /* dev [B][nq][Hi][Di], indexer format             */
+    const float *w_idx;   /* dev [B][nq][Hi]                                 */
+    const void *q_mla;    /* dev [L][B][nq][H][576] bf16                     */
+    float softmax_scale;
+    void *out;            /* dev [L][B][nq][H][512] bf16                     */
+    float *lse;           /* dev [L][B][nq][H] fp32, or NULL                 */
+    int32_t *topk;        /* dev [B][nq][K] int32 (output)                   */
+    int32_t *row_id;      /* dev [B][nq][K] int32 (output)                   */
+} hs_step_args;
+
+/* One decode step of one IndexShare group: indexer score -> top-K ->
+ * fused resolve (with miss copies) -> sparse MLA decode for each of the L
+ * layers.  Everything is enqueued on `stream`; no host synchronisation. */
+hs_status hs_step(hs_pool *pool, const hs_step_args *args, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Introspection (host, synchronising)                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronise the device, read and clear the sticky device error word. */
+hs_status hs_pool_get_error(hs_pool *pool, hs_status *device_status);
+
+/* Synchronise, read the device counters (cumulative since create/reset). */
+hs_status hs_pool_stats(hs_pool *pool, hs_stats *out);
+hs_status hs_pool_reset_stats(hs_pool *pool);
+
+/* Copy one request's residency state to host arrays (any may be NULL):
+ * hot_map [max_tokens], slot_token [C], stamp [C], block_table [max_pages],
+ * host_block_table [max_pages], hot_blocks [C/P], step (1), seq_len (1). */
+hs_status hs_pool_dump_state(hs_pool *pool, int32_t req, int32_t *hot_map,
+                             int32_t *slot_token, uint32_t *stamp,
+                             int32_t *block_table, int32_t *host_block_table,
+                             int32_t *hot_blocks, uint32_t *step,
+                             int32_t *seq_len);
+
+/* Overwrite one request's hot-buffer state (hot_map, slot_token, stamp, step)
+ * from host arrays, e.g. to re-seed a benchmark step.  The rows of the slots
+ * are not touched. */
+hs_status hs_pool_load_state(hs_pool *pool, int32_t req, const int32_t *hot_map,
+                             const int32_t *slot_token, const uint32_t *stamp,
+                             uint32_t step);
+
+/* Number of kernels hs_step enqueues for a batch of B requests x nq queries
+ * (host arithmetic, the same decision hs_step makes); -1 on bad arguments. */
+int32_t hs_step_kernel_count(const hs_pool *pool, int32_t B, int32_t nq);
+
+/* A static English description of a status. */
+const char *hs_status_string(hs_status s);
+
+/* Version of this ABI (major * 100 + minor). */
+int32_t hs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_H */

@@ -140,10 +140,10 @@ void hso_indexer_scores(int idx_fmt, const void *q, const float *w,
                         int N, int nq, int Hi, int Di, float *s)
 {
     int j;
-#pragma omp parallel for schedule(static)
     for (j = 0; j < nq; j++) {
         int visible = N - nq + j + 1;
         int t;
+#pragma omp parallel for schedule(static)
         for (t = 0; t < N; t++) {
             double acc = 0.0;
             int h;

@@ -1,0 +1,401 @@
+// Fused top-K resolve ("Un contexte d'un million sur huit H200", section "Les
+// trois états de résidence"): a selected token whose page is on the GPU is
+// read in place; a token already in the request's hot buffer refreshes its
+// LRU entry; a miss copies exactly one row per layer from pinned host memory
+// into a hot-buffer slot.  No CPU decision: the step counter, the victim
+// choice and the copy list all live on the device.
+//
+// resolve_plan_kernel: one 1024-thread CTA per request.
+//   1. validate the nq lists (ascending, -1 padded, inside the request);
+//   2. merge them into U, their sorted union without duplicates (merge-path
+//      ranks by binary search, then a compaction of first occurrences);
+//   3. classify each u in U: resident page -> in place; hot_map[u] >= 0 -> hit
+//      (stamp = step); else miss; misses are compacted in ascending order;
+//   4. choose victims: among slots with stamp < step, the M smallest keys
+//      (stamp, slot), found by an 8-bit-digit radix select on the stamp plus a
+//      lowest-slot-first cut among equal stamps; victims are compacted in
+//      ascending slot order;
+//   5. the i-th miss takes the i-th victim: hot_map / slot_token / stamp are
+//      updated and the (token, slot) pair goes to the device miss list;
+//   6. every (j, k) entry gets its pool row id.
+// miss_copy_kernel: a grid-stride copy of the miss list, 16-byte vectors,
+// consecutive threads on consecutive bytes of a row (coalesced on both the
+// host-link read and the HBM write).
+#include "hs_internal.h"
+
+namespace hs {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += n;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int y = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += n;
+        }
+        warp_sums[lane] = y;
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+    *total = warp_sums[nw - 1];
+    __syncthreads();
+    return incl - v;
+}
+
+// Stable compaction of indices [0, n) for which pred holds; emit(i, rank).
+template <class Pred, class Emit>
+__device__ __forceinline__ int block_compact(int n, Pred pred, Emit emit, int *warp_sums) {
+    const int seg = (n + kThreads - 1) / kThreads;
+    const int lo = min(n, (int)threadIdx.x * seg), hi = min(n, lo + seg);
+    int c = 0;
+    for (int i = lo; i < hi; i++) c += pred(i) ? 1 : 0;
+    int total;
+    int r = block_excl_scan(c, warp_sums, &total);
+    for (int i = lo; i < hi; i++)
+        if (pred(i)) emit(i, r++);
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ int lower_bound(const int32_t *a, int n, int32_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int upper_bound(const int32_t *a, int n, int32_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= x) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+struct PlanArgs {
+    const int32_t *topk;
+    int nq, K, P, C, hot_pages, maxT, max_pages, L, R;
+    const int32_t *seq_len;
+    const int32_t *block_table;
+    int32_t *hot_map;
+    int32_t *slot_token;
+    uint32_t *stamp;
+    const int32_t *hot_blocks;
+    uint32_t *req_step;
+    int32_t *miss_count;
+    int32_t *miss_tok;
+    int32_t *miss_slot;
+    int32_t *row_id;
+    int32_t *err;
+    unsigned long long *stats;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
+    extern __shared__ int32_t sm[];
+    __shared__ int warp_sums[32];
+    __shared__ int lens[8];
+    __shared__ uint32_t hist[256];
+    __shared__ int sel[4];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int n = a.nq * a.K;
+    int32_t *lst = sm;            // [n] the lists; later: index into U of each miss
+    int32_t *merged = lst + n;    // [n] merged lists; later: miss tokens
+    int32_t *U = merged + n;      // [n] sorted unique union
+    int32_t *uslot = U + n;       // [n] -1 resident, >= 0 slot, -2 miss, -3 unserved
+    int32_t *victim = uslot + n;  // [n] victim slots, ascending
+    const int N = a.seq_len[b];
+    const uint32_t step = a.req_step[b] + 1;
+    const int32_t *tk = a.topk + (size_t)b * n;
+    int32_t *rid = a.row_id + (size_t)b * n;
+    const size_t hm = (size_t)b * a.maxT, sc = (size_t)b * a.C;
+    const int32_t *bt = a.block_table + (size_t)b * a.max_pages;
+    const int32_t *hb = a.hot_blocks + (size_t)b * a.hot_pages;
+
+    // 1. load and validate
+    if (tid < 8) lens[tid] = 0;
+    for (int i = tid; i < n; i += kThreads) lst[i] = tk[i];
+    __syncthreads();
+    bool bad = false;
+    for (int i = tid; i < n; i += kThreads) {
+        const int k = i % a.K;
+        const int32_t v = lst[i];
+        if (v < -1 || v >= N) bad = true;
+        if (k + 1 < a.K) {
+            const int32_t w = lst[i + 1];
+            if (v == -1 ? (w != -1) : (w != -1 && w <= v)) bad = true;
+        }
+        if (v >= 0 && (k + 1 == a.K || lst[i + 1] == -1)) lens[i / a.K] = k + 1;
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) {
+            set_error(a.err, HS_ERR_INDEX_RANGE);
+            a.miss_count[b] = 0;
+        }
+        for (int i = tid; i < n; i += kThreads) rid[i] = -1;
+        return;
+    }
+
+    // 2. merge-path ranks -> merged (ties: lower list first), then dedup into U
+    int total = 0;
+    for (int j = 0; j < a.nq; j++) total += lens[j];
+    for (int i = tid; i < n; i += kThreads) {
+        const int j = i / a.K, k = i - j * a.K;
+        const int32_t x = lst[i];
+        if (x < 0) continue;
+        int pos = k;
+        for (int jj = 0; jj < a.nq; jj++) {
+            if (jj == j) continue;
+            const int32_t *l2 = lst + jj * a.K;
+            pos += jj < j ? upper_bound(l2, lens[jj], x) : lower_bound(l2, lens[jj], x);
+        }
+        merged[pos] = x;
+    }
+    __syncthreads();
+    const int nu = block_compact(
+        total, [&](int p) { return p == 0 || merged[p] != merged[p - 1]; },
+        [&](int p, int r) { U[r] = merged[p]; }, warp_sums);
+
+    // 3. classify; hits refresh their stamp
+    int nres = 0, nhit = 0;
+    for (int i = tid; i < nu; i += kThreads) {
+        const int32_t u = U[i];
+        if (bt[u / a.P] >= 0) {
+            uslot[i] = -1;
+            nres++;
+        } else {
+            const int32_t s = a.hot_map[hm + u];
+            if (s >= 0) {
+                uslot[i] = s;
+                a.stamp[sc + s] = step;
+                nhit++;
+            } else {
+                uslot[i] = -2;
+            }
+        }
+    }
+    {
+        int t0, t1;
+        block_excl_scan(nres, warp_sums, &t0);
+        block_excl_scan(nhit, warp_sums, &t1);
+        if (tid == 0) {
+            atomicAdd(&a.stats[0], (unsigned long long)t0);
+            atomicAdd(&a.stats[1], (unsigned long long)t1);
+        }
+    }
+    int32_t *miss = merged;   // merged is dead now
+    int32_t *missidx = lst;   // lists are dead now
+    const int M = block_compact(
+        nu, [&](int i) { return uslot[i] == -2; },
+        [&](int i, int r) {
+            miss[r] = U[i];
+            missidx[r] = i;
+        },
+        warp_sums);
+
+    // 4. victims: the M smallest (stamp, slot) among slots with stamp < step
+    int served = 0;
+    if (M > 0) {
+        const uint32_t *stp = a.stamp + sc;
+        uint32_t prefix = 0, mask = 0;
+        int need = M;
+        bool enough = true;
+        for (int pass = 0; pass < 4; pass++) {
+            const int shift = 24 - 8 * pass;
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+            for (int s = tid; s < a.C; s += kThreads) {
+                const uint32_t v = stp[s];
+                if (v < step && (v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            const int c = tid < 256 ? (int)hist[tid] : 0;
+            int tot;
+            const int ex = block_excl_scan(c, warp_sums, &tot);
+            if (pass == 0 && tot < M) {
+                enough = false;
+                break;
+            }
+            if (tid < 256 && ex < need && need <= ex + c) {
+                sel[0] = tid;
+                sel[1] = ex;
+            }
+            __syncthreads();
+            prefix |= (uint32_t)sel[0] << shift;
+            mask |= 255u << shift;
+            need -= sel[1];
+            __syncthreads();
+        }
+        if (!enough) {
+            if (tid == 0) set_error(a.err, HS_ERR_CAPACITY);
+            for (int i = tid; i < M; i += kThreads) uslot[missidx[i]] = -3;
+        } else {
+            // lt: stamp < S*, eq: stamp == S* (taken lowest slot first, `need` of them)
+            const uint32_t S = prefix;
+            const int seg = (a.C + kThreads - 1) / kThreads;
+            const int lo = min(a.C, tid * seg), hi = min(a.C, lo + seg);
+            int lt = 0, eq = 0;
+            for (int s = lo; s < hi; s++) {
+                const uint32_t v = stp[s];
+                lt += v < S;
+                eq += (v == S) && (v < step);
+            }
+            for (int i = tid; i < M; i += kThreads) victim[i] = -1;
+            __syncthreads();
+            int tot;
+            const int ex = block_excl_scan((eq << 16) | lt, warp_sums, &tot);
+            int lb = ex & 0xFFFF, eb = ex >> 16;
+            for (int s = lo; s < hi; s++) {
+                const uint32_t v = stp[s];
+                if (v < S) {
+                    const int pos = lb + min(eb, need);
+                    if (pos < M) victim[pos] = s;
+                    lb++;
+                } else if (v == S && v < step) {
+                    if (eb < need && lb + eb < M) victim[lb + eb] = s;
+                    eb++;
+                }
+            }
+            __syncthreads();
+            // 5. assignment: i-th miss (ascending token) -> i-th victim (ascending slot)
+            for (int i = tid; i < M; i += kThreads) {
+                const int32_t s = victim[i], u = miss[i];
+                if (s < 0 || s >= a.C) {  // cannot happen; never write outside the tables
+                    set_error(a.err, HS_ERR_CAPACITY);
+                    uslot[missidx[i]] = -3;
+                    continue;
+                }
+                const int32_t old = a.slot_token[sc + s];
+                if (old >= 0) a.hot_map[hm + old] = -1;
+                a.slot_token[sc + s] = u;
+                a.hot_map[hm + u] = s;
+                a.stamp[sc + s] = step;
+                uslot[missidx[i]] = s;
+                a.miss_tok[(size_t)b * n + i] = u;
+                a.miss_slot[(size_t)b * n + i] = s;
+            }
+            served = M;
+        }
+    }
+    if (tid == 0) {
+        a.miss_count[b] = served;
+        a.req_step[b] = step;
+        atomicAdd(&a.stats[2], (unsigned long long)served);
+        atomicAdd(&a.stats[3], (unsigned long long)served * a.L * a.R);
+    }
+    __syncthreads();
+
+    // 6. row ids
+    for (int i = tid; i < n; i += kThreads) {
+        const int32_t u = tk[i];
+        int32_t r = -1;
+        if (u >= 0) {
+            const int32_t s = uslot[lower_bound(U, nu, u)];
+            if (s == -1)
+                r = bt[u / a.P] * a.P + u % a.P;
+            else if (s >= 0)
+                r = hb[s / a.P] * a.P + s % a.P;
+        }
+        rid[i] = r;
+    }
+}
+
+__global__ void __launch_bounds__(256) miss_copy_kernel(
+    const int32_t *__restrict__ miss_count, const int32_t *__restrict__ miss_tok,
+    const int32_t *__restrict__ miss_slot, int n, const int32_t *__restrict__ host_block_table,
+    const int32_t *__restrict__ hot_blocks, const uint8_t *__restrict__ host_rows,
+    uint8_t *__restrict__ rows, int L, int P, int R, int max_pages, int hot_pages, int32_t *err) {
+    const int b = blockIdx.y;
+    const int M = miss_count[b];
+    const int cpr = R / 16, per_miss = L * cpr;
+    const int64_t total = (int64_t)M * per_miss;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i / per_miss);
+        const int rem = (int)(i - (int64_t)m * per_miss);
+        const int l = rem / cpr, c = rem - l * cpr;
+        const int32_t u = miss_tok[(size_t)b * n + m], s = miss_slot[(size_t)b * n + m];
+        if (u < 0 || u >= max_pages * P || s < 0 || s >= hot_pages * P) {
+            set_error(err, HS_ERR_INVALID_ARG);
+            continue;
+        }
+        const int32_t hblk = host_block_table[(size_t)b * max_pages + u / P];
+        if (hblk < 0) {
+            set_error(err, HS_ERR_INVALID_ARG);
+            continue;
+        }
+        const int32_t dblk = hot_blocks[(size_t)b * hot_pages + s / P];
+        const uint4 *src = (const uint4 *)(host_rows + (((size_t)hblk * L + l) * P + u % P) * R) + c;
+        uint4 *dst = (uint4 *)(rows + (((size_t)dblk * L + l) * P + s % P) * R) + c;
+        *dst = *src;
+    }
+}
+
+size_t plan_smem(int n) { return (size_t)5 * n * 4; }
+
+}  // namespace
+
+cudaError_t resolve_setup(const hs_pool *p) {
+    const size_t sm = plan_smem(p->nq_max * p->cfg.top_k);
+    if (sm > 200 * 1024) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(resolve_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sm);
+}
+
+int resolve_kernel_count(const hs_pool *p, int, int) { return p->cfg.host_blocks > 0 ? 2 : 1; }
+
+cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
+                           cudaStream_t st) {
+    PlanArgs a;
+    a.topk = topk;
+    a.nq = nq;
+    a.K = p->cfg.top_k;
+    a.P = p->cfg.page_tokens;
+    a.C = p->C;
+    a.hot_pages = p->hot_pages;
+    a.maxT = p->cfg.max_tokens;
+    a.max_pages = p->max_pages;
+    a.L = p->cfg.num_mla_layers;
+    a.R = p->R;
+    a.seq_len = p->d.seq_len;
+    a.block_table = p->d.block_table;
+    a.hot_map = p->d.hot_map;
+    a.slot_token = p->d.slot_token;
+    a.stamp = p->d.stamp;
+    a.hot_blocks = p->d.hot_blocks;
+    a.req_step = p->d.req_step;
+    a.miss_count = p->d.miss_count;
+    a.miss_tok = p->d.miss_tok;
+    a.miss_slot = p->d.miss_slot;
+    a.row_id = row_id;
+    a.err = p->d.err;
+    a.stats = p->d.stats;
+    const int n = nq * a.K;
+    resolve_plan_kernel<<<B, kThreads, plan_smem(n), st>>>(a);
+    if (p->cfg.host_blocks > 0) {
+        // enough CTAs in flight to cover the host link's latency, at any B
+        const int gx = (4 * kNumSMs + B - 1) / B;
+        dim3 grid(gx, B);
+        miss_copy_kernel<<<grid, 256, 0, st>>>(p->d.miss_count, p->d.miss_tok, p->d.miss_slot,
+                                               n, p->d.host_block_table,
+                                               p->d.hot_blocks, p->host_dev, p->d.rows, a.L, a.P,
+                                               a.R, a.max_pages, a.hot_pages, p->d.err);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hs

@@ -1,0 +1,263 @@
+// Top-K selection over indexer scores ("vLLM sert GLM-5.3 en contexte 1M sur
+// 16 H200", section "Comment s'y prendre": the 2048 selected tokens).
+//
+// Radix select on an order-preserving 32-bit key of each fp32 score, 11 + 11
+// + 10 bits, MSB first.  Each pass is one kernel over (chunk, row) CTAs that
+// builds a shared-memory histogram of the still-undecided keys and adds it
+// into a per-row global histogram with integer atomics (order independent);
+// the last CTA of the row (ticket counter) picks the digit of the K-th
+// largest key.  After three passes the threshold key T and the number `need`
+// of keys equal to T to keep are known; two more kernels count, per chunk,
+// keys above / equal to T and write the selected indices in ascending token
+// order (keys equal to T are taken lowest index first).  Every count is an
+// integer, so the result is bit-for-bit deterministic.
+#include "hs_internal.h"
+
+namespace hs {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kPerThread = kTopkChunk / kThreads;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Inclusive scan over the block (blockDim.x a multiple of 32, <= 1024).
+__device__ __forceinline__ int block_incl_scan(int v, int *warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int x = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
+        }
+        warp_sums[lane] = x;
+    }
+    __syncthreads();
+    if (warp > 0) v += warp_sums[warp - 1];
+    __syncthreads();
+    return v;
+}
+
+__global__ void topk_init_kernel(TopkRowState *st, uint32_t *hist, const int32_t *seq_len,
+                                 int nq, int K) {
+    const int row = blockIdx.x;
+    const int b = row / nq, j = row - b * nq;
+    const int vis = seq_len[b] - nq + j + 1;
+    for (int i = threadIdx.x; i < kTopkBins; i += blockDim.x) hist[(size_t)row * kTopkBins + i] = 0;
+    if (threadIdx.x == 0) {
+        TopkRowState s;
+        s.prefix = 0;
+        s.mask = 0;
+        s.need = K;
+        s.take_all = vis <= K;
+        s.ticket = 0;
+        s.visible = vis > 0 ? vis : 0;
+        s.pad[0] = s.pad[1] = 0;
+        st[row] = s;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float *__restrict__ scores,
+                                                             int64_t stride, TopkRowState *st,
+                                                             uint32_t *ghist, int pass) {
+    __shared__ uint32_t sh[kTopkBins];
+    __shared__ int warp_sums[32];
+    __shared__ int is_last;
+    const int row = blockIdx.y, chunk = blockIdx.x, tid = threadIdx.x;
+    const TopkRowState s = st[row];
+    if (s.take_all) return;  // uniform over the row's CTAs
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nbins = pass == 2 ? 1024 : 2048;
+    for (int i = tid; i < nbins; i += kThreads) sh[i] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)chunk * kTopkChunk;
+    const float *src = scores + (size_t)row * stride;
+#pragma unroll
+    for (int k = 0; k < kPerThread; k++) {
+        const int64_t t = base + k * kThreads + tid;
+        if (t < s.visible) {
+            const uint32_t key = order_key(src[t]);
+            if ((key & s.mask) == s.prefix) atomicAdd(&sh[(key >> shift) & (nbins - 1)], 1u);
+        }
+    }
+    __syncthreads();
+    uint32_t *gh = ghist + (size_t)row * kTopkBins;
+    for (int i = tid; i < nbins; i += kThreads) {
+        const uint32_t c = sh[i];
+        if (c) atomicAdd(&gh[i], c);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = atomicAdd(&st[row].ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // Last CTA of this row: walk the bins from the largest key down.  Thread i
+    // holds the two bins at descending positions 2i, 2i+1.
+    int c0 = 0, c1 = 0;
+    const int p0 = 2 * tid, p1 = 2 * tid + 1;
+    if (p0 < nbins) c0 = (int)__ldcg(&gh[nbins - 1 - p0]);
+    if (p1 < nbins) c1 = (int)__ldcg(&gh[nbins - 1 - p1]);
+    const int incl = block_incl_scan(c0 + c1, warp_sums);
+    const int above0 = incl - c0 - c1;  // keys in bins above position p0
+    const int need = s.need;
+    int found_pos = -1, found_above = 0;
+    if (p0 < nbins && above0 < need && need <= above0 + c0) {
+        found_pos = p0;
+        found_above = above0;
+    } else if (p1 < nbins && above0 + c0 < need && need <= above0 + c0 + c1) {
+        found_pos = p1;
+        found_above = above0 + c0;
+    }
+    if (found_pos >= 0) {
+        const uint32_t bin = (uint32_t)(nbins - 1 - found_pos);
+        TopkRowState n = s;
+        n.prefix = s.prefix | (bin << shift);
+        n.mask = s.mask | ((uint32_t)(nbins - 1) << shift);
+        n.need = need - found_above;
+        n.ticket = 0;
+        st[row] = n;
+    }
+    // clear the row histogram for the next pass
+    for (int i = tid; i < kTopkBins; i += kThreads) gh[i] = 0;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_count_kernel(const float *__restrict__ scores,
+                                                              int64_t stride,
+                                                              const TopkRowState *st,
+                                                              int32_t *chunk_cnt, int nchunks) {
+    __shared__ int warp_sums[32];
+    const int row = blockIdx.y, chunk = blockIdx.x, tid = threadIdx.x;
+    const TopkRowState s = st[row];
+    const int64_t base = (int64_t)chunk * kTopkChunk;
+    const float *src = scores + (size_t)row * stride;
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThread; k++) {
+        const int64_t t = base + k * kThreads + tid;
+        if (t < s.visible) {
+            if (s.take_all) {
+                gt++;
+            } else {
+                const uint32_t key = order_key(src[t]);
+                gt += key > s.prefix;
+                eq += key == s.prefix;
+            }
+        }
+    }
+    const int packed = block_incl_scan((eq << 16) | gt, warp_sums);
+    if (tid == kThreads - 1) {
+        int32_t *c = chunk_cnt + ((size_t)row * nchunks + chunk) * 2;
+        c[0] = packed & 0xFFFF;
+        c[1] = packed >> 16;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_write_kernel(const float *__restrict__ scores,
+                                                              int64_t stride,
+                                                              const TopkRowState *st,
+                                                              const int32_t *chunk_cnt,
+                                                              int nchunks, int K, int32_t *topk) {
+    __shared__ int warp_sums[32];
+    __shared__ int before[2], total[2];
+    const int row = blockIdx.y, chunk = blockIdx.x, tid = threadIdx.x;
+    const TopkRowState s = st[row];
+    const int need = s.take_all ? 0 : s.need;
+    if (tid < 32) {
+        int bg = 0, be = 0, tg = 0, te = 0;
+        for (int c = tid; c < nchunks; c += 32) {
+            const int g = chunk_cnt[((size_t)row * nchunks + c) * 2];
+            const int e = chunk_cnt[((size_t)row * nchunks + c) * 2 + 1];
+            tg += g;
+            te += e;
+            if (c < chunk) {
+                bg += g;
+                be += e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            bg += __shfl_xor_sync(0xffffffffu, bg, o);
+            be += __shfl_xor_sync(0xffffffffu, be, o);
+            tg += __shfl_xor_sync(0xffffffffu, tg, o);
+            te += __shfl_xor_sync(0xffffffffu, te, o);
+        }
+        if (tid == 0) {
+            before[0] = bg;
+            before[1] = be;
+            total[0] = tg;
+            total[1] = te;
+        }
+    }
+    __syncthreads();
+    const int64_t base = (int64_t)chunk * kTopkChunk + (int64_t)tid * kPerThread;
+    const float *src = scores + (size_t)row * stride;
+    uint8_t flag[kPerThread];  // 1 = above T, 2 = equal to T
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThread; k++) {
+        const int64_t t = base + k;
+        flag[k] = 0;
+        if (t < s.visible) {
+            if (s.take_all) {
+                flag[k] = 1;
+            } else {
+                const uint32_t key = order_key(src[t]);
+                flag[k] = key > s.prefix ? 1 : (key == s.prefix ? 2 : 0);
+            }
+            gt += flag[k] == 1;
+            eq += flag[k] == 2;
+        }
+    }
+    const int v = (eq << 16) | gt;
+    const int excl = block_incl_scan(v, warp_sums) - v;
+    int gb = before[0] + (excl & 0xFFFF);
+    int eb = before[1] + (excl >> 16);
+    int32_t *out = topk + (size_t)row * K;
+#pragma unroll
+    for (int k = 0; k < kPerThread; k++) {
+        if (flag[k] == 1) {
+            out[gb + min(eb, need)] = (int32_t)(base + k);
+            gb++;
+        } else if (flag[k] == 2) {
+            if (eb < need) out[gb + eb] = (int32_t)(base + k);
+            eb++;
+        }
+    }
+    if (chunk == 0) {
+        const int taken = total[0] + min(total[1], need);
+        for (int i = taken + tid; i < K; i += kThreads) out[i] = -1;
+    }
+}
+
+}  // namespace
+
+int topk_kernel_count(const hs_pool *, int, int) { return 6; }
+
+cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, int B, int nq,
+                        int32_t *topk, cudaStream_t st) {
+    const int rows = B * nq, nch = p->topk_nchunks, K = p->cfg.top_k;
+    topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K);
+    dim3 grid(nch, rows);
+    for (int pass = 0; pass < 3; pass++)
+        topk_hist_kernel<<<grid, kThreads, 0, st>>>(scores, stride, p->d.topk_state,
+                                                    p->d.topk_hist, pass);
+    topk_count_kernel<<<grid, kThreads, 0, st>>>(scores, stride, p->d.topk_state,
+                                                 p->d.topk_chunk, nch);
+    topk_write_kernel<<<grid, kThreads, 0, st>>>(scores, stride, p->d.topk_state,
+                                                 p->d.topk_chunk, nch, K, topk);
+    return cudaGetLastError();
+}
+
+}  // namespace hs

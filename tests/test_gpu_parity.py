@@ -1,0 +1,316 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs (bit-exact indices / state / rows; attention within
+2e-3 + 1e-2 |ref|).  Sizes are small enough for the oracle, yet span several
+tiles, chunks and pages with ragged tails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mla_kv_fp8_gb300 import workload as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _hs():
+    from sparse_mla_kv_fp8_gb300 import hs
+    return hs
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _run(case, steps=None):
+    from harness import Runner
+    r = Runner(case)
+    try:
+        for _ in range(steps or case.steps):
+            r.run_step()
+        st = r.pool.stats()
+        assert st["resident"] == r.stats["resident"]
+        assert st["hits"] == r.stats["hits"]
+        assert st["misses"] == r.stats["misses"]
+        return r.stats
+    finally:
+        r.close()
+
+
+def test_tiny_fp32_mixed_32_steps():
+    """1 request, N=4096 (+1 per step), K=256, 4x32 fp32 indexer, 16 heads,
+    fp32 rows, tail 512, hot 2K=512, 32 steps."""
+    from harness import Case
+    hs = _hs()
+    c = Case("tiny-fp32", B=1, N=4096, K=256, Hi=4, Di=32, idx_fmt=wl.IDX_F32, H=16,
+             row_fmt=wl.ROW_F32_2304, L=1, T=512, mode=hs.HS_MIXED, steps=32, append=1)
+    stats = _run(c)
+    assert stats["misses"] > 0 and stats["hits"] > 0 and stats["resident"] > 0
+
+
+def test_tiny_fp8_mixed():
+    from harness import Case
+    hs = _hs()
+    c = Case("tiny-fp8", B=1, N=4096, K=256, Hi=4, Di=32, idx_fmt=wl.IDX_E4M3, H=16,
+             row_fmt=wl.ROW_E4M3_656, L=1, T=512, mode=hs.HS_MIXED, steps=8, append=1)
+    _run(c)
+
+
+def test_mtp_drawn_recency_zipf_ragged():
+    """MTP3 (4 queries), drawn recency/Zipf streams, ragged lengths, 2 layers."""
+    from harness import Case
+    hs = _hs()
+    c = Case("mtp-drawn", B=3, N=[3000, 2500, 3333], K=128, Hi=8, Di=64, H=32, L=2, T=256,
+             num_spec=3, mode=hs.HS_MIXED, steps=12, source="recency_zipf", check_attn_every=4)
+    stats = _run(c)
+    assert stats["misses"] > 0 and stats["hits"] > 0
+
+
+def test_mtp_indexer_with_scales_and_appends():
+    from harness import Case
+    hs = _hs()
+    c = Case("mtp-indexer", B=2, N=[900, 1234], K=128, Hi=16, Di=32, H=16, L=1, T=128,
+             num_spec=3, mode=hs.HS_MIXED, steps=5, append=4, sigma=True)
+    _run(c)
+
+
+def test_zero_residency_fills_on_demand():
+    from harness import Case
+    hs = _hs()
+    c = Case("zero", B=2, N=5000, K=256, Hi=8, Di=32, H=16, L=2, T=0, mode=hs.HS_ZERO,
+             steps=10, source="uniform_zipf", check_attn_every=3)
+    stats = _run(c)
+    assert stats["resident"] == 0 and stats["misses"] > 0
+
+
+def test_full_residency_real_head_counts():
+    """64x128 E4M3 indexer, 128 MLA heads, ragged lengths, full residency."""
+    from harness import Case
+    hs = _hs()
+    c = Case("full", B=3, N=[2000, 700, 4097], K=256, Hi=64, Di=128, H=128, L=2,
+             mode=hs.HS_FULL, steps=2)
+    stats = _run(c)
+    assert stats["misses"] == 0 and stats["hits"] == 0
+
+
+@pytest.mark.parametrize("num_spec", [0, 3])
+def test_fewer_visible_than_k_pads(num_spec):
+    from harness import Case
+    hs = _hs()
+    c = Case("short", B=2, N=[100, 37], K=256, Hi=8, Di=32, H=16, L=1, T=64,
+             num_spec=num_spec, mode=hs.HS_MIXED, steps=3, append=num_spec + 1)
+    _run(c)
+
+
+def test_hs_step_matches_separate_calls():
+    from harness import Case
+    hs = _hs()
+    c = Case("step", B=2, N=[3000, 2100], K=256, Hi=16, Di=64, H=32, L=3, T=256,
+             mode=hs.HS_MIXED, steps=4, append=1, use_step=True)
+    _run(c)
+
+
+def test_indexer_scores_bit_exact():
+    """hs_indexer_score against the oracle's scores, every visible entry."""
+    from harness import Case, Runner
+    hs = _hs()
+    for case in (Case("s-fp8", B=2, N=[1500, 3001], K=64, Hi=64, Di=128, H=16, num_spec=3,
+                      sigma=True, mode=hs.HS_FULL),
+                 Case("s-f32", B=1, N=777, K=64, Hi=4, Di=32, idx_fmt=wl.IDX_F32, H=16,
+                      mode=hs.HS_FULL)):
+        r = Runner(case)
+        try:
+            q, w, _ = r.step_inputs(1)
+            stride = r.max_tokens
+            sc = torch.full((case.B, r.nq, stride), float("nan"), device=r.dev)
+            r.pool.indexer_score(q, w, case.B, r.nq, sc, stride)
+            torch.cuda.synchronize()
+            for b in range(case.B):
+                N = r.N[b]
+                ref = oracle.indexer_scores(case.idx_fmt, q[b].cpu().numpy(), w[b].cpu().numpy(),
+                                            r.keys[b].cpu().numpy(), r.sig[b].cpu().numpy(), N)
+                got = sc[b, :, :N].cpu().numpy()
+                for j in range(r.nq):
+                    vis = oracle.visible(N, r.nq, j)
+                    np.testing.assert_array_equal(got[j, :vis], ref[j, :vis])
+        finally:
+            r.close()
+
+
+def test_topk_ties_and_special_scores():
+    """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows."""
+    from harness import Case, Runner
+    hs = _hs()
+    case = Case("topk", B=4, N=[20000, 9000, 300, 16385], K=512, Hi=8, Di=32, H=16,
+                num_spec=1, mode=hs.HS_FULL)
+    r = Runner(case)
+    try:
+        stride = r.max_tokens
+        g = torch.Generator().manual_seed(3)
+        sc = torch.randint(0, 40, (case.B, 2, stride), generator=g).float()
+        sc[1] = 0.0                                  # every score equal
+        sc[2, 0, :150] = -torch.arange(150).float()  # negatives and -0 area
+        sc[3, 1] = torch.randn(stride, generator=g)
+        sc = sc.to(r.dev)
+        out = torch.full((case.B, 2, case.K), -9, dtype=torch.int32, device=r.dev)
+        r.pool.topk(sc, stride, case.B, 2, out)
+        torch.cuda.synchronize()
+        s_np = sc.cpu().numpy()
+        for b in range(case.B):
+            for j in range(2):
+                vis = oracle.visible(r.N[b], 2, j)
+                ref = oracle.topk(s_np[b, j], vis, case.K)
+                np.testing.assert_array_equal(out[b, j].cpu().numpy(), ref)
+    finally:
+        r.close()
+
+
+def test_residency_independence_bit_identical():
+    """Full, mixed and zero residency give bit-identical outputs for the same
+    inputs (the row a query reads is the same bytes wherever it lives)."""
+    from harness import Case, Runner
+    hs = _hs()
+    outs = []
+    for mode in (hs.HS_FULL, hs.HS_MIXED, hs.HS_ZERO):
+        c = Case("res", B=2, N=[2500, 3100], K=256, Hi=8, Di=32, H=32, L=2, T=256, mode=mode,
+                 steps=3)
+        r = Runner(c)
+        try:
+            for s in range(1, 4):
+                q, w, qm = r.step_inputs(s)
+                topk = torch.empty((2, 1, 256), dtype=torch.int32, device=r.dev)
+                rid = torch.empty_like(topk)
+                out = torch.empty((2, 2, 1, 32, 512), dtype=torch.bfloat16, device=r.dev)
+                r.pool.step(2, 1, q, w, qm, r.tau, out, topk, rid)
+            torch.cuda.synchronize()
+            outs.append(out.cpu())
+        finally:
+            r.close()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_graph_capture_replay_equals_eager():
+    from harness import Case, Runner
+    hs = _hs()
+    c = Case("graph", B=2, N=[3000, 2000], K=256, Hi=8, Di=32, H=32, L=2, T=256,
+             mode=hs.HS_MIXED, steps=6)
+    eager, graph = Runner(c), Runner(c)
+    try:
+        q, w, qm = eager.step_inputs(1)
+        shp = (2, 1, 256)
+        bufs = {}
+        for name, r in (("eager", eager), ("graph", graph)):
+            bufs[name] = dict(q=q.clone(), w=w.clone(), qm=qm.clone(),
+                              out=torch.zeros((2, 2, 1, 32, 512), dtype=torch.bfloat16, device=r.dev),
+                              topk=torch.zeros(shp, dtype=torch.int32, device=r.dev),
+                              rid=torch.zeros(shp, dtype=torch.int32, device=r.dev))
+        gbuf = bufs["graph"]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                graph.pool.step(2, 1, gbuf["q"], gbuf["w"], gbuf["qm"], graph.tau, gbuf["out"],
+                                gbuf["topk"], gbuf["rid"], stream=s)
+        torch.cuda.synchronize()
+        for step in range(1, 6):
+            qs, ws, qms = eager.step_inputs(step)
+            e = bufs["eager"]
+            e["q"].copy_(qs), e["w"].copy_(ws), e["qm"].copy_(qms)
+            gbuf["q"].copy_(qs), gbuf["w"].copy_(ws), gbuf["qm"].copy_(qms)
+            eager.pool.step(2, 1, e["q"], e["w"], e["qm"], eager.tau, e["out"], e["topk"], e["rid"])
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(e["topk"], gbuf["topk"])
+            assert torch.equal(e["rid"], gbuf["rid"])
+            assert torch.equal(e["out"], gbuf["out"])
+            for b in range(2):
+                se, sg = eager.pool.dump_state(b), graph.pool.dump_state(b)
+                for k in ("hot_map", "slot_token", "stamp", "step"):
+                    np.testing.assert_array_equal(se[k], sg[k])
+        assert graph.pool.get_error() == hs.HS_OK
+        st = graph.pool.stats()
+        assert st["misses"] > 0
+    finally:
+        eager.close()
+        graph.close()
+
+
+def test_out_of_range_index_sets_error_and_recovers():
+    from harness import Case, Runner
+    hs = _hs()
+    c = Case("err", B=1, N=1000, K=64, Hi=8, Di=32, H=16, T=128, mode=hs.HS_MIXED)
+    r = Runner(c)
+    try:
+        topk = torch.arange(64, dtype=torch.int32, device=r.dev).view(1, 1, 64) * 10
+        topk[0, 0, -1] = 5000  # outside the request
+        rid = torch.zeros_like(topk)
+        r.pool.resolve(topk, 1, 1, rid)
+        assert r.pool.get_error() == hs.HS_ERR_INDEX_RANGE
+        assert (rid == -1).all()
+        assert r.pool.get_error() == hs.HS_OK  # read-and-clear
+        # not ascending
+        bad = torch.arange(64, dtype=torch.int32, device=r.dev).flip(0).view(1, 1, 64).contiguous()
+        r.pool.resolve(bad, 1, 1, rid)
+        assert r.pool.get_error() == hs.HS_ERR_INDEX_RANGE
+        # the pool still works afterwards
+        r.run_step()
+    finally:
+        r.close()
+
+
+def test_host_side_capacity_errors():
+    hs = _hs()
+    cfg = hs.make_config(max_requests=2, max_tokens=1024, top_k=64, num_spec=0, tail_tokens=64,
+                         num_mla_layers=1, mla_heads=16, idx_heads=4, idx_dim=32,
+                         gpu_blocks=6, host_blocks=3)
+    pool = hs.Pool(cfg)
+    try:
+        rows = wl.mla_rows(0, 0, 0, 400, 1, wl.ROW_E4M3_656, device="cuda")
+        keys = wl.idx_keys(0, 0, 0, 400, 32, wl.IDX_E4M3, device="cuda")
+        pool.open(0, hs.HS_FULL)
+        with pytest.raises(hs.HSError) as ei:
+            pool.append(0, rows, keys)  # 7 pages > 6 GPU blocks
+        assert ei.value.status == hs.HS_ERR_CAPACITY
+        pool.open(1, hs.HS_MIXED)       # leases 2 hot blocks
+        with pytest.raises(hs.HSError) as ei:
+            pool.append(1, rows, keys)  # 7 host pages > 3 host blocks
+        assert ei.value.status == hs.HS_ERR_HOST_POOL_FULL
+        with pytest.raises(hs.HSError) as ei:
+            pool.open(1, hs.HS_MIXED)   # already open
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HSError) as ei:
+            pool.set_mode(0, hs.HS_ZERO)
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HSError) as ei:
+            pool.resolve(torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"), 3, 1,
+                         torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"))
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG  # B beyond max_requests
+        pool.close_request(1)
+        pool.close_request(0)
+        assert pool.free_gpu_blocks() == 6
+    finally:
+        pool.close()
+
+
+def test_full_to_mixed_flip_keeps_outputs():
+    """A request that flips from full to mixed residency between steps keeps
+    producing the oracle's results; its freed blocks return to the pool."""
+    from harness import Case, Runner
+    hs = _hs()
+    c = Case("flip", B=2, N=[2600, 1900], K=128, Hi=8, Di=32, H=16, L=2, T=256, mode=hs.HS_FULL,
+             steps=6, append=1)
+    r = Runner(c)
+    try:
+        r.run_step()
+        r.run_step()
+        free0 = r.pool.free_gpu_blocks()
+        r.flip_to_mixed(0)
+        assert r.pool.free_gpu_blocks() > free0
+        for _ in range(4):
+            r.run_step()
+    finally:
+        r.close()
