@@ -1,6 +1,7 @@
 // Private declarations shared by the translation units of libhs.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,6 +72,8 @@ struct hs_pool {
     uint8_t *host_base;      // host pointer of the pinned host pool
     uint8_t *host_dev;       // the same memory as seen from the device
     hs::DevPtrs d;
+    CUtensorMap key_map;     // TMA map of the indexer key slab (E4M3, dim 128)
+    bool has_key_map;
     // host mirrors
     std::vector<int32_t> seq_len;
     std::vector<int32_t> mode;  // -1 = closed

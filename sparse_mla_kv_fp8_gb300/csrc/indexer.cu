@@ -3,13 +3,26 @@
 //
 //   s[b][j][t] = sum_h w[b][j][h] * ReLU(sigma[b][t] * (q[b][j][h][:] . k[b][t][:]))
 //
-// General kernel: one CTA per 128-token tile of one request; the tile's keys
-// and the request's queries are decoded to fp32 in shared memory; each thread
-// owns one token and loops over (query, head).  Sums are fp32; with the
-// synthetic inputs they are exact, so the result does not depend on order.
+// Tensor-core kernel (E4M3 keys, head dim 128, nq*Hi <= 256): the dense
+// contraction D[token][(j,h)] = k[token] . q[j][h] runs on tcgen05 with FP8
+// operands (kind::f8f6f4, fp32 accumulate):
+//   A = 128 keys x 128 B (K-major, 128-byte swizzle), brought by TMA from the
+//       request's key slab, kStages-deep ring;
+//   B = the request's nq*Hi query rows (same layout), staged once per CTA;
+//   D = 128 TMEM lanes x nq*Hi columns, two accumulators (double buffer).
+// Warp 0 issues TMA, warp 1 issues MMAs, warps 2-5 (one thread per token =
+// one TMEM lane) read D, apply sigma, ReLU and the head weights and write the
+// scores (coalesced).  Every mbarrier wait is bounded.
+//
+// General kernel (any format / dims): one CTA per 128-token tile of one
+// request; keys and queries decoded to fp32 in shared memory; each thread
+// owns one token and loops over (query, head).
+//
+// All sums are fp32; with the synthetic inputs they are exact, so results
+// do not depend on the order of summation (tensor core or not).
 #include <cuda_fp8.h>
 
-#include "hs_internal.h"
+#include "tc.cuh"
 
 namespace hs {
 namespace {
@@ -72,6 +85,179 @@ __global__ void __launch_bounds__(kTile) indexer_simt_kernel(
     }
 }
 
+
+// ------------------------------------------------------------------------
+// tensor-core path
+// ------------------------------------------------------------------------
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;
+constexpr int kTileBytes = kTile * 128;  // 128 tokens x 128 B
+
+struct IdxTcArgs {
+    const uint8_t *q;  // [B][nq*Hi][128] E4M3
+    const float *w;    // [B][nq*Hi]
+    const float *ksc;  // [maxR][maxT]
+    const int32_t *seq_len;
+    float *scores;
+    int64_t stride;
+    int nq, Hi, maxT, tiles_per_cta, ncols, tmem_cols;
+    int32_t *err;
+};
+
+struct IdxTcSmem {
+    static constexpr int q_off = 0;                             // 32 KB, 1024-aligned
+    static constexpr int k_off = 256 * 128;                     // stages, 1024-aligned
+    static constexpr int w_off = k_off + kTcStages * kTileBytes;
+    static constexpr int bar_off = w_off + 256 * 4;
+    static constexpr int tslot_off = bar_off + (2 * kTcStages + 5) * 8;
+    static constexpr int bytes = tslot_off + 16 + 1024;         // + alignment slack
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IdxTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *qs = smem + IdxTcSmem::q_off;
+    uint8_t *ks = smem + IdxTcSmem::k_off;
+    float *wsm = (float *)(smem + IdxTcSmem::w_off);
+    uint64_t *full = (uint64_t *)(smem + IdxTcSmem::bar_off);
+    uint64_t *empty = full + kTcStages;
+    uint64_t *tfull = empty + kTcStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint32_t *tslot = (uint32_t *)(smem + IdxTcSmem::tslot_off);
+
+    const int b = blockIdx.y;
+    const int N = a.seq_len[b];
+    const int ntiles = (N + kTile - 1) / kTile;
+    const int tile0 = blockIdx.x * a.tiles_per_cta;
+    const int tile1 = min(ntiles, tile0 + a.tiles_per_cta);
+    if (tile0 >= tile1) return;  // uniform over the CTA
+    const int nt = tile1 - tile0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // queries -> 128-byte-swizzled K-major rows; head weights -> smem
+    const uint8_t *qb = a.q + (size_t)b * a.ncols * 128;
+    for (int i = threadIdx.x; i < a.ncols * 8; i += kTcThreads) {
+        const int r = i >> 3, c = i & 7;
+        *(uint4 *)(qs + tc::sw128_offset(r, c)) = *(const uint4 *)(qb + r * 128 + c * 16);
+    }
+    for (int i = threadIdx.x; i < a.ncols; i += kTcThreads) wsm[i] = a.w[(size_t)b * a.ncols + i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; s++) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int k = 0; k < 2; k++) {
+            tc::mbar_init(&tfull[k], 1);
+            tc::mbar_init(&tempty[k], 128);
+        }
+        tc::mbar_init(done, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tslot, a.tmem_cols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::prefetch_tensormap(&kmap);
+            int issued = 0;
+            for (int it = 0; it < nt; it++) {
+                const int s = it % kTcStages;
+                const uint32_t ph = (it / kTcStages) & 1;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1, a.err)) break;
+                tc::mbar_expect_tx(&full[s], kTileBytes);
+                tc::tma_load_2d(ks + s * kTileBytes, &kmap, &full[s], 0,
+                                b * a.maxT + (tile0 + it) * kTile);
+                issued++;
+            }
+            // never leave with a copy in flight
+            for (int it = max(0, issued - kTcStages); it < issued; it++)
+                tc::mbar_wait(&full[it % kTcStages], (it / kTcStages) & 1, a.err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::instr_desc(128, a.ncols, 0, 0, 0, 0);
+            const uint32_t qaddr = tc::smem_addr(qs);
+            for (int it = 0; it < nt; it++) {
+                const int s = it % kTcStages;
+                const uint32_t ph = (it / kTcStages) & 1;
+                const int acc = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!tc::mbar_wait(&tempty[acc], aph ^ 1, a.err)) break;
+                if (!tc::mbar_wait(&full[s], ph, a.err)) break;
+                tc::fence_after_sync();
+                const uint32_t kaddr = tc::smem_addr(ks + s * kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++) {
+                    const uint64_t ad = tc::smem_desc_sw128(kaddr + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(qaddr + kk * 32, 16, 1024);
+                    tc::mma_f8f6f4(tmem + acc * a.ncols, ad, bd, idesc, kk > 0);
+                }
+                tc::mma_commit(&empty[s]);
+                tc::mma_commit(&tfull[acc]);
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, a.err);
+        }
+    } else {
+        const int sp = warp & 3;  // TMEM sub-partition this warp may read
+        const int row = sp * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+        for (int it = 0; it < nt; it++) {
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!tc::mbar_wait(&tfull[acc], aph, a.err)) break;
+            tc::fence_after_sync();
+            const int t = (tile0 + it) * kTile + row;
+            const float sig = t < N ? a.ksc[(size_t)b * a.maxT + t] : 0.f;
+            const uint32_t tb = lane_base + acc * a.ncols;
+            for (int j = 0; j < a.nq; j++) {
+                float accs = 0.f;
+                for (int h0 = 0; h0 < a.Hi; h0 += 16) {
+                    float v[16];
+                    tc::tmem_ld16(tb + j * a.Hi + h0, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const float x = sig * v[i];
+                        accs = fmaf(wsm[j * a.Hi + h0 + i], x > 0.f ? x : 0.f, accs);
+                    }
+                }
+                if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = accs;
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(&tempty[acc]);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+bool tc_eligible(const hs_pool *p, int nq) {
+    const int ncols = nq * p->cfg.idx_heads;
+    return p->cfg.idx_fmt == HS_IDX_E4M3 && p->cfg.idx_dim == 128 && ncols % 16 == 0 &&
+           ncols >= 16 && ncols <= 256 && p->has_key_map;
+}
+
+int tmem_cols_for(int ncols) {
+    int c = 32;
+    while (c < 2 * ncols) c <<= 1;
+    return c;
+}
+
 size_t simt_smem(const hs_pool *p, int nq) {
     const int Hi = p->cfg.idx_heads, Di = p->cfg.idx_dim;
     return ((size_t)nq * Hi * Di + nq * Hi + (size_t)kTile * (Di + 1)) * 4;
@@ -85,15 +271,65 @@ cudaError_t indexer_setup(const hs_pool *p) {
     cudaError_t e = cudaFuncSetAttribute(indexer_simt_kernel<0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             120 * 1024);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(indexer_simt_kernel<1>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
 }
 
 int indexer_kernel_count(const hs_pool *, int, int) { return 1; }
 
+// Tiles per CTA for a grid of (chunks, B): the fewest waves, then the most
+// CTAs, given how many CTAs fit on one SM.
+static int pick_tiles_per_cta(int ntiles, int B, int per_sm) {
+    const long slots = (long)kNumSMs * per_sm;
+    int best = ntiles;
+    double best_t = 1e30;
+    for (int tpc = 1; tpc <= ntiles; tpc++) {
+        const long chunks = (ntiles + tpc - 1) / tpc;
+        const long ctas = chunks * B;
+        const long waves = (ctas + slots - 1) / slots;
+        const double t = (double)waves * tpc + 0.02 * tpc;  // small bias to larger tiles
+        if (t < best_t) {
+            best_t = t;
+            best = tpc;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w, int B, int nq,
                                  float *scores, int64_t stride, cudaStream_t st) {
     const int maxT = p->cfg.max_tokens;
+    if (tc_eligible(p, nq)) {
+        IdxTcArgs a;
+        a.q = (const uint8_t *)q;
+        a.w = w;
+        a.ksc = p->d.idx_scale;
+        a.seq_len = p->d.seq_len;
+        a.scores = scores;
+        a.stride = stride;
+        a.nq = nq;
+        a.Hi = p->cfg.idx_heads;
+        a.maxT = maxT;
+        a.ncols = nq * p->cfg.idx_heads;
+        a.tmem_cols = tmem_cols_for(a.ncols);
+        a.err = p->d.err;
+        const int per_sm_tmem = 512 / a.tmem_cols;
+        const int per_sm_smem = (228 * 1024) / (IdxTcSmem::bytes + 1024);
+        const int per_sm = per_sm_tmem < per_sm_smem ? per_sm_tmem : per_sm_smem;
+        // never co-schedule more CTAs than TMEM holds: pad the smem request
+        int smem = IdxTcSmem::bytes;
+        const int cap = (228 * 1024) / per_sm - 1024;
+        if (per_sm == 1 && smem < 116 * 1024) smem = 116 * 1024;
+        else if (smem < cap && per_sm_tmem < per_sm_smem) smem = cap;
+        const int ntiles = (maxT + kTile - 1) / kTile;
+        a.tiles_per_cta = pick_tiles_per_cta(ntiles, B, per_sm);
+        dim3 grid((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta, B);
+        indexer_tc_kernel<<<grid, kTcThreads, smem, st>>>(p->key_map, a);
+        return cudaGetLastError();
+    }
     dim3 grid((maxT + kTile - 1) / kTile, B);
     const size_t sm = simt_smem(p, nq);
     if (p->cfg.idx_fmt == HS_IDX_E4M3)

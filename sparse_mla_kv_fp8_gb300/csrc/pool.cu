@@ -2,6 +2,7 @@
 // orchestration of one decode step.  Nothing here runs on the decode path
 // except hs_step's enqueue sequence, which makes no host decision that
 // depends on device data.
+#include <cudaTypedefs.h>
 #include <string.h>
 
 #include <algorithm>
@@ -10,6 +11,37 @@
 #include "hs_internal.h"
 
 namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D view of the key slab: rows = max_requests * max_tokens, 128 bytes
+// each; one TMA box = 128 rows x 128 bytes with the 128-byte swizzle the
+// tensor core reads.
+bool make_key_map(hs_pool *p) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {128, (cuuint64_t)p->cfg.max_requests * (cuuint64_t)p->cfg.max_tokens};
+    cuuint64_t gstride[1] = {128};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(&p->key_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p->d.idx_keys, gdim, gstride,
+                     box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 constexpr size_t kAlign = 256;
 
@@ -243,6 +275,14 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->d.miss_slot = (int32_t *)(b + extra[8]);
     p->d.attn_part = (float *)(b + extra[9]);
 
+    p->has_key_map = false;
+    if (cfg->idx_fmt == HS_IDX_E4M3 && cfg->idx_dim == 128) {
+        if (!make_key_map(p)) {
+            delete p;
+            return HS_ERR_CUDA;
+        }
+        p->has_key_map = true;
+    }
     const size_t maxR = cfg->max_requests;
     p->seq_len.assign(maxR, 0);
     p->mode.assign(maxR, -1);

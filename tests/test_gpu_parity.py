@@ -314,3 +314,31 @@ def test_full_to_mixed_flip_keeps_outputs():
             r.run_step()
     finally:
         r.close()
+
+
+def test_indexer_tensor_core_pipeline_wraps():
+    """Enough tiles per CTA that the TMA ring and the two TMEM accumulators
+    wrap several times (MTP3: 256 MMA columns, one CTA per SM)."""
+    from harness import Case, Runner
+    hs = _hs()
+    case = Case("s-wrap", B=2, N=[40000, 33333], K=64, Hi=64, Di=128, H=16, num_spec=3,
+                sigma=True, mode=hs.HS_FULL)
+    r = Runner(case)
+    try:
+        for s in (1, 2):
+            q, w, _ = r.step_inputs(s)
+            stride = r.max_tokens
+            sc = torch.full((case.B, r.nq, stride), float("nan"), device=r.dev)
+            r.pool.indexer_score(q, w, case.B, r.nq, sc, stride)
+            torch.cuda.synchronize()
+            assert r.pool.get_error() == hs.HS_OK
+            for b in range(case.B):
+                N = r.N[b]
+                ref = oracle.indexer_scores(case.idx_fmt, q[b].cpu().numpy(), w[b].cpu().numpy(),
+                                            r.keys[b].cpu().numpy(), r.sig[b].cpu().numpy(), N)
+                got = sc[b, :, :N].cpu().numpy()
+                for j in range(r.nq):
+                    vis = oracle.visible(N, r.nq, j)
+                    np.testing.assert_array_equal(got[j, :vis], ref[j, :vis])
+    finally:
+        r.close()
