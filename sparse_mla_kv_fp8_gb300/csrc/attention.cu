@@ -4,6 +4,23 @@
 // first 512 dims the value:
 //   z = scale * q . row,  out = sum softmax(z) * row[:512],  lse = ln sum exp(z)
 //
+// Tensor-core kernel (E4M3 rows, head count a multiple of 64): one CTA owns
+// one query, 64 heads and a range of the K entries, and computes in the
+// transposed form so that both products are M=128 tcgen05 MMAs with bf16
+// operands and fp32 accumulators in TMEM:
+//   S^T[row][head] = R[row][:576] . Q[head][:576]   M=128 rows,  N=64, K=576
+//   O^T[dim][head] += R[row][dim] * P[row][head]    M=128 dims x4, N=64, K=128 rows
+// TMEM: two S^T buffers (2 x 64 columns) + O^T (4 x 64 columns).  The rows of
+// a 128-row chunk are dequantised (E4M3 x group scale -> bf16) by 8 loader
+// warps straight into nine 16 KB K-blocks with the 128-byte swizzle; the
+// same K-blocks are the K-major A operand of S^T and the MN-major A operand
+// of O^T, so each row is converted once.  Softmax warps (thread = row = TMEM
+// lane) keep a per-head reference max in the log2 domain and rescale O^T
+// only when a chunk raises a head's maximum by more than 2^8; P^T (bf16) is
+// written over the rope K-block once S^T no longer needs it.  Per-K-block
+// mbarriers let the conversion of chunk c+1 overlap the O^T MMAs of chunk c.
+// Every wait is bounded.
+//
 // General kernel (any head count that is a multiple of 8, both row formats):
 // a CTA owns (query, 8 heads, a range of the K entries); each chunk of 32
 // rows is dequantised to fp32 in shared memory; warp w is head w, lane l is
@@ -14,7 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include "hs_internal.h"
+#include "tc.cuh"
 
 namespace hs {
 namespace {
@@ -156,61 +173,530 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restri
     if (lse && threadIdx.x == 0) lse[rh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
 }
 
+
+// ------------------------------------------------------------------------
+// tensor-core path
+// ------------------------------------------------------------------------
+constexpr int kTcRows = 128;         // rows per chunk (MMA M of S^T, K of O^T)
+constexpr int kTcHeads = 64;         // heads per CTA (MMA N)
+constexpr int kKBlocks = 9;          // 576 dims / 64
+constexpr int kRBlock = kTcRows * 128;     // 16 KB: 128 rows x 64 bf16
+constexpr int kQBlock = kTcHeads * 128;    // 8 KB: 64 heads x 64 bf16
+constexpr int kLoaderWarps = 8;
+constexpr int kAttnThreads = (6 + kLoaderWarps) * 32;
+constexpr float kRescaleLog2 = 8.f;  // rescale O^T when a max grows by > 2^8
+
+struct AttnTcSmem {
+    static constexpr int r_off = 0;                              // 9 x 16 KB
+    static constexpr int q_off = r_off + kKBlocks * kRBlock;     // 9 x 8 KB
+    static constexpr int f_off = q_off + kKBlocks * kQBlock;     // floats
+    static constexpr int nf = 64 * 3 + 4 * 64;                   // mref, lsum, alpha, red[4][64]
+    static constexpr int bar_off = f_off + nf * 4;
+    static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 3;
+    static constexpr int tslot_off = bar_off + nbar * 8;
+    static constexpr int bytes = tslot_off + 16 + 1024;          // + alignment slack
+};
+static_assert(AttnTcSmem::bytes <= 232448, "attention smem");
+
+struct AttnTcArgs {
+    const __nv_bfloat16 *q;  // [rows][H][576]
+    const int32_t *row_id;   // [rows][K]
+    const uint8_t *pool;
+    int layer, L, P, H, K, splits, kc, max_row;
+    float scale_log2;
+    __nv_bfloat16 *out;      // [rows][H][512]
+    float *lse;
+    float *part;             // [rows][H][splits][514]
+    int32_t *err;
+};
+
+__device__ __forceinline__ bool bar_or_softmax(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *(uint32_t *)&v;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *rb = smem + AttnTcSmem::r_off;
+    uint8_t *qb = smem + AttnTcSmem::q_off;
+    float *mref = (float *)(smem + AttnTcSmem::f_off);
+    float *lsum = mref + 64;
+    float *alpha = lsum + 64;
+    float *red = alpha + 64;  // [4][64]
+    uint64_t *kb_full = (uint64_t *)(smem + AttnTcSmem::bar_off);
+    uint64_t *kb_empty = kb_full + kKBlocks;
+    uint64_t *s_full = kb_empty + kKBlocks;
+    uint64_t *s_empty = s_full + 2;
+    uint64_t *p_full = s_empty + 2;
+    uint64_t *o_done = p_full + 1;
+    uint64_t *mma_done = o_done + 1;
+    uint32_t *tslot = (uint32_t *)(smem + AttnTcSmem::tslot_off);
+
+    const int qr = blockIdx.x, hh = blockIdx.y, split = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k0 = split * a.kc, k1 = min(a.K, k0 + a.kc);
+    const int nchunks = (k1 - k0 + kTcRows - 1) / kTcRows;
+    const int32_t *ids = a.row_id + (size_t)qr * a.K;
+
+    // queries of this CTA's 64 heads -> nine K-major 128-byte-swizzled blocks
+    const __nv_bfloat16 *qsrc = a.q + ((size_t)qr * a.H + hh * kTcHeads) * kLatent;
+    for (int i = threadIdx.x; i < kTcHeads * 72; i += kAttnThreads) {
+        const int h = i / 72, c16 = i - h * 72;  // 72 chunks of 16 B per head
+        const int kb = c16 >> 3, c = c16 & 7;
+        const uint4 v = *(const uint4 *)((const uint8_t *)(qsrc + (size_t)h * kLatent) + c16 * 16);
+        *(uint4 *)(qb + kb * kQBlock + tc::sw128_offset(h, c)) = v;
+    }
+    if (threadIdx.x < 64) {
+        mref[threadIdx.x] = -INFINITY;
+        lsum[threadIdx.x] = 0.f;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kKBlocks; i++) {
+            tc::mbar_init(&kb_full[i], kLoaderWarps);
+            tc::mbar_init(&kb_empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            tc::mbar_init(&s_full[i], 1);
+            tc::mbar_init(&s_empty[i], 128);
+        }
+        tc::mbar_init(p_full, 128);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(mma_done, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
+    const uint32_t o_col = 128;   // O^T tiles: columns [128 + 64 g, ...)
+
+    if (warp == 0) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::instr_desc(128, kTcHeads, 1, 1, 0, 0);
+            const uint32_t idesc_o = tc::instr_desc(128, kTcHeads, 1, 1, 1, 1);
+            const uint32_t r_addr = tc::smem_addr(rb), q_addr = tc::smem_addr(qb);
+            const uint32_t p_addr = r_addr + 8 * kRBlock;
+            bool ok = true;
+            for (int c = 0; c < nchunks && ok; c++) {
+                const int buf = c & 1;
+                const uint32_t ph = c & 1;
+                if (!(ok = tc::mbar_wait(&s_empty[buf], ((c >> 1) & 1) ^ 1, a.err))) break;
+                for (int kb = 0; kb < kKBlocks && ok; kb++) {
+                    if (!(ok = tc::mbar_wait(&kb_full[kb], ph, a.err))) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++) {
+                        const uint64_t ad = tc::smem_desc_sw128(r_addr + kb * kRBlock + kk * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(q_addr + kb * kQBlock + kk * 32, 16, 1024);
+                        tc::mma_f16(tmem + s_col + buf * kTcHeads, ad, bd, idesc_s, (kb | kk) != 0);
+                    }
+                }
+                if (!ok) break;
+                tc::mma_commit(&s_full[buf]);
+                // O^T += V^T P^T once the softmax warps wrote P^T(c)
+                if (!(ok = tc::mbar_wait(p_full, ph, a.err))) break;
+                tc::fence_after_sync();
+                for (int g = 0; g < 4; g++) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {
+                        const uint64_t ad = tc::smem_desc_sw128(r_addr + 2 * g * kRBlock + kk * 2048, kRBlock, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(p_addr + kk * 2048, kRBlock, 1024);
+                        tc::mma_f16(tmem + o_col + g * kTcHeads, ad, bd, idesc_o, (c | kk) != 0);
+                    }
+                    tc::mma_commit(&kb_empty[2 * g]);
+                    tc::mma_commit(&kb_empty[2 * g + 1]);
+                }
+                tc::mma_commit(&kb_empty[8]);
+                tc::mma_commit(o_done);
+            }
+            // every MMA issued by this thread has completed before TMEM is freed
+            tc::mma_commit(mma_done);
+            tc::mbar_wait(mma_done, 0, a.err);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------ row loaders
+        const int tl = threadIdx.x - 6 * 32;  // 0..255
+        for (int c = 0; c < nchunks; c++) {
+            // this thread converts rows r = tl/8 + 32u (u = 0..3), 16-byte chunk tl%8
+            const uint8_t *src[4];
+            float4 sc[4];
+            const int c8 = tl & 7;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int r = (tl >> 3) + 32 * u;
+                const int k = k0 + c * kTcRows + r;
+                int32_t id = k < k1 ? ids[k] : -1;
+                if (id >= a.max_row) {
+                    if (c8 == 0) set_error(a.err, HS_ERR_INDEX_RANGE);
+                    id = -1;
+                }
+                src[u] = nullptr;
+                sc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (id >= 0) {
+                    const size_t blk = (size_t)(id / a.P), off = (size_t)(id % a.P);
+                    src[u] = a.pool + ((blk * a.L + a.layer) * a.P + off) * 656;
+                    sc[u] = *(const float4 *)(src[u] + 512);
+                }
+            }
+            bool ok = true;
+            for (int kb = 0; kb < kKBlocks; kb++) {
+                uint2 raw[4];
+                uint4 rope[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    raw[u] = make_uint2(0, 0);
+                    rope[u] = make_uint4(0, 0, 0, 0);
+                    if (src[u]) {
+                        if (kb < 8)
+                            raw[u] = __ldg((const uint2 *)(src[u] + kb * 64 + c8 * 8));
+                        else
+                            rope[u] = __ldg((const uint4 *)(src[u] + 528 + c8 * 16));
+                    }
+                }
+                const bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
+                if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst = rb + kb * kRBlock;
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const int r = (tl >> 3) + 32 * u;
+                    uint4 v;
+                    if (kb < 8) {
+                        const float s = kb < 2 ? sc[u].x : kb < 4 ? sc[u].y : kb < 6 ? sc[u].z : sc[u].w;
+                        const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&raw[u];
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pp[e], __NV_E4M3);
+                            const float2 f2 = __half22float2(__half2(h2));
+                            f[2 * e] = f2.x * s;
+                            f[2 * e + 1] = f2.y * s;
+                        }
+                        v.x = pack_bf16(f[0], f[1]);
+                        v.y = pack_bf16(f[2], f[3]);
+                        v.z = pack_bf16(f[4], f[5]);
+                        v.w = pack_bf16(f[6], f[7]);
+                    } else {
+                        v = rope[u];
+                    }
+                    *(uint4 *)(dst + tc::sw128_offset(r, c8)) = v;
+                }
+                tc::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&kb_full[kb]);
+            }
+            if (!ok) break;
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------- softmax + epilogue
+        const int sp = warp & 3;
+        const int r = sp * 32 + lane;  // row of the chunk == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+        float lp[64];
+#pragma unroll
+        for (int h = 0; h < 64; h++) lp[h] = 0.f;
+        bool ok = true;
+        for (int c = 0; c < nchunks; c++) {
+            const int buf = c & 1;
+            const int k = k0 + c * kTcRows + r;
+            const int32_t id = k < k1 ? ids[k] : -1;
+            const bool valid = id >= 0 && id < a.max_row;
+            const bool w = tc::mbar_wait(&s_full[buf], (c >> 1) & 1, a.err);
+            if (bar_or_softmax(!w)) {  // all 128 threads leave together
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t sbase = lane_base + s_col + buf * kTcHeads;
+            // pass 1: does any head's maximum grow by more than 2^8?
+            bool need = false;
+#pragma unroll
+            for (int h0 = 0; h0 < 64; h0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(sbase + h0, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float z = valid ? sv[i] * a.scale_log2 : -INFINITY;
+                    need |= z > mref[h0 + i] + kRescaleLog2;
+                }
+            }
+            if (bar_or_softmax(need)) {
+                // chunk maximum of every head across the 128 rows
+#pragma unroll
+                for (int h0 = 0; h0 < 64; h0 += 16) {
+                    float sv[16];
+                    tc::tmem_ld16(sbase + h0, sv);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        float m = valid ? sv[i] * a.scale_log2 : -INFINITY;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (lane == 0) red[sp * 64 + h0 + i] = m;
+                    }
+                }
+                bar_softmax();
+                if (r < 64) {
+                    const float cm = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
+                    const float mo = mref[r];
+                    const float mn = fmaxf(mo, cm);
+                    alpha[r] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+                    mref[r] = mn;
+                }
+                bar_softmax();
+#pragma unroll
+                for (int h = 0; h < 64; h++) lp[h] *= alpha[h];
+                if (c > 0) {
+                    // O^T holds chunks < c: wait for them, then scale column h by alpha[h]
+                    const bool wo = tc::mbar_wait(o_done, (c - 1) & 1, a.err);
+                    if (bar_or_softmax(!wo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    for (int g = 0; g < 4; g++) {
+#pragma unroll
+                        for (int h0 = 0; h0 < 64; h0 += 16) {
+                            float ov[16];
+                            const uint32_t ta = lane_base + o_col + g * kTcHeads + h0;
+                            tc::tmem_ld16(ta, ov);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; i++) ov[i] *= alpha[h0 + i];
+                            tc::tmem_st16(ta, ov);
+                        }
+                    }
+                    tc::tmem_st_wait();
+                }
+            }
+            // pass 2: P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
+            uint8_t *prow = rb + 8 * kRBlock;
+#pragma unroll
+            for (int h0 = 0; h0 < 64; h0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(sbase + h0, sv);
+                tc::tmem_ld_wait();
+                float pv[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float m = mref[h0 + i];
+                    const float z = valid ? sv[i] * a.scale_log2 : -INFINITY;
+                    pv[i] = (m == -INFINITY) ? 0.f : exp2f(z - m);
+                    lp[h0 + i] += pv[i];
+                }
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    uint4 v;
+                    v.x = pack_bf16(pv[8 * half + 0], pv[8 * half + 1]);
+                    v.y = pack_bf16(pv[8 * half + 2], pv[8 * half + 3]);
+                    v.z = pack_bf16(pv[8 * half + 4], pv[8 * half + 5]);
+                    v.w = pack_bf16(pv[8 * half + 6], pv[8 * half + 7]);
+                    *(uint4 *)(prow + tc::sw128_offset(r, (h0 >> 3) + half)) = v;
+                }
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(&s_empty[buf]);
+            tc::fence_async_smem();
+            tc::mbar_arrive(p_full);
+        }
+        // ---- epilogue: l per head, then O^T / l -> out (or partials)
+#pragma unroll
+        for (int h = 0; h < 64; h++) {
+            float v = lp[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[sp * 64 + h] = v;
+        }
+        bar_softmax();
+        if (r < 64) lsum[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
+        bar_softmax();
+        const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
+        if (!bar_or_softmax(!fin)) {
+            tc::fence_after_sync();
+            for (int g = 0; g < 4; g++) {
+                const int d = g * 128 + r;
+#pragma unroll
+                for (int h0 = 0; h0 < 64; h0 += 16) {
+                    float ov[16];
+                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const int h = hh * kTcHeads + h0 + i;
+                        if (a.splits == 1) {
+                            const float l = lsum[h0 + i];
+                            a.out[((size_t)qr * a.H + h) * kNope + d] =
+                                __float2bfloat16(l > 0.f ? ov[i] / l : 0.f);
+                        } else {
+                            a.part[(((size_t)qr * a.H + h) * a.splits + split) * (kNope + 2) + d] = ov[i];
+                        }
+                    }
+                }
+            }
+            if (r < 64) {
+                const int h = hh * kTcHeads + r;
+                const float l = lsum[r], m = mref[r];
+                if (a.splits == 1) {
+                    if (a.lse) a.lse[(size_t)qr * a.H + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                } else {
+                    float *pp = a.part + (((size_t)qr * a.H + h) * a.splits + split) * (kNope + 2);
+                    pp[kNope] = l > 0.f ? m : -INFINITY;
+                    pp[kNope + 1] = l;
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 size_t simt_smem() { return ((size_t)kHeadsPerCta * kLatent + (size_t)kChunk * kRowStride) * 4; }
 
 }  // namespace
 
-int attention_splits(const hs_pool *p, int B, int nq) {
-    const int rows = B * nq;
-    const int ctas = rows * (p->cfg.mla_heads / kHeadsPerCta);
+static int simt_splits(const hs_pool_config &c, int rows) {
+    const int ctas = rows * (c.mla_heads / kHeadsPerCta);
     int s = (2 * kNumSMs + ctas - 1) / ctas;
     s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
-    // at least one chunk of rows per split
-    const int maxs = (p->cfg.top_k + kChunk - 1) / kChunk;
-    return s > maxs ? maxs : s;
+    const int maxs = (c.top_k + kChunk - 1) / kChunk;  // at least one chunk per split
+    s = s > maxs ? maxs : s;
+    const int kc = ((c.top_k + s - 1) / s + kChunk - 1) / kChunk * kChunk;
+    return (c.top_k + kc - 1) / kc;
+}
+
+static bool tc_eligible(const hs_pool_config &c) {
+    return c.row_fmt == HS_ROW_E4M3_656 && c.mla_heads % kTcHeads == 0;
+}
+
+// One CTA per SM (shared memory): the fewest chunk-waves, then fewer splits.
+static int tc_splits(const hs_pool_config &c, int rows) {
+    const int chunks = (c.top_k + kTcRows - 1) / kTcRows;
+    const int base = rows * (c.mla_heads / kTcHeads);
+    int best = 1;
+    long best_cost = -1;
+    for (int s = 1; s <= chunks && s <= kMaxSplits; s++) {
+        const long cps = (chunks + s - 1) / s;
+        const long waves = ((long)base * s + kNumSMs - 1) / kNumSMs;
+        const long cost = waves * cps * 4 + (s > 1 ? 1 : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    const int kc = ((c.top_k + best - 1) / best + kTcRows - 1) / kTcRows * kTcRows;
+    return (c.top_k + kc - 1) / kc;
+}
+
+static int splits_for(const hs_pool_config &c, int rows) {
+    return tc_eligible(c) ? tc_splits(c, rows) : simt_splits(c, rows);
 }
 
 int attention_kernel_count(const hs_pool *p, int B, int nq) {
-    const int K = p->cfg.top_k;
-    int s = attention_splits(p, B, nq);
-    const int kc = ((K + s - 1) / s + kChunk - 1) / kChunk * kChunk;
-    s = (K + kc - 1) / kc;
-    return s > 1 ? 2 : 1;
+    return splits_for(p->cfg, B * nq) > 1 ? 2 : 1;
+}
+
+size_t attention_partial_floats(const hs_pool_config *c) {
+    size_t worst = 0;
+    const int nq = c->num_spec + 1;
+    for (int rows = 1; rows <= c->max_requests * nq; rows++) {
+        const int s = splits_for(*c, rows);
+        if (s > 1) {
+            const size_t need = (size_t)rows * c->mla_heads * s * (kNope + 2);
+            worst = need > worst ? need : worst;
+        }
+    }
+    return worst;
 }
 
 cudaError_t attention_setup(const hs_pool *p) {
-    (void)p;
-    return cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)simt_smem());
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)simt_smem());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                AttnTcSmem::bytes);
 }
 
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
                              int B, int nq, float scale, void *out, float *lse, cudaStream_t st) {
-    AttnArgs a;
-    a.q = (const __nv_bfloat16 *)q;
-    a.row_id = row_id;
-    a.pool = p->d.rows;
-    a.layer = layer;
-    a.L = p->cfg.num_mla_layers;
-    a.P = p->cfg.page_tokens;
-    a.R = p->R;
-    a.fmt = p->cfg.row_fmt;
-    a.H = p->cfg.mla_heads;
-    a.K = p->cfg.top_k;
-    a.splits = attention_splits(p, B, nq);
-    a.kc = ((a.K + a.splits - 1) / a.splits + kChunk - 1) / kChunk * kChunk;
-    a.splits = (a.K + a.kc - 1) / a.kc;
-    a.scale_log2 = scale * kLog2e;
-    a.out = (__nv_bfloat16 *)out;
-    a.lse = lse;
-    a.part = p->d.attn_part;
-    a.max_row = (int)(p->cfg.gpu_blocks * p->cfg.page_tokens);
-    a.err = p->d.err;
     const int rows = B * nq;
-    dim3 grid(rows, a.H / kHeadsPerCta, a.splits);
-    attn_simt_kernel<<<grid, 256, simt_smem(), st>>>(a);
-    if (a.splits > 1)
-        attn_combine_kernel<<<rows * a.H, 128, 0, st>>>(p->d.attn_part, a.splits, a.out, lse);
+    const int K = p->cfg.top_k;
+    const int splits = splits_for(p->cfg, rows);
+    if (tc_eligible(p->cfg)) {
+        AttnTcArgs a;
+        a.q = (const __nv_bfloat16 *)q;
+        a.row_id = row_id;
+        a.pool = p->d.rows;
+        a.layer = layer;
+        a.L = p->cfg.num_mla_layers;
+        a.P = p->cfg.page_tokens;
+        a.H = p->cfg.mla_heads;
+        a.K = K;
+        a.splits = splits;
+        a.kc = ((K + splits - 1) / splits + kTcRows - 1) / kTcRows * kTcRows;
+        a.max_row = (int)(p->cfg.gpu_blocks * p->cfg.page_tokens);
+        a.scale_log2 = scale * kLog2e;
+        a.out = (__nv_bfloat16 *)out;
+        a.lse = lse;
+        a.part = p->d.attn_part;
+        a.err = p->d.err;
+        dim3 grid(rows, a.H / kTcHeads, splits);
+        attn_tc_kernel<<<grid, kAttnThreads, AttnTcSmem::bytes, st>>>(a);
+    } else {
+        AttnArgs a;
+        a.q = (const __nv_bfloat16 *)q;
+        a.row_id = row_id;
+        a.pool = p->d.rows;
+        a.layer = layer;
+        a.L = p->cfg.num_mla_layers;
+        a.P = p->cfg.page_tokens;
+        a.R = p->R;
+        a.fmt = p->cfg.row_fmt;
+        a.H = p->cfg.mla_heads;
+        a.K = K;
+        a.splits = splits;
+        a.kc = ((K + splits - 1) / splits + kChunk - 1) / kChunk * kChunk;
+        a.scale_log2 = scale * kLog2e;
+        a.out = (__nv_bfloat16 *)out;
+        a.lse = lse;
+        a.part = p->d.attn_part;
+        a.max_row = (int)(p->cfg.gpu_blocks * p->cfg.page_tokens);
+        a.err = p->d.err;
+        dim3 grid(rows, a.H / kHeadsPerCta, splits);
+        attn_simt_kernel<<<grid, 256, simt_smem(), st>>>(a);
+    }
+    if (splits > 1)
+        attn_combine_kernel<<<rows * p->cfg.mla_heads, 128, 0, st>>>(p->d.attn_part, splits,
+                                                                   (__nv_bfloat16 *)out, lse);
     return cudaGetLastError();
 }
 

@@ -100,11 +100,11 @@ cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq,
                            cudaStream_t st);
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
                              int B, int nq, float scale, void *out, float *lse, cudaStream_t st);
-int attention_splits(const hs_pool *p, int B, int nq);
 int indexer_kernel_count(const hs_pool *p, int B, int nq);
 int topk_kernel_count(const hs_pool *p, int B, int nq);
 int resolve_kernel_count(const hs_pool *p, int B, int nq);
 int attention_kernel_count(const hs_pool *p, int B, int nq);
 cudaError_t setup_kernel_attributes(const hs_pool *p);
+size_t attention_partial_floats(const hs_pool_config *c);
 
 }  // namespace hs

@@ -92,15 +92,9 @@ Derived derive(const hs_pool_config *c) {
     d.esize = c->idx_fmt == HS_IDX_E4M3 ? 1 : 4;
     d.score_stride = (int64_t)round_up((size_t)c->max_tokens, 64);
     d.nchunks = (c->max_tokens + hs::kTopkChunk - 1) / hs::kTopkChunk;
-    // split-K partials: splits are only used while B*nq*H/8 CTAs do not fill
-    // the GPU, so the largest buffer is bounded by that product.
-    size_t worst = 0;
-    for (int rows = 1; rows <= c->max_requests * d.nq; rows++) {
-        int ctas = rows * (c->mla_heads / 8);
-        int s = std::min(hs::kMaxSplits, std::max(1, (2 * hs::kNumSMs + ctas - 1) / ctas));
-        if (s > 1) worst = std::max(worst, (size_t)rows * c->mla_heads * s * (hs::kNope + 2));
-    }
-    d.attn_part_floats = worst;
+    // split-K partials of the attention (only used while one launch cannot
+    // fill the GPU without splitting the K rows)
+    d.attn_part_floats = hs::attention_partial_floats(c);
     return d;
 }
 

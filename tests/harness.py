@@ -252,7 +252,8 @@ class Runner:
                                            f"{np.abs(g - o).max():.3g}")
                     gl = lse[l, b, j].cpu().numpy()
                     if len(sel):
-                        np.testing.assert_allclose(gl, ls, rtol=1e-4, atol=1e-3)
+                        badl = np.abs(gl - ls) > ATOL + RTOL * np.abs(ls)
+                        assert not badl.any(), f"{c.name}: lse outside tol"
                     else:
                         assert np.isneginf(gl).all() and (g == 0).all()
 

@@ -342,3 +342,26 @@ def test_indexer_tensor_core_pipeline_wraps():
                     np.testing.assert_array_equal(got[j, :vis], ref[j, :vis])
     finally:
         r.close()
+
+
+@pytest.mark.parametrize("name,kw", [
+    # split-K over the 2048 rows (few queries), misses from a drawn stream
+    ("tc-splits", dict(B=2, N=[5000, 9000], K=2048, Hi=8, Di=32, L=2, T=256, steps=3,
+                       source="recency_zipf")),
+    # MTP3: four queries per request, ragged lengths
+    ("tc-mtp", dict(B=3, N=[2100, 3000, 2600], K=512, Hi=64, Di=128, L=2, T=256, num_spec=3,
+                    steps=2)),
+    # fewer visible tokens than K: padded entries are skipped
+    ("tc-short", dict(B=2, N=[300, 1000], K=512, Hi=8, Di=32, L=1, T=64, steps=2, append=1)),
+    # zero residency, every row arrives through the hot buffer
+    ("tc-zero", dict(B=2, N=4000, K=1024, Hi=8, Di=32, L=1, T=0, mode=2, steps=3,
+                     source="uniform_zipf")),
+])
+def test_attention_tensor_core_128_heads(name, kw):
+    """128 heads with E4M3 rows: the tcgen05 attention kernel against the oracle."""
+    from harness import Case
+    hs = _hs()
+    kw = dict(kw)
+    kw.setdefault("mode", hs.HS_MIXED)
+    c = Case(name, H=128, row_fmt=wl.ROW_E4M3_656, **kw)
+    _run(c)
