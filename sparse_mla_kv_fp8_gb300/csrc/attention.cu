@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     const uint32_t tmem = *tslot;
     const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
     const uint32_t o_col = 128;   // O^T tiles: columns [128 + 64 g, ...)
+    const uint32_t l_col = 384;   // per-row running sums of P: [384, 448)
 
     if (warp == 0) {
         // ------------------------------------------------------- MMA issuer
@@ -338,45 +339,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         }
     } else if (warp >= 6) {
         // ------------------------------------------------------ row loaders
+        // Thread tl converts rows r_u = tl/8 + 32u (u = 0..3), 16-byte slice
+        // c8 = tl%8 of each of five stages: the four 128-dim scale groups
+        // (K-blocks 2g, 2g+1) and the rope block.  Loads run one stage ahead
+        // of the conversion; the next chunk's rows are prefetched into L2.
         const int tl = threadIdx.x - 6 * 32;  // 0..255
-        for (int c = 0; c < nchunks; c++) {
-            // this thread converts rows r = tl/8 + 32u (u = 0..3), 16-byte chunk tl%8
+        const int c8 = tl & 7;
+        auto row_ptr = [&](int c, int r) -> const uint8_t * {
+            const int k = k0 + c * kTcRows + r;
+            int32_t id = (c < nchunks && k < k1) ? ids[k] : -1;
+            if (id >= a.max_row) {
+                set_error(a.err, HS_ERR_INDEX_RANGE);
+                id = -1;
+            }
+            if (id < 0) return nullptr;
+            const size_t blk = (size_t)(id / a.P), off = (size_t)(id % a.P);
+            return a.pool + ((blk * a.L + a.layer) * a.P + off) * 656;
+        };
+        auto stage_off = [&](int st) { return st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8; };
+        if (tl < kTcRows) {
+            const uint8_t *pf = row_ptr(0, tl);
+            if (pf) tc::prefetch_l2(pf, 656);
+        }
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; c++) {
             const uint8_t *src[4];
-            float4 sc[4];
-            const int c8 = tl & 7;
+#pragma unroll
+            for (int u = 0; u < 4; u++) src[u] = row_ptr(c, (tl >> 3) + 32 * u);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            uint4 scv[4], cur[4], nxt[4];
 #pragma unroll
             for (int u = 0; u < 4; u++) {
-                const int r = (tl >> 3) + 32 * u;
-                const int k = k0 + c * kTcRows + r;
-                int32_t id = k < k1 ? ids[k] : -1;
-                if (id >= a.max_row) {
-                    if (c8 == 0) set_error(a.err, HS_ERR_INDEX_RANGE);
-                    id = -1;
-                }
-                src[u] = nullptr;
-                sc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (id >= 0) {
-                    const size_t blk = (size_t)(id / a.P), off = (size_t)(id % a.P);
-                    src[u] = a.pool + ((blk * a.L + a.layer) * a.P + off) * 656;
-                    sc[u] = *(const float4 *)(src[u] + 512);
-                }
+                scv[u] = src[u] ? tc::ld_nc16(src[u] + 512) : z;
+                cur[u] = src[u] ? tc::ld_nc16(src[u] + stage_off(0)) : z;
             }
-            bool ok = true;
-            for (int kb = 0; kb < kKBlocks; kb++) {
-                uint2 raw[4];
-                uint4 rope[4];
+            if (tl < kTcRows) {  // warm L2 with the next chunk's rows
+                const uint8_t *pf = row_ptr(c + 1, tl);
+                if (pf) tc::prefetch_l2(pf, 656);
+            }
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    raw[u] = make_uint2(0, 0);
-                    rope[u] = make_uint4(0, 0, 0, 0);
-                    if (src[u]) {
-                        if (kb < 8)
-                            raw[u] = __ldg((const uint2 *)(src[u] + kb * 64 + c8 * 8));
-                        else
-                            rope[u] = __ldg((const uint4 *)(src[u] + 528 + c8 * 16));
-                    }
+            for (int st = 0; st < 5; st++) {
+                if (st + 1 < 5) {
+#pragma unroll
+                    for (int u = 0; u < 4; u++) nxt[u] = src[u] ? tc::ld_nc16(src[u] + stage_off(st + 1)) : z;
                 }
-                const bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
+                const int kb = st < 4 ? 2 * st + (c8 >> 2) : 8;
+                bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
+                if (st < 4) w &= tc::mbar_wait(&kb_empty[kb ^ 1], (c & 1) ^ 1, a.err);
                 if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
                     ok = false;
                     break;
@@ -385,41 +394,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
                     const int r = (tl >> 3) + 32 * u;
-                    uint4 v;
-                    if (kb < 8) {
-                        const float s = kb < 2 ? sc[u].x : kb < 4 ? sc[u].y : kb < 6 ? sc[u].z : sc[u].w;
-                        const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&raw[u];
-                        float f[8];
+                    if (st < 4) {
+                        const uint32_t sb = st == 0 ? scv[u].x : st == 1 ? scv[u].y : st == 2 ? scv[u].z : scv[u].w;
+                        const float scl = __uint_as_float(sb);
+                        const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&cur[u];
+                        uint32_t packed[8];
 #pragma unroll
-                        for (int e = 0; e < 4; e++) {
+                        for (int e = 0; e < 8; e++) {
                             __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pp[e], __NV_E4M3);
                             const float2 f2 = __half22float2(__half2(h2));
-                            f[2 * e] = f2.x * s;
-                            f[2 * e + 1] = f2.y * s;
+                            packed[e] = pack_bf16(f2.x * scl, f2.y * scl);
                         }
-                        v.x = pack_bf16(f[0], f[1]);
-                        v.y = pack_bf16(f[2], f[3]);
-                        v.z = pack_bf16(f[4], f[5]);
-                        v.w = pack_bf16(f[6], f[7]);
+                        const int q0 = (c8 & 3) * 2;
+                        *(uint4 *)(dst + tc::sw128_offset(r, q0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        *(uint4 *)(dst + tc::sw128_offset(r, q0 + 1)) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                     } else {
-                        v = rope[u];
+                        *(uint4 *)(dst + tc::sw128_offset(r, c8)) = cur[u];
                     }
-                    *(uint4 *)(dst + tc::sw128_offset(r, c8)) = v;
                 }
                 tc::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&kb_full[kb]);
+                if (lane == 0) {
+                    if (st < 4) {
+                        tc::mbar_arrive(&kb_full[2 * st]);
+                        tc::mbar_arrive(&kb_full[2 * st + 1]);
+                    } else {
+                        tc::mbar_arrive(&kb_full[8]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; u++) cur[u] = nxt[u];
             }
-            if (!ok) break;
         }
     } else if (warp >= 2) {
         // ---------------------------------------------- softmax + epilogue
+        // Thread = chunk row = TMEM lane.  Per-row running sums of P for each
+        // head live in TMEM columns [l_col, l_col + 64) of the thread's lane.
         const int sp = warp & 3;
-        const int r = sp * 32 + lane;  // row of the chunk == TMEM lane
+        const int r = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
-        float lp[64];
-#pragma unroll
-        for (int h = 0; h < 64; h++) lp[h] = 0.f;
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
             const int buf = c & 1;
@@ -435,15 +448,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             const uint32_t sbase = lane_base + s_col + buf * kTcHeads;
             // pass 1: does any head's maximum grow by more than 2^8?
             bool need = false;
+            {
+                float sv[64];
 #pragma unroll
-            for (int h0 = 0; h0 < 64; h0 += 16) {
-                float sv[16];
-                tc::tmem_ld16(sbase + h0, sv);
+                for (int q = 0; q < 4; q++) tc::tmem_ld16(sbase + 16 * q, sv + 16 * q);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const float z = valid ? sv[i] * a.scale_log2 : -INFINITY;
-                    need |= z > mref[h0 + i] + kRescaleLog2;
+                for (int h = 0; h < 64; h++) {
+                    const float zz = valid ? sv[h] * a.scale_log2 : -INFINITY;
+                    need |= zz > mref[h] + kRescaleLog2;
                 }
             }
             if (bar_or_softmax(need)) {
@@ -470,21 +483,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     mref[r] = mn;
                 }
                 bar_softmax();
-#pragma unroll
-                for (int h = 0; h < 64; h++) lp[h] *= alpha[h];
                 if (c > 0) {
-                    // O^T holds chunks < c: wait for them, then scale column h by alpha[h]
+                    // row sums and O^T hold chunks < c: scale column h by alpha[h]
                     const bool wo = tc::mbar_wait(o_done, (c - 1) & 1, a.err);
                     if (bar_or_softmax(!wo)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    for (int g = 0; g < 4; g++) {
+                    for (int g = 0; g < 5; g++) {  // four O^T tiles, then the row sums
+                        const uint32_t col = g < 4 ? o_col + g * kTcHeads : l_col;
 #pragma unroll
                         for (int h0 = 0; h0 < 64; h0 += 16) {
                             float ov[16];
-                            const uint32_t ta = lane_base + o_col + g * kTcHeads + h0;
+                            const uint32_t ta = lane_base + col + h0;
                             tc::tmem_ld16(ta, ov);
                             tc::tmem_ld_wait();
 #pragma unroll
@@ -495,21 +507,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     tc::tmem_st_wait();
                 }
             }
-            // pass 2: P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
+            // pass 2: P^T row r (bf16) -> the rope K-block (S^T(c) no longer
+            // reads it); the row sums accumulate in TMEM
             uint8_t *prow = rb + 8 * kRBlock;
 #pragma unroll
             for (int h0 = 0; h0 < 64; h0 += 16) {
-                float sv[16];
+                float sv[16], lv[16];
                 tc::tmem_ld16(sbase + h0, sv);
+                if (c > 0) tc::tmem_ld16(lane_base + l_col + h0, lv);
                 tc::tmem_ld_wait();
                 float pv[16];
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
                     const float m = mref[h0 + i];
-                    const float z = valid ? sv[i] * a.scale_log2 : -INFINITY;
-                    pv[i] = (m == -INFINITY) ? 0.f : exp2f(z - m);
-                    lp[h0 + i] += pv[i];
+                    const float zz = valid ? sv[i] * a.scale_log2 : -INFINITY;
+                    pv[i] = (m == -INFINITY) ? 0.f : exp2f(zz - m);
+                    lv[i] = (c > 0 ? lv[i] : 0.f) + pv[i];
                 }
+                tc::tmem_st16(lane_base + l_col + h0, lv);
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
                     uint4 v;
@@ -520,18 +535,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     *(uint4 *)(prow + tc::sw128_offset(r, (h0 >> 3) + half)) = v;
                 }
             }
+            tc::tmem_st_wait();
             tc::fence_before_sync();
             tc::mbar_arrive(&s_empty[buf]);
             tc::fence_async_smem();
             tc::mbar_arrive(p_full);
         }
-        // ---- epilogue: l per head, then O^T / l -> out (or partials)
+        // ---- epilogue: l per head (sum of the row sums over the 128 lanes)
+        if (ok && nchunks > 0) {
 #pragma unroll
-        for (int h = 0; h < 64; h++) {
-            float v = lp[h];
+            for (int h0 = 0; h0 < 64; h0 += 16) {
+                float lv[16];
+                tc::tmem_ld16(lane_base + l_col + h0, lv);
+                tc::tmem_ld_wait();
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) red[sp * 64 + h] = v;
+                for (int i = 0; i < 16; i++) {
+                    float v = lv[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) red[sp * 64 + h0 + i] = v;
+                }
+            }
+        } else if (lane == 0) {
+            for (int h = 0; h < 64; h++) red[sp * 64 + h] = 0.f;
         }
         bar_softmax();
         if (r < 64) lsum[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
@@ -598,7 +624,9 @@ static bool tc_eligible(const hs_pool_config &c) {
     return c.row_fmt == HS_ROW_E4M3_656 && c.mla_heads % kTcHeads == 0;
 }
 
-// One CTA per SM (shared memory): the fewest chunk-waves, then fewer splits.
+// One CTA per SM (shared memory).  Cost in chunk times: waves x (chunks per
+// CTA + about four chunks of start-up: query staging, TMEM allocation and
+// the first chunk's load latency) + one for the combine pass when split.
 static int tc_splits(const hs_pool_config &c, int rows) {
     const int chunks = (c.top_k + kTcRows - 1) / kTcRows;
     const int base = rows * (c.mla_heads / kTcHeads);
@@ -607,7 +635,7 @@ static int tc_splits(const hs_pool_config &c, int rows) {
     for (int s = 1; s <= chunks && s <= kMaxSplits; s++) {
         const long cps = (chunks + s - 1) / s;
         const long waves = ((long)base * s + kNumSMs - 1) / kNumSMs;
-        const long cost = waves * cps * 4 + (s > 1 ? 1 : 0);
+        const long cost = waves * (cps + 4) + (s > 1 ? 1 : 0);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = s;

@@ -212,30 +212,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int sp = warp & 3;  // TMEM sub-partition this warp may read
         const int row = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+        const float *ksc = a.ksc + (size_t)b * a.maxT;
+        int t = tile0 * kTile + row;
+        float sig_next = t < N ? ksc[t] : 0.f;
         for (int it = 0; it < nt; it++) {
             const int acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
-            if (!tc::mbar_wait(&tfull[acc], aph, a.err)) break;
+            const float sig = sig_next;  // loaded one tile ahead
+            if (it + 1 < nt && t + kTile < N) sig_next = ksc[t + kTile];
+            const bool w = tc::mbar_wait(&tfull[acc], aph, a.err);
+            if (!__all_sync(0xffffffffu, w)) break;  // the warp leaves together
             tc::fence_after_sync();
-            const int t = (tile0 + it) * kTile + row;
-            const float sig = t < N ? a.ksc[(size_t)b * a.maxT + t] : 0.f;
             const uint32_t tb = lane_base + acc * a.ncols;
             for (int j = 0; j < a.nq; j++) {
                 float accs = 0.f;
-                for (int h0 = 0; h0 < a.Hi; h0 += 16) {
-                    float v[16];
-                    tc::tmem_ld16(tb + j * a.Hi + h0, v);
+                for (int h0 = 0; h0 < a.Hi; h0 += 64) {
+                    // up to four 16-column loads in flight, one wait
+                    const int n16 = min(4, (a.Hi - h0) >> 4);
+                    float v[64];
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        if (q < n16) tc::tmem_ld16(tb + j * a.Hi + h0 + 16 * q, v + 16 * q);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const float x = sig * v[i];
-                        accs = fmaf(wsm[j * a.Hi + h0 + i], x > 0.f ? x : 0.f, accs);
+                    for (int i = 0; i < 64; i++) {
+                        if (i < 16 * n16) {
+                            const float x = sig * v[i];
+                            accs = fmaf(wsm[j * a.Hi + h0 + i], x > 0.f ? x : 0.f, accs);
+                        }
                     }
                 }
                 if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = accs;
             }
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[acc]);
+            t += kTile;
         }
     }
     tc::fence_before_sync();
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 bool tc_eligible(const hs_pool *p, int nq) {
     const int ncols = nq * p->cfg.idx_heads;
-    return p->cfg.idx_fmt == HS_IDX_E4M3 && p->cfg.idx_dim == 128 && ncols % 16 == 0 &&
+    return p->cfg.idx_fmt == HS_IDX_E4M3 && p->cfg.idx_dim == 128 && p->cfg.idx_heads % 16 == 0 &&
            ncols >= 16 && ncols <= 256 && p->has_key_map;
 }
 
@@ -280,8 +291,9 @@ cudaError_t indexer_setup(const hs_pool *p) {
 
 int indexer_kernel_count(const hs_pool *, int, int) { return 1; }
 
-// Tiles per CTA for a grid of (chunks, B): the fewest waves, then the most
-// CTAs, given how many CTAs fit on one SM.
+// Tiles per CTA for a grid of (chunks, B), given how many CTAs fit on one
+// SM: minimise waves x (tiles per CTA + the fixed cost of starting a CTA,
+// about four tiles' worth: TMEM allocation, query staging, pipeline fill).
 static int pick_tiles_per_cta(int ntiles, int B, int per_sm) {
     const long slots = (long)kNumSMs * per_sm;
     int best = ntiles;
@@ -290,7 +302,7 @@ static int pick_tiles_per_cta(int ntiles, int B, int per_sm) {
         const long chunks = (ntiles + tpc - 1) / tpc;
         const long ctas = chunks * B;
         const long waves = (ctas + slots - 1) / slots;
-        const double t = (double)waves * tpc + 0.02 * tpc;  // small bias to larger tiles
+        const double t = (double)waves * (tpc + 4.0);
         if (t < best_t) {
             best_t = t;
             best = tpc;

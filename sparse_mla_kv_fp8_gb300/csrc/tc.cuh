@@ -78,6 +78,22 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
 
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)ptr), "r"(bytes)
+                 : "memory");
+}
+
+// 16-byte read-only global load, kept in program order with the other
+// volatile asm (so a batch of loads is issued before the first use).
+__device__ __forceinline__ uint4 ld_nc16(const void *ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"((uint64_t)ptr));
+    return v;
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor core / TMA reads).
 __device__ __forceinline__ void fence_async_smem() {
