@@ -214,6 +214,29 @@ hs_status hs_indexer_score(hs_pool *pool, const void *q, const float *w,
 hs_status hs_topk(hs_pool *pool, const float *scores, int64_t score_stride,
                   int32_t B, int32_t nq, int32_t *topk, cudaStream_t stream);
 
+/* The same top-K as hs_topk for callers that cannot allocate device memory
+ * and have no pool: for example a serving engine that reserved most of the
+ * GPU for its own block pool at start-up (a later cudaMalloc would fail or
+ * split that reservation), or host code that must avoid the device-wide
+ * synchronisation of an allocation call.  The paper has no counterpart; this
+ * is a library convenience.
+ *   scores, score_stride, B, nq, K, topk: as for hs_topk (K = top_k);
+ *   seq_len: dev [B] int32 request lengths (query j of request b sees
+ *            t < seq_len[b] - nq + j + 1);
+ *   max_tokens: upper bound of every seq_len[b], <= score_stride.
+ * Scratch: a static area inside this library (578 KiB of device memory,
+ * held on every GPU that loads the library until the process exits).  Nothing is allocated or freed by this call.  Limits: B * nq <= 64
+ * and max_tokens <= 1,048,576; larger requests return HS_ERR_CAPACITY and
+ * enqueue nothing.  The first call on a device looks up the scratch's device
+ * address (host-side set-up, once per device; make that first call before
+ * any stream capture).  All calls share the one scratch area: each call
+ * clears what must start at zero, but two calls whose kernels overlap on the
+ * GPU (different streams, no ordering between them) race on it. */
+hs_status hs_topk_noalloc(const float *scores, int64_t score_stride,
+                          const int32_t *seq_len, int32_t B, int32_t nq,
+                          int32_t K, int32_t max_tokens, int32_t *topk,
+                          cudaStream_t stream);
+
 /* hs_indexer_score + hs_topk with the scores kept in the pool's workspace. */
 hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
                           int32_t B, int32_t nq, int32_t *topk,

@@ -11,6 +11,8 @@
 // keys above / equal to T and write the selected indices in ascending token
 // order (keys equal to T are taken lowest index first).  Every count is an
 // integer, so the result is bit-for-bit deterministic.
+#include <mutex>
+
 #include "hs_internal.h"
 
 namespace hs {
@@ -261,3 +263,85 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
 }
 
 }  // namespace hs
+
+// ---------------------------------------------------------------------------
+// Top-K without any allocation.
+//
+// Some callers cannot allocate device memory at all: a serving engine that
+// reserved most of the GPU for its own block pool at start-up (so a later
+// cudaMalloc fails or fragments that pool), or host code that must not make
+// the device-wide synchronising allocation calls.  For them the radix top-K
+// also runs on a scratch area that lives in this library's own static device
+// memory, with no pool and no workspace argument.  Every GPU that loads the
+// library holds that area (kNoAllocScratchBytes) until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxRows = 64;                      // B * nq
+constexpr int kNoAllocMaxTokens = 1 << 20;               // tokens per request
+constexpr int kNoAllocMaxChunks = kNoAllocMaxTokens / hs::kTopkChunk;
+constexpr size_t kNoAllocStateBytes = sizeof(hs::TopkRowState) * kNoAllocMaxRows;
+constexpr size_t kNoAllocHistBytes = sizeof(uint32_t) * hs::kTopkBins * kNoAllocMaxRows;
+constexpr size_t kNoAllocChunkBytes = sizeof(int32_t) * 2 * kNoAllocMaxChunks * kNoAllocMaxRows;
+constexpr size_t kNoAllocScratchBytes = kNoAllocStateBytes + kNoAllocHistBytes + kNoAllocChunkBytes;
+static_assert(kNoAllocStateBytes % 256 == 0 && kNoAllocHistBytes % 256 == 0, "scratch carving");
+
+// The scratch itself.  Host code must never pass this name to a kernel: on
+// the host it only stands for the symbol.  Its device address comes from
+// cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) uint8_t g_topk_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (set up on first use).
+cudaError_t noalloc_scratch(uint8_t **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_topk_noalloc_scratch);
+        if (e != cudaSuccess || !p) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+        g_noalloc_ptr[dev] = (uint8_t *)p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" hs_status hs_topk_noalloc(const float *scores, int64_t score_stride,
+                                     const int32_t *seq_len, int32_t B, int32_t nq, int32_t K,
+                                     int32_t max_tokens, int32_t *topk, cudaStream_t stream) {
+    if (!scores || !seq_len || !topk || B <= 0 || nq <= 0 || K <= 0 || max_tokens <= 0 ||
+        score_stride < max_tokens)
+        return HS_ERR_INVALID_ARG;
+    if ((int64_t)B * nq > kNoAllocMaxRows || max_tokens > kNoAllocMaxTokens)
+        return HS_ERR_CAPACITY;  // beyond the static scratch
+    uint8_t *base = nullptr;
+    if (noalloc_scratch(&base) != cudaSuccess) {
+        cudaGetLastError();
+        return HS_ERR_CUDA;
+    }
+    hs::TopkRowState *state = (hs::TopkRowState *)base;
+    uint32_t *hist = (uint32_t *)(base + kNoAllocStateBytes);
+    int32_t *chunk = (int32_t *)(base + kNoAllocStateBytes + kNoAllocHistBytes);
+    const int rows = B * nq;
+    const int nch = (max_tokens + hs::kTopkChunk - 1) / hs::kTopkChunk;
+    // the init kernel clears the histograms and the per-row state that the
+    // previous call left behind; the chunk counts are fully rewritten
+    hs::topk_init_kernel<<<rows, 256, 0, stream>>>(state, hist, seq_len, nq, K);
+    dim3 grid(nch, rows);
+    for (int pass = 0; pass < 3; pass++)
+        hs::topk_hist_kernel<<<grid, hs::kThreads, 0, stream>>>(scores, score_stride, state, hist,
+                                                                pass);
+    hs::topk_count_kernel<<<grid, hs::kThreads, 0, stream>>>(scores, score_stride, state, chunk,
+                                                             nch);
+    hs::topk_write_kernel<<<grid, hs::kThreads, 0, stream>>>(scores, score_stride, state, chunk,
+                                                             nch, K, topk);
+    return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}

@@ -91,6 +91,7 @@ hs_pool_stats = _decl("hs_pool_stats", _i32, [_P, ctypes.POINTER(hs_stats)])
 hs_pool_reset_stats = _decl("hs_pool_reset_stats", _i32, [_P])
 hs_pool_dump_state = _decl("hs_pool_dump_state", _i32, [_P, _i32, _P, _P, _P, _P, _P, _P, _P, _P])
 hs_pool_load_state = _decl("hs_pool_load_state", _i32, [_P, _i32, _P, _P, _P, _u32])
+hs_topk_noalloc = _decl("hs_topk_noalloc", _i32, [_P, _i64, _P, _i32, _i32, _i32, _i32, _P, _P])
 hs_step_kernel_count = _decl("hs_step_kernel_count", _i32, [_P, _i32, _i32])
 hs_status_string = _decl("hs_status_string", ctypes.c_char_p, [_i32])
 hs_abi_version = _decl("hs_abi_version", _i32, [])
