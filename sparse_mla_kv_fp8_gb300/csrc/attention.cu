@@ -191,7 +191,8 @@ struct AttnTcSmem {
     static constexpr int q_off = r_off + kKBlocks * kRBlock;     // 9 x 8 KB
     static constexpr int f_off = q_off + kKBlocks * kQBlock;     // floats
     static constexpr int nf = 64 * 3 + 4 * 64;                   // mref, lsum, alpha, red[4][64]
-    static constexpr int bar_off = f_off + nf * 4;
+    static constexpr int ones_off = f_off + nf * 4;                // 128 x 16 bf16 ones
+    static constexpr int bar_off = ones_off + 4096;
     static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 3;
     static constexpr int tslot_off = bar_off + nbar * 8;
     static constexpr int bytes = tslot_off + 16 + 1024;          // + alignment slack
@@ -230,6 +231,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *(uint32_t *)&v;
 }
 
+// 2^x with the hardware approximation (max 2 ulp); 2^-inf = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -239,6 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     float *lsum = mref + 64;
     float *alpha = lsum + 64;
     float *red = alpha + 64;  // [4][64]
+    uint8_t *ones = smem + AttnTcSmem::ones_off;
     uint64_t *kb_full = (uint64_t *)(smem + AttnTcSmem::bar_off);
     uint64_t *kb_empty = kb_full + kKBlocks;
     uint64_t *s_full = kb_empty + kKBlocks;
@@ -266,6 +275,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         mref[threadIdx.x] = -INFINITY;
         lsum[threadIdx.x] = 0.f;
     }
+    for (int i = threadIdx.x; i < 4096 / 16; i += kAttnThreads)  // bf16 1.0 pairs
+        ((uint4 *)ones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKBlocks; i++) {
             tc::mbar_init(&kb_full[i], kLoaderWarps);
@@ -298,6 +309,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         if (lane == 0) {
             const uint32_t idesc_s = tc::instr_desc(128, kTcHeads, 1, 1, 0, 0);
             const uint32_t idesc_o = tc::instr_desc(128, kTcHeads, 1, 1, 1, 1);
+            const uint32_t idesc_l = tc::instr_desc(128, kTcHeads, 1, 1, 0, 1);
+            const uint32_t ones_addr = tc::smem_addr(ones);
             const uint32_t r_addr = tc::smem_addr(rb), q_addr = tc::smem_addr(qb);
             const uint32_t p_addr = r_addr + 8 * kRBlock;
             bool ok = true;
@@ -329,6 +342,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     }
                     tc::mma_commit(&kb_empty[2 * g]);
                     tc::mma_commit(&kb_empty[2 * g + 1]);
+                }
+                // softmax denominators: l[h] += sum_r P[r][h], as ones(128 x 128) P^T,
+                // so every TMEM lane of the l columns holds the same sums
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint64_t ad = tc::smem_desc(ones_addr, 128, 256, 0);
+                    const uint64_t bd = tc::smem_desc_sw128(p_addr + kk * 2048, kRBlock, 1024);
+                    tc::mma_f16(tmem + l_col, ad, bd, idesc_l, (c | kk) != 0);
                 }
                 tc::mma_commit(&kb_empty[8]);
                 tc::mma_commit(o_done);
@@ -428,8 +449,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         }
     } else if (warp >= 2) {
         // ---------------------------------------------- softmax + epilogue
-        // Thread = chunk row = TMEM lane.  Per-row running sums of P for each
-        // head live in TMEM columns [l_col, l_col + 64) of the thread's lane.
+        // Thread = chunk row = TMEM lane.
         const int sp = warp & 3;
         const int r = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
@@ -445,34 +465,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 break;
             }
             tc::fence_after_sync();
+            float z[64];
             const uint32_t sbase = lane_base + s_col + buf * kTcHeads;
-            // pass 1: does any head's maximum grow by more than 2^8?
-            bool need = false;
-            {
-                float sv[64];
 #pragma unroll
-                for (int q = 0; q < 4; q++) tc::tmem_ld16(sbase + 16 * q, sv + 16 * q);
-                tc::tmem_ld_wait();
+            for (int q = 0; q < 4; q++) tc::tmem_ld16(sbase + 16 * q, z + 16 * q);
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&s_empty[buf]);  // S^T(c) is in registers
+            bool need = false;  // does any head's maximum grow by more than 2^8?
 #pragma unroll
-                for (int h = 0; h < 64; h++) {
-                    const float zz = valid ? sv[h] * a.scale_log2 : -INFINITY;
-                    need |= zz > mref[h] + kRescaleLog2;
-                }
+            for (int h = 0; h < 64; h++) {
+                z[h] = valid ? z[h] * a.scale_log2 : -INFINITY;
+                need |= z[h] > mref[h] + kRescaleLog2;
             }
             if (bar_or_softmax(need)) {
                 // chunk maximum of every head across the 128 rows
 #pragma unroll
-                for (int h0 = 0; h0 < 64; h0 += 16) {
-                    float sv[16];
-                    tc::tmem_ld16(sbase + h0, sv);
-                    tc::tmem_ld_wait();
+                for (int h = 0; h < 64; h++) {
+                    float m = z[h];
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        float m = valid ? sv[i] * a.scale_log2 : -INFINITY;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane == 0) red[sp * 64 + h0 + i] = m;
-                    }
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) red[sp * 64 + h] = m;
                 }
                 bar_softmax();
                 if (r < 64) {
@@ -484,14 +497,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 }
                 bar_softmax();
                 if (c > 0) {
-                    // row sums and O^T hold chunks < c: scale column h by alpha[h]
+                    // O^T and l hold chunks < c: wait for them, then scale column h by alpha[h]
                     const bool wo = tc::mbar_wait(o_done, (c - 1) & 1, a.err);
                     if (bar_or_softmax(!wo)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    for (int g = 0; g < 5; g++) {  // four O^T tiles, then the row sums
+                    for (int g = 0; g < 5; g++) {  // four O^T tiles, then the denominators
                         const uint32_t col = g < 4 ? o_col + g * kTcHeads : l_col;
 #pragma unroll
                         for (int h0 = 0; h0 < 64; h0 += 16) {
@@ -505,66 +518,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                         }
                     }
                     tc::tmem_st_wait();
+                    tc::fence_before_sync();
                 }
             }
-            // pass 2: P^T row r (bf16) -> the rope K-block (S^T(c) no longer
-            // reads it); the row sums accumulate in TMEM
+            // P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
             uint8_t *prow = rb + 8 * kRBlock;
 #pragma unroll
-            for (int h0 = 0; h0 < 64; h0 += 16) {
-                float sv[16], lv[16];
-                tc::tmem_ld16(sbase + h0, sv);
-                if (c > 0) tc::tmem_ld16(lane_base + l_col + h0, lv);
-                tc::tmem_ld_wait();
-                float pv[16];
+            for (int c8 = 0; c8 < 8; c8++) {
+                float pv[8];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const float m = mref[h0 + i];
-                    const float zz = valid ? sv[i] * a.scale_log2 : -INFINITY;
-                    pv[i] = (m == -INFINITY) ? 0.f : exp2f(zz - m);
-                    lv[i] = (c > 0 ? lv[i] : 0.f) + pv[i];
+                for (int e = 0; e < 8; e++) {
+                    const float m = mref[c8 * 8 + e];
+                    pv[e] = (m == -INFINITY) ? 0.f : ex2_approx(z[c8 * 8 + e] - m);
                 }
-                tc::tmem_st16(lane_base + l_col + h0, lv);
-#pragma unroll
-                for (int half = 0; half < 2; half++) {
-                    uint4 v;
-                    v.x = pack_bf16(pv[8 * half + 0], pv[8 * half + 1]);
-                    v.y = pack_bf16(pv[8 * half + 2], pv[8 * half + 3]);
-                    v.z = pack_bf16(pv[8 * half + 4], pv[8 * half + 5]);
-                    v.w = pack_bf16(pv[8 * half + 6], pv[8 * half + 7]);
-                    *(uint4 *)(prow + tc::sw128_offset(r, (h0 >> 3) + half)) = v;
-                }
+                uint4 v;
+                v.x = pack_bf16(pv[0], pv[1]);
+                v.y = pack_bf16(pv[2], pv[3]);
+                v.z = pack_bf16(pv[4], pv[5]);
+                v.w = pack_bf16(pv[6], pv[7]);
+                *(uint4 *)(prow + tc::sw128_offset(r, c8)) = v;
             }
-            tc::tmem_st_wait();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&s_empty[buf]);
             tc::fence_async_smem();
             tc::mbar_arrive(p_full);
         }
-        // ---- epilogue: l per head (sum of the row sums over the 128 lanes)
-        if (ok && nchunks > 0) {
-#pragma unroll
-            for (int h0 = 0; h0 < 64; h0 += 16) {
-                float lv[16];
-                tc::tmem_ld16(lane_base + l_col + h0, lv);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float v = lv[i];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) red[sp * 64 + h0 + i] = v;
-                }
-            }
-        } else if (lane == 0) {
-            for (int h = 0; h < 64; h++) red[sp * 64 + h] = 0.f;
-        }
-        bar_softmax();
-        if (r < 64) lsum[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
-        bar_softmax();
+        // ---- epilogue: O^T / l -> out (or unnormalised partials)
         const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
         if (!bar_or_softmax(!fin)) {
             tc::fence_after_sync();
+            // every lane holds the same denominators: stage them in smem
+            if (sp == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float lv[16];
+                    tc::tmem_ld16(lane_base + l_col + 16 * q, lv);
+                    tc::tmem_ld_wait();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; i++) lsum[16 * q + i] = lv[i];
+                    }
+                }
+            }
+            bar_softmax();
             for (int g = 0; g < 4; g++) {
                 const int d = g * 128 + r;
 #pragma unroll
