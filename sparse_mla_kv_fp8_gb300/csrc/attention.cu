@@ -193,7 +193,7 @@ struct AttnTcSmem {
     static constexpr int nf = 64 * 3 + 4 * 64;                   // mref, lsum, alpha, red[4][64]
     static constexpr int ones_off = f_off + nf * 4;                // 128 x 16 bf16 ones
     static constexpr int bar_off = ones_off + 4096;
-    static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 3;
+    static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 5;
     static constexpr int tslot_off = bar_off + nbar * 8;
     static constexpr int bytes = tslot_off + 16 + 1024;          // + alignment slack
 };
@@ -208,6 +208,8 @@ struct AttnTcArgs {
     __nv_bfloat16 *out;      // [rows][H][512]
     float *lse;
     float *part;             // [rows][H][splits][514]
+    int32_t *ticket;         // [rows][H/64] (unused)
+    int cluster;             // splits == 2 launched as 2-CTA clusters
     int32_t *err;
 };
 
@@ -255,6 +257,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     uint64_t *p_full = s_empty + 2;
     uint64_t *o_done = p_full + 1;
     uint64_t *mma_done = o_done + 1;
+    uint64_t *peer_ready = mma_done + 1;  // split 1: split 0's row buffer is free
+    uint64_t *peer_data = peer_ready + 1; // split 0: split 1's partial has arrived
     uint32_t *tslot = (uint32_t *)(smem + AttnTcSmem::tslot_off);
 
     const int qr = blockIdx.x, hh = blockIdx.y, split = blockIdx.z;
@@ -289,6 +293,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         tc::mbar_init(p_full, 128);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(mma_done, 1);
+        tc::mbar_init(peer_ready, 1);
+        tc::mbar_init(peer_data, 128);
         tc::fence_barrier_init();
     }
     if (warp == 1) {
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    if (a.cluster) tc::cluster_sync();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
@@ -541,9 +548,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             tc::fence_async_smem();
             tc::mbar_arrive(p_full);
         }
-        // ---- epilogue: O^T / l -> out (or unnormalised partials)
+        // ---- epilogue
         const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
-        if (!bar_or_softmax(!fin)) {
+        const bool good = !bar_or_softmax(!fin);
+        if (good) {
             tc::fence_after_sync();
             // every lane holds the same denominators: stage them in smem
             if (sp == 0) {
@@ -559,6 +567,87 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 }
             }
             bar_softmax();
+        }
+        const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
+        if (a.cluster) {
+            // ---- two splits in one cluster: split 1 hands (O^T, max, sum) to
+            // split 0 through distributed shared memory; split 0 merges.
+            // Received layout in split 0's row buffer: O [4][128][68] fp32, then
+            // max[64], sum[64].
+            float *rx = (float *)rb;
+            float *rx_m = rx + 4 * 128 * 68;
+            float *rx_l = rx_m + 64;
+            if (split == 1) {
+                const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
+                if (!bar_or_softmax(!w1)) {
+                    const uint32_t dst = tc::mapa(tc::smem_addr(rx), 0);
+                    for (int g = 0; g < 4; g++) {
+#pragma unroll
+                        for (int h0 = 0; h0 < 64; h0 += 16) {
+                            float ov[16];
+                            if (good) {
+                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                tc::tmem_ld_wait();
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                            }
+                            const uint32_t at = dst + (uint32_t)(((g * 128 + r) * 68 + h0) * 4);
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+                        }
+                    }
+                    if (r < 64) {
+                        const float l = good ? lsum[r] : 0.f;
+                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), 0), l > 0.f ? mref[r] : -INFINITY);
+                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), 0), l);
+                    }
+                }
+                // every thread's writes are ordered before its own arrival
+                tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), 0));
+            } else {
+                // the row buffer is idle once every MMA completed: let split 1 write
+                if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), 1));
+                const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
+                if (!bar_or_softmax(!w0)) {
+                    float *wf = red;  // [0,64): weight of split 0, [64,128): split 1, [128,192): 1/L
+                    if (r < 64) {
+                        const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
+                        const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
+                        const float M = fmaxf(m0, m1);
+                        const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+                        const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+                        const float Ls = l0 * w0v + l1 * w1v;
+                        wf[r] = w0v;
+                        wf[64 + r] = w1v;
+                        wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+                        if (a.lse) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+                    }
+                    bar_softmax();
+                    for (int g = 0; g < 4; g++) {
+                        const int d = g * 128 + r;
+#pragma unroll
+                        for (int h0 = 0; h0 < 64; h0 += 16) {
+                            float ov[16];
+                            if (good) {
+                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                tc::tmem_ld_wait();
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                            }
+                            const float *pv = rx + (g * 128 + r) * 68 + h0;
+#pragma unroll
+                            for (int i = 0; i < 16; i++) {
+                                const int h = h0 + i;
+                                const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
+                                a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
+                            }
+                        }
+                    }
+                }
+            }
+        } else if (good) {
             for (int g = 0; g < 4; g++) {
                 const int d = g * 128 + r;
 #pragma unroll
@@ -568,24 +657,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
-                        const int h = hh * kTcHeads + h0 + i;
+                        const int h = h0 + i;
                         if (a.splits == 1) {
-                            const float l = lsum[h0 + i];
-                            a.out[((size_t)qr * a.H + h) * kNope + d] =
-                                __float2bfloat16(l > 0.f ? ov[i] / l : 0.f);
+                            const float l = lsum[h];
+                            a.out[(g0 + h) * kNope + d] = __float2bfloat16(l > 0.f ? ov[i] / l : 0.f);
                         } else {
-                            a.part[(((size_t)qr * a.H + h) * a.splits + split) * (kNope + 2) + d] = ov[i];
+                            a.part[((g0 + h) * a.splits + split) * (kNope + 2) + d] = ov[i];
                         }
                     }
                 }
             }
             if (r < 64) {
-                const int h = hh * kTcHeads + r;
                 const float l = lsum[r], m = mref[r];
                 if (a.splits == 1) {
-                    if (a.lse) a.lse[(size_t)qr * a.H + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    if (a.lse) a.lse[g0 + r] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
                 } else {
-                    float *pp = a.part + (((size_t)qr * a.H + h) * a.splits + split) * (kNope + 2);
+                    float *pp = a.part + ((g0 + r) * a.splits + split) * (kNope + 2);
                     pp[kNope] = l > 0.f ? m : -INFINITY;
                     pp[kNope + 1] = l;
                 }
@@ -644,7 +731,9 @@ static int splits_for(const hs_pool_config &c, int rows) {
 }
 
 int attention_kernel_count(const hs_pool *p, int B, int nq) {
-    return splits_for(p->cfg, B * nq) > 1 ? 2 : 1;
+    const int s = splits_for(p->cfg, B * nq);
+    if (tc_eligible(p->cfg)) return s > 2 ? 2 : 1;
+    return s > 1 ? 2 : 1;
 }
 
 size_t attention_partial_floats(const hs_pool_config *c) {
@@ -690,9 +779,29 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         a.out = (__nv_bfloat16 *)out;
         a.lse = lse;
         a.part = p->d.attn_part;
+        a.ticket = p->d.attn_ticket;
         a.err = p->d.err;
+        a.cluster = splits == 2;
         dim3 grid(rows, a.H / kTcHeads, splits);
-        attn_tc_kernel<<<grid, kAttnThreads, AttnTcSmem::bytes, st>>>(a);
+        if (a.cluster) {
+            // the two splits of a (query, 64 heads) merge through DSMEM
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = grid;
+            lc.blockDim = dim3(kAttnThreads);
+            lc.dynamicSmemBytes = AttnTcSmem::bytes;
+            lc.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 1;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 2;
+            lc.attrs = at;
+            lc.numAttrs = 1;
+            cudaError_t e = cudaLaunchKernelEx(&lc, attn_tc_kernel, a);
+            if (e != cudaSuccess) return e;
+        } else {
+            attn_tc_kernel<<<grid, kAttnThreads, AttnTcSmem::bytes, st>>>(a);
+        }
     } else {
         AttnArgs a;
         a.q = (const __nv_bfloat16 *)q;
@@ -716,7 +825,7 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         dim3 grid(rows, a.H / kHeadsPerCta, splits);
         attn_simt_kernel<<<grid, 256, simt_smem(), st>>>(a);
     }
-    if (splits > 1)
+    if (splits > 2 || (splits == 2 && !tc_eligible(p->cfg)))  // 2 tensor-core splits merge in-cluster
         attn_combine_kernel<<<rows * p->cfg.mla_heads, 128, 0, st>>>(p->d.attn_part, splits,
                                                                    (__nv_bfloat16 *)out, lse);
     return cudaGetLastError();

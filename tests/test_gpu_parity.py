@@ -353,6 +353,9 @@ def test_indexer_tensor_core_pipeline_wraps():
                     steps=2)),
     # fewer visible tokens than K: padded entries are skipped
     ("tc-short", dict(B=2, N=[300, 1000], K=512, Hi=8, Di=32, L=1, T=64, steps=2, append=1)),
+    # two splits per (query, 64 heads): the pair merges through a 2-CTA cluster
+    ("tc-cluster", dict(B=24, N=[2300 + 37 * i for i in range(24)], K=2048, Hi=8, Di=32, L=1,
+                        T=256, steps=1, source="recency_zipf")),
     # zero residency, every row arrives through the hot buffer
     ("tc-zero", dict(B=2, N=4000, K=1024, Hi=8, Di=32, L=1, T=0, mode=2, steps=3,
                      source="uniform_zipf")),
