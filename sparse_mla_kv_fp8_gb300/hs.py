@@ -144,7 +144,7 @@ class Pool:
         dev_bytes, host_bytes = required_bytes(cfg)
         self.dev_bytes, self.host_bytes = dev_bytes, host_bytes
         self.arena = torch.empty(dev_bytes, dtype=torch.uint8, device=device)
-        self.host_arena = (torch.empty(host_bytes, dtype=torch.uint8).pin_memory()
+        self.host_arena = (torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
                            if host_bytes else None)
         h = ctypes.c_void_p()
         check(hs_pool_create(ctypes.byref(cfg), _ptr(self.arena), dev_bytes,

@@ -165,17 +165,20 @@ def page_perm(seed: int, b: int, npages: int) -> np.ndarray:
     return np.random.default_rng(subseed(seed, "perm", b)).permutation(npages)
 
 
-def _distinct_fill(chosen: list, seen: set, target: int, draw, rng, cap_iters=10000):
+def _distinct_fill(chosen: np.ndarray, target: int, draw, rng, cap_iters=1000) -> np.ndarray:
+    """Append draws to `chosen` (first occurrences, in draw order, skipping
+    tokens already there) until it holds `target` tokens."""
     it = 0
-    while len(chosen) < target and it < cap_iters:
-        cand = draw(rng, max(64, 2 * (target - len(chosen))))
-        for t in cand.tolist():
-            if t not in seen:
-                seen.add(t)
-                chosen.append(t)
-                if len(chosen) == target:
-                    break
+    while chosen.shape[0] < target and it < cap_iters:
+        need = target - chosen.shape[0]
+        cand = draw(rng, 4 * need + 256)
+        cand = cand[~np.isin(cand, chosen)]
+        if cand.shape[0]:
+            _, first = np.unique(cand, return_index=True)
+            cand = cand[np.sort(first)][:need]
+            chosen = np.concatenate([chosen, cand.astype(np.int64)])
         it += 1
+    return chosen
 
 
 def drawn_topk(seed: int, b: int, step: int, j: int, vis: int, K: int, P: int,
@@ -228,11 +231,10 @@ def drawn_topk(seed: int, b: int, step: int, j: int, vis: int, K: int, P: int,
         r = np.minimum(r, older - 1)
         return in_page(rng, perm[r])
 
-    chosen: list = []
-    seen: set = set()
-    _distinct_fill(chosen, seen, K // 2, first, rng)
-    _distinct_fill(chosen, seen, K, second, rng)
-    if len(chosen) < K:  # tiny contexts: top up uniformly
-        _distinct_fill(chosen, seen, K, lambda r, n: r.integers(0, vis, n), rng)
-    out[:] = np.sort(np.asarray(chosen[:K], np.int32))
+    chosen = np.zeros(0, np.int64)
+    chosen = _distinct_fill(chosen, K // 2, first, rng)
+    chosen = _distinct_fill(chosen, K, second, rng)
+    if chosen.shape[0] < K:  # tiny contexts: top up uniformly
+        chosen = _distinct_fill(chosen, K, lambda r, n: r.integers(0, vis, n), rng)
+    out[:] = np.sort(chosen[:K].astype(np.int32))
     return out
