@@ -310,6 +310,23 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush, stream, steps
     return {k: v / steps for k, v in acc.items()}
 
 
+# DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
+# scaled x2 to 32 requests), valid only for the kernel source they were taken on.
+TRAFFIC = {"attention": ("attention.cu", "5d5c759173d21239", 2 * (27681792 + 3328)),
+           "indexer": ("indexer.cu", "6ab613166c4483d8", 2 * (138592768 + 3861248))}
+
+
+def _traffic(stage):
+    import hashlib
+    if stage not in TRAFFIC:
+        return None
+    fname, sha, nbytes = TRAFFIC[stage]
+    path = os.path.join(ROOT, "sparse_mla_kv_fp8_gb300", "csrc", fname)
+    with open(path, "rb") as f:
+        cur = hashlib.sha256(f.read()).hexdigest()[:16]
+    return nbytes if cur == sha else None
+
+
 KERNELS = {"indexer": "indexer_tc_kernel", "topk": "topk_*_kernel (6)",
            "resolve": "resolve_plan_kernel", "attention": "attn_tc_kernel"}
 
@@ -332,13 +349,13 @@ def roofline(stage, alg, peaks, w):
         if k == "attention":
             tf = a["flops"] / (ms / 1e3) / 1e12
             out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16_sus"],
-                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": None,
+                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": _traffic(k),
                       "peak_source": peaks["src"] + " bf16 sustained",
                       "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
                       "share_of_step": share[k] / tot, "us_per_launch": ms * 1e3}
         else:
             out[k] = {"kernel": KERNELS[k], "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": None,
+                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": _traffic(k),
                       "peak_source": peaks["src"], "share_of_step": share[k] / tot,
                       "us_per_launch": ms * 1e3}
     dom = max(share, key=share.get)
