@@ -225,7 +225,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_after_sync();
             const uint32_t tb = lane_base + acc * a.ncols;
             for (int j = 0; j < a.nq; j++) {
-                float accs = 0.f;
+                // four independent partial sums (the weighted ReLU terms are summed
+                // in a tree rather than one 64-long dependent chain)
+                float part[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int h0 = 0; h0 < a.Hi; h0 += 64) {
                     // up to four 16-column loads in flight, one wait
                     const int n16 = min(4, (a.Hi - h0) >> 4);
@@ -235,13 +237,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (q < n16) tc::tmem_ld16(tb + j * a.Hi + h0 + 16 * q, v + 16 * q);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 64; i++) {
-                        if (i < 16 * n16) {
-                            const float x = sig * v[i];
-                            accs = fmaf(wsm[j * a.Hi + h0 + i], x > 0.f ? x : 0.f, accs);
+                    for (int q = 0; q < 4; q++) {
+                        if (q < n16) {
+                            const float4 *wq = (const float4 *)(wsm + j * a.Hi + h0 + 16 * q);
+                            float4 wv[4];
+#pragma unroll
+                            for (int u = 0; u < 4; u++) wv[u] = wq[u];  // smem broadcast
+#pragma unroll
+                            for (int u = 0; u < 4; u++) {
+                                const float *ww = (const float *)&wv[u];
+#pragma unroll
+                                for (int e = 0; e < 4; e++) {
+                                    const float x = sig * v[16 * q + 4 * u + e];
+                                    part[e] = fmaf(ww[e], x > 0.f ? x : 0.f, part[e]);
+                                }
+                            }
                         }
                     }
                 }
+                const float accs = (part[0] + part[1]) + (part[2] + part[3]);
                 if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = accs;
             }
             tc::fence_before_sync();
