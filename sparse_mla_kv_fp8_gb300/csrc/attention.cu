@@ -228,6 +228,22 @@ __device__ __forceinline__ bool bar_or_softmax(bool v) {
 
 __device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// The softmax group: warps 2-5 (heads 0-31) and loader warps 6-9 (heads 32-63).
+__device__ __forceinline__ bool bar_or_group(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 2, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void bar_group() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *(uint32_t *)&v;
@@ -288,9 +304,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&s_full[i], 1);
-            tc::mbar_init(&s_empty[i], 128);
+            tc::mbar_init(&s_empty[i], 256);
         }
-        tc::mbar_init(p_full, 128);
+        tc::mbar_init(p_full, 256);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(mma_done, 1);
         tc::mbar_init(peer_ready, 1);
@@ -310,6 +326,97 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
     const uint32_t o_col = 128;   // O^T tiles: columns [128 + 64 g, ...)
     const uint32_t l_col = 384;   // per-row running sums of P: [384, 448)
+
+    // Softmax of one chunk for heads [h_lo, h_lo + 32), run by 128 threads
+    // (thread = chunk row = TMEM lane); the two 32-head halves together form a
+    // 256-thread group.  Returns false (uniformly) when a wait ran out.
+    auto softmax_part = [&](int c, int h_lo) -> bool {
+        const int sp = warp & 3;
+        const int r = sp * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+        const int buf = c & 1;
+        const int k = k0 + c * kTcRows + r;
+        const int32_t id = k < k1 ? ids[k] : -1;
+        const bool valid = id >= 0 && id < a.max_row;
+        const bool w = tc::mbar_wait(&s_full[buf], (c >> 1) & 1, a.err);
+        if (bar_or_group(!w)) return false;
+        tc::fence_after_sync();
+        float z[32];
+        const uint32_t sbase = lane_base + s_col + buf * kTcHeads + h_lo;
+        tc::tmem_ld16(sbase, z);
+        tc::tmem_ld16(sbase + 16, z + 16);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s_empty[buf]);  // S^T(c) is in registers
+        bool need = false;  // does any head's maximum grow by more than 2^8?
+#pragma unroll
+        for (int h = 0; h < 32; h++) {
+            z[h] = valid ? z[h] * a.scale_log2 : -INFINITY;
+            need |= z[h] > mref[h_lo + h] + kRescaleLog2;
+        }
+        if (bar_or_group(need)) {
+            // chunk maximum of every head across the 128 rows
+#pragma unroll
+            for (int h = 0; h < 32; h++) {
+                float m = z[h];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) red[sp * 64 + h_lo + h] = m;
+            }
+            bar_group();
+            if (r < 32) {
+                const int hd = h_lo + r;
+                const float cm = fmaxf(fmaxf(red[hd], red[64 + hd]), fmaxf(red[128 + hd], red[192 + hd]));
+                const float mo = mref[hd];
+                const float mn = fmaxf(mo, cm);
+                alpha[hd] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+                mref[hd] = mn;
+            }
+            bar_group();
+            if (c > 0) {
+                // O^T and l hold chunks < c: wait for them, then scale column h by alpha[h]
+                const bool wo = tc::mbar_wait(o_done, (c - 1) & 1, a.err);
+                if (bar_or_group(!wo)) return false;
+                tc::fence_after_sync();
+                for (int g = 0; g < 5; g++) {  // four O^T tiles, then the denominators
+                    const uint32_t col = (g < 4 ? o_col + g * kTcHeads : l_col) + h_lo;
+#pragma unroll
+                    for (int h0 = 0; h0 < 32; h0 += 16) {
+                        float ov[16];
+                        const uint32_t ta = lane_base + col + h0;
+                        tc::tmem_ld16(ta, ov);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) ov[i] *= alpha[h_lo + h0 + i];
+                        tc::tmem_st16(ta, ov);
+                    }
+                }
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+            }
+        }
+        // P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
+        uint8_t *prow = rb + 8 * kRBlock;
+#pragma unroll
+        for (int c8 = 0; c8 < 4; c8++) {
+            const float4 m0 = *(const float4 *)(mref + h_lo + c8 * 8);
+            const float4 m1 = *(const float4 *)(mref + h_lo + c8 * 8 + 4);
+            const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                pv[e] = (mm[e] == -INFINITY) ? 0.f : ex2_approx(z[c8 * 8 + e] - mm[e]);
+            uint4 v;
+            v.x = pack_bf16(pv[0], pv[1]);
+            v.y = pack_bf16(pv[2], pv[3]);
+            v.z = pack_bf16(pv[4], pv[5]);
+            v.w = pack_bf16(pv[6], pv[7]);
+            *(uint4 *)(prow + tc::sw128_offset(r, (h_lo >> 3) + c8)) = v;
+        }
+        tc::fence_async_smem();
+        tc::mbar_arrive(p_full);
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- MMA issuer
@@ -390,7 +497,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             if (pf) tc::prefetch_l2(pf, 656);
         }
         bool ok = true;
-        for (int c = 0; c < nchunks && ok; c++) {
+        for (int c = 0; c < nchunks; c++) {
+          if (ok) {
             const uint8_t *src[4];
 #pragma unroll
             for (int u = 0; u < 4; u++) src[u] = row_ptr(c, (tl >> 3) + 32 * u);
@@ -453,6 +561,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
 #pragma unroll
                 for (int u = 0; u < 4; u++) cur[u] = nxt[u];
             }
+          }
+            // warps 6-9 also run the softmax of heads 32-63 (the group leaves together)
+            if (warp < 10 && !softmax_part(c, 32)) break;
         }
     } else if (warp >= 2) {
         // ---------------------------------------------- softmax + epilogue
@@ -462,91 +573,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
-            const int buf = c & 1;
-            const int k = k0 + c * kTcRows + r;
-            const int32_t id = k < k1 ? ids[k] : -1;
-            const bool valid = id >= 0 && id < a.max_row;
-            const bool w = tc::mbar_wait(&s_full[buf], (c >> 1) & 1, a.err);
-            if (bar_or_softmax(!w)) {  // all 128 threads leave together
+            if (!softmax_part(c, 0)) {
                 ok = false;
                 break;
             }
-            tc::fence_after_sync();
-            float z[64];
-            const uint32_t sbase = lane_base + s_col + buf * kTcHeads;
-#pragma unroll
-            for (int q = 0; q < 4; q++) tc::tmem_ld16(sbase + 16 * q, z + 16 * q);
-            tc::tmem_ld_wait();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&s_empty[buf]);  // S^T(c) is in registers
-            bool need = false;  // does any head's maximum grow by more than 2^8?
-#pragma unroll
-            for (int h = 0; h < 64; h++) {
-                z[h] = valid ? z[h] * a.scale_log2 : -INFINITY;
-                need |= z[h] > mref[h] + kRescaleLog2;
-            }
-            if (bar_or_softmax(need)) {
-                // chunk maximum of every head across the 128 rows
-#pragma unroll
-                for (int h = 0; h < 64; h++) {
-                    float m = z[h];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (lane == 0) red[sp * 64 + h] = m;
-                }
-                bar_softmax();
-                if (r < 64) {
-                    const float cm = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
-                    const float mo = mref[r];
-                    const float mn = fmaxf(mo, cm);
-                    alpha[r] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
-                    mref[r] = mn;
-                }
-                bar_softmax();
-                if (c > 0) {
-                    // O^T and l hold chunks < c: wait for them, then scale column h by alpha[h]
-                    const bool wo = tc::mbar_wait(o_done, (c - 1) & 1, a.err);
-                    if (bar_or_softmax(!wo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    for (int g = 0; g < 5; g++) {  // four O^T tiles, then the denominators
-                        const uint32_t col = g < 4 ? o_col + g * kTcHeads : l_col;
-#pragma unroll
-                        for (int h0 = 0; h0 < 64; h0 += 16) {
-                            float ov[16];
-                            const uint32_t ta = lane_base + col + h0;
-                            tc::tmem_ld16(ta, ov);
-                            tc::tmem_ld_wait();
-#pragma unroll
-                            for (int i = 0; i < 16; i++) ov[i] *= alpha[h0 + i];
-                            tc::tmem_st16(ta, ov);
-                        }
-                    }
-                    tc::tmem_st_wait();
-                    tc::fence_before_sync();
-                }
-            }
-            // P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
-            uint8_t *prow = rb + 8 * kRBlock;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; c8++) {
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const float m = mref[c8 * 8 + e];
-                    pv[e] = (m == -INFINITY) ? 0.f : ex2_approx(z[c8 * 8 + e] - m);
-                }
-                uint4 v;
-                v.x = pack_bf16(pv[0], pv[1]);
-                v.y = pack_bf16(pv[2], pv[3]);
-                v.z = pack_bf16(pv[4], pv[5]);
-                v.w = pack_bf16(pv[6], pv[7]);
-                *(uint4 *)(prow + tc::sw128_offset(r, c8)) = v;
-            }
-            tc::fence_async_smem();
-            tc::mbar_arrive(p_full);
         }
         // ---- epilogue
         const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
