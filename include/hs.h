@@ -101,7 +101,9 @@ typedef struct {
                                pages' rule (num_spec + 2) * top_k.  Must be a
                                multiple of page_tokens and >= nq * top_k.      */
     int32_t reserved;
-    int64_t gpu_blocks;     /* blocks in the device pool (each P tokens x L rows) */
+    int64_t gpu_blocks;     /* blocks in the device pool (each P tokens x L rows);
+                               gpu_blocks * P <= 2^31 - 1 (row ids are int32) and
+                               gpu_blocks * P * L < 2^32                        */
     int64_t host_blocks;    /* blocks in the pinned host pool (same shape); 0 =
                                no host copies (full residency only)            */
 } hs_pool_config;

@@ -31,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "tc.cuh"
 
 namespace hs {
@@ -329,8 +331,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
 
     // Softmax of one chunk for heads [h_lo, h_lo + 32), run by 128 threads
     // (thread = chunk row = TMEM lane); the two 32-head halves together form a
-    // 256-thread group.  Returns false (uniformly) when a wait ran out.
-    auto softmax_part = [&](int c, int h_lo) -> bool {
+    // 256-thread group.  Returns false (uniformly) when a wait ran out.  With
+    // kLow the scores are re-read from TMEM 16 heads at a time instead of held
+    // in 32 registers (the loader warps run it beside their own live state);
+    // S^T(c) is then released at the end, which costs nothing because S^T(c+2)
+    // cannot start before the row buffer has been refilled after PV(c+1).
+    auto softmax_part = [&](int c, int h_lo, auto low) -> bool {
+        constexpr bool kLow = decltype(low)::value;
+        constexpr int kHeld = kLow ? 16 : 32;
         const int sp = warp & 3;
         const int r = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
@@ -341,27 +349,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         const bool w = tc::mbar_wait(&s_full[buf], (c >> 1) & 1, a.err);
         if (bar_or_group(!w)) return false;
         tc::fence_after_sync();
-        float z[32];
         const uint32_t sbase = lane_base + s_col + buf * kTcHeads + h_lo;
-        tc::tmem_ld16(sbase, z);
-        tc::tmem_ld16(sbase + 16, z + 16);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        tc::mbar_arrive(&s_empty[buf]);  // S^T(c) is in registers
+        float z[kHeld];
+        auto load_scores = [&](int h0) {  // z <- scaled scores of heads h_lo+h0 ..
+            tc::tmem_ld16(sbase + h0, z);
+            if constexpr (!kLow) tc::tmem_ld16(sbase + h0 + 16, z + 16);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < kHeld; h++) z[h] = valid ? z[h] * a.scale_log2 : -INFINITY;
+        };
         bool need = false;  // does any head's maximum grow by more than 2^8?
 #pragma unroll
-        for (int h = 0; h < 32; h++) {
-            z[h] = valid ? z[h] * a.scale_log2 : -INFINITY;
-            need |= z[h] > mref[h_lo + h] + kRescaleLog2;
+        for (int h0 = 0; h0 < 32; h0 += kHeld) {
+            load_scores(h0);
+#pragma unroll
+            for (int h = 0; h < kHeld; h++) need |= z[h] > mref[h_lo + h0 + h] + kRescaleLog2;
         }
+        if constexpr (!kLow) {
+            tc::fence_before_sync();
+            tc::mbar_arrive(&s_empty[buf]);  // S^T(c) is in registers
+        }
+        // kLow: z holds heads [16, 32) now; each later pass starts with the
+        // half it holds and then loads the other
+        int held = 32 - kHeld;
         if (bar_or_group(need)) {
             // chunk maximum of every head across the 128 rows
 #pragma unroll
-            for (int h = 0; h < 32; h++) {
-                float m = z[h];
+            for (int i = 0; i < 32 / kHeld; i++) {
+                const int h0 = i == 0 ? held : 16 - held;
+                if (i > 0) load_scores(h0);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                if (lane == 0) red[sp * 64 + h_lo + h] = m;
+                for (int h = 0; h < kHeld; h++) {
+                    float m = z[h];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) red[sp * 64 + h_lo + h0 + h] = m;
+                }
+                if (i > 0) held = h0;
             }
             bar_group();
             if (r < 32) {
@@ -398,20 +422,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         // P^T row r (bf16) -> the rope K-block (S^T(c) no longer reads it)
         uint8_t *prow = rb + 8 * kRBlock;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; c8++) {
-            const float4 m0 = *(const float4 *)(mref + h_lo + c8 * 8);
-            const float4 m1 = *(const float4 *)(mref + h_lo + c8 * 8 + 4);
-            const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-            float pv[8];
+        for (int i = 0; i < 32 / kHeld; i++) {
+            const int h0 = i == 0 ? held : 16 - held;
+            if (i > 0) load_scores(h0);
 #pragma unroll
-            for (int e = 0; e < 8; e++)
-                pv[e] = (mm[e] == -INFINITY) ? 0.f : ex2_approx(z[c8 * 8 + e] - mm[e]);
-            uint4 v;
-            v.x = pack_bf16(pv[0], pv[1]);
-            v.y = pack_bf16(pv[2], pv[3]);
-            v.z = pack_bf16(pv[4], pv[5]);
-            v.w = pack_bf16(pv[6], pv[7]);
-            *(uint4 *)(prow + tc::sw128_offset(r, (h_lo >> 3) + c8)) = v;
+            for (int c8 = 0; c8 < kHeld / 8; c8++) {
+                const int hb = h_lo + h0 + c8 * 8;
+                const float4 m0 = *(const float4 *)(mref + hb);
+                const float4 m1 = *(const float4 *)(mref + hb + 4);
+                const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++)
+                    pv[e] = (mm[e] == -INFINITY) ? 0.f : ex2_approx(z[c8 * 8 + e] - mm[e]);
+                uint4 v;
+                v.x = pack_bf16(pv[0], pv[1]);
+                v.y = pack_bf16(pv[2], pv[3]);
+                v.z = pack_bf16(pv[4], pv[5]);
+                v.w = pack_bf16(pv[6], pv[7]);
+                *(uint4 *)(prow + tc::sw128_offset(r, (hb >> 3))) = v;
+            }
+        }
+        if constexpr (kLow) {
+            tc::fence_before_sync();
+            tc::mbar_arrive(&s_empty[buf]);  // done reading S^T(c)
         }
         tc::fence_async_smem();
         tc::mbar_arrive(p_full);
@@ -476,94 +510,120 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         // ------------------------------------------------------ row loaders
         // Thread tl converts rows r_u = tl/8 + 32u (u = 0..3), 16-byte slice
         // c8 = tl%8 of each of five stages: the four 128-dim scale groups
-        // (K-blocks 2g, 2g+1) and the rope block.  Loads run one stage ahead
-        // of the conversion; the next chunk's rows are prefetched into L2.
+        // (K-blocks 2g, 2g+1) and the rope block.  Loads run two stages ahead
+        // of the conversion.
         const int tl = threadIdx.x - 6 * 32;  // 0..255
         const int c8 = tl & 7;
-        auto row_ptr = [&](int c, int r) -> const uint8_t * {
+        auto id_at = [&](int c, int r) -> int32_t {
             const int k = k0 + c * kTcRows + r;
-            int32_t id = (c < nchunks && k < k1) ? ids[k] : -1;
+            return (c < nchunks && k < k1) ? ids[k] : -1;
+        };
+        // A row is addressed by its index in 656-byte units from the pool base
+        // (below 2^32 for any pool that fits in HBM); ~0u marks a missing row.
+        auto unit_of = [&](int32_t id) -> uint32_t {
             if (id >= a.max_row) {
                 set_error(a.err, HS_ERR_INDEX_RANGE);
                 id = -1;
             }
-            if (id < 0) return nullptr;
-            const size_t blk = (size_t)(id / a.P), off = (size_t)(id % a.P);
-            return a.pool + ((blk * a.L + a.layer) * a.P + off) * 656;
+            if (id < 0) return ~0u;
+            const uint32_t blk = (uint32_t)(id / a.P), off = (uint32_t)(id % a.P);
+            return (blk * (uint32_t)a.L + (uint32_t)a.layer) * (uint32_t)a.P + off;
         };
-        auto stage_off = [&](int st) { return st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8; };
-        if (tl < kTcRows) {
-            const uint8_t *pf = row_ptr(0, tl);
-            if (pf) tc::prefetch_l2(pf, 656);
-        }
-        bool ok = true;
-        for (int c = 0; c < nchunks; c++) {
-          if (ok) {
-            const uint8_t *src[4];
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        // stage st of row unit ru: 16 bytes of slice c8 and (st < 4) its scale
+        auto ld_stage = [&](uint32_t ru, int st, uint4 &d, uint32_t &sc) {
+            if (ru == ~0u) {
+                d = z;
+                sc = 0;
+                return;
+            }
+            const uint8_t *row = a.pool + (size_t)ru * 656;
+            d = tc::ld_nc16(row + (st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8));
+            sc = st < 4 ? tc::ld_nc4(row + 512 + 4 * st) : 0u;
+        };
+        // The next chunk's row ids load while this chunk converts; its first
+        // stage is issued right after the softmax.
+        uint32_t ru[4];
+        uint4 d0[4], d1[4];
+        uint32_t f0[4], f1[4];
+        int32_t idn[4];
 #pragma unroll
-            for (int u = 0; u < 4; u++) src[u] = row_ptr(c, (tl >> 3) + 32 * u);
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            uint4 scv[4], cur[4], nxt[4];
+        for (int u = 0; u < 4; u++) idn[u] = id_at(0, (tl >> 3) + 32 * u);
+        auto issue_first = [&]() {
 #pragma unroll
             for (int u = 0; u < 4; u++) {
-                scv[u] = src[u] ? tc::ld_nc16(src[u] + 512) : z;
-                cur[u] = src[u] ? tc::ld_nc16(src[u] + stage_off(0)) : z;
+                ru[u] = unit_of(idn[u]);
+                ld_stage(ru[u], 0, d0[u], f0[u]);
             }
-            if (tl < kTcRows) {  // warm L2 with the next chunk's rows
-                const uint8_t *pf = row_ptr(c + 1, tl);
-                if (pf) tc::prefetch_l2(pf, 656);
-            }
+        };
+        issue_first();
+        bool ok = true;
+        for (int c = 0; c < nchunks; c++) {
 #pragma unroll
-            for (int st = 0; st < 5; st++) {
-                if (st + 1 < 5) {
+            for (int u = 0; u < 4; u++) idn[u] = id_at(c + 1, (tl >> 3) + 32 * u);
+            if (ok) {
 #pragma unroll
-                    for (int u = 0; u < 4; u++) nxt[u] = src[u] ? tc::ld_nc16(src[u] + stage_off(st + 1)) : z;
-                }
-                const int kb = st < 4 ? 2 * st + (c8 >> 2) : 8;
-                bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
-                if (st < 4) w &= tc::mbar_wait(&kb_empty[kb ^ 1], (c & 1) ^ 1, a.err);
-                if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
-                    ok = false;
-                    break;
-                }
-                uint8_t *dst = rb + kb * kRBlock;
+                for (int st = 0; st < 5; st++) {
+                    if (st == 0) {
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    const int r = (tl >> 3) + 32 * u;
-                    if (st < 4) {
-                        const uint32_t sb = st == 0 ? scv[u].x : st == 1 ? scv[u].y : st == 2 ? scv[u].z : scv[u].w;
-                        const float scl = __uint_as_float(sb);
-                        const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&cur[u];
-                        uint32_t packed[8];
+                        for (int u = 0; u < 4; u++) ld_stage(ru[u], 1, d1[u], f1[u]);
+                    }
+                    uint4 d2[4];  // loads run two stages ahead of the conversion
+                    uint32_t f2[4];
+                    if (st + 2 < 5) {
 #pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pp[e], __NV_E4M3);
-                            const float2 f2 = __half22float2(__half2(h2));
-                            packed[e] = pack_bf16(f2.x * scl, f2.y * scl);
+                        for (int u = 0; u < 4; u++) ld_stage(ru[u], st + 2, d2[u], f2[u]);
+                    }
+                    const int kb = st < 4 ? 2 * st + (c8 >> 2) : 8;
+                    bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
+                    if (st < 4) w &= tc::mbar_wait(&kb_empty[kb ^ 1], (c & 1) ^ 1, a.err);
+                    if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = rb + kb * kRBlock;
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const int r = (tl >> 3) + 32 * u;
+                        if (st < 4) {
+                            const float scl = __uint_as_float(f0[u]);
+                            const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&d0[u];
+                            uint32_t packed[8];
+#pragma unroll
+                            for (int e = 0; e < 8; e++) {
+                                __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pp[e], __NV_E4M3);
+                                const float2 f2v = __half22float2(__half2(h2));
+                                packed[e] = pack_bf16(f2v.x * scl, f2v.y * scl);
+                            }
+                            const int q0 = (c8 & 3) * 2;
+                            *(uint4 *)(dst + tc::sw128_offset(r, q0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            *(uint4 *)(dst + tc::sw128_offset(r, q0 + 1)) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        } else {
+                            *(uint4 *)(dst + tc::sw128_offset(r, c8)) = d0[u];
                         }
-                        const int q0 = (c8 & 3) * 2;
-                        *(uint4 *)(dst + tc::sw128_offset(r, q0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        *(uint4 *)(dst + tc::sw128_offset(r, q0 + 1)) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    } else {
-                        *(uint4 *)(dst + tc::sw128_offset(r, c8)) = cur[u];
                     }
-                }
-                tc::fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (st < 4) {
-                        tc::mbar_arrive(&kb_full[2 * st]);
-                        tc::mbar_arrive(&kb_full[2 * st + 1]);
-                    } else {
-                        tc::mbar_arrive(&kb_full[8]);
+                    tc::fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (st < 4) {
+                            tc::mbar_arrive(&kb_full[2 * st]);
+                            tc::mbar_arrive(&kb_full[2 * st + 1]);
+                        } else {
+                            tc::mbar_arrive(&kb_full[8]);
+                        }
                     }
-                }
 #pragma unroll
-                for (int u = 0; u < 4; u++) cur[u] = nxt[u];
+                    for (int u = 0; u < 4; u++) {
+                        d0[u] = d1[u];
+                        f0[u] = f1[u];
+                        d1[u] = d2[u];
+                        f1[u] = f2[u];
+                    }
+                }
             }
-          }
             // warps 6-9 also run the softmax of heads 32-63 (the group leaves together)
-            if (warp < 10 && !softmax_part(c, 32)) break;
+            if (warp < 10 && !softmax_part(c, 32, std::true_type{})) break;
+            if (ok) issue_first();  // lands before PV(c) frees the first K-blocks
         }
     } else if (warp >= 2) {
         // ---------------------------------------------- softmax + epilogue
@@ -573,7 +633,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
-            if (!softmax_part(c, 0)) {
+            if (!softmax_part(c, 0, std::false_type{})) {
                 ok = false;
                 break;
             }

@@ -66,6 +66,10 @@ bool valid_config(const hs_pool_config *c) {
     if (c->idx_fmt != HS_IDX_E4M3 && c->idx_fmt != HS_IDX_F32) return false;
     if (c->gpu_blocks < 0 || c->host_blocks < 0) return false;
     if (c->gpu_blocks > INT32_MAX || c->host_blocks > INT32_MAX) return false;
+    // device row ids are int32; the attention addresses a row by its index in
+    // row units of the pool, a uint32
+    if (c->gpu_blocks * c->page_tokens > INT32_MAX) return false;
+    if (c->gpu_blocks * c->page_tokens * c->num_mla_layers > (int64_t)UINT32_MAX) return false;
     if (c->idx_fmt == HS_IDX_E4M3 && c->idx_dim % 16 != 0) return false;
     if (c->mla_heads % 8 != 0) return false;
     const int nq = c->num_spec + 1;

@@ -150,6 +150,12 @@ __device__ __forceinline__ uint4 ld_nc16(const void *ptr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_nc4(const void *ptr) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"((uint64_t)ptr));
+    return v;
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor core / TMA reads).
 __device__ __forceinline__ void fence_async_smem() {

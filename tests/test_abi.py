@@ -68,6 +68,8 @@ def test_required_bytes_is_host_arithmetic(hs):
     dict(num_spec=3, top_k=4096),       # union too large for one CTA
     dict(idx_dim=20),                   # E4M3 keys need 16-byte rows
     dict(row_fmt=7), dict(idx_fmt=9), dict(gpu_blocks=-1),
+    dict(gpu_blocks=1 << 25),           # 2^31 device rows: ids are int32
+    dict(gpu_blocks=(1 << 24) + 1, num_mla_layers=256),  # > 2^32 row units
 ])
 def test_required_bytes_rejects_bad_configs(hs, bad):
     c = _cfg(hs, **bad)
