@@ -184,8 +184,8 @@ constexpr int kTcHeads = 64;         // heads per CTA (MMA N)
 constexpr int kKBlocks = 9;          // 576 dims / 64
 constexpr int kRBlock = kTcRows * 128;     // 16 KB: 128 rows x 64 bf16
 constexpr int kQBlock = kTcHeads * 128;    // 8 KB: 64 heads x 64 bf16
-constexpr int kLoaderWarps = 8;
-constexpr int kAttnThreads = (6 + kLoaderWarps) * 32;
+constexpr int kWorkerWarps = 12;  // warps 2-13: rows, softmax, epilogue
+constexpr int kAttnThreads = (2 + kWorkerWarps) * 32;
 constexpr float kRescaleLog2 = 8.f;  // rescale O^T when a max grows by > 2^8
 
 struct AttnTcSmem {
@@ -195,7 +195,7 @@ struct AttnTcSmem {
     static constexpr int nf = 64 * 3 + 4 * 64;                   // mref, lsum, alpha, red[4][64]
     static constexpr int ones_off = f_off + nf * 4;                // 128 x 16 bf16 ones
     static constexpr int bar_off = ones_off + 4096;
-    static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 5;
+    static constexpr int nbar = 2 * kKBlocks + 2 + 2 + 6;
     static constexpr int tslot_off = bar_off + nbar * 8;
     static constexpr int bytes = tslot_off + 16 + 1024;          // + alignment slack
 };
@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     uint64_t *mma_done = o_done + 1;
     uint64_t *peer_ready = mma_done + 1;  // split 1: split 0's row buffer is free
     uint64_t *peer_data = peer_ready + 1; // split 0: split 1's partial has arrived
+    uint64_t *q_full = peer_data + 1;     // the query blocks are in shared memory
     uint32_t *tslot = (uint32_t *)(smem + AttnTcSmem::tslot_off);
 
     const int qr = blockIdx.x, hh = blockIdx.y, split = blockIdx.z;
@@ -285,14 +286,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     const int nchunks = (k1 - k0 + kTcRows - 1) / kTcRows;
     const int32_t *ids = a.row_id + (size_t)qr * a.K;
 
-    // queries of this CTA's 64 heads -> nine K-major 128-byte-swizzled blocks
-    const __nv_bfloat16 *qsrc = a.q + ((size_t)qr * a.H + hh * kTcHeads) * kLatent;
-    for (int i = threadIdx.x; i < kTcHeads * 72; i += kAttnThreads) {
-        const int h = i / 72, c16 = i - h * 72;  // 72 chunks of 16 B per head
-        const int kb = c16 >> 3, c = c16 & 7;
-        const uint4 v = *(const uint4 *)((const uint8_t *)(qsrc + (size_t)h * kLatent) + c16 * 16);
-        *(uint4 *)(qb + kb * kQBlock + tc::sw128_offset(h, c)) = v;
-    }
     if (threadIdx.x < 64) {
         mref[threadIdx.x] = -INFINITY;
         lsum[threadIdx.x] = 0.f;
@@ -301,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         ((uint4 *)ones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKBlocks; i++) {
-            tc::mbar_init(&kb_full[i], kLoaderWarps);
+            tc::mbar_init(&kb_full[i], kWorkerWarps);
             tc::mbar_init(&kb_empty[i], 1);
         }
         for (int i = 0; i < 2; i++) {
@@ -313,6 +306,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         tc::mbar_init(mma_done, 1);
         tc::mbar_init(peer_ready, 1);
         tc::mbar_init(peer_data, 128);
+        tc::mbar_init(q_full, kWorkerWarps);
         tc::fence_barrier_init();
     }
     if (warp == 1) {
@@ -461,7 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             const uint32_t ones_addr = tc::smem_addr(ones);
             const uint32_t r_addr = tc::smem_addr(rb), q_addr = tc::smem_addr(qb);
             const uint32_t p_addr = r_addr + 8 * kRBlock;
-            bool ok = true;
+            bool ok = nchunks == 0 || tc::mbar_wait(q_full, 0, a.err);
             for (int c = 0; c < nchunks && ok; c++) {
                 const int buf = c & 1;
                 const uint32_t ph = c & 1;
@@ -506,20 +500,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, a.err);
         }
-    } else if (warp >= 6) {
-        // ------------------------------------------------------ row loaders
-        // Thread tl converts rows r_u = tl/8 + 32u (u = 0..3), 16-byte slice
-        // c8 = tl%8 of each of five stages: the four 128-dim scale groups
-        // (K-blocks 2g, 2g+1) and the rope block.  Loads run two stages ahead
-        // of the conversion.
-        const int tl = threadIdx.x - 6 * 32;  // 0..255
-        const int c8 = tl & 7;
+    } else if (warp >= 2) {
+        // ------------------------------------------------------- row workers
+        // Twelve warps convert each chunk.  A stage is one 128-dim scale group
+        // (K-blocks 2g and 2g+1) or the rope block; its 1024 (row, 16-byte
+        // slice) units go to worker wi as units wi + 384u: slice c8 = wi % 8 of
+        // rows wi/8 + 48u (u = 0, 1, and 2 for wi < 256).  Loads run two
+        // stages ahead of the conversion.  Warps 2-9 also run the softmax
+        // (heads 0-31 on warps 2-5, 32-63 on warps 6-9) and warps 2-5 the
+        // epilogue.
+        const int wi = threadIdx.x - 64;  // 0..383
+        const int c8 = wi & 7;
+        const int nu = wi < 256 ? 3 : 2;
         auto id_at = [&](int c, int r) -> int32_t {
             const int k = k0 + c * kTcRows + r;
             return (c < nchunks && k < k1) ? ids[k] : -1;
         };
         // A row is addressed by its index in 656-byte units from the pool base
-        // (below 2^32 for any pool that fits in HBM); ~0u marks a missing row.
+        // (below 2^32, which pool creation checks); ~0u marks a missing row.
         auto unit_of = [&](int32_t id) -> uint32_t {
             if (id >= a.max_row) {
                 set_error(a.err, HS_ERR_INDEX_RANGE);
@@ -541,38 +539,55 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             d = tc::ld_nc16(row + (st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8));
             sc = st < 4 ? tc::ld_nc4(row + 512 + 4 * st) : 0u;
         };
-        // The next chunk's row ids load while this chunk converts; its first
-        // stage is issued right after the softmax.
-        uint32_t ru[4];
-        uint4 d0[4], d1[4];
-        uint32_t f0[4], f1[4];
-        int32_t idn[4];
+        uint32_t ru[3];
+        uint4 d0[3], d1[3];
+        uint32_t f0[3], f1[3];
+        int32_t idn[3];  // the next chunk's row ids load while this chunk converts
 #pragma unroll
-        for (int u = 0; u < 4; u++) idn[u] = id_at(0, (tl >> 3) + 32 * u);
-        auto issue_first = [&]() {
+        for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(0, (wi >> 3) + 48 * u) : -1;
+        auto issue_first = [&]() {  // row units and stage 0 of the chunk in idn
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
+            for (int u = 0; u < 3; u++) {
                 ru[u] = unit_of(idn[u]);
                 ld_stage(ru[u], 0, d0[u], f0[u]);
             }
         };
-        issue_first();
+        {
+            // this CTA's 64 query heads -> nine K-major 128-byte-swizzled
+            // blocks, staged while the first rows are in flight
+            const uint8_t *qsrc = (const uint8_t *)(a.q + ((size_t)qr * a.H + hh * kTcHeads) * kLatent);
+            uint4 qv[12];
+#pragma unroll
+            for (int j = 0; j < 12; j++) {  // 64 heads x 72 slices of 16 B
+                const int i = wi + 384 * j, h = i / 72, c16 = i - h * 72;
+                qv[j] = tc::ld_nc16(qsrc + (size_t)h * (kLatent * 2) + c16 * 16);
+            }
+            issue_first();
+#pragma unroll
+            for (int j = 0; j < 12; j++) {
+                const int i = wi + 384 * j, h = i / 72, c16 = i - h * 72;
+                *(uint4 *)(qb + (c16 >> 3) * kQBlock + tc::sw128_offset(h, c16 & 7)) = qv[j];
+            }
+            tc::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(q_full);
+        }
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
 #pragma unroll
-            for (int u = 0; u < 4; u++) idn[u] = id_at(c + 1, (tl >> 3) + 32 * u);
+            for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(c + 1, (wi >> 3) + 48 * u) : -1;
             if (ok) {
 #pragma unroll
                 for (int st = 0; st < 5; st++) {
                     if (st == 0) {
 #pragma unroll
-                        for (int u = 0; u < 4; u++) ld_stage(ru[u], 1, d1[u], f1[u]);
+                        for (int u = 0; u < 3; u++) ld_stage(ru[u], 1, d1[u], f1[u]);
                     }
-                    uint4 d2[4];  // loads run two stages ahead of the conversion
-                    uint32_t f2[4];
+                    uint4 d2[3];
+                    uint32_t f2[3];
                     if (st + 2 < 5) {
 #pragma unroll
-                        for (int u = 0; u < 4; u++) ld_stage(ru[u], st + 2, d2[u], f2[u]);
+                        for (int u = 0; u < 3; u++) ld_stage(ru[u], st + 2, d2[u], f2[u]);
                     }
                     const int kb = st < 4 ? 2 * st + (c8 >> 2) : 8;
                     bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
@@ -583,8 +598,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     }
                     uint8_t *dst = rb + kb * kRBlock;
 #pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const int r = (tl >> 3) + 32 * u;
+                    for (int u = 0; u < 3; u++) {
+                        if (u >= nu) continue;
+                        const int r = (wi >> 3) + 48 * u;
                         if (st < 4) {
                             const float scl = __uint_as_float(f0[u]);
                             const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&d0[u];
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                         }
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; u++) {
+                    for (int u = 0; u < 3; u++) {
                         d0[u] = d1[u];
                         f0[u] = f1[u];
                         d1[u] = d2[u];
@@ -621,150 +637,145 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     }
                 }
             }
-            // warps 6-9 also run the softmax of heads 32-63 (the group leaves together)
-            if (warp < 10 && !softmax_part(c, 32, std::true_type{})) break;
-            if (ok) issue_first();  // lands before PV(c) frees the first K-blocks
-        }
-    } else if (warp >= 2) {
-        // ---------------------------------------------- softmax + epilogue
-        // Thread = chunk row = TMEM lane.
-        const int sp = warp & 3;
-        const int r = sp * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
-        bool ok = true;
-        for (int c = 0; c < nchunks; c++) {
-            if (!softmax_part(c, 0, std::false_type{})) {
+            // the softmax groups leave together when a wait ran out
+            if (warp < 10 && !softmax_part(c, warp < 6 ? 0 : 32, std::true_type{})) {
                 ok = false;
                 break;
             }
+            if (ok) issue_first();  // lands before PV(c) frees the first K-blocks
         }
-        // ---- epilogue
-        const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
-        const bool good = !bar_or_softmax(!fin);
-        if (good) {
-            tc::fence_after_sync();
-            // every lane holds the same denominators: stage them in smem
-            if (sp == 0) {
+        if (warp < 6) {  // epilogue: thread = output dim row = TMEM lane
+            const int sp = warp & 3;
+            const int r = sp * 32 + lane;
+            const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+            // ---- epilogue
+            const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
+            const bool good = !bar_or_softmax(!fin);
+            if (good) {
+                tc::fence_after_sync();
+                // every lane holds the same denominators: stage them in smem
+                if (sp == 0) {
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float lv[16];
-                    tc::tmem_ld16(lane_base + l_col + 16 * q, lv);
-                    tc::tmem_ld_wait();
-                    if (lane == 0) {
+                    for (int q = 0; q < 4; q++) {
+                        float lv[16];
+                        tc::tmem_ld16(lane_base + l_col + 16 * q, lv);
+                        tc::tmem_ld_wait();
+                        if (lane == 0) {
 #pragma unroll
-                        for (int i = 0; i < 16; i++) lsum[16 * q + i] = lv[i];
-                    }
-                }
-            }
-            bar_softmax();
-        }
-        const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
-        if (a.cluster) {
-            // ---- two splits in one cluster: split 1 hands (O^T, max, sum) to
-            // split 0 through distributed shared memory; split 0 merges.
-            // Received layout in split 0's row buffer: O [4][128][68] fp32, then
-            // max[64], sum[64].
-            float *rx = (float *)rb;
-            float *rx_m = rx + 4 * 128 * 68;
-            float *rx_l = rx_m + 64;
-            if (split == 1) {
-                const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
-                if (!bar_or_softmax(!w1)) {
-                    const uint32_t dst = tc::mapa(tc::smem_addr(rx), 0);
-                    for (int g = 0; g < 4; g++) {
-#pragma unroll
-                        for (int h0 = 0; h0 < 64; h0 += 16) {
-                            float ov[16];
-                            if (good) {
-                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                tc::tmem_ld_wait();
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                            }
-                            const uint32_t at = dst + (uint32_t)(((g * 128 + r) * 68 + h0) * 4);
-#pragma unroll
-                            for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
-                        }
-                    }
-                    if (r < 64) {
-                        const float l = good ? lsum[r] : 0.f;
-                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), 0), l > 0.f ? mref[r] : -INFINITY);
-                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), 0), l);
-                    }
-                }
-                // every thread's writes are ordered before its own arrival
-                tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), 0));
-            } else {
-                // the row buffer is idle once every MMA completed: let split 1 write
-                if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), 1));
-                const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
-                if (!bar_or_softmax(!w0)) {
-                    float *wf = red;  // [0,64): weight of split 0, [64,128): split 1, [128,192): 1/L
-                    if (r < 64) {
-                        const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
-                        const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
-                        const float M = fmaxf(m0, m1);
-                        const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
-                        const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
-                        const float Ls = l0 * w0v + l1 * w1v;
-                        wf[r] = w0v;
-                        wf[64 + r] = w1v;
-                        wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
-                        if (a.lse) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-                    }
-                    bar_softmax();
-                    for (int g = 0; g < 4; g++) {
-                        const int d = g * 128 + r;
-#pragma unroll
-                        for (int h0 = 0; h0 < 64; h0 += 16) {
-                            float ov[16];
-                            if (good) {
-                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                tc::tmem_ld_wait();
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                            }
-                            const float *pv = rx + (g * 128 + r) * 68 + h0;
-#pragma unroll
-                            for (int i = 0; i < 16; i++) {
-                                const int h = h0 + i;
-                                const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
-                                a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
-                            }
+                            for (int i = 0; i < 16; i++) lsum[16 * q + i] = lv[i];
                         }
                     }
                 }
+                bar_softmax();
             }
-        } else if (good) {
-            for (int g = 0; g < 4; g++) {
-                const int d = g * 128 + r;
+            const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
+            if (a.cluster) {
+                // ---- two splits in one cluster: split 1 hands (O^T, max, sum) to
+                // split 0 through distributed shared memory; split 0 merges.
+                // Received layout in split 0's row buffer: O [4][128][68] fp32, then
+                // max[64], sum[64].
+                float *rx = (float *)rb;
+                float *rx_m = rx + 4 * 128 * 68;
+                float *rx_l = rx_m + 64;
+                if (split == 1) {
+                    const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
+                    if (!bar_or_softmax(!w1)) {
+                        const uint32_t dst = tc::mapa(tc::smem_addr(rx), 0);
+                        for (int g = 0; g < 4; g++) {
 #pragma unroll
-                for (int h0 = 0; h0 < 64; h0 += 16) {
-                    float ov[16];
-                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                    tc::tmem_ld_wait();
+                            for (int h0 = 0; h0 < 64; h0 += 16) {
+                                float ov[16];
+                                if (good) {
+                                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                    tc::tmem_ld_wait();
+                                } else {
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int h = h0 + i;
-                        if (a.splits == 1) {
-                            const float l = lsum[h];
-                            a.out[(g0 + h) * kNope + d] = __float2bfloat16(l > 0.f ? ov[i] / l : 0.f);
-                        } else {
-                            a.part[((g0 + h) * a.splits + split) * (kNope + 2) + d] = ov[i];
+                                    for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                                }
+                                const uint32_t at = dst + (uint32_t)(((g * 128 + r) * 68 + h0) * 4);
+#pragma unroll
+                                for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+                            }
+                        }
+                        if (r < 64) {
+                            const float l = good ? lsum[r] : 0.f;
+                            tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), 0), l > 0.f ? mref[r] : -INFINITY);
+                            tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), 0), l);
                         }
                     }
-                }
-            }
-            if (r < 64) {
-                const float l = lsum[r], m = mref[r];
-                if (a.splits == 1) {
-                    if (a.lse) a.lse[g0 + r] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    // every thread's writes are ordered before its own arrival
+                    tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), 0));
                 } else {
-                    float *pp = a.part + ((g0 + r) * a.splits + split) * (kNope + 2);
-                    pp[kNope] = l > 0.f ? m : -INFINITY;
-                    pp[kNope + 1] = l;
+                    // the row buffer is idle once every MMA completed: let split 1 write
+                    if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), 1));
+                    const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
+                    if (!bar_or_softmax(!w0)) {
+                        float *wf = red;  // [0,64): weight of split 0, [64,128): split 1, [128,192): 1/L
+                        if (r < 64) {
+                            const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
+                            const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
+                            const float M = fmaxf(m0, m1);
+                            const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+                            const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+                            const float Ls = l0 * w0v + l1 * w1v;
+                            wf[r] = w0v;
+                            wf[64 + r] = w1v;
+                            wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+                            if (a.lse) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+                        }
+                        bar_softmax();
+                        for (int g = 0; g < 4; g++) {
+                            const int d = g * 128 + r;
+#pragma unroll
+                            for (int h0 = 0; h0 < 64; h0 += 16) {
+                                float ov[16];
+                                if (good) {
+                                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                    tc::tmem_ld_wait();
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                                }
+                                const float *pv = rx + (g * 128 + r) * 68 + h0;
+#pragma unroll
+                                for (int i = 0; i < 16; i++) {
+                                    const int h = h0 + i;
+                                    const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
+                                    a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else if (good) {
+                for (int g = 0; g < 4; g++) {
+                    const int d = g * 128 + r;
+#pragma unroll
+                    for (int h0 = 0; h0 < 64; h0 += 16) {
+                        float ov[16];
+                        tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {
+                            const int h = h0 + i;
+                            if (a.splits == 1) {
+                                const float l = lsum[h];
+                                a.out[(g0 + h) * kNope + d] = __float2bfloat16(l > 0.f ? ov[i] / l : 0.f);
+                            } else {
+                                a.part[((g0 + h) * a.splits + split) * (kNope + 2) + d] = ov[i];
+                            }
+                        }
+                    }
+                }
+                if (r < 64) {
+                    const float l = lsum[r], m = mref[r];
+                    if (a.splits == 1) {
+                        if (a.lse) a.lse[g0 + r] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    } else {
+                        float *pp = a.part + ((g0 + r) * a.splits + split) * (kNope + 2);
+                        pp[kNope] = l > 0.f ? m : -INFINITY;
+                        pp[kNope + 1] = l;
+                    }
                 }
             }
         }
