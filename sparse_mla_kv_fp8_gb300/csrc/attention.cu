@@ -628,6 +628,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                             tc::mbar_arrive(&kb_full[8]);
                         }
                     }
+                    if (st == 4 && c8 == 0) {
+                        // warm L2 with the next chunk's rows (their ids have
+                        // arrived by now), so that its loads hit L2
+#pragma unroll
+                        for (int u = 0; u < 3; u++)
+                            if (idn[u] >= 0 && idn[u] < a.max_row)
+                                tc::prefetch_l2(a.pool + (size_t)unit_of(idn[u]) * 656, 656);
+                    }
 #pragma unroll
                     for (int u = 0; u < 3; u++) {
                         d0[u] = d1[u];
