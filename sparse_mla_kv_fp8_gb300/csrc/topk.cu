@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "hs_internal.h"
+#include "tc.cuh"
 
 namespace hs {
 namespace {
@@ -243,13 +244,223 @@ __global__ void __launch_bounds__(kThreads) topk_write_kernel(const float *__res
     }
 }
 
+// ---------------------------------------------------------------------------
+// One-launch top-K for rows of up to 8 x 1024 x 32 tokens.  A row is owned by
+// a cluster of G CTAs (1024 threads each); thread t of CTA g holds the keys of
+// tokens g*1024*E + t*E + [0, E) in registers, so the scores are read once.
+// The same three radix passes run on those registers: each CTA builds its
+// shared-memory histogram, the cluster barrier publishes it, and every CTA
+// sums the G histograms over distributed shared memory and takes the same
+// decision.  Selected indices are then written in ascending order from
+// block scans plus the totals of the lower-ranked CTAs.  All counts are
+// integers: the result equals the multi-kernel path's bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterMax = 8;
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kClusterThreads, 1)
+topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
+                    const int32_t *seq_len, int nq, int K, int32_t *topk) {
+    __shared__ uint32_t hist[2][kTopkBins];
+    __shared__ int warp_sums[32];
+    __shared__ uint32_t decided[3];  // prefix, mask, need of the next pass
+    __shared__ int totals[2];        // this CTA's keys above / equal to T
+    const int G = gridDim.x, g = (int)cta_rank(), row = blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int b = row / nq, j = row - b * nq;
+    const int vis = max(0, seq_len[b] - nq + j + 1);
+    const bool take_all = vis <= K;
+    const int64_t base = ((int64_t)g * kClusterThreads + tid) * E;
+    const float *src = scores + (size_t)row * stride;
+
+    uint32_t key[E];
+    uint32_t valid = 0;  // bit e: token base + e is visible
+#pragma unroll
+    for (int e = 0; e < E; e += 4) {
+        const int64_t t = base + e;
+        if (vec4 && t + 3 < vis) {
+            const float4 f = *(const float4 *)(src + t);
+            key[e] = order_key(f.x);
+            key[e + 1] = order_key(f.y);
+            key[e + 2] = order_key(f.z);
+            key[e + 3] = order_key(f.w);
+            valid |= 0xFu << e;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                key[e + i] = 0;
+                if (t + i < vis) {
+                    key[e + i] = order_key(src[t + i]);
+                    valid |= 1u << (e + i);
+                }
+            }
+        }
+    }
+
+    uint32_t prefix = 0, mask = 0, need = take_all ? 0u : (uint32_t)K;
+    if (!take_all) {  // uniform over the cluster: every CTA of the row sees vis
+#pragma unroll 1
+        for (int pass = 0; pass < 3; pass++) {
+            const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const int nbins = pass == 2 ? 1024 : 2048;
+            uint32_t *h = hist[pass & 1];
+            for (int i = tid; i < nbins; i += kClusterThreads) h[i] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < E; e++) {
+                const bool in = ((valid >> e) & 1u) && (key[e] & mask) == prefix;
+                const uint32_t bin = in ? (key[e] >> shift) & (uint32_t)(nbins - 1) : 0xFFFFFFFFu;
+                const uint32_t same = __match_any_sync(0xffffffffu, bin);
+                if (in && lane == __ffs(same) - 1) atomicAdd(&h[bin], (uint32_t)__popc(same));
+            }
+            // every CTA's histogram is complete and visible to the cluster
+            tc::cluster_sync();
+            // thread i: bins at descending positions 2i, 2i+1, summed over the cluster
+            uint32_t c0 = 0, c1 = 0;
+            const int p0 = 2 * tid, p1 = 2 * tid + 1;
+            const uint32_t a0 = tc::smem_addr(&h[nbins - 1 - min(p0, nbins - 1)]);
+            const uint32_t a1 = tc::smem_addr(&h[nbins - 1 - min(p1, nbins - 1)]);
+            for (int r = 0; r < G; r++) {
+                if (p0 < nbins) c0 += ld_cluster_u32(tc::mapa(a0, (uint32_t)r));
+                if (p1 < nbins) c1 += ld_cluster_u32(tc::mapa(a1, (uint32_t)r));
+            }
+            const int incl = block_incl_scan((int)(c0 + c1), warp_sums);
+            const int above0 = incl - (int)(c0 + c1);
+            const int nd = (int)need;
+            int found_pos = -1, found_above = 0;
+            if (p0 < nbins && above0 < nd && nd <= above0 + (int)c0) {
+                found_pos = p0;
+                found_above = above0;
+            } else if (p1 < nbins && above0 + (int)c0 < nd && nd <= above0 + (int)(c0 + c1)) {
+                found_pos = p1;
+                found_above = above0 + (int)c0;
+            }
+            if (found_pos >= 0) {
+                const uint32_t bin = (uint32_t)(nbins - 1 - found_pos);
+                decided[0] = prefix | (bin << shift);
+                decided[1] = mask | ((uint32_t)(nbins - 1) << shift);
+                decided[2] = (uint32_t)(nd - found_above);
+            }
+            __syncthreads();
+            prefix = decided[0];
+            mask = decided[1];
+            need = decided[2];
+            // (the next pass writes the other histogram buffer; this one is
+            // rewritten two passes later, after every CTA has passed the
+            // next cluster barrier and so finished reading it)
+        }
+    }
+
+    // keys above / equal to the threshold T = prefix, in token order
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if ((valid >> e) & 1u) {
+            gt += take_all || key[e] > prefix;
+            eq += !take_all && key[e] == prefix;
+        }
+    }
+    const int v = (eq << 16) | gt;  // at most 1024 * 32 of each
+    const int incl = block_incl_scan(v, warp_sums);
+    if (tid == kClusterThreads - 1) {
+        totals[0] = incl & 0xFFFF;
+        totals[1] = incl >> 16;
+    }
+    tc::cluster_sync();
+    int bg = 0, be = 0, tg = 0, te = 0;
+    for (int r = 0; r < G; r++) {
+        const int cg = (int)ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[0]), (uint32_t)r));
+        const int ce = (int)ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[1]), (uint32_t)r));
+        tg += cg;
+        te += ce;
+        if (r < g) {
+            bg += cg;
+            be += ce;
+        }
+    }
+    const int excl = incl - v;
+    bg += excl & 0xFFFF;
+    be += excl >> 16;
+    int32_t *out = topk + (size_t)row * K;
+    const int nd = (int)need;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if (!((valid >> e) & 1u)) continue;
+        if (take_all || key[e] > prefix) {
+            out[bg + min(be, nd)] = (int32_t)(base + e);
+            bg++;
+        } else if (key[e] == prefix) {
+            if (be < nd) out[bg + be] = (int32_t)(base + e);
+            be++;
+        }
+    }
+    if (g == 0) {
+        const int taken = tg + min(te, nd);
+        for (int i = taken + tid; i < K; i += kClusterThreads) out[i] = -1;
+    }
+    tc::cluster_sync();  // peers may still be reading this CTA's totals
+}
+
+// Elements per thread for the one-launch path, or 0 when rows are too long.
+// Prefers the widest cluster that keeps every row's CTAs in one wave.
+int cluster_elems(int max_tokens, int rows) {
+    int best = 0;
+    for (int e : {8, 16, 32}) {
+        const int G = (max_tokens + kClusterThreads * e - 1) / (kClusterThreads * e);
+        if (G > kClusterMax) continue;
+        if (best == 0) best = e;
+        if ((int64_t)rows * G <= kNumSMs) return e;
+    }
+    return best;
+}
+
 }  // namespace
 
-int topk_kernel_count(const hs_pool *, int, int) { return 6; }
+int topk_kernel_count(const hs_pool *p, int B, int nq) {
+    return cluster_elems(p->cfg.max_tokens, B * nq) ? 1 : 6;
+}
 
 cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, int B, int nq,
                         int32_t *topk, cudaStream_t st) {
     const int rows = B * nq, nch = p->topk_nchunks, K = p->cfg.top_k;
+    const int E = cluster_elems(p->cfg.max_tokens, rows);
+    if (E) {
+        const int G = (p->cfg.max_tokens + kClusterThreads * E - 1) / (kClusterThreads * E);
+        cudaLaunchConfig_t lc = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)G;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        lc.gridDim = dim3((unsigned)G, (unsigned)rows);
+        lc.blockDim = dim3(kClusterThreads);
+        lc.dynamicSmemBytes = 0;
+        lc.stream = st;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
+        if (E == 8)
+            return cudaLaunchKernelEx(&lc, topk_cluster_kernel<8>, scores, stride, vec4,
+                                      (const int32_t *)p->d.seq_len, nq, K, topk);
+        if (E == 16)
+            return cudaLaunchKernelEx(&lc, topk_cluster_kernel<16>, scores, stride, vec4,
+                                      (const int32_t *)p->d.seq_len, nq, K, topk);
+        return cudaLaunchKernelEx(&lc, topk_cluster_kernel<32>, scores, stride, vec4,
+                                  (const int32_t *)p->d.seq_len, nq, K, topk);
+    }
     topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K);
     dim3 grid(nch, rows);
     for (int pass = 0; pass < 3; pass++)
