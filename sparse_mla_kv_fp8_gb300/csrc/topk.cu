@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kThreads) topk_write_kernel(const float *__res
 // ---------------------------------------------------------------------------
 constexpr int kClusterThreads = 1024;
 constexpr int kClusterMax = 8;
+constexpr int kClusterSmem = (8 + 2) * kTopkBins * 4;  // histogram copies + merged pair
 
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
     uint32_t v;
@@ -270,22 +271,37 @@ __device__ __forceinline__ uint32_t cta_rank() {
     return r;
 }
 
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+constexpr int kHistCopies = 8;  // per-warp-group histograms: fewer colliding atomics
+
 template <int E>
 __global__ void __launch_bounds__(kClusterThreads, 1)
 topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
                     const int32_t *seq_len, int nq, int K, int32_t *topk) {
-    __shared__ uint32_t hist[2][kTopkBins];
+    extern __shared__ __align__(16) uint32_t tk_smem[];
+    uint32_t *copies = tk_smem;                            // [kHistCopies][2048]
+    uint32_t *merged = tk_smem + kHistCopies * kTopkBins;  // [2][2048], read by the cluster
     __shared__ int warp_sums[32];
     __shared__ uint32_t decided[3];  // prefix, mask, need of the next pass
     __shared__ int totals[2];        // this CTA's keys above / equal to T
     const int G = gridDim.x, g = (int)cta_rank(), row = blockIdx.y, tid = threadIdx.x;
-    const int lane = tid & 31;
     const int b = row / nq, j = row - b * nq;
     const int vis = max(0, seq_len[b] - nq + j + 1);
     const bool take_all = vis <= K;
     const int64_t base = ((int64_t)g * kClusterThreads + tid) * E;
     const float *src = scores + (size_t)row * stride;
 
+    // the histogram copies start zeroed (each merge below re-zeroes them)
+    for (int i = tid; i < kHistCopies * kTopkBins / 4; i += kClusterThreads)
+        ((uint4 *)copies)[i] = make_uint4(0, 0, 0, 0);
     uint32_t key[E];
     uint32_t valid = 0;  // bit e: token base + e is visible
 #pragma unroll
@@ -312,53 +328,70 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
 
     uint32_t prefix = 0, mask = 0, need = take_all ? 0u : (uint32_t)K;
     if (!take_all) {  // uniform over the cluster: every CTA of the row sees vis
+        uint32_t *mine = copies + (threadIdx.x >> 5) % kHistCopies * kTopkBins;
 #pragma unroll 1
         for (int pass = 0; pass < 3; pass++) {
             const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
             const int nbins = pass == 2 ? 1024 : 2048;
-            uint32_t *h = hist[pass & 1];
-            for (int i = tid; i < nbins; i += kClusterThreads) h[i] = 0;
             __syncthreads();
 #pragma unroll
             for (int e = 0; e < E; e++) {
-                const bool in = ((valid >> e) & 1u) && (key[e] & mask) == prefix;
-                const uint32_t bin = in ? (key[e] >> shift) & (uint32_t)(nbins - 1) : 0xFFFFFFFFu;
-                const uint32_t same = __match_any_sync(0xffffffffu, bin);
-                if (in && lane == __ffs(same) - 1) atomicAdd(&h[bin], (uint32_t)__popc(same));
+                if (((valid >> e) & 1u) && (key[e] & mask) == prefix)
+                    atomicAdd(&mine[(key[e] >> shift) & (uint32_t)(nbins - 1)], 1u);
+            }
+            __syncthreads();
+            // this CTA's histogram: the copies summed
+            uint32_t *h = merged + (pass & 1) * kTopkBins;
+            for (int i = tid; i < nbins; i += kClusterThreads) {
+                uint32_t c = 0;
+#pragma unroll
+                for (int k = 0; k < kHistCopies; k++) {
+                    c += copies[k * kTopkBins + i];
+                    copies[k * kTopkBins + i] = 0;  // ready for the next pass
+                }
+                h[i] = c;
             }
             // every CTA's histogram is complete and visible to the cluster
             tc::cluster_sync();
-            // thread i: bins at descending positions 2i, 2i+1, summed over the cluster
-            uint32_t c0 = 0, c1 = 0;
-            const int p0 = 2 * tid, p1 = 2 * tid + 1;
-            const uint32_t a0 = tc::smem_addr(&h[nbins - 1 - min(p0, nbins - 1)]);
-            const uint32_t a1 = tc::smem_addr(&h[nbins - 1 - min(p1, nbins - 1)]);
-            for (int r = 0; r < G; r++) {
-                if (p0 < nbins) c0 += ld_cluster_u32(tc::mapa(a0, (uint32_t)r));
-                if (p1 < nbins) c1 += ld_cluster_u32(tc::mapa(a1, (uint32_t)r));
+            // thread t: descending positions 4t .. 4t+3 (bins nbins-1-4t ...),
+            // summed over the cluster with one 16-byte load per CTA
+            uint32_t c4[4] = {0u, 0u, 0u, 0u};
+            const bool mine4 = 4 * tid < nbins;
+            if (mine4) {
+                const uint32_t at = tc::smem_addr(&h[nbins - 4 - 4 * tid]);
+                uint4 v[kClusterMax];
+#pragma unroll
+                for (int r = 0; r < kClusterMax; r++)
+                    v[r] = r < G ? ld_cluster_v4(tc::mapa(at, (uint32_t)r)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int r = 0; r < kClusterMax; r++) {
+                    c4[0] += v[r].w;  // descending: bin nbins-1-4t first
+                    c4[1] += v[r].z;
+                    c4[2] += v[r].y;
+                    c4[3] += v[r].x;
+                }
             }
-            const int incl = block_incl_scan((int)(c0 + c1), warp_sums);
-            const int above0 = incl - (int)(c0 + c1);
+            const int sum4 = (int)(c4[0] + c4[1] + c4[2] + c4[3]);
+            const int incl = block_incl_scan(sum4, warp_sums);
+            int above = incl - sum4;
             const int nd = (int)need;
-            int found_pos = -1, found_above = 0;
-            if (p0 < nbins && above0 < nd && nd <= above0 + (int)c0) {
-                found_pos = p0;
-                found_above = above0;
-            } else if (p1 < nbins && above0 + (int)c0 < nd && nd <= above0 + (int)(c0 + c1)) {
-                found_pos = p1;
-                found_above = above0 + (int)c0;
-            }
-            if (found_pos >= 0) {
-                const uint32_t bin = (uint32_t)(nbins - 1 - found_pos);
-                decided[0] = prefix | (bin << shift);
-                decided[1] = mask | ((uint32_t)(nbins - 1) << shift);
-                decided[2] = (uint32_t)(nd - found_above);
+            if (mine4) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    if (above < nd && nd <= above + (int)c4[q]) {
+                        const uint32_t bin = (uint32_t)(nbins - 1 - (4 * tid + q));
+                        decided[0] = prefix | (bin << shift);
+                        decided[1] = mask | ((uint32_t)(nbins - 1) << shift);
+                        decided[2] = (uint32_t)(nd - above);
+                    }
+                    above += (int)c4[q];
+                }
             }
             __syncthreads();
             prefix = decided[0];
             mask = decided[1];
             need = decided[2];
-            // (the next pass writes the other histogram buffer; this one is
+            // (the next pass writes the other merged buffer; this one is
             // rewritten two passes later, after every CTA has passed the
             // next cluster barrier and so finished reading it)
         }
@@ -381,14 +414,19 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
     }
     tc::cluster_sync();
     int bg = 0, be = 0, tg = 0, te = 0;
-    for (int r = 0; r < G; r++) {
-        const int cg = (int)ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[0]), (uint32_t)r));
-        const int ce = (int)ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[1]), (uint32_t)r));
-        tg += cg;
-        te += ce;
+    uint32_t tv[2 * kClusterMax];
+#pragma unroll
+    for (int r = 0; r < kClusterMax; r++) {
+        tv[2 * r] = r < G ? ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[0]), (uint32_t)r)) : 0u;
+        tv[2 * r + 1] = r < G ? ld_cluster_u32(tc::mapa(tc::smem_addr(&totals[1]), (uint32_t)r)) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kClusterMax; r++) {
+        tg += (int)tv[2 * r];
+        te += (int)tv[2 * r + 1];
         if (r < g) {
-            bg += cg;
-            be += ce;
+            bg += (int)tv[2 * r];
+            be += (int)tv[2 * r + 1];
         }
     }
     const int excl = incl - v;
@@ -429,6 +467,18 @@ int cluster_elems(int max_tokens, int rows) {
 
 }  // namespace
 
+cudaError_t topk_setup(const hs_pool *) {
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kClusterSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kClusterSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk_cluster_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kClusterSmem);
+    return e;
+}
+
 int topk_kernel_count(const hs_pool *p, int B, int nq) {
     return cluster_elems(p->cfg.max_tokens, B * nq) ? 1 : 6;
 }
@@ -447,7 +497,7 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
         at[0].val.clusterDim.z = 1;
         lc.gridDim = dim3((unsigned)G, (unsigned)rows);
         lc.blockDim = dim3(kClusterThreads);
-        lc.dynamicSmemBytes = 0;
+        lc.dynamicSmemBytes = kClusterSmem;
         lc.stream = st;
         lc.attrs = at;
         lc.numAttrs = 1;
