@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     uint64_t *p_full = s_empty + 2;
     uint64_t *o_done = p_full + 1;
     uint64_t *mma_done = o_done + 1;
-    uint64_t *peer_ready = mma_done + 1;  // split 1: split 0's row buffer is free
-    uint64_t *peer_data = peer_ready + 1; // split 0: split 1's partial has arrived
+    uint64_t *peer_ready = mma_done + 1;  // the peer split's row buffer is free
+    uint64_t *peer_data = peer_ready + 1; // the peer split's partial has arrived
     uint64_t *q_full = peer_data + 1;     // the query blocks are in shared memory
     uint32_t *tslot = (uint32_t *)(smem + AttnTcSmem::tslot_off);
 
@@ -678,79 +678,80 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             }
             const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
             if (a.cluster) {
-                // ---- two splits in one cluster: split 1 hands (O^T, max, sum) to
-                // split 0 through distributed shared memory; split 0 merges.
-                // Received layout in split 0's row buffer: O [4][128][68] fp32, then
-                // max[64], sum[64].
+                // ---- two splits in one cluster merge symmetrically: split s
+                // finishes output dims [256 s, 256 s + 256) (O^T tiles 2s, 2s+1).
+                // Each hands the peer its other two tiles and its (max, sum)
+                // through distributed shared memory.  Received layout in the
+                // row buffer: O [2][128][68] fp32, then max[64], sum[64].
+                const uint32_t peer = 1u - (uint32_t)split;
                 float *rx = (float *)rb;
-                float *rx_m = rx + 4 * 128 * 68;
+                float *rx_m = rx + 2 * 128 * 68;
                 float *rx_l = rx_m + 64;
-                if (split == 1) {
-                    const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
-                    if (!bar_or_softmax(!w1)) {
-                        const uint32_t dst = tc::mapa(tc::smem_addr(rx), 0);
-                        for (int g = 0; g < 4; g++) {
+                // this CTA's row buffer is idle once every MMA completed
+                if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), peer));
+                const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
+                if (!bar_or_softmax(!w1)) {
+                    const uint32_t dst = tc::mapa(tc::smem_addr(rx), peer);
+                    for (int gi = 0; gi < 2; gi++) {
+                        const int g = 2 * (int)peer + gi;
 #pragma unroll
-                            for (int h0 = 0; h0 < 64; h0 += 16) {
-                                float ov[16];
-                                if (good) {
-                                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                    tc::tmem_ld_wait();
-                                } else {
+                        for (int h0 = 0; h0 < 64; h0 += 16) {
+                            float ov[16];
+                            if (good) {
+                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                tc::tmem_ld_wait();
+                            } else {
 #pragma unroll
-                                    for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                                }
-                                const uint32_t at = dst + (uint32_t)(((g * 128 + r) * 68 + h0) * 4);
-#pragma unroll
-                                for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
                             }
-                        }
-                        if (r < 64) {
-                            const float l = good ? lsum[r] : 0.f;
-                            tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), 0), l > 0.f ? mref[r] : -INFINITY);
-                            tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), 0), l);
+                            const uint32_t at = dst + (uint32_t)(((gi * 128 + r) * 68 + h0) * 4);
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
                         }
                     }
-                    // every thread's writes are ordered before its own arrival
-                    tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), 0));
-                } else {
-                    // the row buffer is idle once every MMA completed: let split 1 write
-                    if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), 1));
-                    const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
-                    if (!bar_or_softmax(!w0)) {
-                        float *wf = red;  // [0,64): weight of split 0, [64,128): split 1, [128,192): 1/L
-                        if (r < 64) {
-                            const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
-                            const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
-                            const float M = fmaxf(m0, m1);
-                            const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
-                            const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
-                            const float Ls = l0 * w0v + l1 * w1v;
-                            wf[r] = w0v;
-                            wf[64 + r] = w1v;
-                            wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
-                            if (a.lse) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-                        }
-                        bar_softmax();
-                        for (int g = 0; g < 4; g++) {
-                            const int d = g * 128 + r;
+                    if (r < 64) {
+                        const float l = good ? lsum[r] : 0.f;
+                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), peer), l > 0.f ? mref[r] : -INFINITY);
+                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), peer), l);
+                    }
+                }
+                // every thread's writes are ordered before its own arrival
+                tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), peer));
+                const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
+                if (!bar_or_softmax(!w0)) {
+                    float *wf = red;  // [0,64): own weight, [64,128): the peer's, [128,192): 1/L
+                    if (r < 64) {
+                        const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
+                        const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
+                        const float M = fmaxf(m0, m1);
+                        const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+                        const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+                        const float Ls = l0 * w0v + l1 * w1v;
+                        wf[r] = w0v;
+                        wf[64 + r] = w1v;
+                        wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+                        if (a.lse && split == 0) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+                    }
+                    bar_softmax();
+                    for (int gi = 0; gi < 2; gi++) {
+                        const int g = 2 * split + gi;
+                        const int d = g * 128 + r;
 #pragma unroll
-                            for (int h0 = 0; h0 < 64; h0 += 16) {
-                                float ov[16];
-                                if (good) {
-                                    tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                    tc::tmem_ld_wait();
-                                } else {
+                        for (int h0 = 0; h0 < 64; h0 += 16) {
+                            float ov[16];
+                            if (good) {
+                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                                tc::tmem_ld_wait();
+                            } else {
 #pragma unroll
-                                    for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                                }
-                                const float *pv = rx + (g * 128 + r) * 68 + h0;
+                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                            }
+                            const float *pv = rx + (gi * 128 + r) * 68 + h0;
 #pragma unroll
-                                for (int i = 0; i < 16; i++) {
-                                    const int h = h0 + i;
-                                    const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
-                                    a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
-                                }
+                            for (int i = 0; i < 16; i++) {
+                                const int h = h0 + i;
+                                const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
+                                a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
                             }
                         }
                     }
