@@ -17,7 +17,8 @@
 //      ascending slot order;
 //   5. the i-th miss takes the i-th victim: hot_map / slot_token / stamp are
 //      updated and the (token, slot) pair goes to the device miss list;
-//   6. every (j, k) entry gets its pool row id.
+//   6. every (j, k) entry gets its pool row id (with one list, U is the list
+//      and each entry's row id is written as soon as its slot is known).
 // miss_copy_kernel: a grid-stride copy of the miss list, 16-byte vectors,
 // consecutive threads on consecutive bytes of a row (coalesced on both the
 // host-link read and the HBM write).
@@ -150,62 +151,81 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         return;
     }
 
-    // 2. merge-path ranks -> merged (ties: lower list first), then dedup into U
-    int total = 0;
-    for (int j = 0; j < a.nq; j++) total += lens[j];
-    for (int i = tid; i < n; i += kThreads) {
-        const int j = i / a.K, k = i - j * a.K;
-        const int32_t x = lst[i];
-        if (x < 0) continue;
-        int pos = k;
-        for (int jj = 0; jj < a.nq; jj++) {
-            if (jj == j) continue;
-            const int32_t *l2 = lst + jj * a.K;
-            pos += jj < j ? upper_bound(l2, lens[jj], x) : lower_bound(l2, lens[jj], x);
+    // 2. merge-path ranks -> merged (ties: lower list first), then dedup into
+    // U.  One list is its own union (validated ascending, no duplicates).
+    const bool single = a.nq == 1;
+    int nu;
+    int32_t *miss, *missidx;  // scratch for step 4, whichever arrays are dead by then
+    if (single) {
+        nu = lens[0];
+        miss = merged;
+        missidx = U;
+        U = lst;
+    } else {
+        int total = 0;
+        for (int j = 0; j < a.nq; j++) total += lens[j];
+        for (int i = tid; i < n; i += kThreads) {
+            const int j = i / a.K, k = i - j * a.K;
+            const int32_t x = lst[i];
+            if (x < 0) continue;
+            int pos = k;
+            for (int jj = 0; jj < a.nq; jj++) {
+                if (jj == j) continue;
+                const int32_t *l2 = lst + jj * a.K;
+                pos += jj < j ? upper_bound(l2, lens[jj], x) : lower_bound(l2, lens[jj], x);
+            }
+            merged[pos] = x;
         }
-        merged[pos] = x;
+        __syncthreads();
+        nu = block_compact(
+            total, [&](int p) { return p == 0 || merged[p] != merged[p - 1]; },
+            [&](int p, int r) { U[r] = merged[p]; }, warp_sums);
+        miss = merged;  // merged is dead now
+        missidx = lst;  // lists are dead now
     }
-    __syncthreads();
-    const int nu = block_compact(
-        total, [&](int p) { return p == 0 || merged[p] != merged[p - 1]; },
-        [&](int p, int r) { U[r] = merged[p]; }, warp_sums);
 
     // 3. classify; hits refresh their stamp
-    int nres = 0, nhit = 0;
+    int nres = 0, nhit = 0, nmiss = 0;
     for (int i = tid; i < nu; i += kThreads) {
         const int32_t u = U[i];
-        if (bt[u / a.P] >= 0) {
+        const int32_t blk = bt[u / a.P];
+        if (blk >= 0) {
             uslot[i] = -1;
+            if (single) rid[i] = blk * a.P + u % a.P;  // one list: U[i] is entry i
             nres++;
         } else {
             const int32_t s = a.hot_map[hm + u];
             if (s >= 0) {
                 uslot[i] = s;
                 a.stamp[sc + s] = step;
+                if (single) rid[i] = hb[s / a.P] * a.P + s % a.P;
                 nhit++;
             } else {
                 uslot[i] = -2;
+                nmiss++;
             }
         }
     }
+    if (single)
+        for (int i = nu + tid; i < n; i += kThreads) rid[i] = -1;  // padding
+    int M = 0;
     {
-        int t0, t1;
-        block_excl_scan(nres, warp_sums, &t0);
-        block_excl_scan(nhit, warp_sums, &t1);
+        int tot;  // (hits << 16) | resident: both at most nq * K <= 16384
+        block_excl_scan((nhit << 16) | nres, warp_sums, &tot);
         if (tid == 0) {
-            atomicAdd(&a.stats[0], (unsigned long long)t0);
-            atomicAdd(&a.stats[1], (unsigned long long)t1);
+            atomicAdd(&a.stats[0], (unsigned long long)(tot & 0xFFFF));
+            atomicAdd(&a.stats[1], (unsigned long long)(tot >> 16));
         }
     }
-    int32_t *miss = merged;   // merged is dead now
-    int32_t *missidx = lst;   // lists are dead now
-    const int M = block_compact(
-        nu, [&](int i) { return uslot[i] == -2; },
-        [&](int i, int r) {
-            miss[r] = U[i];
-            missidx[r] = i;
-        },
-        warp_sums);
+    if (__syncthreads_or(nmiss > 0)) {
+        M = block_compact(
+            nu, [&](int i) { return uslot[i] == -2; },
+            [&](int i, int r) {
+                miss[r] = U[i];
+                missidx[r] = i;
+            },
+            warp_sums);
+    }
 
     // 4. victims: the M smallest (stamp, slot) among slots with stamp < step
     int served = 0;
@@ -242,7 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         }
         if (!enough) {
             if (tid == 0) set_error(a.err, HS_ERR_CAPACITY);
-            for (int i = tid; i < M; i += kThreads) uslot[missidx[i]] = -3;
+            for (int i = tid; i < M; i += kThreads) {
+                uslot[missidx[i]] = -3;
+                if (single) rid[missidx[i]] = -1;
+            }
         } else {
             // lt: stamp < S*, eq: stamp == S* (taken lowest slot first, `need` of them)
             const uint32_t S = prefix;
@@ -277,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
                 if (s < 0 || s >= a.C) {  // cannot happen; never write outside the tables
                     set_error(a.err, HS_ERR_CAPACITY);
                     uslot[missidx[i]] = -3;
+                    if (single) rid[missidx[i]] = -1;
                     continue;
                 }
                 const int32_t old = a.slot_token[sc + s];
@@ -285,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
                 a.hot_map[hm + u] = s;
                 a.stamp[sc + s] = step;
                 uslot[missidx[i]] = s;
+                if (single) rid[missidx[i]] = hb[s / a.P] * a.P + s % a.P;
                 a.miss_tok[(size_t)b * n + i] = u;
                 a.miss_slot[(size_t)b * n + i] = s;
             }
@@ -297,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         atomicAdd(&a.stats[2], (unsigned long long)served);
         atomicAdd(&a.stats[3], (unsigned long long)served * a.L * a.R);
     }
+    if (single) return;  // every entry's row id is written above
     __syncthreads();
 
     // 6. row ids
@@ -304,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         const int32_t u = tk[i];
         int32_t r = -1;
         if (u >= 0) {
-            const int32_t s = uslot[lower_bound(U, nu, u)];
+            const int32_t s = uslot[single ? i : lower_bound(U, nu, u)];
             if (s == -1)
                 r = bt[u / a.P] * a.P + u % a.P;
             else if (s >= 0)
