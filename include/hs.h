@@ -263,7 +263,9 @@ hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
  *   out[b][j][h][:512] = sum_k softmax_k(z) * row[:512]   (rows with id -1 skipped)
  *   lse[b][j][h] = ln(sum_k exp(z))                        (if lse != NULL)
  * q: dev [B][nq][H][576] bf16; out: dev [B][nq][H][512] bf16; lse: dev fp32
- * or NULL.  A query with no row gets out = 0, lse = -inf. */
+ * or NULL.  q and out are read and written in 16-byte vectors: both must be
+ * 16-byte aligned (HS_ERR_INVALID_ARG otherwise).  A query with no row gets
+ * out = 0, lse = -inf. */
 hs_status hs_sparse_mla_decode(hs_pool *pool, int32_t layer, const void *q,
                                const int32_t *row_id, int32_t B, int32_t nq,
                                float softmax_scale, void *out, float *lse,
@@ -273,9 +275,9 @@ typedef struct {
     int32_t B, nq;
     const void *q_idx;    /* dev [B][nq][Hi][Di], indexer format             */
     const float *w_idx;   /* dev [B][nq][Hi]                                 */
-    const void *q_mla;    /* dev [L][B][nq][H][576] bf16                     */
+    const void *q_mla;    /* dev [L][B][nq][H][576] bf16, 16-byte aligned    */
     float softmax_scale;
-    void *out;            /* dev [L][B][nq][H][512] bf16                     */
+    void *out;            /* dev [L][B][nq][H][512] bf16, 16-byte aligned    */
     float *lse;           /* dev [L][B][nq][H] fp32, or NULL                 */
     int32_t *topk;        /* dev [B][nq][K] int32 (output)                   */
     int32_t *row_id;      /* dev [B][nq][K] int32 (output)                   */

@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         tc::mbar_init(o_done, 1);
         tc::mbar_init(mma_done, 1);
         tc::mbar_init(peer_ready, 1);
-        tc::mbar_init(peer_data, 128);
+        tc::mbar_init(peer_data, 256);
         tc::mbar_init(q_full, kWorkerWarps);
         tc::fence_barrier_init();
     }
@@ -652,7 +652,130 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             }
             if (ok) issue_first();  // lands before PV(c) frees the first K-blocks
         }
-        if (warp < 6) {  // epilogue: thread = output dim row = TMEM lane
+        if (a.cluster && warp < 10) {
+            // ---- two splits in one cluster merge symmetrically over eight
+            // warps (heads 0-31 on warps 2-5, 32-63 on warps 6-9; thread =
+            // output dim row = TMEM lane): split s finishes output dims
+            // [256 s, 256 s + 256) (O^T tiles 2s, 2s+1) and hands the peer its
+            // other two tiles and its (max, sum) through distributed shared
+            // memory.  Received layout in the row buffer: O as [tile 0..1]
+            // [head/4][128 dims][4 heads] fp32 (consecutive threads on
+            // consecutive 16 bytes), then max[64], sum[64]; the merged bf16
+            // output is staged as [64 heads][256 dims] behind it and leaves in
+            // 16-byte stores.
+            const int sp = warp & 3;
+            const int r = sp * 32 + lane;
+            const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
+            const int hb = warp < 6 ? 0 : 32;
+            const bool fin = ok && nchunks > 0 && tc::mbar_wait(o_done, (nchunks - 1) & 1, a.err);
+            const bool good = !bar_or_group(!fin);
+            if (good) {
+                tc::fence_after_sync();
+                if (warp == 4) {  // every lane holds the same denominators
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        float lv[16];
+                        tc::tmem_ld16(lane_base + l_col + 16 * q, lv);
+                        tc::tmem_ld_wait();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; i++) lsum[16 * q + i] = lv[i];
+                        }
+                    }
+                }
+                bar_group();
+            }
+            const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
+            const uint32_t peer = 1u - (uint32_t)split;
+            float *rx = (float *)rb;
+            float *rx_m = rx + 2 * 16 * 128 * 4;
+            float *rx_l = rx_m + 64;
+            __nv_bfloat16 *ostage = (__nv_bfloat16 *)(rb + 72 * 1024);
+            // this CTA's row buffer is idle once every MMA completed
+            if (warp == 4 && lane == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), peer));
+            const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
+            if (!bar_or_group(!w1)) {
+                const uint32_t dst = tc::mapa(tc::smem_addr(rx), peer);
+                for (int gi = 0; gi < 2; gi++) {
+                    const int g = 2 * (int)peer + gi;
+#pragma unroll
+                    for (int h0 = hb; h0 < hb + 32; h0 += 16) {
+                        float ov[16];
+                        if (good) {
+                            tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                            tc::tmem_ld_wait();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                        }
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) {
+                            const int hq = (h0 >> 2) + q4;
+                            const uint32_t at = dst + (uint32_t)((((gi * 16 + hq) * 128 + r) * 4) * 4);
+                            tc::st_cluster_v4(at, ov[4 * q4], ov[4 * q4 + 1], ov[4 * q4 + 2], ov[4 * q4 + 3]);
+                        }
+                    }
+                }
+                if (warp < 6 && r < 64) {
+                    const float l = good ? lsum[r] : 0.f;
+                    tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), peer), l > 0.f ? mref[r] : -INFINITY);
+                    tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), peer), l);
+                }
+            }
+            // every thread's writes are ordered before its own arrival
+            tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), peer));
+            const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
+            if (!bar_or_group(!w0)) {
+                float *wf = red;  // [0,64): own weight, [64,128): the peer's, [128,192): 1/L
+                if (warp < 6 && r < 64) {
+                    const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
+                    const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
+                    const float M = fmaxf(m0, m1);
+                    const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+                    const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+                    const float Ls = l0 * w0v + l1 * w1v;
+                    wf[r] = w0v;
+                    wf[64 + r] = w1v;
+                    wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+                    if (a.lse && split == 0) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+                }
+                bar_group();
+                for (int gi = 0; gi < 2; gi++) {
+                    const int g = 2 * split + gi;
+#pragma unroll
+                    for (int h0 = hb; h0 < hb + 32; h0 += 16) {
+                        float ov[16];
+                        if (good) {
+                            tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
+                            tc::tmem_ld_wait();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; i++) ov[i] = 0.f;
+                        }
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) {
+                            const int hq = (h0 >> 2) + q4;
+                            const float4 pv = *(const float4 *)(rx + ((gi * 16 + hq) * 128 + r) * 4);
+                            const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                const int h = 4 * hq + e;
+                                const float v = (ov[4 * q4 + e] * wf[h] + pp[e] * wf[64 + h]) * wf[128 + h];
+                                ostage[h * 256 + gi * 128 + r] = __float2bfloat16(v);
+                            }
+                        }
+                    }
+                }
+                bar_group();
+                // 64 heads x 256 dims of bf16: 2048 16-byte vectors over 256 threads
+                const int t = (warp - 2) * 32 + lane;
+                for (int v = t; v < 64 * 32; v += 256) {
+                    const int h = v >> 5, c16 = v & 31;
+                    *(uint4 *)(a.out + (g0 + h) * kNope + split * 256 + c16 * 8) =
+                        *(const uint4 *)(ostage + h * 256 + c16 * 8);
+                }
+            }
+        } else if (!a.cluster && warp < 6) {  // epilogue: thread = output dim row = TMEM lane
             const int sp = warp & 3;
             const int r = sp * 32 + lane;
             const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
@@ -677,86 +800,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 bar_softmax();
             }
             const size_t g0 = (size_t)qr * a.H + hh * kTcHeads;  // first output head row
-            if (a.cluster) {
-                // ---- two splits in one cluster merge symmetrically: split s
-                // finishes output dims [256 s, 256 s + 256) (O^T tiles 2s, 2s+1).
-                // Each hands the peer its other two tiles and its (max, sum)
-                // through distributed shared memory.  Received layout in the
-                // row buffer: O [2][128][68] fp32, then max[64], sum[64].
-                const uint32_t peer = 1u - (uint32_t)split;
-                float *rx = (float *)rb;
-                float *rx_m = rx + 2 * 128 * 68;
-                float *rx_l = rx_m + 64;
-                // this CTA's row buffer is idle once every MMA completed
-                if (r == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), peer));
-                const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
-                if (!bar_or_softmax(!w1)) {
-                    const uint32_t dst = tc::mapa(tc::smem_addr(rx), peer);
-                    for (int gi = 0; gi < 2; gi++) {
-                        const int g = 2 * (int)peer + gi;
-#pragma unroll
-                        for (int h0 = 0; h0 < 64; h0 += 16) {
-                            float ov[16];
-                            if (good) {
-                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                tc::tmem_ld_wait();
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                            }
-                            const uint32_t at = dst + (uint32_t)(((gi * 128 + r) * 68 + h0) * 4);
-#pragma unroll
-                            for (int i = 0; i < 16; i += 4) tc::st_cluster_v4(at + i * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
-                        }
-                    }
-                    if (r < 64) {
-                        const float l = good ? lsum[r] : 0.f;
-                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_m + r), peer), l > 0.f ? mref[r] : -INFINITY);
-                        tc::st_cluster_f32(tc::mapa(tc::smem_addr(rx_l + r), peer), l);
-                    }
-                }
-                // every thread's writes are ordered before its own arrival
-                tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), peer));
-                const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
-                if (!bar_or_softmax(!w0)) {
-                    float *wf = red;  // [0,64): own weight, [64,128): the peer's, [128,192): 1/L
-                    if (r < 64) {
-                        const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
-                        const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
-                        const float M = fmaxf(m0, m1);
-                        const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
-                        const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
-                        const float Ls = l0 * w0v + l1 * w1v;
-                        wf[r] = w0v;
-                        wf[64 + r] = w1v;
-                        wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
-                        if (a.lse && split == 0) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-                    }
-                    bar_softmax();
-                    for (int gi = 0; gi < 2; gi++) {
-                        const int g = 2 * split + gi;
-                        const int d = g * 128 + r;
-#pragma unroll
-                        for (int h0 = 0; h0 < 64; h0 += 16) {
-                            float ov[16];
-                            if (good) {
-                                tc::tmem_ld16(lane_base + o_col + g * kTcHeads + h0, ov);
-                                tc::tmem_ld_wait();
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 16; i++) ov[i] = 0.f;
-                            }
-                            const float *pv = rx + (gi * 128 + r) * 68 + h0;
-#pragma unroll
-                            for (int i = 0; i < 16; i++) {
-                                const int h = h0 + i;
-                                const float v = (ov[i] * wf[h] + pv[i] * wf[64 + h]) * wf[128 + h];
-                                a.out[(g0 + h) * kNope + d] = __float2bfloat16(v);
-                            }
-                        }
-                    }
-                }
-            } else if (good) {
+            if (good) {
                 for (int g = 0; g < 4; g++) {
                     const int d = g * 128 + r;
 #pragma unroll

@@ -493,6 +493,8 @@ hs_status hs_request_close(hs_pool *p, int32_t req) {
     return cuda_status(e);
 }
 
+static bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15) == 0; }
+
 static bool batch_ok(const hs_pool *p, int32_t B, int32_t nq) {
     if (!p || B <= 0 || B > p->cfg.max_requests || nq <= 0 || nq > p->nq_max) return false;
     for (int b = 0; b < B; b++)
@@ -532,14 +534,14 @@ hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const i
                                int32_t B, int32_t nq, float scale, void *out, float *lse,
                                cudaStream_t st) {
     if (!batch_ok(p, B, nq) || !q || !row_id || !out || layer < 0 ||
-        layer >= p->cfg.num_mla_layers)
+        layer >= p->cfg.num_mla_layers || !aligned16(q) || !aligned16(out))
         return HS_ERR_INVALID_ARG;
     return cuda_status(hs::launch_attention(p, layer, q, row_id, B, nq, scale, out, lse, st));
 }
 
 hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
     if (!a || !batch_ok(p, a->B, a->nq) || !a->q_idx || !a->w_idx || !a->q_mla || !a->out ||
-        !a->topk || !a->row_id)
+        !a->topk || !a->row_id || !aligned16(a->q_mla) || !aligned16(a->out))
         return HS_ERR_INVALID_ARG;
     const int B = a->B, nq = a->nq, H = p->cfg.mla_heads, L = p->cfg.num_mla_layers;
     cudaError_t e = hs::launch_indexer_score(p, a->q_idx, a->w_idx, B, nq, p->d.scores,
