@@ -289,6 +289,18 @@ def test_host_side_capacity_errors():
             pool.resolve(torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"), 3, 1,
                          torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"))
         assert ei.value.status == hs.HS_ERR_INVALID_ARG  # B beyond max_requests
+        # q and out are moved in 16-byte vectors: a misaligned pointer is refused
+        # before anything is enqueued
+        qm = torch.zeros(16 * 576 + 8, dtype=torch.bfloat16, device="cuda")
+        rid = torch.full((1, 1, 64), -1, dtype=torch.int32, device="cuda")
+        out = torch.zeros(16 * 512 + 8, dtype=torch.bfloat16, device="cuda")
+        for qq, oo in ((qm[1:], out[:-8]), (qm[:-8], out[1:])):
+            with pytest.raises(hs.HSError) as ei:
+                pool.sparse_mla_decode(0, qq, rid, 1, 1, 0.1, oo, None)
+            assert ei.value.status == hs.HS_ERR_INVALID_ARG
+        pool.sparse_mla_decode(0, qm[:-8], rid, 1, 1, 0.1, out[:-8], None)  # aligned: accepted
+        torch.cuda.synchronize()
+        assert pool.get_error() == hs.HS_OK
         pool.close_request(1)
         pool.close_request(0)
         assert pool.free_gpu_blocks() == 6
