@@ -265,7 +265,10 @@ hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
  * q: dev [B][nq][H][576] bf16; out: dev [B][nq][H][512] bf16; lse: dev fp32
  * or NULL.  q and out are read and written in 16-byte vectors: both must be
  * 16-byte aligned (HS_ERR_INVALID_ARG otherwise).  A query with no row gets
- * out = 0, lse = -inf. */
+ * out = 0, lse = -inf.  With E4M3 rows and a head count that is a multiple of
+ * 64, the products run on the tensor cores with fp16 operands (queries and
+ * dequantised rows converted, fp32 accumulation): their magnitudes must stay
+ * below 65504. */
 hs_status hs_sparse_mla_decode(hs_pool *pool, int32_t layer, const void *q,
                                const int32_t *row_id, int32_t B, int32_t nq,
                                float softmax_scale, void *out, float *lse,

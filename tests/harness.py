@@ -46,6 +46,7 @@ class Case:
     check_attn_every: int = 1
     use_step: bool = False   # call hs_step instead of the separate calls
     gpu_blocks: int = 0      # 0 = enough for the case
+    host_blocks: int = 0     # 0 = every page of the case
     max_tokens: int = 0
 
 
@@ -64,7 +65,7 @@ class Runner:
         pages = sum((n + c.steps * c.append + c.P - 1) // c.P for n in Ns)
         C = c.hot_rows or (c.num_spec + 2) * c.K
         blocks = c.gpu_blocks or (pages + c.B * (C // c.P) + 4)
-        host_blocks = pages + 4  # host copies are always kept (full pages are pre-copied)
+        host_blocks = c.host_blocks or (pages + 4)  # host copies are always kept
         self.cfg = hs.make_config(max_requests=c.B, max_tokens=self.max_tokens, page_tokens=c.P,
                                   top_k=c.K, num_spec=c.num_spec, tail_tokens=c.T,
                                   num_mla_layers=c.L, mla_heads=c.H, idx_heads=c.Hi, idx_dim=c.Di,
@@ -188,17 +189,30 @@ class Runner:
         # append
         if c.append:
             for b in range(B):
-                n0 = self.N[b]
-                r = wl.mla_rows(c.seed, b, n0, c.append, c.L, c.row_fmt, device=self.dev)
-                k = wl.idx_keys(c.seed, b, n0, c.append, c.Di, c.idx_fmt, device=self.dev)
-                sg = (wl.idx_sigma(c.append, self.dev, seed=c.seed, b=b, t0=n0) if c.sigma
-                      else wl.idx_sigma(c.append, self.dev))
-                self.pool.append(b, r, k, sg)
-                self.rows[b] = torch.cat([self.rows[b], r])
-                self.keys[b] = torch.cat([self.keys[b], k])
-                self.sig[b] = torch.cat([self.sig[b], sg])
-                self.N[b] += c.append
+                self.append(b, c.append)
         return res
+
+    def append(self, b, n, on_capacity=None):
+        """Append the next n tokens of request b (rows, keys, scales from the
+        generators) to the pool and to the oracle's copy.  When the pool is
+        full, on_capacity(b) may make room (it returns False to give up)."""
+        c = self.c
+        n0 = self.N[b]
+        r = wl.mla_rows(c.seed, b, n0, n, c.L, c.row_fmt, device=self.dev)
+        k = wl.idx_keys(c.seed, b, n0, n, c.Di, c.idx_fmt, device=self.dev)
+        sg = (wl.idx_sigma(n, self.dev, seed=c.seed, b=b, t0=n0) if c.sigma
+              else wl.idx_sigma(n, self.dev))
+        while True:
+            try:
+                self.pool.append(b, r, k, sg)
+                break
+            except hs.HSError as e:
+                if e.status != hs.HS_ERR_CAPACITY or on_capacity is None or not on_capacity(b):
+                    raise
+        self.rows[b] = torch.cat([self.rows[b], r])
+        self.keys[b] = torch.cat([self.keys[b], k])
+        self.sig[b] = torch.cat([self.sig[b], sg])
+        self.N[b] += n
 
     def _locate(self, rid, st):
         """Pool row ids -> (kind, value) with the request's own tables:

@@ -11,7 +11,11 @@ within |gpu - ref| <= 2e-3 + 1e-2 |ref|.
   * mixed residency with MTP3: 64 requests x 142,000 tokens, tail 4096, hot
     buffer 5 x 2048, drawn recency/Zipf streams, all 220 decode steps;
   * zero residency: 4 requests x 2^20 tokens, all rows in pinned host memory,
-    hot buffers 2 x 2048 filled on demand, drawn uniform/Zipf streams, 64 steps.
+    hot buffers 2 x 2048 filled on demand, drawn uniform/Zipf streams, 64 steps;
+  * agentic growth: 16 requests, 13 turns (a 74,160-token prompt, then 753
+    prompt tokens per turn), 220 decode steps per turn with the real indexer
+    top-K and one appended token per step, GPU pool capped at 20,000 blocks so
+    that requests flip from full to mixed residency mid-trace.
 """
 import math
 
@@ -206,3 +210,127 @@ def test_zero_residency_4x1M_64_steps(hs):
         assert totals["resident"] == 0 and totals["misses"] >= 4 * K
     finally:
         pool.close()
+
+
+def test_agentic_growth_16x13_turns(hs):
+    """The agentic growth trace at full size.  Every step: no device error and
+    every selected row id of every request reads its own token's bytes (all
+    layers, every 8th step; the first and last step of each turn always).  Two
+    requests (the first to flip and one that flips last or never) are
+    followed by the oracle on every step: exact row locations and hot-buffer
+    state, and at each turn's first and last step the exact top-K and
+    sampled attention.  Flips follow the trace's policy: when an append does
+    not fit, the full-residency request with the most pages flips first."""
+    from fullsize import locate
+    B, K, L, P, T, H, Hi, Di, seed = 16, 2048, 4, 64, 4096, 128, 64, 128, 0
+    prompt0, prompt, decode, turns = 74160, 753, 220, 13
+    final = prompt0 + decode + (turns - 1) * (prompt + decode)
+    assert final == 86056
+    max_tokens = (final + P - 1) // P * P
+    pages = max_tokens // P
+    dev = torch.device("cuda")
+    cfg = hs.make_config(max_requests=B, max_tokens=max_tokens, page_tokens=P, top_k=K, num_spec=0,
+                         tail_tokens=T, num_mla_layers=L, mla_heads=H, idx_heads=Hi, idx_dim=Di,
+                         row_fmt=hs.HS_ROW_E4M3_656, idx_fmt=hs.HS_IDX_E4M3,
+                         gpu_blocks=20000, host_blocks=B * pages)
+    pool = hs.Pool(cfg, device=dev)
+    C = pool.C
+    N = [0] * B
+    modes = [hs.HS_FULL] * B
+    truth = [wl.mla_rows(seed, b, 0, final, L, wl.ROW_E4M3_656, device=dev) for b in range(B)]
+    keys = [wl.idx_keys(seed, b, 0, final, Di, wl.IDX_E4M3, device=dev) for b in range(B)]
+    follow = {}   # request -> oracle HotState (from its flip on)
+    flips = []
+
+    def flip_largest():
+        full = [b for b in range(B) if modes[b] == hs.HS_FULL]
+        if not full:
+            return False
+        x = full[int(np.argmax([N[b] for b in full]))]  # most pages, lowest id on ties
+        pool.set_mode(x, hs.HS_MIXED)
+        modes[x] = hs.HS_MIXED
+        flips.append(x)
+        if len(flips) == 1:
+            follow[x] = oracle.HotState(C, max_tokens)
+        return True
+
+    def append(b, n):
+        while True:
+            try:
+                pool.append(b, truth[b][N[b]:N[b] + n], keys[b][N[b]:N[b] + n])
+                break
+            except hs.HSError as e:
+                assert e.status == hs.HS_ERR_CAPACITY and flip_largest()
+        N[b] += n
+
+    for b in range(B):
+        pool.open(b, hs.HS_FULL)
+        append(b, prompt0)
+    torch.cuda.synchronize()
+    last = B - 1  # followed from the start; flips (if at all) late, being the highest id
+    follow[last] = None
+    topk = torch.empty((B, 1, K), dtype=torch.int32, device=dev)
+    rid = torch.empty_like(topk)
+    out = torch.empty((L, B, 1, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((L, B, 1, H), dtype=torch.float32, device=dev)
+    tau = 1.0 / math.sqrt(576)
+    step = 0
+    checked_topk = 0
+    for turn in range(turns):
+        if turn:
+            for b in range(B):
+                append(b, prompt)
+        for d in range(decode):
+            step += 1
+            edge = d == 0 or d == decode - 1
+            q = torch.stack([wl.idx_query(seed, b, step, 1, Hi, Di, wl.IDX_E4M3, dev) for b in range(B)])
+            w = torch.stack([wl.idx_weights(seed, b, step, 1, Hi, dev) for b in range(B)])
+            qm = wl.mla_query(seed, step, B, 1, H, L, dev).contiguous()
+            pool.step(B, 1, q.contiguous(), w.contiguous(), qm, tau, out, topk, rid, lse)
+            torch.cuda.synchronize()
+            assert pool.get_error() == hs.HS_OK, f"turn {turn} step {d}"
+            tk = topk.cpu().numpy()
+            rv = rid.cpu().numpy()
+            if edge or step % 8 == 0:
+                prow = pool.rows_view()
+                for b in range(B):
+                    sel = topk[b, 0]
+                    ok = sel >= 0
+                    ids = rid[b, 0][ok].long()
+                    assert torch.equal(prow[ids // P, :, ids % P], truth[b][sel[ok].long()]), \
+                        f"rows turn {turn} step {d} req {b}"
+            for b in list(follow):
+                if follow[b] is None and modes[b] == hs.HS_MIXED:  # flipped before this step
+                    follow[b] = oracle.HotState(C, max_tokens)
+                hot = follow[b]
+                st = pool.dump_state(b)
+                resident = oracle.page_resident(modes[b], N[b], T, P)
+                if hot is None:  # still full: every selected token is read in place
+                    kind, val = locate(rv[b], st["block_table"], st["hot_blocks"], P, 20000)
+                    sel = tk[b] >= 0
+                    assert (kind[sel] == 1).all() and (val[sel] == tk[b][sel]).all()
+                    continue
+                r = hot.resolve(resident, P, N[b], tk[b])
+                assert r["status"] == 0
+                kind, val = locate(rv[b], st["block_table"], st["hot_blocks"], P, 20000)
+                np.testing.assert_array_equal(kind, r["loc_kind"], err_msg=f"turn {turn} step {d} req {b}")
+                np.testing.assert_array_equal(val, r["loc_val"], err_msg=f"turn {turn} step {d} req {b}")
+                np.testing.assert_array_equal(st["stamp"], hot.stamp)
+                np.testing.assert_array_equal(st["slot_token"], hot.slot_token)
+            if edge:
+                for b in sorted(follow):
+                    kb = keys[b][:N[b]].cpu().numpy()
+                    sc = oracle.indexer_scores(oracle.IDX_E4M3, q[b].cpu().numpy(), w[b].cpu().numpy(),
+                                               kb, np.ones(N[b], np.float32), N[b])
+                    np.testing.assert_array_equal(tk[b, 0], oracle.topk(sc[0], N[b], K))
+                    checked_topk += 1
+                    l = (turn + d) % L
+                    _check_attention(truth[b], qm, out, lse, tk[b, 0], b, 0, l)
+            for b in range(B):
+                append(b, 1)  # the decoded token joins the tail
+    torch.cuda.synchronize()
+    assert N == [final] * B
+    assert flips and flips[0] == 0, flips  # every request is the same size: lowest id first
+    assert hs.HS_FULL in modes              # only as many flips as the cap needs
+    assert checked_topk >= 2 * turns
+    pool.close()

@@ -328,6 +328,53 @@ def test_full_to_mixed_flip_keeps_outputs():
         r.close()
 
 
+def flip_largest_full(r):
+    """Pool-pressure policy of the agentic trace: flip the full-residency
+    request with the most resident pages (lower id on ties) to mixed."""
+    hs = _hs()
+    full = [b for b in range(r.c.B) if r.modes[b] == hs.HS_FULL]
+    if not full:
+        return False
+    pages = [(r.N[b] + r.c.P - 1) // r.c.P for b in full]
+    r.flip_to_mixed(full[int(np.argmax(pages))])  # argmax takes the lowest id on ties
+    return True
+
+
+def test_agentic_growth_flips_under_pool_cap():
+    """The agentic growth trace at reduced size: every request starts with a
+    long prompt, then each turn appends a prompt and decodes token by token
+    with the real indexer top-K; the GPU pool is capped so that requests flip
+    from full to mixed residency mid-trace (largest first).  Every step is
+    compared with the oracle: indices, row locations, hot-buffer state, row
+    bytes and attention."""
+    from harness import Case, Runner
+    hs = _hs()
+    r = Runner(Case("agentic", B=4, N=1500, K=256, H=128, L=2, T=256, mode=hs.HS_FULL,
+                    max_tokens=1792, gpu_blocks=100, host_blocks=4 * 28 + 4, steps=0))
+    try:
+        flips = []
+        for turn in range(5):
+            if turn:
+                for b in range(r.c.B):
+                    before = list(r.modes)
+                    r.append(b, 60, on_capacity=lambda _: flip_largest_full(r))
+                    flips += [x for x in range(r.c.B) if r.modes[x] != before[x]]
+            for _ in range(6):
+                r.run_step()
+                for b in range(r.c.B):
+                    before = list(r.modes)
+                    r.append(b, 1, on_capacity=lambda _: flip_largest_full(r))
+                    flips += [x for x in range(r.c.B) if r.modes[x] != before[x]]
+        assert flips and flips[0] == 0  # the first flip takes the largest, lowest id
+        assert hs.HS_FULL in r.modes    # and only as many as the cap needs
+        st = r.pool.stats()
+        assert (st["resident"], st["hits"], st["misses"]) == (
+            r.stats["resident"], r.stats["hits"], r.stats["misses"])
+        assert r.stats["misses"] > 0
+    finally:
+        r.close()
+
+
 def test_indexer_tensor_core_pipeline_wraps():
     """Enough tiles per CTA that the TMA ring and the two TMEM accumulators
     wrap several times (MTP3: 256 MMA columns, one CTA per SM)."""
