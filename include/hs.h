@@ -322,6 +322,16 @@ hs_status hs_pool_load_state(hs_pool *pool, int32_t req, const int32_t *hot_map,
  * (host arithmetic, the same decision hs_step makes); -1 on bad arguments. */
 int32_t hs_step_kernel_count(const hs_pool *pool, int32_t B, int32_t nq);
 
+/* Failure-path check: enqueue on `stream` one small kernel that waits, with
+ * the same bounded routine every hot-path kernel uses, on an mbarrier that
+ * nothing completes, for limit_cycles SM cycles (1e3 .. 2e9).  The wait runs
+ * out, HS_ERR_TIMEOUT lands in the pool's sticky error word (read and
+ * cleared by hs_pool_get_error) and the context stays usable.  The pages
+ * have no counterpart; it exists so that the timeout path can be tested
+ * without faulting or hanging a GPU.  HS_ERR_INVALID_ARG for a limit out of
+ * range. */
+hs_status hs_check_wait_timeout(hs_pool *pool, int64_t limit_cycles, cudaStream_t stream);
+
 /* A static English description of a status. */
 const char *hs_status_string(hs_status s);
 

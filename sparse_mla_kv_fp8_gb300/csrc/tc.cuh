@@ -50,18 +50,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 constexpr long long kWaitCycles = 2000000000LL;
 
 // Wait for the phase with the given parity; false (and the error word set)
-// when the bound runs out.  Never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+// when `limit` cycles run out.  Never spins forever.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, int32_t *err,
+                                                long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         for (int i = 0; i < 64; i++)
             if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             set_error(err, HS_ERR_TIMEOUT);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+    return mbar_wait_limit(bar, parity, err, kWaitCycles);
 }
 
 // ---------------------------------------------------------------- cluster

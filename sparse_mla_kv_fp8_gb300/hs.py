@@ -92,6 +92,7 @@ hs_pool_reset_stats = _decl("hs_pool_reset_stats", _i32, [_P])
 hs_pool_dump_state = _decl("hs_pool_dump_state", _i32, [_P, _i32, _P, _P, _P, _P, _P, _P, _P, _P])
 hs_pool_load_state = _decl("hs_pool_load_state", _i32, [_P, _i32, _P, _P, _P, _u32])
 hs_topk_noalloc = _decl("hs_topk_noalloc", _i32, [_P, _i64, _P, _i32, _i32, _i32, _i32, _P, _P])
+hs_check_wait_timeout = _decl("hs_check_wait_timeout", _i32, [_P, _i64, _P])
 hs_step_kernel_count = _decl("hs_step_kernel_count", _i32, [_P, _i32, _i32])
 hs_status_string = _decl("hs_status_string", ctypes.c_char_p, [_i32])
 hs_abi_version = _decl("hs_abi_version", _i32, [])
@@ -207,6 +208,10 @@ class Pool:
     def sparse_mla_decode(self, layer, q, row_id, B, nq, scale, out, lse=None, stream=None):
         check(hs_sparse_mla_decode(self.handle, layer, _ptr(q), _ptr(row_id), B, nq, scale,
                                    _ptr(out), _ptr(lse), _stream(stream)), "hs_sparse_mla_decode")
+
+    def check_wait_timeout(self, limit_cycles, stream=None):
+        check(hs_check_wait_timeout(self.handle, limit_cycles, _stream(stream)),
+              "hs_check_wait_timeout")
 
     def step(self, B, nq, q_idx, w_idx, q_mla, scale, out, topk, row_id, lse=None, stream=None):
         a = hs_step_args(B=B, nq=nq, q_idx=_ptr(q_idx), w_idx=_ptr(w_idx), q_mla=_ptr(q_mla),

@@ -262,6 +262,27 @@ def test_out_of_range_index_sets_error_and_recovers():
         r.close()
 
 
+def test_bounded_wait_runs_out_and_context_stays_usable():
+    """Failure detection without a fault: a wait whose mbarrier nothing
+    completes runs out after its limit, HS_ERR_TIMEOUT lands in the sticky
+    error word, and the next calls run normally."""
+    from harness import Case, Runner
+    hs = _hs()
+    r = Runner(Case("after-timeout", B=1, N=600, K=64, Hi=4, Di=32, idx_fmt=wl.IDX_F32, H=16,
+                    row_fmt=wl.ROW_F32_2304, T=128, steps=1))
+    try:
+        with pytest.raises(hs.HSError) as ei:
+            r.pool.check_wait_timeout(10)  # limit below the accepted range
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG
+        r.pool.check_wait_timeout(2_000_000)  # about a millisecond
+        torch.cuda.synchronize()
+        assert r.pool.get_error() == hs.HS_ERR_TIMEOUT
+        assert r.pool.get_error() == hs.HS_OK  # read and cleared
+        r.run_step()                          # the context is still usable
+    finally:
+        r.close()
+
+
 def test_host_side_capacity_errors():
     hs = _hs()
     cfg = hs.make_config(max_requests=2, max_tokens=1024, top_k=64, num_spec=0, tail_tokens=64,
