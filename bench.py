@@ -376,7 +376,7 @@ def roofline(stage, alg, peaks, w):
             tf = a["flops"] / (ms / 1e3) / 1e12
             out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16_sus"],
                       "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": _traffic(k),
-                      "peak_source": peaks["src"] + " bf16 sustained",
+                      "peak_source": peaks["src"] + " bf16 sustained (fp16 operands: the same dense rate)",
                       "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
                       "share_of_step": share[k] / tot, "us_per_launch": ms * 1e3}
         else:

@@ -333,6 +333,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     if (a.cluster) tc::cluster_sync();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
+    // everything above touched only this CTA's shared memory and TMEM: the
+    // setup overlaps the previous kernel's tail; the next kernel may start too
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();
     const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
     const uint32_t o_col = 128;   // O^T tiles: columns [128 + 64 g, ...)
     const uint32_t l_col = 384;   // per-row running sums of P: [384, 448)
@@ -952,25 +956,11 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         a.err = p->d.err;
         a.cluster = splits == 2;
         dim3 grid(rows, a.H / kTcHeads, splits);
-        if (a.cluster) {
-            // the two splits of a (query, 64 heads) merge through DSMEM
-            cudaLaunchConfig_t lc = {};
-            lc.gridDim = grid;
-            lc.blockDim = dim3(kAttnThreads);
-            lc.dynamicSmemBytes = AttnTcSmem::bytes;
-            lc.stream = st;
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = 1;
-            at[0].val.clusterDim.y = 1;
-            at[0].val.clusterDim.z = 2;
-            lc.attrs = at;
-            lc.numAttrs = 1;
-            cudaError_t e = cudaLaunchKernelEx(&lc, attn_tc_kernel, a);
-            if (e != cudaSuccess) return e;
-        } else {
-            attn_tc_kernel<<<grid, kAttnThreads, AttnTcSmem::bytes, st>>>(a);
-        }
+        // the two splits of a (query, 64 heads) merge through DSMEM as a cluster
+        PdlLaunch lc(grid, dim3(kAttnThreads), AttnTcSmem::bytes, st,
+                     a.cluster ? dim3(1, 1, 2) : dim3(1, 1, 1));
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel, a);
+        if (e != cudaSuccess) return e;
     } else {
         AttnArgs a;
         a.q = (const __nv_bfloat16 *)q;

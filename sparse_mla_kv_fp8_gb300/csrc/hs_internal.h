@@ -19,6 +19,32 @@ constexpr int kTopkBins = 2048;    // 11-bit digit
 constexpr int kMaxSplits = 32;     // split-K partials per attention query
 constexpr int kNumSMs = 152;       // GB300
 
+// Launch configuration with programmatic stream serialization (the kernel
+// may start while the previous kernel on the stream finishes; it calls
+// griddepcontrol.wait before its first global memory access) and, when
+// cluster_z > 1, a (1, 1, cluster_z) or (cluster_x, 1, 1) cluster.
+struct PdlLaunch {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attrs[2];
+    PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st, dim3 cluster = dim3(1, 1, 1)) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+        if (cluster.x * cluster.y * cluster.z > 1) {
+            attrs[1].id = cudaLaunchAttributeClusterDimension;
+            attrs[1].val.clusterDim.x = cluster.x;
+            attrs[1].val.clusterDim.y = cluster.y;
+            attrs[1].val.clusterDim.z = cluster.z;
+            cfg.numAttrs = 2;
+        }
+    }
+};
+
 // Per-row state of the radix top-K (one row = one (request, query)).
 struct TopkRowState {
     uint32_t prefix;   // high digits of the threshold key found so far

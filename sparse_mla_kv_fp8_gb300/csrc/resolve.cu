@@ -23,6 +23,7 @@
 // consecutive threads on consecutive bytes of a row (coalesced on both the
 // host-link read and the HBM write).
 #include "hs_internal.h"
+#include "tc.cuh"
 
 namespace hs {
 namespace {
@@ -113,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     __shared__ uint32_t hist[256];
     __shared__ int sel[4];
     const int b = blockIdx.x, tid = threadIdx.x;
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();  // the lists come from the previous kernel
     const int n = a.nq * a.K;
     int32_t *lst = sm;            // [n] the lists; later: index into U of each miss
     int32_t *merged = lst + n;    // [n] merged lists; later: miss tokens
@@ -345,6 +348,8 @@ __global__ void __launch_bounds__(256) miss_copy_kernel(
     const int32_t *__restrict__ miss_slot, int n, const int32_t *__restrict__ host_block_table,
     const int32_t *__restrict__ hot_blocks, const uint8_t *__restrict__ host_rows,
     uint8_t *__restrict__ rows, int L, int P, int R, int max_pages, int hot_pages, int32_t *err) {
+    hs::tc::grid_dep_launch();
+    hs::tc::grid_dep_wait();  // the miss lists come from the plan kernel
     const int b = blockIdx.y;
     const int M = miss_count[b];
     const int cpr = R / 16, per_miss = L * cpr;
@@ -411,15 +416,22 @@ cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq,
     a.err = p->d.err;
     a.stats = p->d.stats;
     const int n = nq * a.K;
-    resolve_plan_kernel<<<B, kThreads, plan_smem(n), st>>>(a);
+    {
+        PdlLaunch lc(dim3(B), dim3(kThreads), plan_smem(n), st);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, resolve_plan_kernel, a);
+        if (e != cudaSuccess) return e;
+    }
     if (p->cfg.host_blocks > 0) {
         // enough CTAs in flight to cover the host link's latency, at any B
         const int gx = (4 * kNumSMs + B - 1) / B;
         dim3 grid(gx, B);
-        miss_copy_kernel<<<grid, 256, 0, st>>>(p->d.miss_count, p->d.miss_tok, p->d.miss_slot,
-                                               n, p->d.host_block_table,
-                                               p->d.hot_blocks, p->host_dev, p->d.rows, a.L, a.P,
-                                               a.R, a.max_pages, a.hot_pages, p->d.err);
+        PdlLaunch lc(grid, dim3(256), 0, st);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count,
+                                           (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
+                                           n, (const int32_t *)p->d.host_block_table,
+                                           (const int32_t *)p->d.hot_blocks, (const uint8_t *)p->host_dev,
+                                           p->d.rows, a.L, a.P, a.R, a.max_pages, a.hot_pages, p->d.err);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

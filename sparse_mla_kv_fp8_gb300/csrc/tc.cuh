@@ -155,6 +155,16 @@ __device__ __forceinline__ uint4 ld_nc16(const void *ptr) {
     return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; grid_dep_wait() blocks until that kernel has completed and its
+// memory is visible, so nothing before it may touch global memory.
+// grid_dep_launch() lets the next kernel start early (it still waits).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_nc4(const void *ptr) {
     uint32_t v;
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"((uint64_t)ptr));

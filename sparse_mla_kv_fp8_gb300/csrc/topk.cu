@@ -293,15 +293,18 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
     __shared__ uint32_t decided[3];  // prefix, mask, need of the next pass
     __shared__ int totals[2];        // this CTA's keys above / equal to T
     const int G = gridDim.x, g = (int)cta_rank(), row = blockIdx.y, tid = threadIdx.x;
+    // the histogram copies start zeroed (each merge below re-zeroes them);
+    // this shared-memory setup may overlap the previous kernel's tail
+    for (int i = tid; i < kHistCopies * kTopkBins / 4; i += kClusterThreads)
+        ((uint4 *)copies)[i] = make_uint4(0, 0, 0, 0);
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();
     const int b = row / nq, j = row - b * nq;
     const int vis = max(0, seq_len[b] - nq + j + 1);
     const bool take_all = vis <= K;
     const int64_t base = ((int64_t)g * kClusterThreads + tid) * E;
     const float *src = scores + (size_t)row * stride;
 
-    // the histogram copies start zeroed (each merge below re-zeroes them)
-    for (int i = tid; i < kHistCopies * kTopkBins / 4; i += kClusterThreads)
-        ((uint4 *)copies)[i] = make_uint4(0, 0, 0, 0);
     uint32_t key[E];
     uint32_t valid = 0;  // bit e: token base + e is visible
 #pragma unroll
@@ -489,26 +492,16 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
     const int E = cluster_elems(p->cfg.max_tokens, rows);
     if (E) {
         const int G = (p->cfg.max_tokens + kClusterThreads * E - 1) / (kClusterThreads * E);
-        cudaLaunchConfig_t lc = {};
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = (unsigned)G;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        lc.gridDim = dim3((unsigned)G, (unsigned)rows);
-        lc.blockDim = dim3(kClusterThreads);
-        lc.dynamicSmemBytes = kClusterSmem;
-        lc.stream = st;
-        lc.attrs = at;
-        lc.numAttrs = 1;
+        PdlLaunch lc(dim3((unsigned)G, (unsigned)rows), dim3(kClusterThreads), kClusterSmem, st,
+                     dim3((unsigned)G, 1, 1));
         const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
         if (E == 8)
-            return cudaLaunchKernelEx(&lc, topk_cluster_kernel<8>, scores, stride, vec4,
+            return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<8>, scores, stride, vec4,
                                       (const int32_t *)p->d.seq_len, nq, K, topk);
         if (E == 16)
-            return cudaLaunchKernelEx(&lc, topk_cluster_kernel<16>, scores, stride, vec4,
+            return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<16>, scores, stride, vec4,
                                       (const int32_t *)p->d.seq_len, nq, K, topk);
-        return cudaLaunchKernelEx(&lc, topk_cluster_kernel<32>, scores, stride, vec4,
+        return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<32>, scores, stride, vec4,
                                   (const int32_t *)p->d.seq_len, nq, K, topk);
     }
     topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K);
