@@ -214,7 +214,6 @@ struct AttnTcArgs {
     __nv_bfloat16 *out;      // [rows][H][512]
     float *lse;
     float *part;             // [rows][H][splits][514]
-    int32_t *ticket;         // [rows][H/64] (unused)
     int cluster;             // splits == 2 launched as 2-CTA clusters
     int32_t *err;
 };
@@ -952,7 +951,6 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         a.out = (__nv_bfloat16 *)out;
         a.lse = lse;
         a.part = p->d.attn_part;
-        a.ticket = p->d.attn_ticket;
         a.err = p->d.err;
         a.cluster = splits == 2;
         dim3 grid(rows, a.H / kTcHeads, splits);

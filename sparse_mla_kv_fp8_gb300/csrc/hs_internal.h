@@ -78,7 +78,6 @@ struct DevPtrs {
     int32_t *miss_tok;          // [maxR][nq*K]
     int32_t *miss_slot;         // [maxR][nq*K]
     float *attn_part;           // split-K partials
-    int32_t *attn_ticket;       // per (query, 64-head group): split CTAs done
 };
 
 }  // namespace hs

@@ -129,7 +129,6 @@ hs_layout carve(const hs_pool_config *c, const Derived &d, size_t *extra_offs /*
     extra_offs[7] = cv.take(maxR * (size_t)d.nq * c->top_k * 4);      // miss tok
     extra_offs[8] = cv.take(maxR * (size_t)d.nq * c->top_k * 4);      // miss slot
     extra_offs[9] = cv.take(d.attn_part_floats * 4 + 16);             // attention partials
-    extra_offs[10] = cv.take(rows * (size_t)(c->mla_heads / 64 + 1) * 4);  // split tickets
     L.row_bytes = d.R;
     L.max_pages = d.max_pages;
     L.hot_rows = d.C;
@@ -273,7 +272,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->d.miss_tok = (int32_t *)(b + extra[7]);
     p->d.miss_slot = (int32_t *)(b + extra[8]);
     p->d.attn_part = (float *)(b + extra[9]);
-    p->d.attn_ticket = (int32_t *)(b + extra[10]);
 
     p->has_key_map = false;
     if (cfg->idx_fmt == HS_IDX_E4M3 && cfg->idx_dim == 128) {
@@ -310,7 +308,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     ms(p->d.err, 0, 16);
     ms(p->d.stats, 0, 32);
     ms(p->d.miss_count, 0, maxR * 4);
-    ms(p->d.attn_ticket, 0, maxR * (size_t)p->nq_max * (cfg->mla_heads / 64 + 1) * 4);
     if (e == cudaSuccess) e = hs::setup_kernel_attributes(p);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {

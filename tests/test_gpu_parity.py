@@ -140,12 +140,16 @@ def test_indexer_scores_bit_exact():
             r.close()
 
 
-def test_topk_ties_and_special_scores():
-    """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows."""
+@pytest.mark.parametrize("max_tokens", [0, 200064, 300032])
+def test_topk_ties_and_special_scores(max_tokens):
+    """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows.
+    The row capacity picks the kernel: one cluster launch with 8 keys per
+    thread (up to 20,032 tokens per row here) or 32 (200,064), and the
+    multi-kernel radix select beyond 262,144."""
     from harness import Case, Runner
     hs = _hs()
     case = Case("topk", B=4, N=[20000, 9000, 300, 16385], K=512, Hi=8, Di=32, H=16,
-                num_spec=1, mode=hs.HS_FULL)
+                num_spec=1, mode=hs.HS_FULL, max_tokens=max_tokens)
     r = Runner(case)
     try:
         stride = r.max_tokens
