@@ -337,9 +337,9 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 
 # DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
 # scaled x2 to 32 requests), valid only for the kernel source they were taken on.
-TRAFFIC = {"attention": ("attention.cu", "42d9e51e9e9fa9f5", 2 * (27678208 + 3584)),
-           "indexer": ("indexer.cu", "07fee34d4d82a7ba", 2 * (138589696 + 3918080)),
-           "topk": ("topk.cu", "06f579d674a4b22f", 2 * 4217856)}
+TRAFFIC = {"attention": ("attention.cu", "bd93543c825d34fe", 2 * (27680768 + 17920)),
+           "indexer": ("indexer.cu", "07fee34d4d82a7ba", 2 * (138583296 + 3882496)),
+           "topk": ("topk.cu", "84651904bae7fb98", 2 * 4217856)}
 
 
 def _traffic(stage):
