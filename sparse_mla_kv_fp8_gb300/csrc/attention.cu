@@ -13,16 +13,20 @@
 // rows dominate; magnitudes stay far inside fp16's range for scaled E4M3 rows):
 //   S^T[row][head] = R[row][:576] . Q[head][:576]   M=128 rows,  N=64, K=576
 //   O^T[dim][head] += R[row][dim] * P[row][head]    M=128 dims x4, N=64, K=128 rows
-// TMEM: two S^T buffers (2 x 64 columns) + O^T (4 x 64 columns).  The rows of
-// a 128-row chunk are dequantised (E4M3 x group scale -> fp16) by the worker
-// warps straight into nine 16 KB K-blocks with the 128-byte swizzle; the
+// TMEM: two S^T buffers (2 x 64 columns) + O^T (4 x 64 columns) + the
+// softmax denominators (64 columns, from a ones x P^T MMA).  Warp 0 issues the
+// MMAs, warp 1 owns TMEM, twelve worker warps dequantise the rows of each
+// 128-row chunk (E4M3 x group scale -> fp16) straight into nine 16 KB
+// K-blocks with the 128-byte swizzle; eight of them also run the softmax and
+// four the epilogue.  The
 // same K-blocks are the K-major A operand of S^T and the MN-major A operand
 // of O^T, so each row is converted once.  Softmax warps (thread = row = TMEM
 // lane) keep a per-head reference max in the log2 domain and rescale O^T
 // only when a chunk raises a head's maximum by more than 2^8; P^T (fp16) is
 // written over the rope K-block once S^T no longer needs it.  Per-K-block
 // mbarriers let the conversion of chunk c+1 overlap the O^T MMAs of chunk c.
-// Every wait is bounded.
+// Two row ranges of one query run as a 2-CTA cluster and merge through
+// distributed shared memory.  Every wait is bounded.
 //
 // General kernel (any head count that is a multiple of 8, both row formats):
 // a CTA owns (query, 8 heads, a range of the K entries); each chunk of 32
@@ -233,7 +237,7 @@ __device__ __forceinline__ bool bar_or_softmax(bool v) {
 
 __device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// The softmax group: warps 2-5 (heads 0-31) and loader warps 6-9 (heads 32-63).
+// The softmax group: warps 2-5 (heads 0-31) and warps 6-9 (heads 32-63).
 __device__ __forceinline__ bool bar_or_group(bool v) {
     uint32_t r;
     asm volatile(
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     // (thread = chunk row = TMEM lane); the two 32-head halves together form a
     // 256-thread group.  Returns false (uniformly) when a wait ran out.  With
     // kLow the scores are re-read from TMEM 16 heads at a time instead of held
-    // in 32 registers (the loader warps run it beside their own live state);
+    // in 32 registers (the worker warps run it beside their own live state);
     // S^T(c) is then released at the end, which costs nothing because S^T(c+2)
     // cannot start before the row buffer has been refilled after PV(c+1).
     auto softmax_part = [&](int c, int h_lo, auto low) -> bool {
