@@ -219,6 +219,7 @@ struct AttnTcArgs {
     float *lse;
     float *part;             // [rows][H][splits][514]
     int cluster;             // splits == 2 launched as 2-CTA clusters
+    int q_ready;             // q may be read before waiting for the previous kernel
     int32_t *err;
 };
 
@@ -339,7 +340,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
     // everything above touched only this CTA's shared memory and TMEM: the
     // setup overlaps the previous kernel's tail; the next kernel may start too
     tc::grid_dep_launch();
-    tc::grid_dep_wait();
+    // Only the worker warps touch global memory; they wait for the previous
+    // kernel below (after staging the queries when those were ready before it).
     const uint32_t s_col = 0;     // two S^T buffers: columns [0,64), [64,128)
     const uint32_t o_col = 128;   // O^T tiles: columns [128 + 64 g, ...)
     const uint32_t l_col = 384;   // per-row running sums of P: [384, 448)
@@ -565,8 +567,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         uint4 d0[3], d1[3];
         uint32_t f0[3], f1[3];
         int32_t idn[3];  // the next chunk's row ids load while this chunk converts
-#pragma unroll
-        for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(0, (wi >> 3) + 48 * u) : -1;
         auto issue_first = [&]() {  // row units and stage 0 of the chunk in idn
 #pragma unroll
             for (int u = 0; u < 3; u++) {
@@ -574,17 +574,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 ld_stage(ru[u], 0, d0[u], f0[u]);
             }
         };
-        {
-            // this CTA's 64 query heads -> nine K-major 128-byte-swizzled
-            // blocks, staged while the first rows are in flight
-            const uint8_t *qsrc = (const uint8_t *)(a.q + ((size_t)qr * a.H + hh * kTcHeads) * kLatent);
-            uint4 qv[12];
+        // this CTA's 64 query heads -> nine K-major 128-byte-swizzled blocks
+        const uint8_t *qsrc = (const uint8_t *)(a.q + ((size_t)qr * a.H + hh * kTcHeads) * kLatent);
+        uint4 qv[12];
+        auto q_load = [&]() {
 #pragma unroll
             for (int j = 0; j < 12; j++) {  // 64 heads x 72 slices of 16 B
                 const int i = wi + 384 * j, h = i / 72, c16 = i - h * 72;
                 qv[j] = tc::ld_nc16(qsrc + (size_t)h * (kLatent * 2) + c16 * 16);
             }
-            issue_first();
+        };
+        auto q_store = [&]() {
 #pragma unroll
             for (int j = 0; j < 12; j++) {
                 const int i = wi + 384 * j, h = i / 72, c16 = i - h * 72;
@@ -593,6 +593,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             tc::fence_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(q_full);
+        };
+        if (a.q_ready) {  // the queries overlap the previous kernel's tail
+            q_load();
+            q_store();
+        }
+        tc::grid_dep_wait();  // the row ids come from the previous kernel
+#pragma unroll
+        for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(0, (wi >> 3) + 48 * u) : -1;
+        if (a.q_ready) {
+            issue_first();
+        } else {  // the queries are staged while the first rows are in flight
+            q_load();
+            issue_first();
+            q_store();
         }
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
@@ -934,7 +948,8 @@ cudaError_t attention_setup(const hs_pool *p) {
 }
 
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
-                             int B, int nq, float scale, void *out, float *lse, cudaStream_t st) {
+                             int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
+                             bool q_ready) {
     const int rows = B * nq;
     const int K = p->cfg.top_k;
     const int splits = splits_for(p->cfg, rows);
@@ -957,6 +972,7 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         a.part = p->d.attn_part;
         a.err = p->d.err;
         a.cluster = splits == 2;
+        a.q_ready = q_ready;
         dim3 grid(rows, a.H / kTcHeads, splits);
         // the two splits of a (query, 64 heads) merge through DSMEM as a cluster
         PdlLaunch lc(grid, dim3(kAttnThreads), AttnTcSmem::bytes, st,

@@ -124,8 +124,12 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
                         int32_t *topk, cudaStream_t st);
 cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
                            cudaStream_t st);
+// q_ready: the queries were written before the previous kernel on `st`
+// started (true inside hs_step), so the kernel may stage them before it waits
+// for that kernel.
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
-                             int B, int nq, float scale, void *out, float *lse, cudaStream_t st);
+                             int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
+                             bool q_ready = false);
 int indexer_kernel_count(const hs_pool *p, int B, int nq);
 int topk_kernel_count(const hs_pool *p, int B, int nq);
 int resolve_kernel_count(const hs_pool *p, int B, int nq);

@@ -550,7 +550,8 @@ hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
     for (int l = 0; l < L && e == cudaSuccess; l++) {
         e = hs::launch_attention(p, l, (const uint8_t *)a->q_mla + l * qstride, a->row_id, B, nq,
                                  a->softmax_scale, (uint8_t *)a->out + l * ostride,
-                                 a->lse ? a->lse + (size_t)l * B * nq * H : nullptr, st);
+                                 a->lse ? a->lse + (size_t)l * B * nq * H : nullptr, st,
+                                 /*q_ready=*/true);
     }
     return cuda_status(e);
 }
