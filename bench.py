@@ -337,9 +337,9 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 
 # DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
 # scaled x2 to 32 requests), valid only for the kernel source they were taken on.
-TRAFFIC = {"attention": ("attention.cu", "bd93543c825d34fe", 2 * (27680768 + 17920)),
-           "indexer": ("indexer.cu", "07fee34d4d82a7ba", 2 * (138583296 + 3882496)),
-           "topk": ("topk.cu", "84651904bae7fb98", 2 * 4217856)}
+TRAFFIC = {"attention": ("attention.cu", "b6a9fc4f069a8b6a", 2 * (27685376 + 768)),
+           "indexer": ("indexer.cu", "07fee34d4d82a7ba", 2 * (138583552 + 3590656)),
+           "topk": ("topk.cu", "84651904bae7fb98", 2 * 4217600)}
 
 
 def _traffic(stage):
