@@ -62,8 +62,9 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # nvidia-smi is sampling before the timed region starts
         except Exception:
             self.proc = None
         return self
@@ -238,7 +239,8 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         t_wall = time.perf_counter() - t_wall
         # ---- per-stage timing (same step, eager, events between the stages) ----
-        stage = stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, args.steps)
+        stage = stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream,
+                            min(args.steps, 50))
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     if pool.get_error() != hs.HS_OK:
@@ -603,7 +605,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)  # ~0.6 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--requests", type=int, default=0, help="override requests per GPU")
