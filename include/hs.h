@@ -99,7 +99,11 @@ typedef struct {
     int32_t idx_fmt;        /* hs_idx_format                                    */
     int32_t hot_rows;       /* C: hot-buffer rows per request; 0 selects the
                                pages' rule (num_spec + 2) * top_k.  Must be a
-                               multiple of page_tokens and >= nq * top_k.      */
+                               multiple of page_tokens and >= top_k.  Below
+                               nq * top_k a step can find fewer free slots
+                               than misses: hs_resolve then serves the lowest
+                               missed tokens that fit, leaves the others
+                               unread (row id -1) and reports HS_ERR_CAPACITY */
     int32_t reserved;
     int64_t gpu_blocks;     /* blocks in the device pool (each P tokens x L rows);
                                gpu_blocks * P <= 2^31 - 1 (row ids are int32) and
@@ -254,7 +258,11 @@ hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
  * then exactly one row per layer is copied from pinned host memory into the
  * slot.  row_id: dev [B][nq][K] int32, the pool row (block * P + offset) each
  * entry reads, -1 for padding.  The step number is a per-request device
- * counter incremented by this call (so graph replays keep counting). */
+ * counter incremented by this call (so graph replays keep counting).  With a
+ * hot buffer below nq * K rows a request can have fewer slots not touched in
+ * this step than misses: every such slot takes a miss (lowest tokens first),
+ * the remaining misses get row id -1 (the attention skips them) and
+ * HS_ERR_CAPACITY is set in the sticky error word. */
 hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
                      int32_t *row_id, cudaStream_t stream);
 

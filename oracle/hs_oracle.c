@@ -245,17 +245,21 @@ static int cmp_slotkey(const void *a, const void *b)
  *  3. LRU eviction: the slots not used in this step (stamp < step) are
  *     ordered by (stamp, slot); the first M of them, M = number of misses,
  *     are the victims (never-used slots have stamp 0 and go first).  Fewer
- *     than M such slots is a capacity error.
+ *     than M such slots (only possible with a hot buffer below nq*K rows) is
+ *     a capacity error, handled gracefully: every such slot is a victim, the
+ *     first of the misses in ascending token order take them, the others
+ *     read nothing (located as 0, like padding), and the step still counts.
  *  4. The i-th miss in ascending token order goes to the i-th victim in
  *     ascending slot order (the pages do not say which victim takes which
  *     row; this is our canonical choice).  The evicted token leaves hot_map;
  *     the new token enters it with stamp = step.
  *  5. Each selected entry (j,k) is located: loc_kind 1 = resident, value =
  *     the token; 2 = hot buffer, value = the slot; 0 = padding (-1 entry).
- * Outputs: loc_kind/loc_val [nq][K]; the misses in order (miss_tok,
- * miss_slot, *n_miss); counts[0..3) = resident, hit, miss over U.
- * Returns HSO_OK, HSO_ERR_INDEX_RANGE (an index outside [0,N)) or
- * HSO_ERR_CAPACITY (fewer free-able slots than misses). */
+ * Outputs: loc_kind/loc_val [nq][K]; the misses that got a slot, in order
+ * (miss_tok, miss_slot, *n_miss); counts[0..3) = resident, hit, copied miss
+ * over U.  Returns HSO_OK, HSO_ERR_INDEX_RANGE (an index outside [0,N);
+ * nothing changes) or HSO_ERR_CAPACITY (fewer free-able slots than misses;
+ * the step is carried out as described in 3). */
 int hso_resolve(int32_t *hot_map, int32_t *slot_token, uint32_t *stamp,
                 uint32_t *step_io, int C, const uint8_t *page_resident,
                 int P, int N, const int32_t *idx, int nq, int K,
@@ -307,7 +311,6 @@ int hso_resolve(int32_t *hot_map, int32_t *slot_token, uint32_t *stamp,
             miss_tok[m++] = u;
         }
     }
-    counts[2] = m;
 
     /* 3. victims: least recently used slots not touched in this step */
     for (i = 0; i < C; i++)
@@ -316,10 +319,11 @@ int hso_resolve(int32_t *hot_map, int32_t *slot_token, uint32_t *stamp,
             cand[nc].slot = i;
             nc++;
         }
-    if (nc < m) {
+    if (nc < m) { /* capacity error: the first nc misses get the nc slots */
         status = HSO_ERR_CAPACITY;
-        goto done;
+        m = nc;
     }
+    counts[2] = m;
     qsort(cand, (size_t)nc, sizeof(hso_slotkey), cmp_slotkey);
     for (i = 0; i < m; i++)
         victim[i] = cand[i].slot;
@@ -338,7 +342,7 @@ int hso_resolve(int32_t *hot_map, int32_t *slot_token, uint32_t *stamp,
     *n_miss = m;
     for (i = 0, k = 0; i < nu; i++)
         if (slot_of[i] == -2)
-            slot_of[i] = victim[k++];
+            slot_of[i] = k < m ? victim[k++] : -3; /* -3: a miss left without a slot */
 
     /* 5. locations */
     for (j = 0; j < nq * K; j++) {
@@ -356,6 +360,9 @@ int hso_resolve(int32_t *hot_map, int32_t *slot_token, uint32_t *stamp,
         if (slot_of[lo] == -1) {
             loc_kind[j] = 1;
             loc_val[j] = u;
+        } else if (slot_of[lo] == -3) {
+            loc_kind[j] = 0;
+            loc_val[j] = -1;
         } else {
             loc_kind[j] = 2;
             loc_val[j] = slot_of[lo];

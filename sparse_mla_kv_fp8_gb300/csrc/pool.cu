@@ -74,7 +74,9 @@ bool valid_config(const hs_pool_config *c) {
     if (c->mla_heads % 8 != 0) return false;
     const int nq = c->num_spec + 1;
     const int64_t C = c->hot_rows ? c->hot_rows : (int64_t)(c->num_spec + 2) * c->top_k;
-    if (C % c->page_tokens != 0 || C < (int64_t)nq * c->top_k) return false;
+    // below nq * top_k rows a step may find fewer free slots than misses: it
+    // reports HS_ERR_CAPACITY and serves what fits
+    if (C % c->page_tokens != 0 || C < (int64_t)c->top_k) return false;
     if ((int64_t)nq * c->top_k > 16384) return false;  // resolve keeps the union in smem
     if (C > 16384) return false;
     return true;

@@ -14,7 +14,8 @@
 //   4. choose victims: among slots with stamp < step, the M smallest keys
 //      (stamp, slot), found by an 8-bit-digit radix select on the stamp plus a
 //      lowest-slot-first cut among equal stamps; victims are compacted in
-//      ascending slot order;
+//      ascending slot order (fewer such slots than misses: every one of them
+//      is a victim, the misses beyond read nothing, HS_ERR_CAPACITY);
 //   5. the i-th miss takes the i-th victim: hot_map / slot_token / stamp are
 //      updated and the (token, slot) pair goes to the device miss list;
 //   6. every (j, k) entry gets its pool row id (with one list, U is the list
@@ -230,13 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
             warp_sums);
     }
 
-    // 4. victims: the M smallest (stamp, slot) among slots with stamp < step
+    // 4. victims: the Ms smallest (stamp, slot) among slots with stamp < step,
+    // Ms = min(M, such slots).  With fewer such slots than misses (possible
+    // only with a hot buffer below nq * K rows) the first Ms misses in token
+    // order get a slot, the others read nothing, and HS_ERR_CAPACITY is set.
     int served = 0;
     if (M > 0) {
         const uint32_t *stp = a.stamp + sc;
         uint32_t prefix = 0, mask = 0;
-        int need = M;
-        bool enough = true;
+        int Ms = M, need = M;
         for (int pass = 0; pass < 4; pass++) {
             const int shift = 24 - 8 * pass;
             if (tid < 256) hist[tid] = 0;
@@ -249,10 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
             const int c = tid < 256 ? (int)hist[tid] : 0;
             int tot;
             const int ex = block_excl_scan(c, warp_sums, &tot);
-            if (pass == 0 && tot < M) {
-                enough = false;
-                break;
+            if (pass == 0 && tot < Ms) {  // uniform: tot is the block's total
+                if (tid == 0) set_error(a.err, HS_ERR_CAPACITY);
+                Ms = need = tot;
             }
+            if (Ms == 0) break;
             if (tid < 256 && ex < need && need <= ex + c) {
                 sel[0] = tid;
                 sel[1] = ex;
@@ -263,13 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
             need -= sel[1];
             __syncthreads();
         }
-        if (!enough) {
-            if (tid == 0) set_error(a.err, HS_ERR_CAPACITY);
-            for (int i = tid; i < M; i += kThreads) {
-                uslot[missidx[i]] = -3;
-                if (single) rid[missidx[i]] = -1;
-            }
-        } else {
+        if (Ms > 0) {
             // lt: stamp < S*, eq: stamp == S* (taken lowest slot first, `need` of them)
             const uint32_t S = prefix;
             const int seg = (a.C + kThreads - 1) / kThreads;
@@ -280,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
                 lt += v < S;
                 eq += (v == S) && (v < step);
             }
-            for (int i = tid; i < M; i += kThreads) victim[i] = -1;
+            for (int i = tid; i < Ms; i += kThreads) victim[i] = -1;
             __syncthreads();
             int tot;
             const int ex = block_excl_scan((eq << 16) | lt, warp_sums, &tot);
@@ -289,16 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
                 const uint32_t v = stp[s];
                 if (v < S) {
                     const int pos = lb + min(eb, need);
-                    if (pos < M) victim[pos] = s;
+                    if (pos < Ms) victim[pos] = s;
                     lb++;
                 } else if (v == S && v < step) {
-                    if (eb < need && lb + eb < M) victim[lb + eb] = s;
+                    if (eb < need && lb + eb < Ms) victim[lb + eb] = s;
                     eb++;
                 }
             }
             __syncthreads();
             // 5. assignment: i-th miss (ascending token) -> i-th victim (ascending slot)
-            for (int i = tid; i < M; i += kThreads) {
+            for (int i = tid; i < Ms; i += kThreads) {
                 const int32_t s = victim[i], u = miss[i];
                 if (s < 0 || s >= a.C) {  // cannot happen; never write outside the tables
                     set_error(a.err, HS_ERR_CAPACITY);
@@ -316,8 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
                 a.miss_tok[(size_t)b * n + i] = u;
                 a.miss_slot[(size_t)b * n + i] = s;
             }
-            served = M;
         }
+        for (int i = Ms + tid; i < M; i += kThreads) {  // misses left without a slot
+            uslot[missidx[i]] = -3;
+            if (single) rid[missidx[i]] = -1;
+        }
+        served = Ms;
     }
     if (tid == 0) {
         a.miss_count[b] = served;

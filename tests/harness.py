@@ -48,6 +48,7 @@ class Case:
     gpu_blocks: int = 0      # 0 = enough for the case
     host_blocks: int = 0     # 0 = every page of the case
     max_tokens: int = 0
+    allow_capacity: bool = False  # a hot buffer below nq*K may run short: expect HS_ERR_CAPACITY
 
 
 def _Ns(case):
@@ -151,19 +152,24 @@ class Runner:
                 self.pool.sparse_mla_decode(l, qm[l], row_id, B, nq, self.tau, out[l], lse[l])
         torch.cuda.synchronize()
         err = self.pool.get_error()
-        assert err == hs.HS_OK, f"device error {err}"
         got_idx = topk.cpu().numpy()
         np.testing.assert_array_equal(got_idx, ref_idx, err_msg=f"{c.name} step {s}: top-K")
         # oracle resolve
         res = []
+        short = False
         for b in range(B):
             resident = oracle.page_resident(self.modes[b], self.N[b], c.T, c.P)
             r = self.hot[b].resolve(resident, c.P, self.N[b], ref_idx[b])
-            assert r["status"] == 0
+            short |= r["status"] == oracle.ERR_CAPACITY
+            assert r["status"] == 0 or (c.allow_capacity and r["status"] == oracle.ERR_CAPACITY)
             res.append(r)
             self.stats["resident"] += r["resident"]
             self.stats["hits"] += r["hits"]
             self.stats["misses"] += r["misses"]
+        self.short_steps = getattr(self, "short_steps", 0) + int(short)
+        want = hs.HS_ERR_CAPACITY if short else hs.HS_OK
+        assert err == want, f"{c.name} step {s}: device status {err}, oracle expects {want}"
+        served = [r["loc_kind"] != 0 for r in res]  # entries that read a row
         rid = row_id.cpu().numpy()
         for b in range(B):
             st = self.pool.dump_state(b)
@@ -182,10 +188,11 @@ class Runner:
                 npg = (self.N[b] + c.P - 1) // c.P
                 np.testing.assert_array_equal(st["block_table"][:npg] >= 0, resident[:npg].astype(bool))
             # every resolved row holds the bytes of its token, for every layer
-            self._check_rows(b, ref_idx[b], row_id[b])
-        # attention
+            self._check_rows(b, np.where(served[b], ref_idx[b], -1), row_id[b])
+        # attention over the rows each query actually read
         if s % c.check_attn_every == 0 or s == 1:
-            self._check_attention(qm, out, lse, ref_idx)
+            self._check_attention(qm, out, lse, np.stack([np.where(served[b], ref_idx[b], -1)
+                                                          for b in range(B)]))
         # append
         if c.append:
             for b in range(B):

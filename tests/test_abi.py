@@ -64,7 +64,7 @@ def test_required_bytes_is_host_arithmetic(hs):
 @pytest.mark.parametrize("bad", [
     dict(max_requests=0), dict(top_k=0), dict(page_tokens=0), dict(mla_heads=12),
     dict(hot_rows=100),                 # not a multiple of the page
-    dict(hot_rows=128),                 # below nq * top_k
+    dict(hot_rows=128),                 # below top_k
     dict(num_spec=3, top_k=4096),       # union too large for one CTA
     dict(idx_dim=20),                   # E4M3 keys need 16-byte rows
     dict(row_fmt=7), dict(idx_fmt=9), dict(gpu_blocks=-1),

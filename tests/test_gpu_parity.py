@@ -400,6 +400,29 @@ def test_agentic_growth_flips_under_pool_cap():
         r.close()
 
 
+def test_hot_buffer_below_nq_k_serves_what_fits():
+    """A hot buffer smaller than nq*K (the pages' sizing relaxed): with MTP3
+    and 2K slots, zero residency and four disjoint-ish drawn lists per request,
+    the first steps find fewer free slots than misses.  Each such step reports
+    HS_ERR_CAPACITY, serves the lowest missed tokens that fit, and the
+    attention runs over the rows that were read, all exactly as the oracle;
+    later steps reuse the slots."""
+    from harness import Case, Runner
+    hs = _hs()
+    r = Runner(Case("short-hot", B=3, N=[3000, 2000, 1200], K=64, Hi=8, Di=32, H=128, L=2,
+                    mode=hs.HS_ZERO, num_spec=3, hot_rows=128, source="uniform_zipf",
+                    allow_capacity=True, steps=6))
+    try:
+        for _ in range(6):
+            r.run_step()
+        assert r.short_steps >= 1
+        st = r.pool.stats()
+        assert (st["resident"], st["hits"], st["misses"]) == (
+            r.stats["resident"], r.stats["hits"], r.stats["misses"])
+    finally:
+        r.close()
+
+
 def test_indexer_tensor_core_pipeline_wraps():
     """Enough tiles per CTA that the TMA ring and the two TMEM accumulators
     wrap several times (MTP3: 256 MMA columns, one CTA per SM)."""

@@ -331,11 +331,27 @@ def test_resolve_full_residency_never_misses():
 
 
 def test_resolve_capacity_error_when_buffer_too_small():
+    """Four misses, three slots: a capacity error, handled gracefully (our
+    reading: the pages plan to relax the hot-buffer sizing and say nothing
+    about a shortfall).  The three lowest tokens take the three slots, token
+    13 reads nothing, and the step counts."""
     P, N = 4, 64
     st = oracle.HotState(3, N)
     res = oracle.page_resident(oracle.ZERO, N, 0, P)
     r = st.resolve(res, P, N, np.array([[1, 5, 9, 13]], np.int32))
     assert r["status"] == oracle.ERR_CAPACITY
+    assert r["loc_kind"].tolist() == [[2, 2, 2, 0]]
+    assert r["loc_val"].tolist() == [[0, 1, 2, -1]]
+    assert (r["misses"], r["hits"], r["resident"]) == (3, 0, 0)
+    assert st.slot_token.tolist() == [1, 5, 9] and st.hot_map[13] == -1
+    assert int(st.step[0]) == 1
+    # next step: 13 and 1 again; 1 hits (stamp 2), 13 takes the oldest slot
+    # not used in this step (slot 1: stamp 1, lower than slot 2's)
+    r = st.resolve(res, P, N, np.array([[1, 13, -1, -1]], np.int32))
+    assert r["status"] == 0
+    assert r["loc_kind"].tolist() == [[2, 2, 0, 0]]
+    assert r["loc_val"].tolist() == [[0, 1, -1, -1]]
+    assert st.slot_token.tolist() == [1, 13, 9] and st.hot_map[5] == -1
 
 
 def test_resolve_capacity_rule_always_has_victims():
