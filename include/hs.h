@@ -185,10 +185,15 @@ hs_status hs_append(hs_pool *pool, int32_t req, const void *mla_rows,
                     const void *idx_keys, const float *idx_scale, int32_t n,
                     cudaStream_t stream);
 
-/* Change the residency of a request between steps.  full -> mixed: pages
- * outside the tail window release their GPU blocks (their host copies exist),
- * hot-buffer blocks are leased, every slot starts empty.  Needs a host pool.
- * Other transitions: HS_ERR_INVALID_ARG.  Synchronises `stream`. */
+/* Change the residency of a request between steps ("Les trois états de
+ * résidence": full, mixed, zero), in any direction.  Pages that the new mode
+ * keeps off the GPU (outside the tail window in mixed mode, all of them in
+ * zero mode) release their GPU blocks; pages it keeps on the GPU that are not
+ * there get a block and their rows copied back from the host pool; a hot
+ * buffer is leased when leaving full residency and returned when entering
+ * it; the hot buffer starts empty.  Needs a host pool (HS_ERR_INVALID_ARG
+ * otherwise); HS_ERR_CAPACITY, with nothing changed, when the pool lacks the
+ * blocks.  Synchronises `stream`. */
 hs_status hs_request_set_mode(hs_pool *pool, int32_t req, hs_mode mode,
                               cudaStream_t stream);
 

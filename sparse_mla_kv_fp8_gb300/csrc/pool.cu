@@ -437,32 +437,55 @@ hs_status hs_append(hs_pool *p, int32_t req, const void *mla_rows, const void *i
 
 hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_t st) {
     if (!req_ok(p, req) || p->mode[req] < 0) return HS_ERR_INVALID_ARG;
-    if (p->mode[req] == mode) return HS_OK;
-    if (!(p->mode[req] == HS_FULL && mode == HS_MIXED)) return HS_ERR_INVALID_ARG;
-    if (p->cfg.host_blocks == 0) return HS_ERR_INVALID_ARG;
+    if (mode != HS_FULL && mode != HS_MIXED && mode != HS_ZERO) return HS_ERR_INVALID_ARG;
+    const int cur = p->mode[req];
+    if (cur == mode) return HS_OK;
+    if (p->cfg.host_blocks == 0) return HS_ERR_INVALID_ARG;  // a flip needs the host copies
     const size_t mp = p->max_pages;
     int32_t *bt = p->block_table.data() + req * mp;
     int32_t *hbt = p->host_block_table.data() + req * mp;
+    int32_t *hot = p->hot_blocks.data() + (size_t)req * p->hot_pages;
+    const int P = p->cfg.page_tokens, L = p->cfg.num_mla_layers, R = p->R;
     const int64_t N = p->seq_len[req];
-    const int npages = (int)((N + p->cfg.page_tokens - 1) / p->cfg.page_tokens);
-    const int tail0 = first_tail_page(p, HS_MIXED, N);
-    for (int pg = 0; pg < std::min(tail0, npages); pg++)
-        if (bt[pg] >= 0 && hbt[pg] < 0) return HS_ERR_INVALID_ARG;  // no host copy
-    int freed = 0;
-    for (int pg = 0; pg < std::min(tail0, npages); pg++)
-        if (bt[pg] >= 0) freed++;
-    if ((int)p->free_gpu.size() + freed < p->hot_pages) return HS_ERR_CAPACITY;
-    for (int pg = 0; pg < std::min(tail0, npages); pg++)
-        if (bt[pg] >= 0) {
+    const int npages = (int)((N + P - 1) / P);
+    const int tail0 = first_tail_page(p, mode, N);  // pages >= tail0 are resident afterwards
+    // check everything before touching anything
+    int leave = 0, join = 0;
+    for (int pg = 0; pg < npages; pg++) {
+        if (hbt[pg] < 0) return HS_ERR_INVALID_ARG;  // every page has its host copy
+        if (pg < tail0 && bt[pg] >= 0) leave++;
+        if (pg >= tail0 && bt[pg] < 0) join++;
+    }
+    const int hot_in = (cur == HS_FULL) ? p->hot_pages : 0;   // a hot buffer to lease
+    const int hot_out = (mode == HS_FULL) ? p->hot_pages : 0;  // a hot buffer to return
+    if ((int64_t)p->free_gpu.size() + leave + hot_out < (int64_t)join + hot_in) return HS_ERR_CAPACITY;
+    for (int pg = 0; pg < npages; pg++)
+        if (pg < tail0 && bt[pg] >= 0) {
             p->free_gpu.push_back(bt[pg]);
             bt[pg] = -1;
         }
-    for (int i = 0; i < p->hot_pages; i++) {
-        p->hot_blocks[(size_t)req * p->hot_pages + i] = p->free_gpu.back();
-        p->free_gpu.pop_back();
-    }
-    p->mode[req] = HS_MIXED;
-    cudaError_t e = reset_hot(p, req, st);
+    if (hot_out)
+        for (int i = 0; i < p->hot_pages; i++) {
+            p->free_gpu.push_back(hot[i]);
+            hot[i] = -1;
+        }
+    cudaError_t e = cudaSuccess;
+    const size_t block_bytes = (size_t)L * P * R;
+    for (int pg = tail0; pg < npages && e == cudaSuccess; pg++)
+        if (bt[pg] < 0) {  // back onto the GPU: one block copied from the host pool
+            bt[pg] = p->free_gpu.back();
+            p->free_gpu.pop_back();
+            e = cudaMemcpyAsync(p->d.rows + (size_t)bt[pg] * block_bytes,
+                                p->host_base + (size_t)hbt[pg] * block_bytes, block_bytes,
+                                cudaMemcpyDefault, st);
+        }
+    if (hot_in)
+        for (int i = 0; i < p->hot_pages; i++) {
+            hot[i] = p->free_gpu.back();
+            p->free_gpu.pop_back();
+        }
+    p->mode[req] = mode;
+    if (e == cudaSuccess) e = reset_hot(p, req, st);
     if (e == cudaSuccess) e = upload_tables(p, req, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return cuda_status(e);

@@ -281,8 +281,13 @@ class Runner:
     def flip_to_mixed(self, b):
         """Full -> mixed between steps, on both sides: the oracle's hot buffer
         starts empty and the request's residency becomes the tail window."""
-        self.pool.set_mode(b, hs.HS_MIXED)
-        self.modes[b] = hs.HS_MIXED
+        self.set_mode(b, hs.HS_MIXED)
+
+    def set_mode(self, b, mode):
+        """Any residency change between steps, on both sides: the resident
+        pages follow the new mode and the hot buffer starts empty."""
+        self.pool.set_mode(b, mode)
+        self.modes[b] = mode
         self.hot[b] = oracle.HotState(self.C, self.max_tokens)
 
     def close(self):

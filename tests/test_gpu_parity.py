@@ -308,7 +308,7 @@ def test_host_side_capacity_errors():
             pool.open(1, hs.HS_MIXED)   # already open
         assert ei.value.status == hs.HS_ERR_INVALID_ARG
         with pytest.raises(hs.HSError) as ei:
-            pool.set_mode(0, hs.HS_ZERO)
+            pool.set_mode(0, 7)         # not a residency mode
         assert ei.value.status == hs.HS_ERR_INVALID_ARG
         with pytest.raises(hs.HSError) as ei:
             pool.resolve(torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"), 3, 1,
@@ -396,6 +396,32 @@ def test_agentic_growth_flips_under_pool_cap():
         assert (st["resident"], st["hits"], st["misses"]) == (
             r.stats["resident"], r.stats["hits"], r.stats["misses"])
         assert r.stats["misses"] > 0
+    finally:
+        r.close()
+
+
+def test_residency_round_trips_under_the_oracle():
+    """Residency changes in every direction between steps (full -> mixed ->
+    full, full -> zero -> mixed -> full), with appends in between; every step
+    against the oracle (indices, locations, hot-buffer state, row bytes,
+    attention), and the GPU pool gets every block back."""
+    from harness import Case, Runner
+    hs = _hs()
+    r = Runner(Case("round-trips", B=2, N=[1500, 900], K=128, Hi=8, Di=32, H=128, L=2, T=256,
+                    mode=hs.HS_FULL, append=3, steps=0, max_tokens=1600))
+    try:
+        free0 = r.pool.free_gpu_blocks()
+        plan = [None, (0, hs.HS_MIXED), None, (1, hs.HS_ZERO), None, (0, hs.HS_FULL),
+                (1, hs.HS_MIXED), None, (1, hs.HS_FULL), None]
+        for item in plan:
+            if item is not None:
+                r.set_mode(*item)
+            r.run_step()
+        assert r.modes == [hs.HS_FULL, hs.HS_FULL]
+        # back in full residency every page is on the GPU again, no hot buffer held
+        pages = sum((n + 63) // 64 for n in r.N)
+        assert r.pool.free_gpu_blocks() == free0 - (pages - sum((n + 63) // 64 for n in [1500, 900]))
+        assert r.stats["misses"] > 0 and r.stats["hits"] > 0
     finally:
         r.close()
 
