@@ -287,6 +287,39 @@ hs_status hs_sparse_mla_decode(hs_pool *pool, int32_t layer, const void *q,
                                float softmax_scale, void *out, float *lse,
                                cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Token-partitioned decode on one GPU ("Un contexte d'un million sur huit     */
+/* H200", « Ce qui se passe »: context parallelism shards a request's cache by */
+/* tokens; the global top-K is taken over the shards' candidates and the       */
+/* shards' attention partials are merged by their log-sum-exp).  A request's  */
+/* R shards are R pool requests holding consecutive token ranges; with rows =  */
+/* B * nq, shard r of row i is row r * rows + i of the batched calls.          */
+/* ------------------------------------------------------------------------ */
+
+/* Global top-K from the shards' local top-K lists.  scores: dev fp32 as written
+ * by hs_indexer_score for the R*B shard requests, [R][rows][score_stride];
+ * local_topk: dev [R][rows][K] (hs_topk of the shards: local token indices,
+ * ascending, -1 padded); offsets: dev [R] int32, ascending first global token
+ * of each shard.  Writes topk: dev [rows][K], the K best candidates by score
+ * (equal scores: lower global token first) as global tokens, ascending, -1
+ * padded: exactly hs_topk over the unsharded row, since every token of the
+ * global top-K is in its shard's top-K; and part_topk: dev [R][rows][K], each
+ * shard's entries of that list as local indices (ascending, -1 padded), the
+ * lists its hs_resolve / hs_sparse_mla_decode take.  K = the pool's top_k,
+ * R <= 8, R * K <= 16384 (HS_ERR_CAPACITY beyond, nothing enqueued). */
+hs_status hs_dcp_topk_merge(hs_pool *pool, const float *scores, int64_t score_stride,
+                            const int32_t *local_topk, const int32_t *offsets, int32_t R,
+                            int32_t rows, int32_t *topk, int32_t *part_topk,
+                            cudaStream_t stream);
+
+/* Merge the shards' attention outputs: o_parts dev [R][rows][H][512] bf16 and
+ * lse_parts dev [R][rows][H] fp32 (hs_sparse_mla_decode of each shard over
+ * its part_topk rows) -> out dev [rows][H][512] bf16 = sum_r w_r o_r with
+ * w_r = exp(lse_r - lse), lse = ln sum_r exp(lse_r) (written if lse != NULL).
+ * A shard without rows (lse -inf) weighs nothing.  R <= 8. */
+hs_status hs_dcp_combine(const void *o_parts, const float *lse_parts, int32_t R, int32_t rows,
+                         int32_t H, void *out, float *lse, cudaStream_t stream);
+
 typedef struct {
     int32_t B, nq;
     const void *q_idx;    /* dev [B][nq][Hi][Di], indexer format             */

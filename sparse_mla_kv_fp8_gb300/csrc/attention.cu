@@ -1011,10 +1011,12 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
 cudaError_t indexer_setup(const hs_pool *p);
 cudaError_t resolve_setup(const hs_pool *p);
 cudaError_t topk_setup(const hs_pool *p);
+cudaError_t dcp_setup(const hs_pool *p);
 
 cudaError_t setup_kernel_attributes(const hs_pool *p) {
     cudaError_t e = indexer_setup(p);
     if (e == cudaSuccess) e = topk_setup(p);
+    if (e == cudaSuccess) e = dcp_setup(p);
     if (e == cudaSuccess) e = resolve_setup(p);
     if (e == cudaSuccess) e = attention_setup(p);
     return e;

@@ -93,6 +93,8 @@ hs_pool_dump_state = _decl("hs_pool_dump_state", _i32, [_P, _i32, _P, _P, _P, _P
 hs_pool_load_state = _decl("hs_pool_load_state", _i32, [_P, _i32, _P, _P, _P, _u32])
 hs_topk_noalloc = _decl("hs_topk_noalloc", _i32, [_P, _i64, _P, _i32, _i32, _i32, _i32, _P, _P])
 hs_check_wait_timeout = _decl("hs_check_wait_timeout", _i32, [_P, _i64, _P])
+hs_dcp_topk_merge = _decl("hs_dcp_topk_merge", _i32, [_P, _P, _i64, _P, _P, _i32, _i32, _P, _P, _P])
+hs_dcp_combine = _decl("hs_dcp_combine", _i32, [_P, _P, _i32, _i32, _i32, _P, _P, _P])
 hs_step_kernel_count = _decl("hs_step_kernel_count", _i32, [_P, _i32, _i32])
 hs_status_string = _decl("hs_status_string", ctypes.c_char_p, [_i32])
 hs_abi_version = _decl("hs_abi_version", _i32, [])
@@ -107,6 +109,11 @@ class HSError(RuntimeError):
 def check(status: int, what: str = "hs call") -> None:
     if status != HS_OK:
         raise HSError(status, what)
+
+
+def dcp_combine(o_parts, lse_parts, R, rows, H, out, lse=None, stream=None):
+    check(hs_dcp_combine(_ptr(o_parts), _ptr(lse_parts), R, rows, H, _ptr(out), _ptr(lse),
+                         _stream(stream)), "hs_dcp_combine")
 
 
 def make_config(**kw) -> hs_pool_config:
@@ -208,6 +215,12 @@ class Pool:
     def sparse_mla_decode(self, layer, q, row_id, B, nq, scale, out, lse=None, stream=None):
         check(hs_sparse_mla_decode(self.handle, layer, _ptr(q), _ptr(row_id), B, nq, scale,
                                    _ptr(out), _ptr(lse), _stream(stream)), "hs_sparse_mla_decode")
+
+    def dcp_topk_merge(self, scores, stride, local_topk, offsets, R, rows, topk, part_topk,
+                       stream=None):
+        check(hs_dcp_topk_merge(self.handle, _ptr(scores), stride, _ptr(local_topk),
+                                _ptr(offsets), R, rows, _ptr(topk), _ptr(part_topk),
+                                _stream(stream)), "hs_dcp_topk_merge")
 
     def check_wait_timeout(self, limit_cycles, stream=None):
         check(hs_check_wait_timeout(self.handle, limit_cycles, _stream(stream)),

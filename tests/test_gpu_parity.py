@@ -426,6 +426,80 @@ def test_residency_round_trips_under_the_oracle():
         r.close()
 
 
+def test_dcp_token_shards_match_the_unsharded_request():
+    """Context-parallel decode emulated on one GPU: each of B requests is cut
+    into R consecutive token shards held as R pool requests; the indexer and
+    top-K run per shard, hs_dcp_topk_merge takes the global top-K over the
+    shards' candidates (exactly the oracle's top-K of the whole request) and
+    splits it back per shard, each shard resolves and attends over its part,
+    and hs_dcp_combine merges the partials by their lse (the oracle's
+    attention over the whole top-K, within tolerance)."""
+    hs = _hs()
+    B, R, K, L, H, P, seed = 2, 3, 256, 1, 128, 64, 5
+    lens = [1000, 1024, 980]
+    offs = [0, 1000, 2024]
+    N = sum(lens)
+    dev = torch.device("cuda")
+    cfg = hs.make_config(max_requests=R * B, max_tokens=1024, page_tokens=P, top_k=K,
+                         num_spec=0, tail_tokens=0, num_mla_layers=L, mla_heads=H, idx_heads=64,
+                         idx_dim=128, row_fmt=hs.HS_ROW_E4M3_656, idx_fmt=hs.HS_IDX_E4M3,
+                         gpu_blocks=R * B * 16 + 8)
+    pool = hs.Pool(cfg, device=dev)
+    try:
+        truth = [wl.mla_rows(seed, b, 0, N, L, wl.ROW_E4M3_656, device=dev) for b in range(B)]
+        keys = [wl.idx_keys(seed, b, 0, N, 128, wl.IDX_E4M3, device=dev) for b in range(B)]
+        for r in range(R):
+            for b in range(B):
+                pool.open(r * B + b, hs.HS_FULL)
+                sl = slice(offs[r], offs[r] + lens[r])
+                pool.append(r * B + b, truth[b][sl].contiguous(), keys[b][sl].contiguous())
+        q = torch.stack([wl.idx_query(seed, b, 1, 1, 64, 128, wl.IDX_E4M3, dev) for b in range(B)])
+        w = torch.stack([wl.idx_weights(seed, b, 1, 1, 64, dev) for b in range(B)])
+        qm = wl.mla_query(seed, 1, B, 1, H, L, dev)
+        stride = 1024
+        scores = torch.empty((R * B, 1, stride), dtype=torch.float32, device=dev)
+        pool.indexer_score(q.repeat(R, 1, 1, 1).contiguous(), w.repeat(R, 1, 1).contiguous(),
+                           R * B, 1, scores, stride)
+        local = torch.empty((R * B, 1, K), dtype=torch.int32, device=dev)
+        pool.topk(scores, stride, R * B, 1, local)
+        topk = torch.full((B, 1, K), -7, dtype=torch.int32, device=dev)
+        part = torch.full((R * B, 1, K), -7, dtype=torch.int32, device=dev)
+        pool.dcp_topk_merge(scores, stride, local, torch.tensor(offs, dtype=torch.int32, device=dev),
+                            R, B, topk, part)
+        rid = torch.empty_like(part)
+        pool.resolve(part, R * B, 1, rid)
+        o_parts = torch.empty((R * B, 1, H, 512), dtype=torch.bfloat16, device=dev)
+        lse_parts = torch.empty((R * B, 1, H), dtype=torch.float32, device=dev)
+        tau = 1.0 / math.sqrt(576)
+        pool.sparse_mla_decode(0, qm[0].repeat(R, 1, 1, 1).contiguous(), rid, R * B, 1, tau,
+                               o_parts, lse_parts)
+        out = torch.empty((B, 1, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, 1, H), dtype=torch.float32, device=dev)
+        hs.dcp_combine(o_parts, lse_parts, R, B, H, out, lse)
+        torch.cuda.synchronize()
+        assert pool.get_error() == hs.HS_OK
+        tk, pt = topk.cpu().numpy(), part.cpu().numpy()
+        for b in range(B):
+            s_full = oracle.indexer_scores(oracle.IDX_E4M3, q[b].cpu().numpy(), w[b].cpu().numpy(),
+                                           keys[b].cpu().numpy(), np.ones(N, np.float32), N)
+            ref = oracle.topk(s_full[0], N, K)
+            np.testing.assert_array_equal(tk[b, 0], ref)
+            for r in range(R):
+                mine = ref[(ref >= offs[r]) & (ref < offs[r] + lens[r])] - offs[r]
+                want = np.full(K, -1, np.int32)
+                want[:len(mine)] = mine
+                np.testing.assert_array_equal(pt[r * B + b, 0], want)
+            rows = truth[b][torch.from_numpy(ref).long().to(dev), 0].cpu().numpy()
+            qb = qm[0, b, 0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            o, ls = oracle.attention(oracle.ROW_E4M3_656, qb, rows, tau)
+            g = out[b, 0].float().cpu().numpy()
+            assert (np.abs(g - o) <= 2e-3 + 1e-2 * np.abs(o)).all(), np.abs(g - o).max()
+            gl = lse[b, 0].cpu().numpy()
+            assert (np.abs(gl - ls) <= 2e-3 + 1e-2 * np.abs(ls)).all()
+    finally:
+        pool.close()
+
+
 def test_hot_buffer_below_nq_k_serves_what_fits():
     """A hot buffer smaller than nq*K (the pages' sizing relaxed): with MTP3
     and 2K slots, zero residency and four disjoint-ish drawn lists per request,

@@ -456,3 +456,24 @@ def test_page_constants_fixture_matches_capacity_rule():
     assert pc["hot_rows_per_topk_default"]["value"] * K == (0 + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K
     ns = pc["mtp_speculative_tokens"]["value"]
     assert (ns + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K == 10240
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_topk_of_shard_candidates_equals_topk_of_the_whole(seed):
+    """The property the context-parallel merge rests on: the top-K of a row
+    is the top-K of the union of its shards' top-K lists (ties to the lower
+    token, with heavy ties in the scores)."""
+    rng = np.random.default_rng(seed)
+    N, K = 700, 64
+    s = rng.integers(0, 30, N).astype(np.float32)  # many equal scores
+    whole = oracle.topk(s, N, K)
+    cuts = sorted(rng.choice(np.arange(1, N), 3, replace=False).tolist())
+    bounds = [0] + cuts + [N]
+    cand = []
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        loc = oracle.topk(s[lo:hi], hi - lo, K)
+        cand += [lo + t for t in loc if t >= 0]
+    cand = np.array(cand)
+    order = np.lexsort((cand, -s[cand]))  # score descending, then token ascending
+    merged = np.sort(cand[order[:K]])
+    np.testing.assert_array_equal(merged, whole)
