@@ -269,6 +269,18 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
                       bf16x2_to_f16x2(v.w));
 }
 
+// An E4M3 pair times its group scale s, as fp16: the E4M3 values are exact in
+// fp16 and s = s_hi + s_lo is split into two fp16s, so fma(x, s_hi, x * s_lo)
+// rounds x * s once (up to the ~2^-18 of s that the split drops) in two
+// half2 instructions instead of a widen / fp32 multiply / narrow per value.
+// Below 2^-14 (fp16 subnormals) the split keeps s to 2^-25 absolute, so a
+// value moves by at most 448 * 2^-25 (about 1.3e-5).
+__device__ __forceinline__ uint32_t e4m3x2_scaled(__nv_fp8x2_storage_t v, __half2 s_hi, __half2 s_lo) {
+    const __half2 x = __half2(__nv_cvt_fp8x2_to_halfraw2(v, __NV_E4M3));
+    const __half2 y = __hfma2(x, s_hi, __hmul2(x, s_lo));
+    return *(const uint32_t *)&y;
+}
+
 // 2^x with the hardware approximation (max 2 ulp); 2^-inf = +0.
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -528,13 +540,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         // ------------------------------------------------------- row workers
         // Twelve warps convert each chunk.  A stage is one 128-dim scale group
         // (K-blocks 2g and 2g+1) or the rope block; its 1024 (row, 16-byte
-        // slice) units go to worker wi as units wi + 384u: slice c8 = wi % 8 of
-        // rows wi/8 + 48u (u = 0, 1, and 2 for wi < 256).  Loads run two
+        // slice) units are spread so that worker warp w holds rows 4w + 48u
+        // .. 4w + 48u + 3 (u = 0, 1, and 2 for w < 8), 8 slices each.  Each
+        // 8-lane group takes slices 0-3 or 4-7 of two adjacent rows, i.e. one
+        // K-block: the 128-byte swizzle puts an even and an odd row's chunks
+        // in disjoint bank slots, so the group's 16-byte stores are free of
+        // bank conflicts (slices 0-3 and 4-7 of one row would land in two
+        // K-blocks 16 KB apart, in the same slots); the rope stage swaps the
+        // slice halves of odd rows for the same reason.  Loads run two
         // stages ahead of the conversion.  Warps 2-9 also run the softmax
         // (heads 0-31 on warps 2-5, 32-63 on warps 6-9) and warps 2-5 the
         // epilogue.
         const int wi = threadIdx.x - 64;  // 0..383
-        const int c8 = wi & 7;
+        const int c8 = (lane & 3) | (((lane >> 3) & 1) << 2);
+        const int rw = (wi >> 5) * 4 + ((lane >> 4) & 1) * 2 + ((lane >> 2) & 1);  // row of u = 0
+        const int c8r = c8 ^ ((rw & 1) << 2);  // rope slice
         const int nu = wi < 256 ? 3 : 2;
         auto id_at = [&](int c, int r) -> int32_t {
             const int k = k0 + c * kTcRows + r;
@@ -552,7 +572,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             return (blk * (uint32_t)a.L + (uint32_t)a.layer) * (uint32_t)a.P + off;
         };
         const uint4 z = make_uint4(0, 0, 0, 0);
-        // stage st of row unit ru: 16 bytes of slice c8 and (st < 4) its scale
+        // stage st of row unit ru: 16 bytes of slice c8 (c8r for the rope) and
+        // (st < 4) its scale
         auto ld_stage = [&](uint32_t ru, int st, uint4 &d, uint32_t &sc) {
             if (ru == ~0u) {
                 d = z;
@@ -560,7 +581,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 return;
             }
             const uint8_t *row = a.pool + (size_t)ru * 656;
-            d = tc::ld_nc16(row + (st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8));
+            d = tc::ld_nc16(row + (st < 4 ? 128 * st + 16 * c8 : 528 + 16 * c8r));
             sc = st < 4 ? tc::ld_nc4(row + 512 + 4 * st) : 0u;
         };
         uint32_t ru[3];
@@ -600,7 +621,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         }
         tc::grid_dep_wait();  // the row ids come from the previous kernel
 #pragma unroll
-        for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(0, (wi >> 3) + 48 * u) : -1;
+        for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(0, rw + 48 * u) : -1;
         if (a.q_ready) {
             issue_first();
         } else {  // the queries are staged while the first rows are in flight
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
         bool ok = true;
         for (int c = 0; c < nchunks; c++) {
 #pragma unroll
-            for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(c + 1, (wi >> 3) + 48 * u) : -1;
+            for (int u = 0; u < 3; u++) idn[u] = u < nu ? id_at(c + 1, rw + 48 * u) : -1;
             if (ok) {
 #pragma unroll
                 for (int st = 0; st < 5; st++) {
@@ -636,22 +657,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
 #pragma unroll
                     for (int u = 0; u < 3; u++) {
                         if (u >= nu) continue;
-                        const int r = (wi >> 3) + 48 * u;
+                        const int r = rw + 48 * u;
                         if (st < 4) {
                             const float scl = __uint_as_float(f0[u]);
+                            const __half s_hi = __float2half_rn(scl);
+                            const __half2 shi2 = __half2half2(s_hi);
+                            const __half2 slo2 = __half2half2(__float2half_rn(scl - __half2float(s_hi)));
                             const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&d0[u];
                             uint32_t packed[8];
 #pragma unroll
-                            for (int e = 0; e < 8; e++) {
-                                __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pp[e], __NV_E4M3);
-                                const float2 f2v = __half22float2(__half2(h2));
-                                packed[e] = pack_f16(f2v.x * scl, f2v.y * scl);
-                            }
+                            for (int e = 0; e < 8; e++) packed[e] = e4m3x2_scaled(pp[e], shi2, slo2);
                             const int q0 = (c8 & 3) * 2;
                             *(uint4 *)(dst + tc::sw128_offset(r, q0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                             *(uint4 *)(dst + tc::sw128_offset(r, q0 + 1)) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                         } else {
-                            *(uint4 *)(dst + tc::sw128_offset(r, c8)) = bf16x8_to_f16x8(d0[u]);  // rope
+                            *(uint4 *)(dst + tc::sw128_offset(r, c8r)) = bf16x8_to_f16x8(d0[u]);  // rope
                         }
                     }
                     tc::fence_async_smem();
