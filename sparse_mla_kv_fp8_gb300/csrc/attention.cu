@@ -647,8 +647,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                         for (int u = 0; u < 3; u++) ld_stage(ru[u], st + 2, d2[u], f2[u]);
                     }
                     const int kb = st < 4 ? 2 * st + (c8 >> 2) : 8;
-                    bool w = tc::mbar_wait(&kb_empty[kb], (c & 1) ^ 1, a.err);
-                    if (st < 4) w &= tc::mbar_wait(&kb_empty[kb ^ 1], (c & 1) ^ 1, a.err);
+                    // K-blocks 2st and 2st+1 are released by one commit pair
+                    // after the same O^T MMAs: one wait covers both
+                    const bool w = tc::mbar_wait(&kb_empty[st < 4 ? 2 * st : 8], (c & 1) ^ 1, a.err);
                     if (!__all_sync(0xffffffffu, w)) {  // the warp leaves together
                         ok = false;
                         break;
