@@ -49,13 +49,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Upper bound of one wait, in SM clock cycles (about a second at 2 GHz).
 constexpr long long kWaitCycles = 2000000000LL;
 
-// Wait for the phase with the given parity; false (and the error word set)
-// when `limit` cycles run out.  Never spins forever.
-__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, int32_t *err,
-                                                long long limit) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The polling loop of a wait whose phase had not completed at the first
+// look, kept out of line: the hot loops inline only the first try_wait, which
+// keeps their instruction footprint small.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *err,
+                                            long long limit) {
     const long long t0 = clock64();
     while (true) {
+#pragma unroll 1
         for (int i = 0; i < 64; i++)
             if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > limit) {
@@ -63,6 +64,14 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, 
             return false;
         }
     }
+}
+
+// Wait for the phase with the given parity; false (and the error word set)
+// when `limit` cycles run out.  Never spins forever.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, int32_t *err,
+                                                long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, limit);
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
