@@ -338,21 +338,23 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 
 
 # DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
-# scaled x2 to 32 requests), valid only for the kernel source they were taken on.
-TRAFFIC = {"attention": ("attention.cu", "b6a9fc4f069a8b6a", 2 * (27685376 + 768)),
-           "indexer": ("indexer.cu", "07fee34d4d82a7ba", 2 * (138583552 + 3590656)),
-           "topk": ("topk.cu", "84651904bae7fb98", 2 * 4217600)}
+# scaled x2 to 32 requests), valid only for the kernel sources they were taken
+# on (the kernel's .cu and the shared device header, hashed together).
+TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "933a9b322fe33ee4", 2 * (27639424 + 2432)),
+           "indexer": (("indexer.cu", "tc.cuh"), "7f865c4af972bae9", 2 * (138576384 + 2607744)),
+           "topk": (("topk.cu", "tc.cuh"), "857b81922f2dd024", 2 * 4217600)}
 
 
 def _traffic(stage):
     import hashlib
     if stage not in TRAFFIC:
         return None
-    fname, sha, nbytes = TRAFFIC[stage]
-    path = os.path.join(ROOT, "sparse_mla_kv_fp8_gb300", "csrc", fname)
-    with open(path, "rb") as f:
-        cur = hashlib.sha256(f.read()).hexdigest()[:16]
-    return nbytes if cur == sha else None
+    files, sha, nbytes = TRAFFIC[stage]
+    h = hashlib.sha256()
+    for fname in files:
+        with open(os.path.join(ROOT, "sparse_mla_kv_fp8_gb300", "csrc", fname), "rb") as f:
+            h.update(f.read())
+    return nbytes if h.hexdigest()[:16] == sha else None
 
 
 KERNELS = {"indexer": "indexer_tc_kernel", "topk": "topk_cluster_kernel",
