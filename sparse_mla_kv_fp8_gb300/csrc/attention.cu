@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_data), peer));
             const bool w0 = tc::mbar_wait_cluster(peer_data, 0, a.err);
             if (!bar_or_group(!w0)) {
-                float *wf = red;  // [0,64): own weight, [64,128): the peer's, [128,192): 1/L
+                float *wf = red;  // [0,64): own weight / L, [64,128): the peer's weight / L
                 if (warp < 6 && r < 64) {
                     const float l0 = good ? lsum[r] : 0.f, l1 = rx_l[r];
                     const float m0 = l0 > 0.f ? mref[r] : -INFINITY, m1 = rx_m[r];
@@ -791,9 +791,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                     const float w0v = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
                     const float w1v = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
                     const float Ls = l0 * w0v + l1 * w1v;
-                    wf[r] = w0v;
-                    wf[64 + r] = w1v;
-                    wf[128 + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                    wf[r] = w0v * inv;
+                    wf[64 + r] = w1v * inv;
                     if (a.lse && split == 0) a.lse[g0 + r] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
                 }
                 bar_group();
@@ -813,11 +813,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                         for (int q4 = 0; q4 < 4; q4++) {
                             const int hq = (h0 >> 2) + q4;
                             const float4 pv = *(const float4 *)(rx + ((gi * 16 + hq) * 128 + r) * 4);
+                            const float4 fa = *(const float4 *)(wf + 4 * hq);       // broadcast
+                            const float4 fb = *(const float4 *)(wf + 64 + 4 * hq);  // broadcast
                             const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+                            const float wa[4] = {fa.x, fa.y, fa.z, fa.w};
+                            const float wb[4] = {fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
                             for (int e = 0; e < 4; e++) {
                                 const int h = 4 * hq + e;
-                                const float v = (ov[4 * q4 + e] * wf[h] + pp[e] * wf[64 + h]) * wf[128 + h];
+                                const float v = fmaf(ov[4 * q4 + e], wa[e], pp[e] * wb[e]);
                                 ostage[h * 256 + gi * 128 + r] = __float2bfloat16(v);
                             }
                         }
