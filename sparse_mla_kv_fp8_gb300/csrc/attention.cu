@@ -749,7 +749,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             float *rx_l = rx_m + 64;
             __nv_bfloat16 *ostage = (__nv_bfloat16 *)(rb + 72 * 1024);
             // this CTA's row buffer is idle once every MMA completed
-            if (warp == 4 && lane == 0) tc::mbar_arrive_remote(tc::mapa(tc::smem_addr(peer_ready), peer));
+            // (relaxed: it hands over no data; this CTA's MMAs were seen done
+            // through o_done above)
+            if (warp == 4 && lane == 0) tc::mbar_arrive_remote_relaxed(tc::mapa(tc::smem_addr(peer_ready), peer));
             const bool w1 = tc::mbar_wait_cluster(peer_ready, 0, a.err);
             if (!bar_or_group(!w1)) {
                 const uint32_t dst = tc::mapa(tc::smem_addr(rx), peer);
