@@ -340,9 +340,9 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 # DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
 # scaled x2 to 32 requests), valid only for the kernel sources they were taken
 # on (the kernel's .cu and the shared device header, hashed together).
-TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "933a9b322fe33ee4", 2 * (27639424 + 2432)),
-           "indexer": (("indexer.cu", "tc.cuh"), "7f865c4af972bae9", 2 * (138576384 + 2607744)),
-           "topk": (("topk.cu", "tc.cuh"), "857b81922f2dd024", 2 * 4217600)}
+TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "064ca91a8c94fe16", 2 * (27639552 + 7872)),
+           "indexer": (("indexer.cu", "tc.cuh"), "9a866511fdda6dfb", 2 * (138579328 + 2516224)),
+           "topk": (("topk.cu", "tc.cuh"), "d5606232ac340f23", 2 * 4217856)}
 
 
 def _traffic(stage):
