@@ -342,12 +342,13 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 # on (the kernel's .cu and the shared device header, hashed together).
 TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "064ca91a8c94fe16", 2 * (27639552 + 7872)),
            "indexer": (("indexer.cu", "tc.cuh"), "9a866511fdda6dfb", 2 * (138579328 + 2516224)),
-           "topk": (("topk.cu", "tc.cuh"), "d5606232ac340f23", 2 * 4217856)}
+           "topk": (("topk.cu", "tc.cuh"), "cf9fadfe87a5a0c2", 2 * 4227328)}
 
 
-def _traffic(stage):
+def _traffic(stage, w):
     import hashlib
-    if stage not in TRAFFIC:
+    # the figures are per launch of the 32-request workload only
+    if stage not in TRAFFIC or w != WORKLOAD:
         return None
     files, sha, nbytes = TRAFFIC[stage]
     h = hashlib.sha256()
@@ -379,13 +380,13 @@ def roofline(stage, alg, peaks, w):
         if k == "attention":
             tf = a["flops"] / (ms / 1e3) / 1e12
             out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16_sus"],
-                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": _traffic(k),
+                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": _traffic(k, w),
                       "peak_source": peaks["src"] + " bf16 sustained (fp16 operands: the same dense rate)",
                       "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
                       "share_of_step": share[k] / tot, "us_per_launch": ms * 1e3}
         else:
             out[k] = {"kernel": KERNELS[k], "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": _traffic(k),
+                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": _traffic(k, w),
                       "peak_source": peaks["src"], "share_of_step": share[k] / tot,
                       "us_per_launch": ms * 1e3}
     dom = max(share, key=share.get)

@@ -456,26 +456,25 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
 }
 
 // Elements per thread for the one-launch path, or 0 when rows are too long.
-// Prefers the widest cluster that keeps every row's CTAs in one wave.
+// Measured on GB300 with rows of 65,536 tokens: 16 keys per thread (4-CTA
+// clusters) beat 8 keys (8-CTA clusters: 38.9 against 21.6 us at 16 rows)
+// and 32 keys (2-CTA clusters: 28.7 against 22.5 us at 32 rows): the cluster
+// barriers and distributed-shared-memory merges grow with the cluster, the
+// histogram work with the keys per thread.  So 16 keys per thread while
+// every row's CTAs fit one wave; otherwise 32, whose rows cost fewer CTA-
+// microseconds (2 x 28.7 against 4 x 22.5) and fit one wave up to twice as
+// many rows.
 int cluster_elems(int max_tokens, int rows) {
-    int best = 0;
-    for (int e : {8, 16, 32}) {
-        const int G = (max_tokens + kClusterThreads * e - 1) / (kClusterThreads * e);
-        if (G > kClusterMax) continue;
-        if (best == 0) best = e;
-        if ((int64_t)rows * G <= kNumSMs) return e;
-    }
-    return best;
+    auto ctas = [&](int e) { return (max_tokens + kClusterThreads * e - 1) / (kClusterThreads * e); };
+    if (ctas(16) <= kClusterMax && (int64_t)rows * ctas(16) <= kNumSMs) return 16;
+    return ctas(32) <= kClusterMax ? 32 : 0;
 }
 
 }  // namespace
 
 cudaError_t topk_setup(const hs_pool *) {
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kClusterSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kClusterSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(topk_cluster_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kClusterSmem);
@@ -495,9 +494,6 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
         PdlLaunch lc(dim3((unsigned)G, (unsigned)rows), dim3(kClusterThreads), kClusterSmem, st,
                      dim3((unsigned)G, 1, 1));
         const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
-        if (E == 8)
-            return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<8>, scores, stride, vec4,
-                                      (const int32_t *)p->d.seq_len, nq, K, topk);
         if (E == 16)
             return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<16>, scores, stride, vec4,
                                       (const int32_t *)p->d.seq_len, nq, K, topk);
