@@ -16,9 +16,10 @@
 // TMEM: two S^T buffers (2 x 64 columns) + O^T (4 x 64 columns) + the
 // softmax denominators (64 columns, from a ones x P^T MMA).  Warp 0 issues the
 // MMAs, warp 1 owns TMEM, twelve worker warps dequantise the rows of each
-// 128-row chunk (E4M3 x group scale -> fp16) straight into nine 16 KB
-// K-blocks with the 128-byte swizzle; eight of them also run the softmax and
-// four the epilogue.  The
+// 128-row chunk (E4M3 x group scale -> fp16, in half2 with the scale split
+// into two fp16s) straight into nine 16 KB K-blocks with the 128-byte
+// swizzle; eight of them also run the softmax, and four (eight in a 2-CTA
+// cluster) the epilogue.  The
 // same K-blocks are the K-major A operand of S^T and the MN-major A operand
 // of O^T, so each row is converted once.  Softmax warps (thread = row = TMEM
 // lane) keep a per-head reference max in the log2 domain and rescale O^T
