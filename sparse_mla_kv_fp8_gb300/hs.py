@@ -112,8 +112,8 @@ def check(status: int, what: str = "hs call") -> None:
 
 
 def dcp_combine(o_parts, lse_parts, R, rows, H, out, lse=None, stream=None):
-    check(hs_dcp_combine(_ptr(o_parts), _ptr(lse_parts), R, rows, H, _ptr(out), _ptr(lse),
-                         _stream(stream)), "hs_dcp_combine")
+    check(hs_dcp_combine(_dev(o_parts, "o_parts"), _dev(lse_parts, "lse_parts"), R, rows, H,
+                         _dev(out, "out"), _dev(lse, "lse"), _stream(stream)), "hs_dcp_combine")
 
 
 def make_config(**kw) -> hs_pool_config:
@@ -133,8 +133,23 @@ def required_bytes(cfg: hs_pool_config):
     return d.value, h.value
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _ptr(t, what="argument"):
+    """Pointer of a contiguous tensor in host or device memory (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, what="argument"):
+    """Pointer of a contiguous CUDA tensor, for the header's "dev" arguments
+    (None -> NULL): a host tensor here is rejected before anything runs."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what}: expected a CUDA tensor (a device pointer), got {t.device}")
+    return _ptr(t, what)
 
 
 def _stream(stream):
@@ -155,8 +170,9 @@ class Pool:
         self.host_arena = (torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
                            if host_bytes else None)
         h = ctypes.c_void_p()
-        check(hs_pool_create(ctypes.byref(cfg), _ptr(self.arena), dev_bytes,
-                             _ptr(self.host_arena), host_bytes, ctypes.byref(h)), "hs_pool_create")
+        check(hs_pool_create(ctypes.byref(cfg), _dev(self.arena, "arena"), dev_bytes,
+                             _ptr(self.host_arena, "host arena"), host_bytes, ctypes.byref(h)),
+              "hs_pool_create")
         self.handle = h
         lay = hs_layout()
         check(hs_pool_get_layout(self.handle, ctypes.byref(lay)), "hs_pool_get_layout")
@@ -183,8 +199,8 @@ class Pool:
 
     def append(self, req: int, rows, keys, scale=None, stream=None):
         n = rows.shape[0]
-        check(hs_append(self.handle, req, _ptr(rows), _ptr(keys), _ptr(scale), n, _stream(stream)),
-              "hs_append")
+        check(hs_append(self.handle, req, _ptr(rows, "rows"), _ptr(keys, "keys"),
+                        _ptr(scale, "scale"), n, _stream(stream)), "hs_append")
 
     def set_mode(self, req: int, mode: int, stream=None):
         check(hs_request_set_mode(self.handle, req, mode, _stream(stream)), "hs_request_set_mode")
@@ -197,39 +213,41 @@ class Pool:
 
     # ---- decode-step calls ----
     def indexer_score(self, q, w, B, nq, scores, stride, stream=None):
-        check(hs_indexer_score(self.handle, _ptr(q), _ptr(w), B, nq, _ptr(scores), stride,
-                               _stream(stream)), "hs_indexer_score")
+        check(hs_indexer_score(self.handle, _dev(q, "q"), _dev(w, "w"), B, nq,
+                               _dev(scores, "scores"), stride, _stream(stream)), "hs_indexer_score")
 
     def topk(self, scores, stride, B, nq, out, stream=None):
-        check(hs_topk(self.handle, _ptr(scores), stride, B, nq, _ptr(out), _stream(stream)),
-              "hs_topk")
+        check(hs_topk(self.handle, _dev(scores, "scores"), stride, B, nq, _dev(out, "out"),
+                      _stream(stream)), "hs_topk")
 
     def indexer_topk(self, q, w, B, nq, out, stream=None):
-        check(hs_indexer_topk(self.handle, _ptr(q), _ptr(w), B, nq, _ptr(out), _stream(stream)),
-              "hs_indexer_topk")
+        check(hs_indexer_topk(self.handle, _dev(q, "q"), _dev(w, "w"), B, nq, _dev(out, "out"),
+                              _stream(stream)), "hs_indexer_topk")
 
     def resolve(self, topk, B, nq, row_id, stream=None):
-        check(hs_resolve(self.handle, _ptr(topk), B, nq, _ptr(row_id), _stream(stream)),
-              "hs_resolve")
+        check(hs_resolve(self.handle, _dev(topk, "topk"), B, nq, _dev(row_id, "row_id"),
+                         _stream(stream)), "hs_resolve")
 
     def sparse_mla_decode(self, layer, q, row_id, B, nq, scale, out, lse=None, stream=None):
-        check(hs_sparse_mla_decode(self.handle, layer, _ptr(q), _ptr(row_id), B, nq, scale,
-                                   _ptr(out), _ptr(lse), _stream(stream)), "hs_sparse_mla_decode")
+        check(hs_sparse_mla_decode(self.handle, layer, _dev(q, "q"), _dev(row_id, "row_id"), B, nq,
+                                   scale, _dev(out, "out"), _dev(lse, "lse"), _stream(stream)),
+              "hs_sparse_mla_decode")
 
     def dcp_topk_merge(self, scores, stride, local_topk, offsets, R, rows, topk, part_topk,
                        stream=None):
-        check(hs_dcp_topk_merge(self.handle, _ptr(scores), stride, _ptr(local_topk),
-                                _ptr(offsets), R, rows, _ptr(topk), _ptr(part_topk),
-                                _stream(stream)), "hs_dcp_topk_merge")
+        check(hs_dcp_topk_merge(self.handle, _dev(scores, "scores"), stride,
+                                _dev(local_topk, "local_topk"), _dev(offsets, "offsets"), R, rows,
+                                _dev(topk, "topk"), _dev(part_topk, "part_topk"), _stream(stream)),
+              "hs_dcp_topk_merge")
 
     def check_wait_timeout(self, limit_cycles, stream=None):
         check(hs_check_wait_timeout(self.handle, limit_cycles, _stream(stream)),
               "hs_check_wait_timeout")
 
     def step(self, B, nq, q_idx, w_idx, q_mla, scale, out, topk, row_id, lse=None, stream=None):
-        a = hs_step_args(B=B, nq=nq, q_idx=_ptr(q_idx), w_idx=_ptr(w_idx), q_mla=_ptr(q_mla),
-                         softmax_scale=scale, out=_ptr(out), lse=_ptr(lse), topk=_ptr(topk),
-                         row_id=_ptr(row_id))
+        a = hs_step_args(B=B, nq=nq, q_idx=_dev(q_idx, "q_idx"), w_idx=_dev(w_idx, "w_idx"),
+                         q_mla=_dev(q_mla, "q_mla"), softmax_scale=scale, out=_dev(out, "out"),
+                         lse=_dev(lse, "lse"), topk=_dev(topk, "topk"), row_id=_dev(row_id, "row_id"))
         check(hs_step(self.handle, ctypes.byref(a), _stream(stream)), "hs_step")
 
     def step_kernel_count(self, B, nq) -> int:

@@ -104,3 +104,17 @@ def test_null_pool_calls_are_rejected(hs):
     assert hs.hs_resolve(None, None, 1, 1, None, None) == hs.HS_ERR_INVALID_ARG
     assert hs.hs_step(None, None, None) == hs.HS_ERR_INVALID_ARG
     assert hs.hs_pool_free_gpu_blocks(None) == -1
+
+
+def test_binding_rejects_host_and_strided_tensors_for_device_arguments(hs):
+    """The binding's marshalling: a "dev" argument must be a contiguous CUDA
+    tensor, checked before any call reaches the library (no GPU needed: a CPU
+    tensor is refused outright)."""
+    import torch
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        hs._dev(torch.zeros(4), "q")
+    with pytest.raises(ValueError, match="contiguous"):
+        hs._ptr(torch.zeros(4, 4).t(), "rows")
+    assert hs._dev(None) is None and hs._ptr(None) is None
+    t = torch.zeros(8)
+    assert hs._ptr(t).value == t.data_ptr()
