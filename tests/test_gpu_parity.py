@@ -243,6 +243,67 @@ def test_graph_capture_replay_equals_eager():
         graph.close()
 
 
+def test_graph_replay_stays_valid_across_residency_changes():
+    """A step captured as a CUDA graph at full residency replays correctly
+    after the requests change residency between replays (full -> mixed ->
+    zero -> full): every launch of the step depends only on the pool's
+    configuration, the residency lives in device tables.  The replays are
+    compared bit for bit with eager steps of a twin pool taking the same
+    changes (eager residency changes are checked against the oracle in
+    test_residency_round_trips_under_the_oracle)."""
+    from harness import Case, Runner
+    hs = _hs()
+    c = Case("graph-modes", B=2, N=[3000, 2000], K=256, Hi=8, Di=32, H=32, L=2, T=256,
+             mode=hs.HS_FULL, steps=8)
+    eager, graph = Runner(c), Runner(c)
+    flips = {3: hs.HS_MIXED, 5: hs.HS_ZERO, 7: hs.HS_FULL}
+    try:
+        q, w, qm = eager.step_inputs(1)
+        shp = (2, 1, 256)
+        bufs = {}
+        for name, r in (("eager", eager), ("graph", graph)):
+            bufs[name] = dict(q=q.clone(), w=w.clone(), qm=qm.clone(),
+                              out=torch.zeros((2, 2, 1, 32, 512), dtype=torch.bfloat16, device=r.dev),
+                              topk=torch.zeros(shp, dtype=torch.int32, device=r.dev),
+                              rid=torch.zeros(shp, dtype=torch.int32, device=r.dev))
+        gbuf = bufs["graph"]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                graph.pool.step(2, 1, gbuf["q"], gbuf["w"], gbuf["qm"], graph.tau, gbuf["out"],
+                                gbuf["topk"], gbuf["rid"], stream=s)
+        torch.cuda.synchronize()
+        for step in range(1, 9):
+            if step in flips:
+                for r in (eager, graph):
+                    for b in range(2):
+                        r.pool.set_mode(b, flips[step])
+                torch.cuda.synchronize()
+            qs, ws, qms = eager.step_inputs(step)
+            e = bufs["eager"]
+            e["q"].copy_(qs), e["w"].copy_(ws), e["qm"].copy_(qms)
+            gbuf["q"].copy_(qs), gbuf["w"].copy_(ws), gbuf["qm"].copy_(qms)
+            eager.pool.step(2, 1, e["q"], e["w"], e["qm"], eager.tau, e["out"], e["topk"], e["rid"])
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(e["topk"], gbuf["topk"]), f"step {step}: top-K"
+            assert torch.equal(e["rid"], gbuf["rid"]), f"step {step}: row ids"
+            assert torch.equal(e["out"], gbuf["out"]), f"step {step}: attention"
+            for b in range(2):
+                se, sg = eager.pool.dump_state(b), graph.pool.dump_state(b)
+                for k in ("hot_map", "slot_token", "stamp", "step", "block_table"):
+                    np.testing.assert_array_equal(se[k], sg[k], err_msg=f"step {step} req {b}: {k}")
+        assert eager.pool.get_error() == hs.HS_OK
+        assert graph.pool.get_error() == hs.HS_OK
+        st = graph.pool.stats()
+        assert st["misses"] > 0 and st["resident"] > 0
+    finally:
+        eager.close()
+        graph.close()
+
+
 def test_out_of_range_index_sets_error_and_recovers():
     from harness import Case, Runner
     hs = _hs()
