@@ -36,7 +36,9 @@
  *   - Hot-path calls (hs_indexer_score, hs_topk, hs_indexer_topk, hs_resolve,
  *     hs_sparse_mla_decode, hs_step) only enqueue work on `stream`: no host
  *     synchronisation, no allocation, no branch on device data.  They may be
- *     captured in a CUDA graph and replayed.
+ *     captured in a CUDA graph and replayed.  What they launch depends only
+ *     on the pool's configuration and the call's B and nq, so a captured
+ *     graph stays valid when requests change residency between replays.
  *   - A pool is not thread-safe; use it from one host thread and one stream
  *     at a time.
  *   - Batch index b of a hot-path call is request id b (0 <= b < B).
