@@ -38,7 +38,8 @@
  *     synchronisation, no allocation, no branch on device data.  They may be
  *     captured in a CUDA graph and replayed.  What they launch depends only
  *     on the pool's configuration and the call's B and nq, so a captured
- *     graph stays valid when requests change residency between replays.
+ *     graph stays valid when requests change residency or grow (hs_append)
+ *     between replays.
  *   - A pool is not thread-safe; use it from one host thread and one stream
  *     at a time.
  *   - Batch index b of a hot-path call is request id b (0 <= b < B).

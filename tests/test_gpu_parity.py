@@ -243,6 +243,58 @@ def test_graph_capture_replay_equals_eager():
         graph.close()
 
 
+def _graph_twins(case, between, steps):
+    """Capture one hs_step of `case` as a CUDA graph on one pool and replay it
+    for `steps` steps beside eager steps of a twin pool, calling
+    between(step, runner) on both before each step; outputs and device state
+    must match bit for bit.  Returns the graph pool's counters."""
+    from harness import Runner
+    hs = _hs()
+    eager, graph = Runner(case), Runner(case)
+    B, K, H, L = case.B, case.K, case.H, case.L
+    try:
+        q, w, qm = eager.step_inputs(1)
+        shp = (B, 1, K)
+        bufs = {}
+        for name, r in (("eager", eager), ("graph", graph)):
+            bufs[name] = dict(q=q.clone(), w=w.clone(), qm=qm.clone(),
+                              out=torch.zeros((L, B, 1, H, 512), dtype=torch.bfloat16, device=r.dev),
+                              topk=torch.zeros(shp, dtype=torch.int32, device=r.dev),
+                              rid=torch.zeros(shp, dtype=torch.int32, device=r.dev))
+        gbuf, e = bufs["graph"], bufs["eager"]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                graph.pool.step(B, 1, gbuf["q"], gbuf["w"], gbuf["qm"], graph.tau, gbuf["out"],
+                                gbuf["topk"], gbuf["rid"], stream=s)
+        torch.cuda.synchronize()
+        for step in range(1, steps + 1):
+            for r in (eager, graph):
+                between(step, r)
+            torch.cuda.synchronize()
+            qs, ws, qms = eager.step_inputs(step)
+            for buf in (e, gbuf):
+                buf["q"].copy_(qs), buf["w"].copy_(ws), buf["qm"].copy_(qms)
+            eager.pool.step(B, 1, e["q"], e["w"], e["qm"], eager.tau, e["out"], e["topk"], e["rid"])
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(e["topk"], gbuf["topk"]), f"step {step}: top-K"
+            assert torch.equal(e["rid"], gbuf["rid"]), f"step {step}: row ids"
+            assert torch.equal(e["out"], gbuf["out"]), f"step {step}: attention"
+            for b in range(B):
+                se, sg = eager.pool.dump_state(b), graph.pool.dump_state(b)
+                for k in ("hot_map", "slot_token", "stamp", "step", "block_table", "seq_len"):
+                    np.testing.assert_array_equal(se[k], sg[k], err_msg=f"step {step} req {b}: {k}")
+        assert eager.pool.get_error() == hs.HS_OK
+        assert graph.pool.get_error() == hs.HS_OK
+        return graph.pool.stats()
+    finally:
+        eager.close()
+        graph.close()
+
+
 def test_graph_replay_stays_valid_across_residency_changes():
     """A step captured as a CUDA graph at full residency replays correctly
     after the requests change residency between replays (full -> mixed ->
@@ -251,57 +303,40 @@ def test_graph_replay_stays_valid_across_residency_changes():
     compared bit for bit with eager steps of a twin pool taking the same
     changes (eager residency changes are checked against the oracle in
     test_residency_round_trips_under_the_oracle)."""
-    from harness import Case, Runner
+    from harness import Case
     hs = _hs()
     c = Case("graph-modes", B=2, N=[3000, 2000], K=256, Hi=8, Di=32, H=32, L=2, T=256,
              mode=hs.HS_FULL, steps=8)
-    eager, graph = Runner(c), Runner(c)
     flips = {3: hs.HS_MIXED, 5: hs.HS_ZERO, 7: hs.HS_FULL}
-    try:
-        q, w, qm = eager.step_inputs(1)
-        shp = (2, 1, 256)
-        bufs = {}
-        for name, r in (("eager", eager), ("graph", graph)):
-            bufs[name] = dict(q=q.clone(), w=w.clone(), qm=qm.clone(),
-                              out=torch.zeros((2, 2, 1, 32, 512), dtype=torch.bfloat16, device=r.dev),
-                              topk=torch.zeros(shp, dtype=torch.int32, device=r.dev),
-                              rid=torch.zeros(shp, dtype=torch.int32, device=r.dev))
-        gbuf = bufs["graph"]
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                graph.pool.step(2, 1, gbuf["q"], gbuf["w"], gbuf["qm"], graph.tau, gbuf["out"],
-                                gbuf["topk"], gbuf["rid"], stream=s)
-        torch.cuda.synchronize()
-        for step in range(1, 9):
-            if step in flips:
-                for r in (eager, graph):
-                    for b in range(2):
-                        r.pool.set_mode(b, flips[step])
-                torch.cuda.synchronize()
-            qs, ws, qms = eager.step_inputs(step)
-            e = bufs["eager"]
-            e["q"].copy_(qs), e["w"].copy_(ws), e["qm"].copy_(qms)
-            gbuf["q"].copy_(qs), gbuf["w"].copy_(ws), gbuf["qm"].copy_(qms)
-            eager.pool.step(2, 1, e["q"], e["w"], e["qm"], eager.tau, e["out"], e["topk"], e["rid"])
-            g.replay()
-            torch.cuda.synchronize()
-            assert torch.equal(e["topk"], gbuf["topk"]), f"step {step}: top-K"
-            assert torch.equal(e["rid"], gbuf["rid"]), f"step {step}: row ids"
-            assert torch.equal(e["out"], gbuf["out"]), f"step {step}: attention"
-            for b in range(2):
-                se, sg = eager.pool.dump_state(b), graph.pool.dump_state(b)
-                for k in ("hot_map", "slot_token", "stamp", "step", "block_table"):
-                    np.testing.assert_array_equal(se[k], sg[k], err_msg=f"step {step} req {b}: {k}")
-        assert eager.pool.get_error() == hs.HS_OK
-        assert graph.pool.get_error() == hs.HS_OK
-        st = graph.pool.stats()
-        assert st["misses"] > 0 and st["resident"] > 0
-    finally:
-        eager.close()
-        graph.close()
+
+    def between(step, r):
+        if step in flips:
+            for b in range(c.B):
+                r.pool.set_mode(b, flips[step])
+
+    st = _graph_twins(c, between, 8)
+    assert st["misses"] > 0 and st["resident"] > 0
+
+
+def test_graph_replay_stays_valid_across_appends():
+    """A decode loop replays one captured step graph while every request grows
+    by 40 tokens between replays (mixed residency: the tail window slides and
+    pages leave it for the host pool): lengths, tables and step counters live
+    on the device, so the replays match eager steps of a twin pool bit for
+    bit (eager appends are checked against the oracle in
+    test_mtp_indexer_with_scales_and_appends)."""
+    from harness import Case
+    hs = _hs()
+    c = Case("graph-append", B=2, N=[3000, 2000], K=256, Hi=8, Di=32, H=32, L=2, T=256,
+             mode=hs.HS_MIXED, steps=8, append=40)
+
+    def between(step, r):
+        if step > 1:
+            for b in range(c.B):
+                r.append(b, 40)
+
+    st = _graph_twins(c, between, 8)
+    assert st["misses"] > 0 and st["resident"] > 0
 
 
 def test_out_of_range_index_sets_error_and_recovers():
