@@ -42,7 +42,11 @@
  *     between replays.
  *   - A pool is not thread-safe; use it from one host thread and one stream
  *     at a time.
- *   - Batch index b of a hot-path call is request id b (0 <= b < B).
+ *   - Batch index b of a hot-path call is request id b (0 <= b < B).  Calls
+ *     that score, select or resolve tokens (hs_indexer_score, hs_topk,
+ *     hs_indexer_topk, hs_resolve, hs_step) need every request to hold at
+ *     least nq tokens (the step's own tokens are already in the cache):
+ *     otherwise HS_ERR_INVALID_ARG and nothing is enqueued.
  */
 #ifndef HS_H
 #define HS_H

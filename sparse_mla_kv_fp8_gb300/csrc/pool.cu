@@ -524,23 +524,32 @@ static bool batch_ok(const hs_pool *p, int32_t B, int32_t nq) {
     return true;
 }
 
+// Calls that score, select or resolve a request's tokens also need the cache
+// to hold the step's own nq tokens (N >= nq; an empty request is refused).
+static bool step_batch_ok(const hs_pool *p, int32_t B, int32_t nq) {
+    if (!batch_ok(p, B, nq)) return false;
+    for (int b = 0; b < B; b++)
+        if (p->seq_len[b] < nq) return false;
+    return true;
+}
+
 hs_status hs_indexer_score(hs_pool *p, const void *q, const float *w, int32_t B, int32_t nq,
                            float *scores, int64_t stride, cudaStream_t st) {
-    if (!batch_ok(p, B, nq) || !q || !w || !scores || stride < p->cfg.max_tokens)
+    if (!step_batch_ok(p, B, nq) || !q || !w || !scores || stride < p->cfg.max_tokens)
         return HS_ERR_INVALID_ARG;
     return cuda_status(hs::launch_indexer_score(p, q, w, B, nq, scores, stride, st));
 }
 
 hs_status hs_topk(hs_pool *p, const float *scores, int64_t stride, int32_t B, int32_t nq,
                   int32_t *topk, cudaStream_t st) {
-    if (!batch_ok(p, B, nq) || !scores || !topk || stride < p->cfg.max_tokens)
+    if (!step_batch_ok(p, B, nq) || !scores || !topk || stride < p->cfg.max_tokens)
         return HS_ERR_INVALID_ARG;
     return cuda_status(hs::launch_topk(p, scores, stride, B, nq, topk, st));
 }
 
 hs_status hs_indexer_topk(hs_pool *p, const void *q, const float *w, int32_t B, int32_t nq,
                           int32_t *topk, cudaStream_t st) {
-    if (!batch_ok(p, B, nq) || !q || !w || !topk) return HS_ERR_INVALID_ARG;
+    if (!step_batch_ok(p, B, nq) || !q || !w || !topk) return HS_ERR_INVALID_ARG;
     cudaError_t e = hs::launch_indexer_score(p, q, w, B, nq, p->d.scores, p->score_stride, st);
     if (e == cudaSuccess) e = hs::launch_topk(p, p->d.scores, p->score_stride, B, nq, topk, st);
     return cuda_status(e);
@@ -548,7 +557,7 @@ hs_status hs_indexer_topk(hs_pool *p, const void *q, const float *w, int32_t B, 
 
 hs_status hs_resolve(hs_pool *p, const int32_t *topk, int32_t B, int32_t nq, int32_t *row_id,
                      cudaStream_t st) {
-    if (!batch_ok(p, B, nq) || !topk || !row_id) return HS_ERR_INVALID_ARG;
+    if (!step_batch_ok(p, B, nq) || !topk || !row_id) return HS_ERR_INVALID_ARG;
     return cuda_status(hs::launch_resolve(p, topk, B, nq, row_id, st));
 }
 
@@ -562,7 +571,7 @@ hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const i
 }
 
 hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
-    if (!a || !batch_ok(p, a->B, a->nq) || !a->q_idx || !a->w_idx || !a->q_mla || !a->out ||
+    if (!a || !step_batch_ok(p, a->B, a->nq) || !a->q_idx || !a->w_idx || !a->q_mla || !a->out ||
         !a->topk || !a->row_id || !aligned16(a->q_mla) || !aligned16(a->out))
         return HS_ERR_INVALID_ARG;
     const int B = a->B, nq = a->nq, H = p->cfg.mla_heads, L = p->cfg.num_mla_layers;

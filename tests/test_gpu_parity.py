@@ -143,7 +143,7 @@ def test_indexer_scores_bit_exact():
 @pytest.mark.parametrize("max_tokens", [0, 200064, 300032])
 def test_topk_ties_and_special_scores(max_tokens):
     """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows.
-    The row capacity picks the kernel: one cluster launch with 8 keys per
+    The row capacity picks the kernel: one cluster launch with 16 keys per
     thread (up to 20,032 tokens per row here) or 32 (200,064), and the
     multi-kernel radix select beyond 262,144."""
     from harness import Case, Runner
@@ -410,6 +410,17 @@ def test_host_side_capacity_errors():
             pool.resolve(torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"), 3, 1,
                          torch.zeros((3, 1, 64), dtype=torch.int32, device="cuda"))
         assert ei.value.status == hs.HS_ERR_INVALID_ARG  # B beyond max_requests
+        # request 0 holds no token (its append was refused): calls that score,
+        # select or resolve its tokens are refused before anything is enqueued
+        with pytest.raises(hs.HSError) as ei:
+            pool.resolve(torch.zeros((1, 1, 64), dtype=torch.int32, device="cuda"), 1, 1,
+                         torch.zeros((1, 1, 64), dtype=torch.int32, device="cuda"))
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG
+        with pytest.raises(hs.HSError) as ei:
+            pool.indexer_topk(torch.zeros((1, 1, 4, 32), dtype=torch.uint8, device="cuda"),
+                              torch.ones((1, 1, 4), device="cuda"), 1, 1,
+                              torch.zeros((1, 1, 64), dtype=torch.int32, device="cuda"))
+        assert ei.value.status == hs.HS_ERR_INVALID_ARG
         # q and out are moved in 16-byte vectors: a misaligned pointer is refused
         # before anything is enqueued
         qm = torch.zeros(16 * 576 + 8, dtype=torch.bfloat16, device="cuda")
