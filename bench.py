@@ -341,7 +341,7 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
 # scaled x2 to 32 requests), valid only for the kernel sources they were taken
 # on (the kernel's .cu and the shared device header, hashed together).
 TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "b1be9eaf94bcde78", 2 * (27643264 + 3392)),
-           "indexer": (("indexer.cu", "tc.cuh"), "9a866511fdda6dfb", 2 * (138579328 + 2516224)),
+           "indexer": (("indexer.cu", "tc.cuh"), "9a84ea0a9b297437", 2 * (138577152 + 2479616)),
            "topk": (("topk.cu", "tc.cuh"), "cf9fadfe87a5a0c2", 2 * 4227328)}
 
 

@@ -130,11 +130,21 @@ static double idx_elem(int fmt, const void *base, size_t i)
 /* Reading: the pages name an indexer with heads and nothing more.  We take
  * the lightning-indexer form
  *     s[j][t] = sum_h w[j][h] * ReLU(sigma[t] * (q[j][h][:] . k[t][:]))
- * with ReLU(x) = x if x > 0 else +0.  Query j of the nq queries of a step
+ * with ReLU(x) = x if x > 0 else +0.  Compiling with -DHSO_IDENTITY_GATE
+ * takes the identity gate instead (gate(x) = x), the other plain reading of
+ * the unnamed indexer; hso_gate_is_identity() says which one was built.  Query j of the nq queries of a step
  * sees tokens t in [0, N - nq + j + 1) (its own position included); the other
  * entries are set to -inf.
  *   q: [nq][Hi][Di], w: [nq][Hi] fp32, keys: [N][Di], sigma: [N] fp32,
  *   s: [nq][N] fp32 (output). */
+#ifdef HSO_IDENTITY_GATE
+#define HSO_GATE(x) (x)
+int hso_gate_is_identity(void) { return 1; }
+#else
+#define HSO_GATE(x) ((x) > 0.0 ? (x) : 0.0)
+int hso_gate_is_identity(void) { return 0; }
+#endif
+
 void hso_indexer_scores(int idx_fmt, const void *q, const float *w,
                         const void *keys, const float *sigma,
                         int N, int nq, int Hi, int Di, float *s)
@@ -158,7 +168,7 @@ void hso_indexer_scores(int idx_fmt, const void *q, const float *w,
                     dot += idx_elem(idx_fmt, q, ((size_t)j * Hi + h) * Di + d) *
                            idx_elem(idx_fmt, keys, (size_t)t * Di + d);
                 x = (double)sigma[t] * dot;
-                acc += (double)w[j * Hi + h] * (x > 0.0 ? x : 0.0);
+                acc += (double)w[j * Hi + h] * HSO_GATE(x);
             }
             s[(size_t)j * N + t] = (float)acc;
         }

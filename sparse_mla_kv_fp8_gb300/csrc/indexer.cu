@@ -20,6 +20,10 @@
 //
 // All sums are fp32; with the synthetic inputs they are exact, so results
 // do not depend on the order of summation (tensor core or not).
+//
+// The gate is ReLU (the lightning-indexer form); building with
+// -DHS_INDEXER_IDENTITY_GATE takes the identity instead, the other plain
+// reading of the pages' unnamed indexer.
 #include <cuda_fp8.h>
 
 #include "tc.cuh"
@@ -28,6 +32,14 @@ namespace hs {
 namespace {
 
 constexpr int kTile = 128;
+
+#ifdef HS_INDEXER_IDENTITY_GATE
+constexpr bool kReluGate = false;
+#else
+constexpr bool kReluGate = true;
+#endif
+
+__device__ __forceinline__ float gate(float x) { return kReluGate ? (x > 0.f ? x : 0.f) : x; }
 
 __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
     __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)v, __NV_E4M3);
@@ -79,7 +91,7 @@ __global__ void __launch_bounds__(kTile) indexer_simt_kernel(
             float dot = 0.f;
             for (int d = 0; d < Di; d++) dot = fmaf(qh[d], kt[r * ks + d], dot);
             const float x = sig * dot;
-            acc = fmaf(wf[j * Hi + h], x > 0.f ? x : 0.f, acc);
+            acc = fmaf(wf[j * Hi + h], gate(x), acc);
         }
         scores[((size_t)b * nq + j) * stride + t] = acc;
     }
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                                 for (int e = 0; e < 4; e++) {
                                     const float x = sig * v[16 * q + 4 * u + e];
-                                    part[e] = fmaf(ww[e], x > 0.f ? x : 0.f, part[e]);
+                                    part[e] = fmaf(ww[e], gate(x), part[e]);
                                 }
                             }
                         }

@@ -99,12 +99,13 @@ def test_generator_rows_roundtrip_within_e4m3_step():
 # --------------------------------------------------------------------------
 # indexer: exact integer recomputation
 # --------------------------------------------------------------------------
-def _int_recompute(qi, ki, wk, sig_e, N, nq):
+def _int_recompute(qi, ki, wk, sig_e, N, nq, relu_gate=True):
     """Closed form in integers.  q = qi/8, k = ki/8, w = 2^-wk, sigma = 2^sig_e:
     s = sum_h 2^-wk * max(2^sig_e * (qi.ki)/64, 0), returned as an exact
-    rational via integers scaled by 2^(6+3+1)."""
+    rational via integers scaled by 2^(6+3+1).  relu_gate=False drops the
+    max (the identity gate)."""
     dots = np.einsum("jhd,td->jht", qi.astype(np.int64), ki.astype(np.int64))  # units 2^-6
-    relu = np.maximum(dots, 0)
+    relu = np.maximum(dots, 0) if relu_gate else dots
     # term = 2^-wk * 2^sig_e * dot * 2^-6 ; scale everything by 2^10
     scale = (2 ** (3 - wk))[:, :, None].astype(np.int64)           # 2^-wk * 2^3
     sig = (2 ** (sig_e + 1))[None, None, :].astype(np.int64)      # 2^sig_e * 2^1
@@ -138,6 +139,41 @@ def test_indexer_scores_exact_int64(fmt, Hi, Di, bound, nq, N, sig):
     got = oracle.indexer_scores(fmt, q, w, k, sigma, N)
     want = _int_recompute(qi, ki, wk, sig_e, N, nq)
     np.testing.assert_array_equal(got.astype(np.float64), want)
+
+
+def test_indexer_identity_gate_build(tmp_path):
+    """The oracle built with -DHSO_IDENTITY_GATE (the other plain reading of the
+    gate) against the same integer closed form without the max; the default
+    build reports the ReLU gate."""
+    import ctypes
+    import subprocess
+    lib_path = str(tmp_path / "liboracle_identity.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-DHSO_IDENTITY_GATE", os.path.join(os.path.dirname(oracle.__file__), "hs_oracle.c"), "-o",
+                    lib_path, "-lm"], check=True)
+    lib = ctypes.CDLL(lib_path)
+    assert lib.hso_gate_is_identity() == 1
+    assert oracle._load().hso_gate_is_identity() == 0
+    rng = np.random.default_rng(11)
+    nq, Hi, Di, N = 2, 4, 32, 40
+    qi = rng.integers(-8, 9, (nq, Hi, Di))
+    ki = rng.integers(-8, 9, (N, Di))
+    wk = rng.integers(0, 4, (nq, Hi))
+    sig_e = rng.integers(-1, 2, N)
+    q = np.ascontiguousarray(torch.from_numpy(qi / 8.0).float().to(torch.float8_e4m3fn)
+                             .view(torch.uint8).numpy())
+    k = np.ascontiguousarray(torch.from_numpy(ki / 8.0).float().to(torch.float8_e4m3fn)
+                             .view(torch.uint8).numpy())
+    w = np.ascontiguousarray((2.0 ** -wk).astype(np.float32))
+    sigma = np.ascontiguousarray((2.0 ** sig_e).astype(np.float32))
+    out = np.empty((nq, N), np.float32)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    lib.hso_indexer_scores(ctypes.c_int(oracle.IDX_E4M3), p(q), p(w), p(k), p(sigma),
+                           ctypes.c_int(N), ctypes.c_int(nq), ctypes.c_int(Hi), ctypes.c_int(Di),
+                           p(out))
+    want = _int_recompute(qi, ki, wk, sig_e, N, nq, relu_gate=False)
+    np.testing.assert_array_equal(out.astype(np.float64), want)
+    assert (want[np.isfinite(want)] < 0).any()  # the identity gate keeps negative terms
 
 
 def test_indexer_generator_values_are_exact_grid():
