@@ -337,8 +337,8 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
     return {k: v / steps for k, v in acc.items()}
 
 
-# DRAM bytes per launch from ncu (profiles/dram_traffic_full_residency_16x65536.md,
-# scaled x2 to 32 requests), valid only for the kernel sources they were taken
+# DRAM bytes per launch from one ncu capture of 16 requests (scaled x2 to 32
+# requests), valid only for the kernel sources they were taken
 # on (the kernel's .cu and the shared device header, hashed together).
 TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "b1be9eaf94bcde78", 2 * (27643264 + 3392)),
            "indexer": (("indexer.cu", "tc.cuh"), "9a84ea0a9b297437", 2 * (138577152 + 2479616)),

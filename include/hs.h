@@ -67,7 +67,11 @@ typedef enum {
     HS_ERR_HOST_POOL_FULL = 4,  /* no free block in the pinned host pool        */
     HS_ERR_INDEX_RANGE = 5,     /* a selected index outside [0, seq_len)        */
     HS_ERR_TIMEOUT = 6,         /* a bounded device wait ran out                */
-    HS_ERR_CUDA = 7             /* a CUDA runtime call failed                   */
+    HS_ERR_CUDA = 7,            /* a CUDA runtime call failed                   */
+    HS_ERR_RANGE = 8            /* a value beyond the fp16 range of the tensor-core
+                                   attention (a row's group scale s with
+                                   448 * s > 65504, a query or rope value
+                                   above 65504 in magnitude)               */
 } hs_status;
 
 /* Storage format of one MLA latent row (576 values = 512 nope + 64 rope). */
@@ -241,7 +245,10 @@ hs_status hs_topk(hs_pool *pool, const float *scores, int64_t score_stride,
  *   scores, score_stride, B, nq, K, topk: as for hs_topk (K = top_k);
  *   seq_len: dev [B] int32 request lengths (query j of request b sees
  *            t < seq_len[b] - nq + j + 1);
- *   max_tokens: upper bound of every seq_len[b], <= score_stride.
+ *   max_tokens: tokens of each score row the call may read, <= score_stride;
+ *            a query sees min(seq_len[b] - nq + j + 1, max_tokens) tokens, so
+ *            a seq_len[b] beyond max_tokens is clamped on the device and no
+ *            score past max_tokens is read.
  * Scratch: a static area inside this library (578 KiB of device memory,
  * held on every GPU that loads the library until the process exits).  Nothing is allocated or freed by this call.  Limits: B * nq <= 64
  * and max_tokens <= 1,048,576; larger requests return HS_ERR_CAPACITY and
@@ -288,17 +295,20 @@ hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
  * out = 0, lse = -inf.  With E4M3 rows and a head count that is a multiple of
  * 64, the products run on the tensor cores with fp16 operands (queries and
  * dequantised rows converted, fp32 accumulation): their magnitudes must stay
- * below 65504. */
+ * below 65504.  A row whose group scale s has 448 * s > 65504, or a query or
+ * rope value beyond 65504 in magnitude, sets HS_ERR_RANGE in the sticky error
+ * word (the output of that query is then not meaningful). */
 hs_status hs_sparse_mla_decode(hs_pool *pool, int32_t layer, const void *q,
                                const int32_t *row_id, int32_t B, int32_t nq,
                                float softmax_scale, void *out, float *lse,
                                cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
-/* Token-partitioned decode on one GPU ("Un contexte d'un million sur huit     */
-/* H200", « Ce qui se passe »: context parallelism shards a request's cache by */
-/* tokens; the global top-K is taken over the shards' candidates and the       */
-/* shards' attention partials are merged by their log-sum-exp).  A request's  */
+/* Token-partitioned decode on one GPU ("vLLM sert GLM-5.3 en contexte 1M sur */
+/* 16 H200", « Le mécanisme »: decode context parallelism spreads the KV cache */
+/* over the GPUs by tokens and gathers the fragments at every layer; here the  */
+/* global top-K is taken over the shards' candidates and the shards' attention */
+/* partials are merged by their log-sum-exp).  A request's                     */
 /* R shards are R pool requests holding consecutive token ranges; with rows =  */
 /* B * nq, shard r of row i is row r * rows + i of the batched calls.          */
 /* ------------------------------------------------------------------------ */

@@ -265,6 +265,21 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// Does any of eight bf16 values exceed fp16's range (|x| > 65504, which fp16
+// rounds to infinity; NaN and infinity count too)?
+__device__ __forceinline__ bool bf16x8_beyond_f16(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        bad |= (w[i] & 0x7FFFu) > 0x477Fu || ((w[i] >> 16) & 0x7FFFu) > 0x477Fu;
+    return bad;
+}
+
+// Largest E4M3 magnitude times a group scale must stay inside fp16.
+constexpr float kMaxF16 = 65504.f;
+constexpr float kMaxE4M3 = 448.f;
+
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
     return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                       bf16x2_to_f16x2(v.w));
@@ -606,10 +621,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                 qv[j] = tc::ld_nc16(qsrc + (size_t)h * (kLatent * 2) + c16 * 16);
             }
         };
+        bool range_bad = false;  // a value beyond fp16's range (reported once at the end)
         auto q_store = [&]() {
 #pragma unroll
             for (int j = 0; j < 12; j++) {
                 const int i = wi + 384 * j, h = i / 72, c16 = i - h * 72;
+                range_bad |= bf16x8_beyond_f16(qv[j]);
                 *(uint4 *)(qb + (c16 >> 3) * kQBlock + tc::sw128_offset(h, c16 & 7)) = bf16x8_to_f16x8(qv[j]);
             }
             tc::fence_async_smem();
@@ -662,6 +679,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                         const int r = rw + 48 * u;
                         if (st < 4) {
                             const float scl = __uint_as_float(f0[u]);
+                            range_bad |= kMaxE4M3 * fabsf(scl) > kMaxF16;
                             const __half s_hi = __float2half_rn(scl);
                             const __half2 shi2 = __half2half2(s_hi);
                             const __half2 slo2 = __half2half2(__float2half_rn(scl - __half2float(s_hi)));
@@ -673,6 +691,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
                             *(uint4 *)(dst + tc::sw128_offset(r, q0)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                             *(uint4 *)(dst + tc::sw128_offset(r, q0 + 1)) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                         } else {
+                            range_bad |= bf16x8_beyond_f16(d0[u]);
                             *(uint4 *)(dst + tc::sw128_offset(r, c8r)) = bf16x8_to_f16x8(d0[u]);  // rope
                         }
                     }
@@ -710,6 +729,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(AttnTcArgs a) 
             }
             if (ok) issue_first();  // lands before PV(c) frees the first K-blocks
         }
+        if (range_bad) set_error(a.err, HS_ERR_RANGE);
         if (a.cluster && warp < 10) {
             // ---- two splits in one cluster merge symmetrically over eight
             // warps (heads 0-31 on warps 2-5, 32-63 on warps 6-9; thread =

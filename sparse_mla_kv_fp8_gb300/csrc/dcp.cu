@@ -1,8 +1,9 @@
-// Token-partitioned decode on one GPU ("Un contexte d'un million sur huit
-// H200", section "Ce qui se passe": decode context parallelism shards a
-// request's cache by tokens, each shard selects its own candidates, the global
-// top-K is taken over the union and the shards' attention partials are merged
-// by their log-sum-exp).  Two kernels:
+// Token-partitioned decode on one GPU ("vLLM sert GLM-5.3 en contexte 1M sur
+// 16 H200", section "Le mécanisme": decode context parallelism spreads a
+// request's KV cache over the GPUs by tokens and gathers the fragments at
+// every layer).  Here each shard selects its own candidates, the global top-K
+// is taken over the union and the shards' attention partials are merged by
+// their log-sum-exp.  Two kernels:
 //
 // dcp_merge_kernel, one CTA per row (request, query): the R partitions' local
 //   top-K lists with their scores become candidates keyed by (score, lower
@@ -23,8 +24,12 @@ namespace {
 constexpr int kMergeThreads = 1024;
 constexpr int kMergeMax = 16384;  // R * K candidates per row
 
+// Order-preserving key of an fp32 score.  -0 is first made +0: the two
+// compare equal, so they must tie (and go to the lower token) like any other
+// equal scores, not rank -0 below +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -21,9 +21,7 @@
 // All sums are fp32; with the synthetic inputs they are exact, so results
 // do not depend on the order of summation (tensor core or not).
 //
-// The gate is ReLU (the lightning-indexer form); building with
-// -DHS_INDEXER_IDENTITY_GATE takes the identity instead, the other plain
-// reading of the pages' unnamed indexer.
+// The gate is ReLU (the lightning-indexer form).
 #include <cuda_fp8.h>
 
 #include "tc.cuh"
@@ -33,13 +31,7 @@ namespace {
 
 constexpr int kTile = 128;
 
-#ifdef HS_INDEXER_IDENTITY_GATE
-constexpr bool kReluGate = false;
-#else
-constexpr bool kReluGate = true;
-#endif
-
-__device__ __forceinline__ float gate(float x) { return kReluGate ? (x > 0.f ? x : 0.f) : x; }
+__device__ __forceinline__ float gate(float x) { return x > 0.f ? x : 0.f; }
 
 __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
     __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)v, __NV_E4M3);

@@ -186,7 +186,7 @@ int first_tail_page(const hs_pool *p, int mode, int64_t N) {
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 100; }
+int32_t hs_abi_version(void) { return 101; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -198,6 +198,7 @@ const char *hs_status_string(hs_status s) {
         case HS_ERR_INDEX_RANGE: return "selected index outside the request";
         case HS_ERR_TIMEOUT: return "bounded device wait ran out";
         case HS_ERR_CUDA: return "CUDA runtime error";
+        case HS_ERR_RANGE: return "value beyond the fp16 range of the tensor-core attention";
     }
     return "unknown status";
 }

@@ -22,8 +22,12 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kPerThread = kTopkChunk / kThreads;
 
+// Order-preserving key of an fp32 score.  -0 is first made +0: the two
+// compare equal, so they must tie (and go to the lower token) like any other
+// equal scores, not rank -0 below +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -52,11 +56,13 @@ __device__ __forceinline__ int block_incl_scan(int v, int *warp_sums) {
     return v;
 }
 
+// vis is clamped to max_tokens: the later kernels read scores up to it, so a
+// length beyond the score rows (a caller's device data) never reads past them.
 __global__ void topk_init_kernel(TopkRowState *st, uint32_t *hist, const int32_t *seq_len,
-                                 int nq, int K) {
+                                 int nq, int K, int max_tokens) {
     const int row = blockIdx.x;
     const int b = row / nq, j = row - b * nq;
-    const int vis = seq_len[b] - nq + j + 1;
+    const int vis = min(seq_len[b] - nq + j + 1, max_tokens);
     for (int i = threadIdx.x; i < kTopkBins; i += blockDim.x) hist[(size_t)row * kTopkBins + i] = 0;
     if (threadIdx.x == 0) {
         TopkRowState s;
@@ -500,7 +506,8 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
         return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<32>, scores, stride, vec4,
                                   (const int32_t *)p->d.seq_len, nq, K, topk);
     }
-    topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K);
+    topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K,
+                                            p->cfg.max_tokens);
     dim3 grid(nch, rows);
     for (int pass = 0; pass < 3; pass++)
         topk_hist_kernel<<<grid, kThreads, 0, st>>>(scores, stride, p->d.topk_state,
@@ -583,8 +590,10 @@ extern "C" hs_status hs_topk_noalloc(const float *scores, int64_t score_stride,
     const int rows = B * nq;
     const int nch = (max_tokens + hs::kTopkChunk - 1) / hs::kTopkChunk;
     // the init kernel clears the histograms and the per-row state that the
-    // previous call left behind; the chunk counts are fully rewritten
-    hs::topk_init_kernel<<<rows, 256, 0, stream>>>(state, hist, seq_len, nq, K);
+    // previous call left behind (the chunk counts are fully rewritten), and
+    // clamps each row's visible length to max_tokens, so a seq_len[b] beyond
+    // it reads no score past the caller's rows
+    hs::topk_init_kernel<<<rows, 256, 0, stream>>>(state, hist, seq_len, nq, K, max_tokens);
     dim3 grid(nch, rows);
     for (int pass = 0; pass < 3; pass++)
         hs::topk_hist_kernel<<<grid, hs::kThreads, 0, stream>>>(scores, score_stride, state, hist,

@@ -26,6 +26,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 # ---- enums (include/hs.h) ----
 HS_OK, HS_ERR_INVALID_ARG, HS_ERR_ARENA_TOO_SMALL, HS_ERR_CAPACITY = 0, 1, 2, 3
 HS_ERR_HOST_POOL_FULL, HS_ERR_INDEX_RANGE, HS_ERR_TIMEOUT, HS_ERR_CUDA = 4, 5, 6, 7
+HS_ERR_RANGE = 8
 HS_ROW_E4M3_656, HS_ROW_F32_2304 = 0, 1
 HS_IDX_E4M3, HS_IDX_F32 = 0, 1
 HS_FULL, HS_MIXED, HS_ZERO = 0, 1, 2

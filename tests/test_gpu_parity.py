@@ -158,6 +158,18 @@ def test_topk_ties_and_special_scores(max_tokens):
         sc[1] = 0.0                                  # every score equal
         sc[2, 0, :150] = -torch.arange(150).float()  # negatives and -0 area
         sc[3, 1] = torch.randn(stride, generator=g)
+        # the K-th largest score is a zero and +0 / -0 alternate among the
+        # zeros: equal scores, so the lowest tokens of either sign are taken
+        z = torch.zeros(stride)
+        z[1::2] = -0.0
+        z[:300:3] = torch.arange(1, 101).float()   # 100 positives spread out
+        z[7000:9000] = -1.0                          # below the zeros
+        sc[0, 1] = z
+        sc[3, 0] = -1.0
+        sc[3, 0, :5000] = torch.where(torch.arange(5000) % 50 == 0, torch.tensor(2.0),
+                                      torch.where(torch.arange(5000) % 2 == 0, torch.tensor(-0.0),
+                                                  torch.tensor(0.0)))
+        assert (torch.signbit(sc[0, 1]) & (sc[0, 1] == 0)).any()
         sc = sc.to(r.dev)
         out = torch.full((case.B, 2, case.K), -9, dtype=torch.int32, device=r.dev)
         r.pool.topk(sc, stride, case.B, 2, out)
@@ -603,6 +615,61 @@ def test_dcp_token_shards_match_the_unsharded_request():
             assert (np.abs(g - o) <= 2e-3 + 1e-2 * np.abs(o)).all(), np.abs(g - o).max()
             gl = lse[b, 0].cpu().numpy()
             assert (np.abs(gl - ls) <= 2e-3 + 1e-2 * np.abs(ls)).all()
+    finally:
+        pool.close()
+
+
+def test_dcp_topk_merge_signed_zero_threshold():
+    """hs_dcp_topk_merge when the K-th best score is a zero and +0 / -0 are
+    mixed across and inside the shards: equal scores, so the merged list is
+    the oracle's top-K of the whole row (lower global tokens first)."""
+    hs = _hs()
+    R, B, K, P = 3, 2, 256, 64
+    lens, offs = [500, 640, 450], [0, 500, 1140]
+    N = sum(lens)
+    dev = torch.device("cuda")
+    cfg = hs.make_config(max_requests=R * B, max_tokens=640, page_tokens=P, top_k=K,
+                         num_spec=0, tail_tokens=0, num_mla_layers=1, mla_heads=16, idx_heads=8,
+                         idx_dim=32, row_fmt=hs.HS_ROW_E4M3_656, idx_fmt=hs.HS_IDX_E4M3,
+                         gpu_blocks=R * B * 10 + 4)
+    pool = hs.Pool(cfg, device=dev)
+    try:
+        for r in range(R):
+            for b in range(B):
+                pool.open(r * B + b, hs.HS_FULL)
+                pool.append(r * B + b, wl.mla_rows(0, b, offs[r], lens[r], 1, wl.ROW_E4M3_656, dev),
+                            wl.idx_keys(0, b, offs[r], lens[r], 32, wl.IDX_E4M3, dev))
+        g = torch.Generator().manual_seed(8)
+        whole = torch.zeros((B, N))
+        whole[:, ::2] = -0.0
+        for b in range(B):
+            pos = torch.randperm(N, generator=g)[:90 + 40 * b]
+            whole[b, pos] = torch.rand(len(pos), generator=g) + 0.5  # fewer than K positives
+            neg = torch.randperm(N, generator=g)[:400]
+            whole[b, neg] = -torch.rand(len(neg), generator=g) - 0.5
+        stride = 640
+        scores = torch.full((R * B, 1, stride), float("nan"))
+        for r in range(R):
+            for b in range(B):
+                scores[r * B + b, 0, :lens[r]] = whole[b, offs[r]:offs[r] + lens[r]]
+        scores = scores.to(dev)
+        local = torch.empty((R * B, 1, K), dtype=torch.int32, device=dev)
+        pool.topk(scores, stride, R * B, 1, local)
+        topk = torch.full((B, 1, K), -7, dtype=torch.int32, device=dev)
+        part = torch.full((R * B, 1, K), -7, dtype=torch.int32, device=dev)
+        pool.dcp_topk_merge(scores, stride, local, torch.tensor(offs, dtype=torch.int32, device=dev),
+                            R, B, topk, part)
+        torch.cuda.synchronize()
+        assert pool.get_error() == hs.HS_OK
+        sc = scores.cpu().numpy()
+        for r in range(R):
+            for b in range(B):
+                ref = oracle.topk(sc[r * B + b, 0], lens[r], K)
+                np.testing.assert_array_equal(local[r * B + b, 0].cpu().numpy(), ref)
+        for b in range(B):
+            ref = oracle.topk(whole[b].numpy(), N, K)
+            assert (whole[b].numpy()[ref] == 0).any()  # the threshold is a zero
+            np.testing.assert_array_equal(topk[b, 0].cpu().numpy(), ref)
     finally:
         pool.close()
 

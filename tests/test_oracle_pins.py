@@ -226,6 +226,22 @@ def test_topk_brute_force_tiny(seed):
     np.testing.assert_array_equal(got, _brute_topk(s, vis, K))
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_signed_zeros_tie(seed):
+    """-0 and +0 are equal scores: they tie like any other equal scores and
+    go to the lower index (brute force on tiny rows of +-0 and +-1)."""
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(4, 11))
+    s = np.zeros(n, np.float32)
+    s[rng.random(n) < 0.5] = -0.0
+    s[rng.integers(0, n, 2)] = rng.choice(np.array([1.0, -1.0], np.float32), 2)
+    s[rng.integers(0, n)] = -0.0
+    assert np.signbit(s[s == 0]).any()
+    K = int(rng.integers(1, n))
+    got = oracle.topk(s, n, K)
+    np.testing.assert_array_equal(got, _brute_topk(s, n, K))
+
+
 def test_topk_invariants_large_with_ties():
     rng = np.random.default_rng(5)
     N, K = 5000, 777
@@ -325,11 +341,18 @@ def test_resolve_matches_history_replay(nq, K, C, mode):
     st = oracle.HotState(C, N)
     ref = HistoryLRU(C)
     hot_before = set()
+    zipf_p = np.zeros(N)
+    zipf_p[rng.permutation(N)] = np.arange(1, N + 1, dtype=np.float64) ** -1.1
+    zipf_p /= zipf_p.sum()
+    total_hits = total_misses = evictions = 0
     for step in range(40):
         # skewed draws so that hits, misses and evictions all happen
         idx = np.full((nq, K), -1, np.int32)
         for j in range(nq):
-            pool = rng.choice(N, size=K, replace=False, p=None if step % 5 else None)
+            # four steps in five draw from a Zipf law over a fixed permutation
+            # (repeats: hits and refreshed stamps), the fifth uniformly (a
+            # burst of misses that evicts)
+            pool = rng.choice(N, size=K, replace=False, p=None if step % 5 == 4 else zipf_p)
             idx[j] = np.sort(pool)
         r = st.resolve(resident, P, N, idx)
         assert r["status"] == 0
@@ -351,7 +374,12 @@ def test_resolve_matches_history_replay(nq, K, C, mode):
             if t >= 0:
                 assert st.hot_map[t] == c
         assert (st.hot_map >= 0).sum() == len(held)
+        evictions += len(hot_before - set(held))
+        total_hits += r["hits"]
+        total_misses += r["misses"]
         hot_before = set(held)
+    # the draws did what they are for
+    assert total_hits > 0 and total_misses > 0 and evictions > 0
 
 
 def test_resolve_full_residency_never_misses():
@@ -486,12 +514,42 @@ def test_attention_closed_forms():
     assert (o == 0).all() and np.isneginf(lse).all()
 
 
-def test_page_constants_fixture_matches_capacity_rule():
+def test_hot_buffer_sizing_follows_the_printed_rule():
+    """The pages print the hot-buffer sizes: 2 x top-K rows per request, and
+    (num_speculative_tokens + 2) x top-K under MTP (fixture constants, each
+    cited).  The library derives C from the config when hot_rows = 0: its
+    arena size must equal that of a config stating C explicitly by the
+    printed rule, and differ from one stating a neighbouring size.  The
+    oracle's resolve must then always find victims at that C, even when every
+    step's nq lists are disjoint from each other and from the last step's."""
+    from sparse_mla_kv_fp8_gb300 import build, hs
+    build.build()
     pc = _json("page_constants.json")
     K = pc["top_k"]["value"]
-    assert pc["hot_rows_per_topk_default"]["value"] * K == (0 + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K
+    for ns, C in ((0, pc["hot_rows_per_topk_default"]["value"] * K),
+                  (pc["mtp_speculative_tokens"]["value"],
+                   (pc["mtp_speculative_tokens"]["value"] + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K)):
+        base = dict(max_requests=2, max_tokens=16384, page_tokens=64, top_k=K, num_spec=ns,
+                    tail_tokens=4096, num_mla_layers=4, mla_heads=128, idx_heads=64, idx_dim=128,
+                    gpu_blocks=600, host_blocks=600)
+        derived = hs.required_bytes(hs.make_config(**base))
+        assert derived == hs.required_bytes(hs.make_config(hot_rows=C, **base))
+        assert derived != hs.required_bytes(hs.make_config(hot_rows=C - 64, **base))
+        assert derived != hs.required_bytes(hs.make_config(hot_rows=C + 64, **base))
+    # C = (ns + 2) K at the MTP3 sizing, scaled down to K = 8 so the oracle
+    # runs quickly; adversarial lists: every query of every step new
     ns = pc["mtp_speculative_tokens"]["value"]
-    assert (ns + pc["hot_rows_per_topk_mtp_offset"]["value"]) * K == 10240
+    nq, k = ns + 1, 8
+    Cs = (ns + pc["hot_rows_per_topk_mtp_offset"]["value"]) * k
+    P, N = 4, 4000
+    st = oracle.HotState(Cs, N)
+    res = oracle.page_resident(oracle.ZERO, N, 0, P)
+    t = 0
+    for _ in range(20):
+        idx = np.arange(t, t + nq * k, dtype=np.int32).reshape(nq, k)
+        t += nq * k
+        r = st.resolve(res, P, N, idx)
+        assert r["status"] == 0 and r["misses"] == nq * k
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -513,3 +571,65 @@ def test_topk_of_shard_candidates_equals_topk_of_the_whole(seed):
     order = np.lexsort((cand, -s[cand]))  # score descending, then token ascending
     merged = np.sort(cand[order[:K]])
     np.testing.assert_array_equal(merged, whole)
+
+
+@pytest.mark.parametrize("nq", [1, 4])
+def test_zero_residency_start_gives_full_residency_outputs(nq):
+    """Resolve + attention in the oracle, run from a zero-residency start and
+    from full residency over the same top-K lists: each entry reads a row
+    from its own place (the truth for a resident page, a hot-buffer slot
+    filled by the miss copies otherwise), and the attention outputs are
+    identical step after step ("Les trois états de résidence": a request
+    that starts with empty slots receives its rows as the indexer asks for
+    them).  The hot buffer is simulated as slot arrays filled with the host
+    rows of the misses; a wrong slot, a missed copy or a stale entry changes
+    the output."""
+    rng = np.random.default_rng(nq)
+    P, N, K, H = 8, 400, 24, 4
+    C = (nq + 1) * K
+    g = torch.Generator().manual_seed(31)
+    truth = wl.encode_rows(torch.randn((N, 576), generator=g), oracle.ROW_E4M3_656).numpy()
+    hot = {oracle.ZERO: oracle.HotState(C, N), oracle.FULL: oracle.HotState(C, N),
+           oracle.MIXED: oracle.HotState(C, N)}
+    slots = {m: np.zeros((C, truth.shape[1]), np.uint8) for m in hot}
+    tau = 1.0 / math.sqrt(576)
+    hits = 0
+    for step in range(12):
+        idx = np.full((nq, K), -1, np.int32)
+        for j in range(nq):
+            lo = 0 if step % 3 else 200  # revisit a region: hits after misses
+            n = K if j % 2 == 0 else K - 5
+            idx[j, :n] = np.sort(rng.choice(np.arange(lo, lo + 200), n, replace=False))
+        q = torch.randn((nq, H, 576), generator=g).to(torch.bfloat16)
+        outs = {}
+        for mode, st in hot.items():
+            res = oracle.page_resident(mode, N, 64, P)
+            r = st.resolve(res, P, N, idx)
+            assert r["status"] == 0
+            for u, c in zip(r["miss_tok"], r["miss_slot"]):
+                slots[mode][c] = truth[u]  # the miss copy: exactly one row
+            if mode == oracle.ZERO:
+                hits += r["hits"]
+            per_q = []
+            for j in range(nq):
+                rows = []
+                for k in range(K):
+                    kind, val = r["loc_kind"][j, k], r["loc_val"][j, k]
+                    if kind == 1:
+                        rows.append(truth[val])
+                    elif kind == 2:
+                        rows.append(slots[mode][val])
+                rows = np.stack(rows)
+                qb = q[j].view(torch.int16).numpy().view(np.uint16)
+                per_q.append(oracle.attention(oracle.ROW_E4M3_656, qb, rows, tau))
+            outs[mode] = per_q
+        for j in range(nq):
+            for mode in (oracle.ZERO, oracle.MIXED):
+                np.testing.assert_array_equal(outs[mode][j][0], outs[oracle.FULL][j][0])
+                np.testing.assert_array_equal(outs[mode][j][1], outs[oracle.FULL][j][1])
+            # and equal to the attention over the selected truth rows
+            sel = idx[j][idx[j] >= 0]
+            qb = q[j].view(torch.int16).numpy().view(np.uint16)
+            o, l = oracle.attention(oracle.ROW_E4M3_656, qb, truth[sel], tau)
+            np.testing.assert_array_equal(outs[oracle.FULL][j][0], o)
+    assert hits > 0
