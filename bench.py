@@ -1,13 +1,29 @@
 #!/usr/bin/env python
 """Decode-step benchmark of the sparse-MLA path on one GB300 (or N, weak scaling).
 
-One step = indexer score -> top-K -> fused resolve -> sparse MLA decode of the
-4 MLA layers of one IndexShare group, captured in a CUDA graph and replayed.
-Workload (default): full residency, 32 requests x 65,536 tokens, top-K 2048,
-64x128 E4M3 indexer, 128 MLA heads over 576-dim latent rows stored as 656-B
-FP8 rows, page 64, 4 layers.  Synthetic seeded inputs, resident in HBM
-before the timed region; L2 is flushed (256 MiB write, then a 256 MiB read of a
-second buffer, so no dirty lines carry into the step) before every timed step.
+One step = indexer score -> top-K -> fused resolve (plan + miss copies from
+pinned host memory) -> sparse MLA decode of the 4 MLA layers of one
+IndexShare group, captured in a CUDA graph and replayed.
+
+Workloads (``--workload``; the headline line is the first, the others are
+reported as secondary lines in the same JSON object):
+  c3  mixed residency, MTP3: 64 requests x 142,000 tokens, 4 queries per step,
+      top-K 2048, tail 4096 resident, hot buffer (3+2) x 2048 rows, every page
+      in pinned host memory.  The indexer and top-K run on their own inputs;
+      the lists fed to the resolve and the attention are the drawn
+      recency/Zipf stream of the trace; steps 1-20 warm the hot buffers up,
+      the timed steps are the steady state from step 21 on.
+  c2  full residency: 32 requests x 65,536 tokens, one query, every row on the
+      GPU; the resolve reads the indexer's own top-K.
+  c5  zero residency: 4 requests x 2^20 tokens, every row in pinned host
+      memory, hot buffers 2 x 2048 start empty and fill on demand (uniform +
+      Zipf stream); the timed steps are the trace's steps 1.. from the empty
+      state (the warm-up steps run first and the hot buffers are then emptied).
+All: 64x128 E4M3 indexer, 128 MLA heads over 576-dim latent rows stored as
+656-B FP8 rows, page 64, 4 layers.  Synthetic seeded inputs, resident in HBM
+(or pinned host memory, for the host-only rows) before the timed region; L2
+is flushed (256 MiB write, then a 256 MiB read of a second buffer) before
+every timed step.
 
 Output: one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (the only reference implementation there is) on a bounded sample instead.
@@ -30,8 +46,16 @@ if ROOT not in sys.path:
 METRIC = ("resolved top-K rows/s & decode-step µs per layer at 1 GB300; "
           "% of HBM/host-link peak")
 
-WORKLOAD = dict(name="full_residency_32x65536_k2048", B=32, N=65536, nq=1, K=2048, Hi=64, Di=128,
-                H=128, L=4, P=64, seed=0)
+_COMMON = dict(K=2048, Hi=64, Di=128, H=128, L=4, P=64, seed=0)
+WORKLOADS = {
+    "c3": dict(_COMMON, name="mixed_mtp3_64x142000_k2048", B=64, N=142000, nq=4, T=4096,
+               mode="mixed", source="recency_zipf", warm=20, restart=False, steps=200),
+    "c2": dict(_COMMON, name="full_residency_32x65536_k2048", B=32, N=65536, nq=1, T=0,
+               mode="full", source="indexer", warm=0, restart=False, steps=1000),
+    "c5": dict(_COMMON, name="zero_residency_4x1048576_k2048", B=4, N=1 << 20, nq=1, T=0,
+               mode="zero", source="uniform_zipf", warm=0, restart=True, steps=64),
+}
+WORKLOAD = WORKLOADS["c2"]  # the full-residency launch configuration (full-size tests)
 
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -104,20 +128,35 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+def _mode(hs, w):
+    return {"full": hs.HS_FULL, "mixed": hs.HS_MIXED, "zero": hs.HS_ZERO}[w["mode"]]
+
+
 def setup_pool(w, device):
+    """The workload's pool: every request open in its residency mode and
+    filled with its N tokens (rows, indexer keys).  Full residency keeps no
+    host copies; the other modes keep every page in pinned host memory and
+    lease the tail window and the hot buffer from the device pool."""
     import torch
     from sparse_mla_kv_fp8_gb300 import hs
     from sparse_mla_kv_fp8_gb300 import workload as wl
-    B, N, P, L = w["B"], w["N"], w["P"], w["L"]
-    pages = B * ((N + P - 1) // P)
-    cfg = hs.make_config(max_requests=B, max_tokens=N, page_tokens=P, top_k=w["K"],
-                         num_spec=w["nq"] - 1, tail_tokens=0, num_mla_layers=L,
+    B, N, P, L, K = w["B"], w["N"], w["P"], w["L"], w["K"]
+    ns = w["nq"] - 1
+    pages = (N + P - 1) // P
+    if w["mode"] == "full":
+        gpu_blocks, host_blocks = B * pages, 0
+    else:
+        C = (ns + 2) * K
+        tail_pages = 0 if w["mode"] == "zero" else (w["T"] + P - 1) // P + 1
+        gpu_blocks, host_blocks = B * (tail_pages + C // P) + 8, B * pages
+    cfg = hs.make_config(max_requests=B, max_tokens=pages * P, page_tokens=P, top_k=K,
+                         num_spec=ns, tail_tokens=w["T"], num_mla_layers=L,
                          mla_heads=w["H"], idx_heads=w["Hi"], idx_dim=w["Di"],
                          row_fmt=hs.HS_ROW_E4M3_656, idx_fmt=hs.HS_IDX_E4M3,
-                         gpu_blocks=pages, host_blocks=0)
+                         gpu_blocks=gpu_blocks, host_blocks=host_blocks)
     pool = hs.Pool(cfg, device=device)
     for b in range(B):
-        pool.open(b, hs.HS_FULL)
+        pool.open(b, _mode(hs, w))
         for t0 in range(0, N, 16384):
             n = min(16384, N - t0)
             rows = wl.mla_rows(w["seed"], b, t0, n, L, wl.ROW_E4M3_656, device=device)
@@ -139,13 +178,15 @@ def step_inputs(w, s, device):
     return q, wt, qm
 
 
-def algorithmic(w):
+def algorithmic(w, misses_per_step=0.0):
     """Algorithmic bytes / flops the method must move per launch of each stage."""
-    B, N, nq, K, Hi, Di, H, R = w["B"], w["N"], w["nq"], w["K"], w["Hi"], w["Di"], w["H"], 656
+    B, N, nq, K, Hi, Di, H, L, R = (w["B"], w["N"], w["nq"], w["K"], w["Hi"], w["Di"], w["H"],
+                                    w["L"], 656)
     return {
         "indexer": dict(bytes=B * N * (Di + 4) + B * nq * Hi * (Di + 4), flops=2 * B * nq * N * Hi * Di),
         "topk": dict(bytes=B * nq * K * 4, flops=0),
-        "resolve": dict(bytes=B * nq * K * 4 * 3, flops=0),
+        "resolve_plan": dict(bytes=B * nq * K * 4 * 3, flops=0),
+        "miss_copy": dict(bytes=misses_per_step * L * R, flops=0),
         "attention": dict(bytes=B * nq * K * R + B * nq * H * 576 * 2 + B * nq * H * 512 * 2,
                           flops=2 * B * nq * K * H * 1088),
     }
@@ -166,17 +207,50 @@ def whole_job_rows_per_s(world: int, rows_per_step_per_rank: int, ms_per_step: f
     return world * rows_per_step_per_rank / (ms_per_step / 1e3)
 
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+class Trace:
+    """The top-K lists the resolve reads, step by step.  For the indexer
+    source they are the indexer's own output; for drawn sources the trace's
+    lists of every step the run needs are staged on the device up front and
+    copied into the resolve's input buffer before each step (input staging,
+    outside the timed events)."""
+
+    def __init__(self, w, device, first_step, n_steps):
+        import torch
+        from sparse_mla_kv_fp8_gb300 import workload as wl
+        self.w = w
+        self.drawn = w["source"] != "indexer"
+        self.first = first_step
+        self.n = n_steps
+        self.buf = torch.empty((w["B"], w["nq"], w["K"]), dtype=torch.int32, device=device)
+        if self.drawn:
+            lists = wl.drawn_streams(w["seed"], w["B"], range(first_step, first_step + n_steps),
+                                     w["nq"], w["N"], w["K"], w["P"], w["source"], w["T"])
+            self.dev = torch.from_numpy(lists).to(device)
+            self.host = torch.from_numpy(lists).pin_memory()
+
+    def load(self, s):
+        """Put step s's lists into the resolve's input buffer."""
+        if self.drawn:
+            self.buf.copy_(self.dev[(s - self.first) % self.n], non_blocking=True)
+
+
+def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
+    """Time `steps` decode steps of workload w (after `warmup` untimed ones);
+    return the result dictionary of that workload."""
     import torch
     from sparse_mla_kv_fp8_gb300 import hs
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    w = dict(WORKLOAD)
-    if args.requests:
-        w["B"] = args.requests
     B, nq, K, L, H = w["B"], w["nq"], w["K"], w["L"], w["H"]
+    drawn = w["source"] != "indexer"
+    n_warm = max(warmup, w["warm"]) if not w["restart"] else warmup
+    stage_steps = min(steps, 20)
+    e2e_steps = min(steps, 50)
+    # steps of the trace: warm-up, timed, stage timing, end to end
+    first_timed = 1 if w["restart"] else n_warm + 1
+    total_trace = (first_timed - 1) + steps + stage_steps + e2e_steps
+    trace = Trace(w, device, 1, max(total_trace, n_warm))
     pool = setup_pool(w, device)
     tau = 1.0 / math.sqrt(576)
     n_inputs = 4
@@ -185,7 +259,7 @@ def run_ours(args, rank, world, local_rank):
     wt = inputs[0][1].clone()
     qm = inputs[0][2].clone()
     out = torch.empty((L, B, nq, H, 512), dtype=torch.bfloat16, device=device)
-    topk = torch.empty((B, nq, K), dtype=torch.int32, device=device)
+    topk = torch.empty((B, nq, K), dtype=torch.int32, device=device)  # the indexer's top-K
     rid = torch.empty((B, nq, K), dtype=torch.int32, device=device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     scrub = torch.zeros(256 << 20, dtype=torch.uint8, device=device)
@@ -194,33 +268,50 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()  # write a buffer larger than L2 ...
         scrub.max()    # ... then read another, so the write-back of those dirty lines lands here
 
-    stream = torch.cuda.Stream(device)
-    stream.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)  # eager warm-up
-        stream.synchronize()
-        with torch.cuda.graph(graph, stream=stream):
-            pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)
-    torch.cuda.synchronize()
-    if pool.get_error() != hs.HS_OK:
-        raise RuntimeError("device error during warm-up")
+    def enqueue_step(st):
+        if drawn:
+            # the indexer and top-K on their own inputs, the resolve and the
+            # attention on the trace's lists
+            pool.indexer_topk(q, wt, B, nq, topk, stream=st)
+            pool.resolve(trace.buf, B, nq, rid, stream=st)
+            for l in range(L):
+                pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=st)
+        else:
+            pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=st)
 
-    def load(i):
+    def load(i, s):
         a, b_, c = inputs[i % n_inputs]
         q.copy_(a)
         wt.copy_(b_)
         qm.copy_(c)
+        trace.load(s)
 
+    stream = torch.cuda.Stream(device)
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    # the warm-up steps run eagerly once (step 1), then through the graph
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            load(i)
+        load(0, 1)
+        enqueue_step(stream)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            enqueue_step(stream)
+    torch.cuda.synchronize()
+    # capturing recorded the launches without running them: step 1 ran once
+    if pool.get_error() != hs.HS_OK:
+        raise RuntimeError("device error during warm-up")
+    with torch.cuda.stream(stream):
+        for i in range(1, n_warm):
+            load(i, 1 + i)
             graph.replay()
     torch.cuda.synchronize()
+    if w["restart"]:
+        reset_hot_state(pool, w)
+    pool.reset_stats()
 
     # ---- timed region: graph replays, L2 flushed before each step ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -228,8 +319,8 @@ def run_ours(args, rank, world, local_rank):
     t_wall = time.perf_counter()
     with ClockSampler(local_rank) as clk:
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                load(i)
+            for i in range(steps):
+                load(i, first_timed + i)
                 flush_l2()
                 starts[i].record(stream)
                 graph.replay()
@@ -238,81 +329,120 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall
-        # ---- per-stage timing (same step, eager, events between the stages) ----
-        stage = stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream,
-                            min(args.steps, 50))
+    timed_stats = pool.stats()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     if pool.get_error() != hs.HS_OK:
         raise RuntimeError("device error in the timed region")
     if world > 1:
         total_ms = max_over_ranks(total_ms, device)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
     rows_per_step = B * nq * K * L
     value = whole_job_rows_per_s(world, rows_per_step, ms_per_step)
+    misses_per_step = timed_stats["misses"] / steps
 
+    # ---- per-stage timing (the next steps of the trace, eager, events between stages) ----
+    stage = stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, stream,
+                        stage_steps, first_timed + steps)
     # ---- end to end: host inputs in, result out, through the public API ----
-    e2e = end_to_end(pool, w, inputs, stream, args.steps, device)
+    e2e = end_to_end(pool, w, inputs, trace, stream, e2e_steps, device,
+                     first_timed + steps + stage_steps)
+    if pool.get_error() != hs.HS_OK:
+        raise RuntimeError("device error after the timed region")
 
     peaks = _peaks()
-    alg = algorithmic(w)
-    roof, roof_all = roofline(stage, alg, peaks, w)
-    step_bytes = alg["indexer"]["bytes"] + alg["topk"]["bytes"] + alg["resolve"]["bytes"] + L * alg["attention"]["bytes"]
+    alg = algorithmic(w, misses_per_step)
+    link = host_link_peak(device) if (w["mode"] != "full" and not args.no_host_link) else None
+    roof, roof_all = roofline(stage, alg, peaks, w, ms_per_step, link)
+    step_bytes = (alg["indexer"]["bytes"] + alg["topk"]["bytes"] + alg["resolve_plan"]["bytes"]
+                  + L * alg["attention"]["bytes"])
     res = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "rows/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": ms_per_step,
         "us_per_layer": ms_per_step * 1e3 / L,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f16",
-        "dtype_note": "indexer: E4M3 MMA operands, fp32 accumulate; attention (the dominant kernel): E4M3 rows dequantised to fp16 MMA operands with fp16 queries and probabilities, fp32 accumulate and softmax",
-        "data": "synthetic (seeded; indexer values m/8 in E4M3, latent N(0,1) quantised to E4M3 + fp32 group scales)",
-        "config": {"workload": w["name"], "requests_per_gpu": B, "tokens_per_request": w["N"],
-                   "queries_per_request": nq, "top_k": K, "indexer": f"{w['Hi']}x{w['Di']} e4m3",
-                   "mla_heads": H, "latent": 576, "row_bytes": 656, "mla_layers": L,
-                   "page_tokens": w["P"], "residency": "full", "graph": "cuda graph replay",
-                   "l2": "flushed before each timed step (256 MiB write, then a 256 MiB read of a second buffer)"},
+        "value": value,
         "stage_us": {k: v * 1e3 for k, v in stage.items()},
         "hbm_frac_step": (step_bytes / (ms_per_step / 1e3)) / (peaks["hbm"] * 1e9),
+        "hbm_frac_step_note": "algorithmic HBM bytes of the step (indexer keys, top-K, resolve, "
+                              "the L layers' rows, queries and outputs) / step time / measured "
+                              "HBM copy peak",
         "roofline": roof,
         "stage_roofline": roof_all,
-        "host_link": host_link(device) if not args.no_host_link else None,
         "e2e": e2e,
-        "gpu_launches": pool.step_kernel_count(B, nq) * args.steps,
+        "gpu_launches": pool.step_kernel_count(B, nq) * steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
+        "misses_per_step": misses_per_step,
+        "resident_per_step": timed_stats["resident"] / steps,
+        "hits_per_step": timed_stats["hits"] / steps,
+        "config": config_of(w, steps),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if link is not None:
+        ms_copy = stage["miss_copy"]
+        nbytes = misses_per_step * L * 656
+        ach = nbytes / (ms_copy / 1e3) / 1e9 if ms_copy > 0 else 0.0
+        res["host_link"] = {
+            "miss_bytes_per_step": nbytes, "us_miss_copy": ms_copy * 1e3, "achieved_gbs": ach,
+            "peak_gbs": link["peak_gbs"], "peak_source": link["source"], "frac": ach / link["peak_gbs"],
+            "peak_candidates": link["candidates"],
+            "timed": "miss-copy kernel span (hs_miss_copy, events on its stream) over the misses of "
+                     "the stage-timing steps; bytes = the timed steps' mean misses x L x 656"}
+    if rank == 0 and headline and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     pool.close()
+    del pool
+    torch.cuda.empty_cache()
     return res
+
+
+def reset_hot_state(pool, w):
+    """Every request's hot buffer back to empty, step counter 0 (the state a
+    zero-residency request starts in)."""
+    import numpy as np
+    empty_map = np.full(pool.cfg.max_tokens, -1, np.int32)
+    empty_slots = np.full(pool.C, -1, np.int32)
+    zero_stamp = np.zeros(pool.C, np.uint32)
+    for b in range(w["B"]):
+        pool.load_state(b, empty_map, empty_slots, zero_stamp, 0)
+
+
+def config_of(w, steps):
+    return {"workload": w["name"], "requests_per_gpu": w["B"], "tokens_per_request": w["N"],
+            "queries_per_request": w["nq"], "top_k": w["K"], "indexer": f"{w['Hi']}x{w['Di']} e4m3",
+            "mla_heads": w["H"], "latent": 576, "row_bytes": 656, "mla_layers": w["L"],
+            "page_tokens": w["P"], "residency": w["mode"], "tail_tokens": w["T"],
+            "hot_rows": (w["nq"] + 1) * w["K"] if w["mode"] != "full" else 0,
+            "topk_source": ("the indexer's own top-K" if w["source"] == "indexer" else
+                            f"drawn {w['source'].replace('_', '/')} stream; the indexer and top-K "
+                            f"run on their own inputs"),
+            "timed_steps": (f"trace steps 1..{steps} from empty hot buffers" if w["restart"] else
+                            f"trace steps {w['warm'] + 1}.. ({steps} steps, steady state)"
+                            if w["warm"] else f"{steps} steps"),
+            "graph": "cuda graph replay",
+            "l2": "flushed before each timed step (256 MiB write, then a 256 MiB read of a second buffer)"}
 
 
 HOLD_CYCLES = 1_000_000  # ~0.5 ms of SM clock: longer than enqueueing one step's stages
 
 
-def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, steps):
+def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, stream, steps,
+                first_step):
     """Average ms per launch of each stage, CUDA events on the launching stream
-    (the stages are queued behind a spin kernel, so they run back to back)."""
+    (the stages are queued behind a spin kernel, so they run back to back).
+    Trace steps first_step.. (the hot-buffer state keeps evolving)."""
     import torch
     B, nq, L = w["B"], w["nq"], w["L"]
     tau = 1.0 / math.sqrt(576)
-    acc = {"indexer": 0.0, "topk": 0.0, "resolve": 0.0, "attention": 0.0}
-    scores = pool_scores = None
-    stride = w["N"]
+    names = ["indexer", "topk", "resolve_plan", "miss_copy", "attention"]
+    acc = {k: 0.0 for k in names}
+    stride = pool.cfg.max_tokens
     scores = torch.empty((B, nq, stride), dtype=torch.float32, device=q.device)
     for i in range(steps):
         a, b_, c = inputs[i % len(inputs)]
         q.copy_(a)
         wt.copy_(b_)
         qm.copy_(c)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 + L)]
+        trace.load(first_step + i)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5 + L)]
         with torch.cuda.stream(stream):
             flush_l2()
             # hold the stream while the host enqueues every stage, so that the
@@ -323,157 +453,124 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, flush_l2, stream, st
             ev[1].record(stream)
             pool.topk(scores, stride, B, nq, topk, stream=stream)
             ev[2].record(stream)
-            pool.resolve(topk, B, nq, rid, stream=stream)
+            pool.resolve_plan(trace.buf if trace.drawn else topk, B, nq, rid, stream=stream)
             ev[3].record(stream)
+            pool.miss_copy(B, nq, stream=stream)
+            ev[4].record(stream)
             for l in range(L):
                 pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=stream)
-                ev[4 + l].record(stream)
+                ev[5 + l].record(stream)
         torch.cuda.synchronize()
-        acc["indexer"] += ev[0].elapsed_time(ev[1])
-        acc["topk"] += ev[1].elapsed_time(ev[2])
-        acc["resolve"] += ev[2].elapsed_time(ev[3])
-        acc["attention"] += ev[3].elapsed_time(ev[3 + L]) / L
-    del pool_scores
+        for k in range(4):
+            acc[names[k]] += ev[k].elapsed_time(ev[k + 1])
+        acc["attention"] += ev[4].elapsed_time(ev[4 + L]) / L
+    del scores
     return {k: v / steps for k, v in acc.items()}
 
 
-# DRAM bytes per launch from one ncu capture of 16 requests (scaled x2 to 32
-# requests), valid only for the kernel sources they were taken
-# on (the kernel's .cu and the shared device header, hashed together).
-TRAFFIC = {"attention": (("attention.cu", "tc.cuh"), "b1be9eaf94bcde78", 2 * (27643264 + 3392)),
-           "indexer": (("indexer.cu", "tc.cuh"), "9a84ea0a9b297437", 2 * (138577152 + 2479616)),
-           "topk": (("topk.cu", "tc.cuh"), "cf9fadfe87a5a0c2", 2 * 4227328)}
-
-
-def _traffic(stage, w):
-    import hashlib
-    # the figures are per launch of the 32-request workload only
-    if stage not in TRAFFIC or w != WORKLOAD:
-        return None
-    files, sha, nbytes = TRAFFIC[stage]
-    h = hashlib.sha256()
-    for fname in files:
-        with open(os.path.join(ROOT, "sparse_mla_kv_fp8_gb300", "csrc", fname), "rb") as f:
-            h.update(f.read())
-    return nbytes if h.hexdigest()[:16] == sha else None
-
-
 KERNELS = {"indexer": "indexer_tc_kernel", "topk": "topk_cluster_kernel",
-           "resolve": "resolve_plan_kernel", "attention": "attn_tc_kernel"}
+           "resolve_plan": "resolve_plan_kernel", "miss_copy": "miss_copy_kernel",
+           "attention": "attn_tc_kernel"}
 
 
-def roofline(stage, alg, peaks, w):
+def roofline(stage, alg, peaks, w, ms_per_step, link):
     """Roofline of every stage; the one with the largest share of the step is
-    the headline.  The attention is a bf16 tensor-core contraction above the
-    ridge (425 flop/B vs ~285 for the measured peaks): tensor-bound against the
-    sustained bf16 peak (it is timed inside a long step).  The indexer, top-K
-    and resolve are memory-bound against the measured HBM copy bandwidth."""
+    the headline.  Each stage is timed alone between events, so the burst
+    peaks apply.  The attention is a 16-bit tensor-core contraction above the
+    ridge (425 flop/B against ~280 for the measured peaks): tensor-bound
+    against the burst bf16 peak (fp16 has the same dense rate).  The
+    indexer, top-K and resolve plan are memory-bound against the measured HBM
+    copy bandwidth; the miss copy against the host link.  Shares are stage
+    time x launches per step / the step's time (stages overlap a little
+    inside the step, so the shares can sum above 1)."""
     L = w["L"]
-    share = {"indexer": stage["indexer"], "topk": stage["topk"], "resolve": stage["resolve"],
-             "attention": stage["attention"] * L}
-    tot = sum(share.values())
+    counts = {"indexer": 1, "topk": 1, "resolve_plan": 1, "miss_copy": 1, "attention": L}
     out = {}
-    for k in share:
+    for k, n in counts.items():
         ms = stage[k]
+        if ms <= 0:
+            continue
         a = alg[k]
         gbs = a["bytes"] / (ms / 1e3) / 1e9
+        share = ms * n / ms_per_step
         if k == "attention":
             tf = a["flops"] / (ms / 1e3) / 1e12
-            out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16_sus"],
-                      "unit": "TFLOP/s", "frac": tf / peaks["bf16_sus"], "traffic": _traffic(k, w),
-                      "peak_source": peaks["src"] + " bf16 sustained (fp16 operands: the same dense rate)",
+            out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
+                      "unit": "TFLOP/s", "frac": tf / peaks["bf16"], "traffic": None,
+                      "peak_source": peaks["src"] + " bf16 burst (the stage is timed alone; fp16 "
+                                                    "operands have the same dense rate)",
                       "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
-                      "share_of_step": share[k] / tot, "us_per_launch": ms * 1e3}
+                      "share_of_step": share, "us_per_launch": ms * 1e3}
+        elif k == "miss_copy":
+            if link is None or a["bytes"] == 0:
+                continue
+            out[k] = {"kernel": KERNELS[k], "bound": "host_link", "achieved": gbs,
+                      "peak": link["peak_gbs"], "unit": "GB/s", "frac": gbs / link["peak_gbs"],
+                      "traffic": None, "peak_source": link["source"], "share_of_step": share,
+                      "us_per_launch": ms * 1e3}
         else:
             out[k] = {"kernel": KERNELS[k], "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": _traffic(k, w),
-                      "peak_source": peaks["src"], "share_of_step": share[k] / tot,
+                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": None,
+                      "peak_source": peaks["src"] + " HBM copy", "share_of_step": share,
                       "us_per_launch": ms * 1e3}
-    dom = max(share, key=share.get)
+    dom = max(out, key=lambda k: out[k]["share_of_step"])
     return out[dom], out
 
 
-def host_link(device, steps=10):
-    """Miss traffic over the host link: a zero-residency batch (4 requests x
-    65,536 tokens, 4 layers) whose hot buffers are emptied before every call,
-    so each hs_resolve copies 4 x 2048 rows x 4 layers from pinned host memory.
-    Peak: a pinned-host -> device cudaMemcpyAsync of 1 GiB."""
-    import numpy as np
+def host_link_peak(device, nbytes=1 << 30):
+    """The host link's measured rate for reads of pinned host memory: the
+    higher of a 1 GiB cudaMemcpyAsync (copy engines) and the library's
+    zero-copy read kernel (hs_host_read_probe, the miss copy's loads) over
+    the same 1 GiB."""
     import torch
     from sparse_mla_kv_fp8_gb300 import hs
-    from sparse_mla_kv_fp8_gb300 import workload as wl
-    B, N, K, L, P = 4, 65536, 2048, 4, 64
-    pages = N // P
-    cfg = hs.make_config(max_requests=B, max_tokens=N, page_tokens=P, top_k=K, num_spec=0,
-                         tail_tokens=0, num_mla_layers=L, mla_heads=128, idx_heads=64,
-                         idx_dim=128, row_fmt=hs.HS_ROW_E4M3_656, idx_fmt=hs.HS_IDX_E4M3,
-                         gpu_blocks=B * (2 * K // P) + 8, host_blocks=B * pages)
-    pool = hs.Pool(cfg, device=device)
-    for b in range(B):
-        pool.open(b, hs.HS_ZERO)
-        pool.append(b, wl.mla_rows(7, b, 0, N, L, wl.ROW_E4M3_656, device=device),
-                    torch.zeros((N, 128), dtype=torch.uint8, device=device))
-    idx = np.stack([wl.drawn_topk(7, b, 1, 0, N, K, P, "uniform_zipf")[None] for b in range(B)])
-    topk = torch.from_numpy(idx).to(device)
-    rid = torch.empty_like(topk)
-    empty_map = np.full(N, -1, np.int32)
-    empty_slots = np.full(pool.C, -1, np.int32)
-    zero_stamp = np.zeros(pool.C, np.uint32)
-    times = []
-    for i in range(steps + 2):
-        for b in range(B):
-            pool.load_state(b, empty_map, empty_slots, zero_stamp, 0)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(HOLD_CYCLES)  # the copy kernels start without waiting for the host
-        e0.record()
-        pool.resolve(topk, B, 1, rid)
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= 2:
-            times.append(e0.elapsed_time(e1))
-    st = pool.stats()
-    pool.close()
-    misses_per_call = B * K
-    nbytes = misses_per_call * L * 656
-    ms = statistics.median(times)
-    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
-    dst = torch.empty(1 << 30, dtype=torch.uint8, device=device)
-    pk = []
-    for i in range(4):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        dst.copy_(src, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        pk.append((1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9)
-    peak = max(pk)
-    ach = nbytes / (ms / 1e3) / 1e9
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    src.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    res = {}
+    for name in ("memcpy", "zero_copy_kernel"):
+        best = 0.0
+        for i in range(4):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if name == "memcpy":
+                dst.copy_(src, non_blocking=True)
+            else:
+                hs.host_read_probe(src, dst, nbytes)
+            e1.record()
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        res[name] = best
     del src, dst
-    return {"workload": "zero residency, 4 requests x 65,536 tokens, 4 layers, hot buffers emptied "
-                        "before each call: 8192 misses x 4 layers x 656 B per hs_resolve",
-            "bytes_per_call": nbytes, "us_per_call": ms * 1e3, "achieved_gbs": ach,
-            "peak_gbs": peak, "peak_source": "measured cudaMemcpyAsync pinned host -> device, 1 GiB",
-            "frac": ach / peak, "timed": "resolve plan + miss copy (events around hs_resolve)",
-            "misses_counted": int(st["misses"])}
+    name = max(res, key=res.get)
+    return {"peak_gbs": res[name], "candidates": res,
+            "source": ("measured 1 GiB pinned host -> device, the higher of cudaMemcpyAsync and "
+                       f"the zero-copy read kernel: {name}")}
 
 
-def end_to_end(pool, w, inputs, stream, steps, device):
+def end_to_end(pool, w, inputs, trace, stream, steps, device, first_step):
     """Same metric through the public API with pinned-host inputs and a
     device->host read of the step's output inside the timed region.  Every
-    step copies its own inputs in and its own output back; the copies run on
-    two copy streams (the two copy engines) so that step i+1's inputs and
-    step i-1's output move while step i computes (double-buffered device
-    inputs and outputs, ordered by events)."""
+    step copies its own inputs in (indexer queries and weights, the MLA
+    queries of the L layers and, for drawn workloads, the step's top-K lists)
+    and its own output back; the copies run on two copy streams (the two copy
+    engines) so that step i+1's inputs and step i-1's output move while step
+    i computes (double-buffered device inputs and outputs, ordered by
+    events)."""
     import torch
     B, nq, K, L, H = w["B"], w["nq"], w["K"], w["L"], w["H"]
+    drawn = trace.drawn
     tau = 1.0 / math.sqrt(576)
     host_in = [(a.cpu().pin_memory(), b.cpu().pin_memory(), c.cpu().pin_memory()) for a, b, c in inputs]
-    dev_in = [tuple(torch.empty_like(t) for t in inputs[0]) for _ in range(2)]
+    dev_in = [tuple(torch.empty_like(t) for t in inputs[0]) + (torch.empty_like(trace.buf),)
+              for _ in range(2)]
     outs = [torch.empty((L, B, nq, H, 512), dtype=torch.bfloat16, device=device) for _ in range(2)]
     topk = torch.empty((B, nq, K), dtype=torch.int32, device=device)
     rid = torch.empty_like(topk)
     host_out = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+    if drawn:
+        h2d += trace.buf.numel() * 4
     d2h = host_out.numel() * host_out.element_size()
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=False)
@@ -486,7 +583,7 @@ def end_to_end(pool, w, inputs, stream, steps, device):
     stream.wait_event(ev0)
     s_out.wait_event(ev0)
     for i in range(steps):
-        q, wt, qm = dev_in[i % 2]
+        q, wt, qm, tk_in = dev_in[i % 2]
         out = outs[i % 2]
         with torch.cuda.stream(s_in):
             if i >= 2:
@@ -495,11 +592,19 @@ def end_to_end(pool, w, inputs, stream, steps, device):
             q.copy_(a, non_blocking=True)
             wt.copy_(b_, non_blocking=True)
             qm.copy_(c, non_blocking=True)
+            if drawn:
+                tk_in.copy_(trace.host[(first_step + i - trace.first) % trace.n], non_blocking=True)
             in_done[i].record(s_in)
         stream.wait_event(in_done[i])
         if i >= 2:
             stream.wait_event(out_done[i - 2])  # step i-2's output has left this buffer
-        pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)
+        if drawn:
+            pool.indexer_topk(q, wt, B, nq, topk, stream=stream)
+            pool.resolve(tk_in, B, nq, rid, stream=stream)
+            for l in range(L):
+                pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=stream)
+        else:
+            pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)
         comp_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])
@@ -517,49 +622,56 @@ def end_to_end(pool, w, inputs, stream, steps, device):
 # ---------------------------------------------------------------------------
 # CPU oracle timing
 # ---------------------------------------------------------------------------
-def oracle_request_step(w, b, s):
+def oracle_request_step(w, b, s, queries=None):
     """One request x one step of the workload through the CPU oracle: indexer
-    over all N tokens, top-K, resolve (full residency), attention of the L
-    layers.  Returns (seconds, rows)."""
+    over all N tokens, top-K, resolve (the workload's residency, a fresh hot
+    buffer) of the lists the workload resolves (the indexer's own, or the
+    drawn trace's), attention of the L layers over them.  `queries` limits
+    the sample to some of the step's nq queries (all by default).  Returns
+    (seconds, rows)."""
     import numpy as np
+    import torch
     import oracle
     from sparse_mla_kv_fp8_gb300 import workload as wl
     N, nq, K, L, H, P = w["N"], w["nq"], w["K"], w["L"], w["H"], w["P"]
+    js = list(range(nq)) if queries is None else list(queries)
     keys = wl.idx_keys(w["seed"], b, 0, N, w["Di"], wl.IDX_E4M3).numpy()
-    q = wl.idx_query(w["seed"], b, s, nq, w["Hi"], w["Di"], wl.IDX_E4M3).numpy()
-    wt = wl.idx_weights(w["seed"], b, s, nq, w["Hi"]).numpy()
-    qm = wl.mla_query(w["seed"], s, 1, nq, H, L).view(__import__("torch").int16).numpy().view(np.uint16)
+    q = wl.idx_query(w["seed"], b, s, nq, w["Hi"], w["Di"], wl.IDX_E4M3).numpy()[js]
+    wt = wl.idx_weights(w["seed"], b, s, nq, w["Hi"]).numpy()[js]
+    qm = wl.mla_query(w["seed"], s, 1, nq, H, L).view(torch.int16).numpy().view(np.uint16)
     sigma = np.ones(N, np.float32)
-    hot = oracle.HotState(2 * K, N)
-    resident = oracle.page_resident(oracle.FULL, N, 0, P)
+    if w["source"] != "indexer":
+        drawn = np.stack([wl.drawn_topk(w["seed"], b, s, j, oracle.visible(N, nq, j), K, P,
+                                        w["source"], w["T"]) for j in range(nq)])
+    mode = {"full": oracle.FULL, "mixed": oracle.MIXED, "zero": oracle.ZERO}[w["mode"]]
+    hot = oracle.HotState((nq + 1) * K, N)
+    resident = oracle.page_resident(mode, N, w["T"], P)
     t0 = time.perf_counter()
     s_all = oracle.indexer_scores(oracle.IDX_E4M3, q, wt, keys, sigma, N)
-    idx = np.stack([oracle.topk(s_all[j], oracle.visible(N, nq, j), K) for j in range(nq)])
+    idx = np.stack([oracle.topk(s_all[i], oracle.visible(N, nq, j), K) for i, j in enumerate(js)])
     t_sel = time.perf_counter() - t0
-    r = hot.resolve(resident, P, N, idx)
+    if w["source"] != "indexer":
+        idx = drawn[js]
+    t0 = time.perf_counter()
+    r = hot.resolve(resident, P, N, np.ascontiguousarray(idx))
+    t_res = time.perf_counter() - t0
     assert r["status"] == 0
     # the rows the selection reads (input preparation, not timed)
     sel = np.unique(idx[idx >= 0])
-    rows = {}
-    for t in sel.tolist():
-        rows[t] = None
-    import torch
-    needed = torch.from_numpy(sel).long()
-    blocks = sorted(set((needed // 1024).tolist()))
     allrows = {}
-    for blk in blocks:
+    for blk in sorted(set((sel // 1024).tolist())):
         chunk = wl.mla_rows(w["seed"], b, blk * 1024, min(1024, N - blk * 1024), L, wl.ROW_E4M3_656)
         for t in sel[(sel >= blk * 1024) & (sel < blk * 1024 + 1024)].tolist():
             allrows[t] = chunk[t - blk * 1024]
     t1 = time.perf_counter()
     tau = 1.0 / math.sqrt(576)
-    for j in range(nq):
-        ids = idx[j][idx[j] >= 0]
+    for i, j in enumerate(js):
+        ids = idx[i][idx[i] >= 0]
         for l in range(L):
             rr = np.stack([allrows[t][l].numpy() for t in ids.tolist()])
             oracle.attention(oracle.ROW_E4M3_656, qm[l, 0, j], rr, tau)
     t_att = time.perf_counter() - t1
-    return t_sel + t_att, nq * K * L
+    return t_sel + t_res + t_att, len(js) * K * L
 
 
 def cpu_baseline(w, budget_s=20.0):
@@ -573,46 +685,99 @@ def cpu_baseline(w, budget_s=20.0):
         if secs > budget_s:
             break
     return {"value": rows / secs, "unit": "rows/s", "cores": oracle.omp_threads(), "kind": "oracle",
-            "sample": f"{n} request-step(s) of the workload (indexer over {w['N']} tokens, "
-                      f"top-{w['K']}, resolve, {w['L']} layers x {w['H']} heads attention), "
-                      f"rows/s = selected rows x layers / oracle seconds"}
+            "sample": f"{n} request-step(s) of the workload (indexer over {w['N']} tokens x "
+                      f"{w['nq']} queries, top-{w['K']}, resolve, {w['L']} layers x {w['H']} heads "
+                      f"attention), rows/s = selected rows x layers / oracle seconds"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     import oracle
-    w = dict(WORKLOAD)
+    w = dict(WORKLOADS[args.workload if args.workload != "all" else "c3"])
+    # each step is a bounded sample: one request, one of its nq queries (in
+    # turn), the indexer over all its tokens and the L layers' attention
     for i in range(args.warmup):
-        oracle_request_step(w, i % w["B"], 1000 + i)
+        oracle_request_step(w, i % w["B"], 1000 + i, queries=[i % w["nq"]])
     secs, rows = 0.0, 0
     for i in range(args.steps):
-        dt, r = oracle_request_step(w, i % w["B"], 1 + i)
+        dt, r = oracle_request_step(w, i % w["B"], 1 + i, queries=[i % w["nq"]])
         secs += dt
         rows += r
     value = rows / secs
+    cfg = config_of(w, args.steps)
+    sample = ("each step = 1 request x 1 of its queries x 1 decode step of the workload "
+              "(indexer over all its tokens, top-K, resolve, the L layers' attention)")
+    cfg["sample"] = sample
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w["name"], "requests_per_gpu": w["B"],
-                       "tokens_per_request": w["N"], "top_k": w["K"], "mla_layers": w["L"],
-                       "sample": "one request per step"},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.omp_threads(),
-                             "kind": "oracle",
-                             "sample": "each step = 1 request x 1 decode step of the workload"},
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, local_rank):
+    order = ["c3", "c2", "c5"] if args.workload == "all" else [args.workload]
+    head = order[0]
+    w = dict(WORKLOADS[head])
+    if args.requests:
+        w["B"] = args.requests
+    steps = args.steps or w["steps"]
+    r = run_workload(w, args, rank, world, local_rank, steps, args.warmup, headline=True)
+    res = {
+        "metric": METRIC,
+        "value": r["value"],
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"],
+        "us_per_layer": r["us_per_layer"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "dtype_note": "indexer: E4M3 MMA operands, fp32 accumulate; attention (the dominant kernel): "
+                      "E4M3 rows dequantised to fp16 MMA operands with fp16 queries and "
+                      "probabilities, fp32 accumulate and softmax",
+        "data": "synthetic (seeded; indexer values m/8 in E4M3, latent N(0,1) quantised to E4M3 + "
+                "fp32 group scales; drawn top-K streams stand in for the agentic traces)",
+    }
+    for k in ("config", "roofline", "e2e", "gpu_launches", "clocks", "cpu_baseline", "host_link",
+              "stage_us", "stage_roofline", "hbm_frac_step", "hbm_frac_step_note",
+              "misses_per_step", "hits_per_step", "resident_per_step", "wall_s_timed_region"):
+        if k in r:
+            res[k] = r[k]
+    if not args.no_secondary:
+        sec = {}
+        for name in order[1:]:
+            ws = dict(WORKLOADS[name])
+            sr = run_workload(ws, args, rank, world, local_rank, ws["steps"] if not args.steps
+                              else min(args.steps, ws["steps"]), args.warmup, headline=False)
+            sec[name] = {k: sr[k] for k in ("config", "value", "ms_per_step", "us_per_layer",
+                                           "roofline", "stage_us", "stage_roofline",
+                                           "hbm_frac_step", "host_link", "misses_per_step",
+                                           "hits_per_step", "resident_per_step", "e2e", "clocks",
+                                           "gpu_launches") if k in sr}
+        if sec:
+            res["secondary"] = sec
+    return res
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)  # ~0.6 s timed: several clock samples
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0 = the workload's default)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--requests", type=int, default=0, help="override requests per GPU")
+    ap.add_argument("--workload", default="all", choices=["all", "c3", "c2", "c5"],
+                    help="all = c3 headline with c2 and c5 as secondary lines")
+    ap.add_argument("--requests", type=int, default=0, help="override requests per GPU (headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-host-link", action="store_true")
     args = ap.parse_args()
@@ -622,6 +787,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
+        if args.steps == 0:
+            args.steps = 3
         res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)

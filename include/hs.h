@@ -285,6 +285,18 @@ hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
 hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
                      int32_t *row_id, cudaStream_t stream);
 
+/* The two halves of hs_resolve, for callers that time them apart or run the
+ * copy on another stream (ordered after the plan by an event):
+ * hs_resolve_plan does the union, classification, LRU update and row ids,
+ * and leaves the step's miss lists in the pool's workspace; hs_miss_copy then
+ * copies exactly one row per miss and layer from pinned host memory into its
+ * hot-buffer slot.  hs_miss_copy must follow the plan it copies for, with the
+ * same B and nq, before the next plan; the rows of the misses are only there
+ * once it has run.  hs_resolve = hs_resolve_plan + hs_miss_copy. */
+hs_status hs_resolve_plan(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
+                          int32_t *row_id, cudaStream_t stream);
+hs_status hs_miss_copy(hs_pool *pool, int32_t B, int32_t nq, cudaStream_t stream);
+
 /* Sparse MLA decode of one layer over the resolved rows ("Ce qui se passe"):
  *   z[b][j][h][k] = softmax_scale * q[b][j][h][:576] . row(row_id[b][j][k])[:576]
  *   out[b][j][h][:512] = sum_k softmax_k(z) * row[:512]   (rows with id -1 skipped)
@@ -394,6 +406,17 @@ int32_t hs_step_kernel_count(const hs_pool *pool, int32_t B, int32_t nq);
  * without faulting or hanging a GPU.  HS_ERR_INVALID_ARG for a limit out of
  * range. */
 hs_status hs_check_wait_timeout(hs_pool *pool, int64_t limit_cycles, cudaStream_t stream);
+
+/* Host-link probe: copy `bytes` of pinned host memory (host_src, allocated
+ * with cudaHostAlloc / torch pin_memory) into device memory (dev_dst) with a
+ * kernel that reads the host memory through its device mapping, 16-byte
+ * loads, four in flight per thread, `ctas` CTAs of 256 threads (0 = four per
+ * SM): the same zero-copy reads as the miss copy, for measuring the rate the
+ * host link gives them.  Both pointers 16-byte aligned, bytes a multiple of
+ * 16.  Async on `stream`.  The pages have no counterpart; it exists so that
+ * miss traffic can be reported against the link's measured rate. */
+hs_status hs_host_read_probe(const void *host_src, void *dev_dst, size_t bytes, int32_t ctas,
+                             cudaStream_t stream);
 
 /* A static English description of a status. */
 const char *hs_status_string(hs_status s);

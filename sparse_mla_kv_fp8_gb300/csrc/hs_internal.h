@@ -124,6 +124,9 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
                         int32_t *topk, cudaStream_t st);
 cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
                            cudaStream_t st);
+cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, int nq,
+                                int32_t *row_id, cudaStream_t st);
+cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st);
 // q_ready: the queries were written before the previous kernel on `st`
 // started (true inside hs_step), so the kernel may stage them before it waits
 // for that kernel.

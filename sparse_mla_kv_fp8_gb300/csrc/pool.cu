@@ -562,6 +562,17 @@ hs_status hs_resolve(hs_pool *p, const int32_t *topk, int32_t B, int32_t nq, int
     return cuda_status(hs::launch_resolve(p, topk, B, nq, row_id, st));
 }
 
+hs_status hs_resolve_plan(hs_pool *p, const int32_t *topk, int32_t B, int32_t nq, int32_t *row_id,
+                          cudaStream_t st) {
+    if (!step_batch_ok(p, B, nq) || !topk || !row_id) return HS_ERR_INVALID_ARG;
+    return cuda_status(hs::launch_resolve_plan(p, topk, B, nq, row_id, st));
+}
+
+hs_status hs_miss_copy(hs_pool *p, int32_t B, int32_t nq, cudaStream_t st) {
+    if (!step_batch_ok(p, B, nq)) return HS_ERR_INVALID_ARG;
+    return cuda_status(hs::launch_miss_copy(p, B, nq, st));
+}
+
 hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const int32_t *row_id,
                                int32_t B, int32_t nq, float scale, void *out, float *lse,
                                cudaStream_t st) {

@@ -391,8 +391,8 @@ cudaError_t resolve_setup(const hs_pool *p) {
 
 int resolve_kernel_count(const hs_pool *p, int, int) { return p->cfg.host_blocks > 0 ? 2 : 1; }
 
-cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
-                           cudaStream_t st) {
+cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, int nq,
+                                int32_t *row_id, cudaStream_t st) {
     PlanArgs a;
     a.topk = topk;
     a.nq = nq;
@@ -423,6 +423,13 @@ cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq,
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, resolve_plan_kernel, a);
         if (e != cudaSuccess) return e;
     }
+    return cudaGetLastError();
+}
+
+// The miss copy of the last plan (its miss lists stay in the pool's workspace
+// until the next plan).
+cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st) {
+    const int n = nq * p->cfg.top_k;
     if (p->cfg.host_blocks > 0) {
         // enough CTAs in flight to cover the host link's latency, at any B
         const int gx = (4 * kNumSMs + B - 1) / B;
@@ -432,10 +439,17 @@ cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq,
                                            (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
                                            n, (const int32_t *)p->d.host_block_table,
                                            (const int32_t *)p->d.hot_blocks, (const uint8_t *)p->host_dev,
-                                           p->d.rows, a.L, a.P, a.R, a.max_pages, a.hot_pages, p->d.err);
+                                           p->d.rows, p->cfg.num_mla_layers, p->cfg.page_tokens, p->R,
+                                           p->max_pages, p->hot_pages, p->d.err);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
+                           cudaStream_t st) {
+    cudaError_t e = launch_resolve_plan(p, topk, B, nq, row_id, st);
+    return e == cudaSuccess ? launch_miss_copy(p, B, nq, st) : e;
 }
 
 }  // namespace hs

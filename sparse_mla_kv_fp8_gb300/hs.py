@@ -84,6 +84,9 @@ hs_indexer_score = _decl("hs_indexer_score", _i32, [_P, _P, _P, _i32, _i32, _P, 
 hs_topk = _decl("hs_topk", _i32, [_P, _P, _i64, _i32, _i32, _P, _P])
 hs_indexer_topk = _decl("hs_indexer_topk", _i32, [_P, _P, _P, _i32, _i32, _P, _P])
 hs_resolve = _decl("hs_resolve", _i32, [_P, _P, _i32, _i32, _P, _P])
+hs_resolve_plan = _decl("hs_resolve_plan", _i32, [_P, _P, _i32, _i32, _P, _P])
+hs_miss_copy = _decl("hs_miss_copy", _i32, [_P, _i32, _i32, _P])
+hs_host_read_probe = _decl("hs_host_read_probe", _i32, [_P, _P, _sz, _i32, _P])
 hs_sparse_mla_decode = _decl("hs_sparse_mla_decode", _i32,
                              [_P, _i32, _P, _P, _i32, _i32, _f32, _P, _P, _P])
 hs_step = _decl("hs_step", _i32, [_P, ctypes.POINTER(hs_step_args), _P])
@@ -110,6 +113,12 @@ class HSError(RuntimeError):
 def check(status: int, what: str = "hs call") -> None:
     if status != HS_OK:
         raise HSError(status, what)
+
+
+def host_read_probe(host_src, dev_dst, nbytes, ctas=0, stream=None):
+    """Zero-copy read of pinned host memory into device memory (host-link probe)."""
+    check(hs_host_read_probe(_ptr(host_src, "host_src"), _dev(dev_dst, "dev_dst"), nbytes, ctas,
+                             _stream(stream)), "hs_host_read_probe")
 
 
 def dcp_combine(o_parts, lse_parts, R, rows, H, out, lse=None, stream=None):
@@ -228,6 +237,13 @@ class Pool:
     def resolve(self, topk, B, nq, row_id, stream=None):
         check(hs_resolve(self.handle, _dev(topk, "topk"), B, nq, _dev(row_id, "row_id"),
                          _stream(stream)), "hs_resolve")
+
+    def resolve_plan(self, topk, B, nq, row_id, stream=None):
+        check(hs_resolve_plan(self.handle, _dev(topk, "topk"), B, nq, _dev(row_id, "row_id"),
+                              _stream(stream)), "hs_resolve_plan")
+
+    def miss_copy(self, B, nq, stream=None):
+        check(hs_miss_copy(self.handle, B, nq, _stream(stream)), "hs_miss_copy")
 
     def sparse_mla_decode(self, layer, q, row_id, B, nq, scale, out, lse=None, stream=None):
         check(hs_sparse_mla_decode(self.handle, layer, _dev(q, "q"), _dev(row_id, "row_id"), B, nq,

@@ -238,3 +238,34 @@ def drawn_topk(seed: int, b: int, step: int, j: int, vis: int, K: int, P: int,
         chosen = _distinct_fill(chosen, K, lambda r, n: r.integers(0, vis, n), rng)
     out[:] = np.sort(chosen[:K].astype(np.int32))
     return out
+
+
+def _streams_worker(args):
+    seed, b, steps, nq, N, K, P, kind, T = args
+    older = (max(N - T, 0) // P) if kind == "recency_zipf" else (N + P - 1) // P
+    perm = page_perm(seed, b, max(older, 1))
+    cdf = zipf_cdf(perm.shape[0])
+    out = np.empty((len(steps), nq, K), np.int32)
+    for i, s in enumerate(steps):
+        for j in range(nq):
+            vis = N - nq + j + 1
+            out[i, j] = drawn_topk(seed, b, s, j, vis, K, P, kind, T, perm, cdf)
+    return out
+
+
+def drawn_streams(seed: int, B: int, steps, nq: int, N: int, K: int, P: int, kind: str,
+                  T: int = 0, procs: int | None = None) -> np.ndarray:
+    """[len(steps)][B][nq][K] drawn top-K lists of B requests of N tokens,
+    generated in parallel by spawned worker processes (which never touch
+    CUDA, so they may start after the caller's first GPU call)."""
+    import multiprocessing as mp
+    import os
+    steps = list(steps)
+    procs = procs or max(1, min(B, len(os.sched_getaffinity(0))))
+    args = [(seed, b, steps, nq, N, K, P, kind, T) for b in range(B)]
+    if procs == 1:
+        per_req = [_streams_worker(a) for a in args]
+    else:
+        with mp.get_context("spawn").Pool(procs) as pool:
+            per_req = pool.map(_streams_worker, args)
+    return np.stack(per_req, axis=1)

@@ -3,9 +3,6 @@ translation and stream generation in a spawn pool (started before any CUDA
 work in the worker processes; the workers never touch CUDA)."""
 from __future__ import annotations
 
-import multiprocessing as mp
-import os
-
 import numpy as np
 
 
@@ -28,25 +25,7 @@ def locate(rid: np.ndarray, block_table: np.ndarray, hot_blocks: np.ndarray, P: 
     return kind.astype(np.int32), val.astype(np.int32)
 
 
-def _streams_worker(args):
-    from sparse_mla_kv_fp8_gb300 import workload as wl
-    seed, b, steps, nq, N, K, P, kind, T = args
-    older = (max(N - T, 0) // P) if kind == "recency_zipf" else (N + P - 1) // P
-    perm = wl.page_perm(seed, b, max(older, 1))
-    cdf = wl.zipf_cdf(perm.shape[0])
-    out = np.empty((len(steps), nq, K), np.int32)
-    for i, s in enumerate(steps):
-        for j in range(nq):
-            vis = N - nq + j + 1
-            out[i, j] = wl.drawn_topk(seed, b, s, j, vis, K, P, kind, T, perm, cdf)
-    return out
-
-
 def drawn_streams(seed, B, steps, nq, N, K, P, kind, T=0, procs=None):
     """[len(steps)][B][nq][K] drawn top-K lists, generated in parallel."""
-    procs = procs or min(B, len(os.sched_getaffinity(0)))
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(procs) as pool:
-        per_req = pool.map(_streams_worker,
-                           [(seed, b, list(steps), nq, N, K, P, kind, T) for b in range(B)])
-    return np.stack(per_req, axis=1)
+    from sparse_mla_kv_fp8_gb300 import workload as wl
+    return wl.drawn_streams(seed, B, steps, nq, N, K, P, kind, T, procs)

@@ -749,3 +749,53 @@ def test_attention_tensor_core_128_heads(name, kw):
     kw.setdefault("mode", hs.HS_MIXED)
     c = Case(name, H=128, row_fmt=wl.ROW_E4M3_656, **kw)
     _run(c)
+
+
+def test_resolve_plan_then_miss_copy_equals_resolve():
+    """hs_resolve_plan followed by hs_miss_copy (the two halves, here with the
+    copy on a second stream ordered by an event) leaves the same row ids,
+    hot-buffer state and row bytes as hs_resolve, step after step, against
+    the oracle."""
+    from harness import Case, Runner
+    hs = _hs()
+    case = Case("split", B=3, N=[3000, 2500, 4100], K=256, Hi=8, Di=32, H=16, L=2, T=256,
+                num_spec=1, mode=hs.HS_MIXED, steps=6, source="recency_zipf")
+    a, b = Runner(case), Runner(case)
+    try:
+        side = torch.cuda.Stream()
+        for s in range(1, 7):
+            idx = a.drawn(s)
+            tk = torch.from_numpy(idx).to(a.dev)
+            ra, rb = torch.empty_like(tk), torch.empty_like(tk)
+            a.pool.resolve(tk, case.B, 2, ra)
+            b.pool.resolve_plan(tk, case.B, 2, rb)
+            ev = torch.cuda.Event()
+            ev.record()
+            side.wait_event(ev)
+            b.pool.miss_copy(case.B, 2, stream=side)
+            torch.cuda.synchronize()
+            assert a.pool.get_error() == hs.HS_OK and b.pool.get_error() == hs.HS_OK
+            assert torch.equal(ra, rb)
+            for r in range(case.B):
+                sa, sb = a.pool.dump_state(r), b.pool.dump_state(r)
+                for k in ("hot_map", "slot_token", "stamp", "step"):
+                    np.testing.assert_array_equal(sa[k], sb[k])
+                b._check_rows(r, np.where(idx[r] >= 0, idx[r], -1), rb[r])
+        assert a.pool.stats() == b.pool.stats() and b.pool.stats()["misses"] > 0
+    finally:
+        a.close()
+        b.close()
+
+
+def test_host_read_probe_copies_pinned_host_memory():
+    hs = _hs()
+    n = (48 << 20) + 4096
+    src = torch.randint(0, 256, (n,), dtype=torch.uint8).pin_memory()
+    dst = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    hs.host_read_probe(src, dst, n)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src)
+    dst.zero_()
+    hs.host_read_probe(src, dst, 4096 + 16, ctas=3)
+    torch.cuda.synchronize()
+    assert torch.equal(dst[:4112].cpu(), src[:4112]) and int(dst[4112:].sum()) == 0
