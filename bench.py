@@ -3,7 +3,8 @@
 
 One step = indexer score -> top-K -> fused resolve (plan + miss copies from
 pinned host memory) -> sparse MLA decode of the 4 MLA layers of one
-IndexShare group, captured in a CUDA graph and replayed.
+IndexShare group, captured in a CUDA graph and replayed; the miss copy of
+layer l+1 runs on a second stream while the attention of layer l runs.
 
 Workloads (``--workload``; the headline line is the first, the others are
 reported as secondary lines in the same JSON object):
@@ -271,11 +272,10 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
     def enqueue_step(st):
         if drawn:
             # the indexer and top-K on their own inputs, the resolve and the
-            # attention on the trace's lists
+            # attention (hs_resolve_attend: per-layer miss copies overlapping
+            # the attention of the layer before) on the trace's lists
             pool.indexer_topk(q, wt, B, nq, topk, stream=st)
-            pool.resolve(trace.buf, B, nq, rid, stream=st)
-            for l in range(L):
-                pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=st)
+            pool.resolve_attend(trace.buf, B, nq, qm, tau, out, rid, stream=st)
         else:
             pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=st)
 
@@ -600,9 +600,7 @@ def end_to_end(pool, w, inputs, trace, stream, steps, device, first_step):
             stream.wait_event(out_done[i - 2])  # step i-2's output has left this buffer
         if drawn:
             pool.indexer_topk(q, wt, B, nq, topk, stream=stream)
-            pool.resolve(tk_in, B, nq, rid, stream=stream)
-            for l in range(L):
-                pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=stream)
+            pool.resolve_attend(tk_in, B, nq, qm, tau, out, rid, stream=stream)
         else:
             pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)
         comp_done[i].record(stream)

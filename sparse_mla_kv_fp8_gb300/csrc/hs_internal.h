@@ -100,6 +100,15 @@ struct hs_pool {
     hs::DevPtrs d;
     CUtensorMap key_map;     // TMA map of the indexer key slab (E4M3, dim 128)
     bool has_key_map;
+    // a second stream and L events, made at creation, on which the miss copy of
+    // layer l+1 runs while the attention of layer l runs on the caller's stream
+    cudaStream_t side = nullptr;
+    std::vector<cudaEvent_t> layer_ev;
+    ~hs_pool() {
+        for (cudaEvent_t ev : layer_ev)
+            if (ev) cudaEventDestroy(ev);
+        if (side) cudaStreamDestroy(side);
+    }
     // host mirrors
     std::vector<int32_t> seq_len;
     std::vector<int32_t> mode;  // -1 = closed
@@ -126,7 +135,9 @@ cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq,
                            cudaStream_t st);
 cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, int nq,
                                 int32_t *row_id, cudaStream_t st);
-cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st);
+// Miss rows of layers [l0, l1) (l1 < 0: through the last layer).
+cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0 = 0,
+                             int l1 = -1);
 // q_ready: the queries were written before the previous kernel on `st`
 // started (true inside hs_step), so the kernel may stage them before it waits
 // for that kernel.

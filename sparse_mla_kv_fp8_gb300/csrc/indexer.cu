@@ -10,9 +10,12 @@
 //       request's key slab, kStages-deep ring;
 //   B = the request's nq*Hi query rows (same layout), staged once per CTA;
 //   D = 128 TMEM lanes x nq*Hi columns, two accumulators (double buffer).
-// Warp 0 issues TMA, warp 1 issues MMAs, warps 2-5 (one thread per token =
+// Warp 0 issues TMA, warp 1 issues MMAs, warps 2-9 (one thread per token =
 // one TMEM lane) read D, apply sigma, ReLU and the head weights and write the
-// scores (coalesced).  Every mbarrier wait is bounded.
+// scores (coalesced): with an even nq, warps 2-5 take the even queries and
+// warps 6-9 the odd ones (two warps per TMEM sub-partition, so that each
+// SMSP has a second warp to issue while the other waits); with one query
+// only warps 2-5 work.  Every mbarrier wait is bounded.
 //
 // General kernel (any format / dims): one CTA per 128-token tile of one
 // request; keys and queries decoded to fp32 in shared memory; each thread
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kTile) indexer_simt_kernel(
 // tensor-core path
 // ------------------------------------------------------------------------
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
 constexpr int kTileBytes = kTile * 128;  // 128 tokens x 128 B
 
 struct IdxTcArgs {
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int k = 0; k < 2; k++) {
             tc::mbar_init(&tfull[k], 1);
-            tc::mbar_init(&tempty[k], 128);
+            tc::mbar_init(&tempty[k], (a.nq % 2 == 0) ? 256 : 128);
         }
         tc::mbar_init(done, 1);
         tc::fence_barrier_init();
@@ -212,8 +215,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, a.err);
         }
-    } else {
+    } else if (warp < 6 || a.nq % 2 == 0) {
         const int sp = warp & 3;  // TMEM sub-partition this warp may read
+        const int half = (warp - 2) >> 2;  // queries j = half, half + jstep, ...
+        const int jstep = (a.nq % 2 == 0) ? 2 : 1;
         const int row = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
         const float *ksc = a.ksc + (size_t)b * a.maxT;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!__all_sync(0xffffffffu, w)) break;  // the warp leaves together
             tc::fence_after_sync();
             const uint32_t tb = lane_base + acc * a.ncols;
-            for (int j = 0; j < a.nq; j++) {
+            for (int j = half; j < a.nq; j += jstep) {
                 // four independent partial sums (the weighted ReLU terms are summed
                 // in a tree rather than one 64-long dependent chain)
                 float part[4] = {0.f, 0.f, 0.f, 0.f};

@@ -345,36 +345,52 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(256) miss_copy_kernel(
+// Rows of layers [l0, l1) of every miss; 16-byte units, two loads in flight
+// per thread.  Few registers (at most 32 per thread at 256 threads), so that
+// its CTAs fit on an SM beside an attention CTA when the copy of one layer
+// runs concurrently with the attention of the previous one.
+__global__ void __launch_bounds__(256, 8) miss_copy_kernel(
     const int32_t *__restrict__ miss_count, const int32_t *__restrict__ miss_tok,
     const int32_t *__restrict__ miss_slot, int n, const int32_t *__restrict__ host_block_table,
     const int32_t *__restrict__ hot_blocks, const uint8_t *__restrict__ host_rows,
-    uint8_t *__restrict__ rows, int L, int P, int R, int max_pages, int hot_pages, int32_t *err) {
+    uint8_t *__restrict__ rows, int L, int l0, int l1, int P, int R, int max_pages, int hot_pages,
+    int32_t *err) {
     hs::tc::grid_dep_launch();
     hs::tc::grid_dep_wait();  // the miss lists come from the plan kernel
     const int b = blockIdx.y;
     const int M = miss_count[b];
-    const int cpr = R / 16, per_miss = L * cpr;
+    const int cpr = R / 16, nl = l1 - l0, per_miss = nl * cpr;
     const int64_t total = (int64_t)M * per_miss;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    auto unit = [&](int64_t i, const uint4 *&src, uint4 *&dst) -> bool {
         const int m = (int)(i / per_miss);
         const int rem = (int)(i - (int64_t)m * per_miss);
-        const int l = rem / cpr, c = rem - l * cpr;
+        const int l = l0 + rem / cpr, c = rem % cpr;
         const int32_t u = miss_tok[(size_t)b * n + m], s = miss_slot[(size_t)b * n + m];
         if (u < 0 || u >= max_pages * P || s < 0 || s >= hot_pages * P) {
             set_error(err, HS_ERR_INVALID_ARG);
-            continue;
+            return false;
         }
         const int32_t hblk = host_block_table[(size_t)b * max_pages + u / P];
         if (hblk < 0) {
             set_error(err, HS_ERR_INVALID_ARG);
-            continue;
+            return false;
         }
         const int32_t dblk = hot_blocks[(size_t)b * hot_pages + s / P];
-        const uint4 *src = (const uint4 *)(host_rows + (((size_t)hblk * L + l) * P + u % P) * R) + c;
-        uint4 *dst = (uint4 *)(rows + (((size_t)dblk * L + l) * P + s % P) * R) + c;
-        *dst = *src;
+        src = (const uint4 *)(host_rows + (((size_t)hblk * L + l) * P + u % P) * R) + c;
+        dst = (uint4 *)(rows + (((size_t)dblk * L + l) * P + s % P) * R) + c;
+        return true;
+    };
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += 2 * stride) {
+        const uint4 *s0, *s1 = nullptr;
+        uint4 *d0, *d1 = nullptr;
+        const bool ok0 = unit(i, s0, d0);
+        const bool ok1 = i + stride < total && unit(i + stride, s1, d1);
+        uint4 v0, v1;
+        if (ok0) v0 = *s0;
+        if (ok1) v1 = *s1;
+        if (ok0) *d0 = v0;
+        if (ok1) *d1 = v1;
     }
 }
 
@@ -428,8 +444,9 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
 
 // The miss copy of the last plan (its miss lists stay in the pool's workspace
 // until the next plan).
-cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st) {
+cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0, int l1) {
     const int n = nq * p->cfg.top_k;
+    if (l1 < 0) l1 = p->cfg.num_mla_layers;
     if (p->cfg.host_blocks > 0) {
         // enough CTAs in flight to cover the host link's latency, at any B
         const int gx = (4 * kNumSMs + B - 1) / B;
@@ -439,8 +456,8 @@ cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st) {
                                            (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
                                            n, (const int32_t *)p->d.host_block_table,
                                            (const int32_t *)p->d.hot_blocks, (const uint8_t *)p->host_dev,
-                                           p->d.rows, p->cfg.num_mla_layers, p->cfg.page_tokens, p->R,
-                                           p->max_pages, p->hot_pages, p->d.err);
+                                           p->d.rows, p->cfg.num_mla_layers, l0, l1, p->cfg.page_tokens,
+                                           p->R, p->max_pages, p->hot_pages, p->d.err);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

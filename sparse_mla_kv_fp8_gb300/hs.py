@@ -90,6 +90,8 @@ hs_host_read_probe = _decl("hs_host_read_probe", _i32, [_P, _P, _sz, _i32, _P])
 hs_sparse_mla_decode = _decl("hs_sparse_mla_decode", _i32,
                              [_P, _i32, _P, _P, _i32, _i32, _f32, _P, _P, _P])
 hs_step = _decl("hs_step", _i32, [_P, ctypes.POINTER(hs_step_args), _P])
+hs_resolve_attend = _decl("hs_resolve_attend", _i32,
+                          [_P, _P, _i32, _i32, _P, _f32, _P, _P, _P, _P])
 hs_pool_get_error = _decl("hs_pool_get_error", _i32, [_P, ctypes.POINTER(_i32)])
 hs_pool_stats = _decl("hs_pool_stats", _i32, [_P, ctypes.POINTER(hs_stats)])
 hs_pool_reset_stats = _decl("hs_pool_reset_stats", _i32, [_P])
@@ -266,6 +268,11 @@ class Pool:
                          q_mla=_dev(q_mla, "q_mla"), softmax_scale=scale, out=_dev(out, "out"),
                          lse=_dev(lse, "lse"), topk=_dev(topk, "topk"), row_id=_dev(row_id, "row_id"))
         check(hs_step(self.handle, ctypes.byref(a), _stream(stream)), "hs_step")
+
+    def resolve_attend(self, topk, B, nq, q_mla, scale, out, row_id, lse=None, stream=None):
+        check(hs_resolve_attend(self.handle, _dev(topk, "topk"), B, nq, _dev(q_mla, "q_mla"), scale,
+                                _dev(out, "out"), _dev(lse, "lse"), _dev(row_id, "row_id"),
+                                _stream(stream)), "hs_resolve_attend")
 
     def step_kernel_count(self, B, nq) -> int:
         return int(hs_step_kernel_count(self.handle, B, nq))

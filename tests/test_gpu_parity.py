@@ -799,3 +799,56 @@ def test_host_read_probe_copies_pinned_host_memory():
     hs.host_read_probe(src, dst, 4096 + 16, ctas=3)
     torch.cuda.synchronize()
     assert torch.equal(dst[:4112].cpu(), src[:4112]) and int(dst[4112:].sum()) == 0
+
+
+def test_resolve_attend_overlapped_copies_equal_separate_calls():
+    """hs_resolve_attend (the miss copy split by layer, layers 1..L-1 copied on
+    the pool's second stream while the attention of the layer before runs)
+    gives bit-identical row ids, state and outputs to hs_resolve followed by
+    hs_sparse_mla_decode per layer, eager and replayed from a CUDA graph, on
+    a mixed-residency pool with misses every step."""
+    from harness import Case, Runner
+    hs = _hs()
+    case = Case("overlap", B=3, N=[3000, 2500, 4100], K=256, Hi=8, Di=32, H=128, L=3, T=256,
+                num_spec=1, mode=hs.HS_MIXED, steps=8, source="recency_zipf")
+    a, b = Runner(case), Runner(case)
+    try:
+        B, nq, L, H = case.B, 2, case.L, case.H
+        tk = torch.empty((B, nq, case.K), dtype=torch.int32, device=a.dev)
+        ra, rb = torch.empty_like(tk), torch.empty_like(tk)
+        oa = torch.empty((L, B, nq, H, 512), dtype=torch.bfloat16, device=a.dev)
+        ob, la, lb = torch.empty_like(oa), torch.empty((L, B, nq, H), device=a.dev), None
+        lb = torch.empty_like(la)
+        qm = torch.empty((L, B, nq, H, 576), dtype=torch.bfloat16, device=a.dev)
+        st = torch.cuda.Stream()
+        graph = None
+        for s in range(1, 9):
+            tk.copy_(torch.from_numpy(a.drawn(s)))
+            qm.copy_(a.step_inputs(s)[2])
+            a.pool.resolve(tk, B, nq, ra)
+            for l in range(L):
+                a.pool.sparse_mla_decode(l, qm[l], ra, B, nq, a.tau, oa[l], la[l])
+            if s <= 4:
+                b.pool.resolve_attend(tk, B, nq, qm, a.tau, ob, rb, lb)
+            else:
+                if graph is None:
+                    torch.cuda.synchronize()
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=st):
+                        b.pool.resolve_attend(tk, B, nq, qm, a.tau, ob, rb, lb, stream=st)
+                graph.replay()
+            torch.cuda.synchronize()
+            assert a.pool.get_error() == hs.HS_OK and b.pool.get_error() == hs.HS_OK
+            assert torch.equal(ra, rb), f"step {s}: row ids"
+            assert torch.equal(oa, ob), f"step {s}: outputs"
+            assert torch.equal(la, lb), f"step {s}: lse"
+            for r in range(B):
+                sa, sb = a.pool.dump_state(r), b.pool.dump_state(r)
+                for k in ("hot_map", "slot_token", "stamp", "step"):
+                    np.testing.assert_array_equal(sa[k], sb[k])
+        assert a.pool.stats() == b.pool.stats() and b.pool.stats()["misses"] > 0
+        # and the outputs of the last step against the oracle
+        a._check_attention(qm, ob, lb, a.drawn(8))
+    finally:
+        a.close()
+        b.close()
