@@ -362,7 +362,9 @@ cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w
         const int ntiles = (maxT + kTile - 1) / kTile;
         a.tiles_per_cta = pick_tiles_per_cta(ntiles, B, per_sm);
         dim3 grid((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta, B);
-        indexer_tc_kernel<<<grid, kTcThreads, smem, st>>>(p->key_map, a);
+        // the second group of epilogue warps works only with an even query count
+        const int threads = (nq % 2 == 0) ? kTcThreads : kTcThreads - 128;
+        indexer_tc_kernel<<<grid, threads, smem, st>>>(p->key_map, a);
         return cudaGetLastError();
     }
     dim3 grid((maxT + kTile - 1) / kTile, B);

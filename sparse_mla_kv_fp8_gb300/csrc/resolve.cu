@@ -345,11 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     }
 }
 
-// Rows of layers [l0, l1) of every miss; 16-byte units, two loads in flight
-// per thread.  Few registers (at most 32 per thread at 256 threads), so that
-// its CTAs fit on an SM beside an attention CTA when the copy of one layer
-// runs concurrently with the attention of the previous one.
-__global__ void __launch_bounds__(256, 8) miss_copy_kernel(
+// Rows of layers [l0, l1) of every miss; 16-byte units, four loads in flight
+// per thread.  The grid is small (about two 128-thread CTAs per SM over all
+// requests) and each CTA light (at most 64 registers per thread, no shared
+// memory), so that it runs on the SMs beside the attention CTAs when the copy
+// of one layer overlaps the attention of the previous one: the copy is bound
+// by the host link, and a few MB in flight saturate it.
+constexpr int kCopyThreads = 128;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads, 8) miss_copy_kernel(
     const int32_t *__restrict__ miss_count, const int32_t *__restrict__ miss_tok,
     const int32_t *__restrict__ miss_slot, int n, const int32_t *__restrict__ host_block_table,
     const int32_t *__restrict__ hot_blocks, const uint8_t *__restrict__ host_rows,
@@ -362,35 +367,39 @@ __global__ void __launch_bounds__(256, 8) miss_copy_kernel(
     const int cpr = R / 16, nl = l1 - l0, per_miss = nl * cpr;
     const int64_t total = (int64_t)M * per_miss;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    auto unit = [&](int64_t i, const uint4 *&src, uint4 *&dst) -> bool {
-        const int m = (int)(i / per_miss);
-        const int rem = (int)(i - (int64_t)m * per_miss);
-        const int l = l0 + rem / cpr, c = rem % cpr;
-        const int32_t u = miss_tok[(size_t)b * n + m], s = miss_slot[(size_t)b * n + m];
-        if (u < 0 || u >= max_pages * P || s < 0 || s >= hot_pages * P) {
-            set_error(err, HS_ERR_INVALID_ARG);
-            return false;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total;
+         i0 += kCopyUnroll * stride) {
+        const uint4 *src[kCopyUnroll];
+        uint4 *dst[kCopyUnroll];
+        uint4 v[kCopyUnroll];
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; k++) {
+            src[k] = nullptr;
+            const int64_t i = i0 + k * stride;
+            if (i >= total) continue;
+            const int m = (int)(i / per_miss);
+            const int rem = (int)(i - (int64_t)m * per_miss);
+            const int l = l0 + rem / cpr, c = rem % cpr;
+            const int32_t u = miss_tok[(size_t)b * n + m], s = miss_slot[(size_t)b * n + m];
+            if (u < 0 || u >= max_pages * P || s < 0 || s >= hot_pages * P) {
+                set_error(err, HS_ERR_INVALID_ARG);
+                continue;
+            }
+            const int32_t hblk = host_block_table[(size_t)b * max_pages + u / P];
+            if (hblk < 0) {
+                set_error(err, HS_ERR_INVALID_ARG);
+                continue;
+            }
+            const int32_t dblk = hot_blocks[(size_t)b * hot_pages + s / P];
+            src[k] = (const uint4 *)(host_rows + (((size_t)hblk * L + l) * P + u % P) * R) + c;
+            dst[k] = (uint4 *)(rows + (((size_t)dblk * L + l) * P + s % P) * R) + c;
         }
-        const int32_t hblk = host_block_table[(size_t)b * max_pages + u / P];
-        if (hblk < 0) {
-            set_error(err, HS_ERR_INVALID_ARG);
-            return false;
-        }
-        const int32_t dblk = hot_blocks[(size_t)b * hot_pages + s / P];
-        src = (const uint4 *)(host_rows + (((size_t)hblk * L + l) * P + u % P) * R) + c;
-        dst = (uint4 *)(rows + (((size_t)dblk * L + l) * P + s % P) * R) + c;
-        return true;
-    };
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += 2 * stride) {
-        const uint4 *s0, *s1 = nullptr;
-        uint4 *d0, *d1 = nullptr;
-        const bool ok0 = unit(i, s0, d0);
-        const bool ok1 = i + stride < total && unit(i + stride, s1, d1);
-        uint4 v0, v1;
-        if (ok0) v0 = *s0;
-        if (ok1) v1 = *s1;
-        if (ok0) *d0 = v0;
-        if (ok1) *d1 = v1;
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; k++)
+            if (src[k]) v[k] = *src[k];
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; k++)
+            if (src[k]) *dst[k] = v[k];
     }
 }
 
@@ -448,10 +457,11 @@ cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, i
     const int n = nq * p->cfg.top_k;
     if (l1 < 0) l1 = p->cfg.num_mla_layers;
     if (p->cfg.host_blocks > 0) {
-        // enough CTAs in flight to cover the host link's latency, at any B
-        const int gx = (4 * kNumSMs + B - 1) / B;
+        // about two CTAs per SM in all: enough loads in flight to cover the
+        // host link's latency, few enough to leave the SMs to the attention
+        const int gx = (2 * kNumSMs + B - 1) / B;
         dim3 grid(gx, B);
-        PdlLaunch lc(grid, dim3(256), 0, st);
+        PdlLaunch lc(grid, dim3(kCopyThreads), 0, st);
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count,
                                            (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
                                            n, (const int32_t *)p->d.host_block_table,
