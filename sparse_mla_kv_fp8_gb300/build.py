@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libhs.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["pool.cu", "indexer.cu", "topk.cu", "resolve.cu", "attention.cu", "diag.cu", "dcp.cu"]
+SOURCES = ["pool.cu", "indexer.cu", "topk.cu", "resolve.cu", "attention.cu", "attention_pair.cu",
+           "diag.cu", "dcp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

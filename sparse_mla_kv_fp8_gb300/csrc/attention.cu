@@ -964,12 +964,25 @@ static int tc_splits(const hs_pool_config &c, int rows) {
     return (c.top_k + kc - 1) / kc;
 }
 
+bool pair_eligible(const hs_pool *p);
+int pair_splits(const hs_pool_config &c, int rows);
+cudaError_t pair_setup(const hs_pool *p);
+cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
+                                  int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
+                                  bool q_ready);
+
+static bool pair_cfg(const hs_pool_config &c) {
+    return c.row_fmt == HS_ROW_E4M3_656 && c.mla_heads % 128 == 0;
+}
+
 static int splits_for(const hs_pool_config &c, int rows) {
+    if (pair_cfg(c)) return pair_splits(c, rows);
     return tc_eligible(c) ? tc_splits(c, rows) : simt_splits(c, rows);
 }
 
 int attention_kernel_count(const hs_pool *p, int B, int nq) {
     const int s = splits_for(p->cfg, B * nq);
+    if (pair_cfg(p->cfg)) return s > 1 ? 2 : 1;
     if (tc_eligible(p->cfg)) return s > 2 ? 2 : 1;
     return s > 1 ? 2 : 1;
 }
@@ -991,6 +1004,8 @@ cudaError_t attention_setup(const hs_pool *p) {
     cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)simt_smem());
     if (e != cudaSuccess) return e;
+    e = pair_setup(p);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 AttnTcSmem::bytes);
 }
@@ -1001,6 +1016,15 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
     const int rows = B * nq;
     const int K = p->cfg.top_k;
     const int splits = splits_for(p->cfg, rows);
+    if (pair_cfg(p->cfg)) {
+        if (!pair_eligible(p)) return cudaErrorInvalidValue;
+        cudaError_t e = launch_pair_attention(p, layer, q, row_id, B, nq, scale, out, lse, st, q_ready);
+        if (e != cudaSuccess) return e;
+        if (splits > 1)
+            attn_combine_kernel<<<rows * p->cfg.mla_heads, 128, 0, st>>>(p->d.attn_part, splits,
+                                                                       (__nv_bfloat16 *)out, lse);
+        return cudaGetLastError();
+    }
     if (tc_eligible(p->cfg)) {
         AttnTcArgs a;
         a.q = (const __nv_bfloat16 *)q;

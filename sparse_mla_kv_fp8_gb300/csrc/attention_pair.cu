@@ -1,0 +1,743 @@
+// Sparse MLA decode on a pair of CTAs that split the latent dimensions
+// ("Un contexte d'un million sur huit H200", section "Ce qui se passe":
+// attention reads only the K selected latent rows; absorbed-MLA form, the
+// 576-dim row is the key and its first 512 dims the value):
+//   z = scale * q . row,  out = sum softmax(z) * row[:512],  lse = ln sum exp(z)
+//
+// One 2-CTA cluster owns one query, 128 heads and a range of the K entries,
+// processed in chunks of 128 rows.  CTA r holds nope dims [256 r, 256 r + 256)
+// and rope dims [32 r, 32 r + 32) of every row of the chunk and of the 128
+// query heads, and computes with heads on the MMA M axis (M = 128):
+//   S_r = Q_r R_r^T    (S[head][row] over the CTA's 288 dims; the queries'
+//                       nope half is the A operand in tensor memory, the rope
+//                       half bf16 x bf16 from shared memory)
+//   S   = S_0 + S_1    (each CTA sends the other the partial sums of the 64
+//                       heads the other normalises, 16 KB per half chunk,
+//                       through distributed shared memory)
+//   P   = exp2(S - m)  (CTA r runs the softmax of heads [64 r, 64 r + 64):
+//                       one thread per (head, half chunk), so the row maximum
+//                       and sum are per-thread; a lazy reference maximum per
+//                       head, raised only when a chunk exceeds it by > 2^8)
+//   O_r += P V_r       (V_r: the CTA's 256 nope dims, two N = 128 MMAs; the
+//                       P rows of the other CTA's heads arrive by a bulk copy)
+// TMEM (512 columns): queries' nope half [0,128) (fp16 pairs), S [128,256),
+// O [256,512).  Rows reach shared memory by TMA: per chunk a gather of the
+// four nope K-blocks of the CTA's half (64 E4M3 bytes per row) into a
+// three-stage ring and of the rope half straight into its 64-byte-swizzled
+// operand tile; four converter warps dequantise each K-block (E4M3 x the
+// row's group scale, read from global memory -> fp16, the scale split into
+// two fp16s) into
+// 128-byte-swizzled operand tiles, double buffered by chunk, so that chunk
+// c+1's K-blocks are converted while chunk c's P V products run.
+// Warp 0 issues the MMAs, warp 1 owns TMEM and issues the gathers, warps 2-9
+// run the exchange, softmax, rescale and epilogue (thread = TMEM lane = head,
+// one warp per (lane quarter, half chunk)), warps 10-13 convert.
+// Every wait is bounded; on a time-out the kernel records HS_ERR_TIMEOUT,
+// skips the remaining work and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "tc.cuh"
+
+namespace hs {
+namespace {
+
+constexpr int kRowsPerChunk = 128;
+constexpr int kPairHeads = 128;
+constexpr int kPairThreads = 448;  // 14 warps
+constexpr int kRingStages = 3;
+constexpr int kKbBytes = 16384;    // 128 rows x 64 fp16 (128-byte swizzle)
+constexpr int kRawKb = 8192;       // 128 rows x 64 E4M3 bytes
+constexpr float kRescaleLog2 = 8.f;
+constexpr float kLog2eP = 1.4426950408889634f;
+constexpr float kLn2P = 0.6931471805599453f;
+constexpr float kMaxF16P = 65504.f;
+constexpr uint32_t kPFullBytes = 2 * 64 * 128 + 64 * 4;  // the peer's P rows + rescale factors
+
+struct PairSmem {
+    static constexpr int rn = 0;                              // 2 buffers x 4 K-blocks (fp16)
+    static constexpr int pb = rn + 2 * 4 * kKbBytes;          // P: 2 K-blocks (fp16)
+    static constexpr int ring = pb + 2 * kKbBytes;            // raw K-block stages
+    static constexpr int qr = ring + kRingStages * kRawKb;    // queries' rope half (bf16, 64-byte swizzle)
+    static constexpr int rr = qr + 8192;                      // rows' rope half (bf16, 64-byte swizzle)
+    static constexpr int srx = rr + 8192;                     // received partial S: [16][64] float4
+    static constexpr int alpha_rx = srx + 16384;              // [64] peer's rescale factors
+    static constexpr int lm_rx = alpha_rx + 256;              // [2][64] peer's l, m
+    static constexpr int mx = lm_rx + 512;                    // [2][64] half-chunk maxima
+    static constexpr int lsum = mx + 512;                     // [2][64] half-chunk sums
+    static constexpr int bars = lsum + 512;
+    static constexpr int nbar = 40;
+    static constexpr int tslot = bars + nbar * 8;
+    static constexpr int bytes = tslot + 16 + 1024;           // + alignment slack
+};
+static_assert(PairSmem::bytes <= 232448, "pair attention shared memory");
+// leaves room on the SM for a light miss-copy CTA next to it
+static_assert(PairSmem::bytes + 1024 + 1024 <= 233472, "pair attention co-residency");
+
+struct PairArgs {
+    const __nv_bfloat16 *q;  // [rows][H][576]
+    const int32_t *row_id;   // [rows][K]
+    const uint8_t *pool;     // block pool base (the rows' scales are read from it)
+    int layer, L, P, H, K, splits, kc, max_row;
+    float scale_log2;
+    __nv_bfloat16 *out;      // [rows][H][512]
+    float *lse;
+    float *part;             // [rows][H][splits][514]
+    int q_ready;
+    int32_t *err;
+};
+
+// Bounded wait by every lane of a warp; true when all lanes saw the phase.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity, int32_t *err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait_cluster(bar, parity, err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// OR of a flag over the 256 softmax threads (named barrier 1) or over the
+// 128 threads of one CTA's own heads (barrier 2).
+__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *(uint32_t *)&v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *(uint32_t *)&v;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_scaled(__nv_fp8x2_storage_t v, __half2 s_hi, __half2 s_lo) {
+    const __half2 x = __half2(__nv_cvt_fp8x2_to_halfraw2(v, __NV_E4M3));
+    const __half2 y = __hfma2(x, s_hi, __hmul2(x, s_lo));
+    return *(const uint32_t *)&y;
+}
+
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t w) {
+    return (w & 0x7FFFu) > 0x477Fu || ((w >> 16) & 0x7FFFu) > 0x477Fu;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap map64, const __grid_constant__ CUtensorMap map64s,
+                     PairArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *rn = smem + PairSmem::rn;
+    uint8_t *pb = smem + PairSmem::pb;
+    uint8_t *ring = smem + PairSmem::ring;
+    uint8_t *qr = smem + PairSmem::qr;
+    uint8_t *rr = smem + PairSmem::rr;
+    float4 *srx = (float4 *)(smem + PairSmem::srx);
+    float *alpha_rx = (float *)(smem + PairSmem::alpha_rx);
+    float *lm_rx = (float *)(smem + PairSmem::lm_rx);
+    float *mxs = (float *)(smem + PairSmem::mx);
+    float *lss = (float *)(smem + PairSmem::lsum);
+    uint64_t *bar = (uint64_t *)(smem + PairSmem::bars);
+    uint64_t *ring_full = bar;            // [3]
+    uint64_t *ring_empty = bar + 3;       // [3]
+    uint64_t *kbf = bar + 10;             // [2][4]
+    uint64_t *kbfree = bar + 18;          // [2][2]
+    uint64_t *rr_full = bar + 22;
+    uint64_t *rr_free = bar + 23;
+    uint64_t *s_full = bar + 24;
+    uint64_t *s_free = bar + 25;
+    uint64_t *srx_full = bar + 26;        // [2]: one per half chunk
+    uint64_t *srx_free = bar + 28;
+    uint64_t *p_full = bar + 29;
+    uint64_t *pb_free = bar + 30;
+    uint64_t *o_ready = bar + 31;
+    uint64_t *o_done = bar + 32;
+    uint64_t *q_full = bar + 33;
+    uint64_t *lm_full = bar + 34;
+    uint64_t *mma_done = bar + 35;
+    uint32_t *tslot = (uint32_t *)(smem + PairSmem::tslot);
+
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const uint32_t peer = rank ^ 1u;
+    const int split = blockIdx.x >> 1, qrow = blockIdx.y, hg = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k0 = split * a.kc, k1 = min(a.K, k0 + a.kc);
+    const int nch = k1 > k0 ? (k1 - k0 + kRowsPerChunk - 1) / kRowsPerChunk : 0;
+    const int32_t *ids = a.row_id + (size_t)qrow * a.K;
+    const size_t head0 = (size_t)qrow * a.H + (size_t)hg * kPairHeads;  // first head row
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; i++) {
+            tc::mbar_init(&ring_full[i], 1);
+            tc::mbar_init(&ring_empty[i], 4);
+        }
+        for (int i = 0; i < 2; i++) {
+            tc::mbar_init(&srx_full[i], 1);
+            for (int k = 0; k < 4; k++) tc::mbar_init(&kbf[i * 4 + k], 4);
+            for (int k = 0; k < 2; k++) tc::mbar_init(&kbfree[i * 2 + k], 1);
+        }
+        tc::mbar_init(rr_full, 1);
+        tc::mbar_init(rr_free, 1);
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(s_free, 8);
+        tc::mbar_init(srx_free, 2);
+        tc::mbar_init(p_full, 1);
+        tc::mbar_init(pb_free, 2);
+        tc::mbar_init(o_ready, 8);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(q_full, 8);
+        tc::mbar_init(lm_full, 1);
+        tc::mbar_init(mma_done, 1);
+        tc::fence_barrier_init();
+        // the first phase of every barrier the peer completes with transaction
+        // bytes is armed now, before the peer can send (each later phase is
+        // armed by the thread that waited for the phase before it)
+        if (nch > 0) {
+            tc::mbar_expect_tx(&srx_full[0], 64 * 64 * 4);
+            tc::mbar_expect_tx(&srx_full[1], 64 * 64 * 4);
+            tc::mbar_expect_tx(p_full, kPFullBytes);
+            tc::mbar_expect_tx(lm_full, 512);
+        }
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tslot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();  // both CTAs' barriers exist before any remote arrival
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    tc::grid_dep_launch();
+    const uint32_t QN = 0, SC = 128, OC = 256;  // TMEM column bases
+    bool ok = true;
+    bool range_bad = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMAs
+        tc::grid_dep_wait();
+        if (lane == 0 && nch > 0) {
+            const uint32_t id_rope = tc::instr_desc(128, 128, 1, 1, 0, 0);  // bf16 x bf16
+            const uint32_t id_s = tc::instr_desc(128, 128, 0, 0, 0, 0);     // fp16 (A in TMEM) x fp16
+            const uint32_t id_o = tc::instr_desc(128, 128, 0, 0, 0, 1);     // P (K-major) x V (MN-major)
+            const uint32_t rn_a = tc::smem_addr(rn), pb_a = tc::smem_addr(pb);
+            const uint32_t qr_a = tc::smem_addr(qr), rr_a = tc::smem_addr(rr);
+            ok = tc::mbar_wait(q_full, 0, a.err);
+            for (int it = 0; it <= nch && ok; it++) {
+                if (it < nch) {  // S(it)
+                    const int c = it, b = c & 1;
+                    if (c >= 1 && !(ok = tc::mbar_wait(s_free, (c - 1) & 1, a.err))) break;
+                    if (!(ok = tc::mbar_wait(rr_full, c & 1, a.err))) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 2; kk++) {
+                        const uint64_t ad = tc::smem_desc(qr_a + kk * 32, 16, 512, 4);
+                        const uint64_t bd = tc::smem_desc(rr_a + kk * 32, 16, 512, 4);
+                        tc::mma_f16(tmem + SC, ad, bd, id_rope, kk);
+                    }
+                    tc::mma_commit(rr_free);
+                    for (int kb = 0; kb < 4 && ok; kb++) {
+                        if (!(ok = tc::mbar_wait(&kbf[b * 4 + kb], (c >> 1) & 1, a.err))) break;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int kk = 0; kk < 4; kk++) {
+                            const uint64_t bd = tc::smem_desc_sw128(rn_a + (b * 4 + kb) * kKbBytes + kk * 32, 16, 1024);
+                            tc::mma_f16_tmem_a(tmem + SC, tmem + QN + kb * 32 + kk * 8, bd, id_s, 1);
+                        }
+                    }
+                    if (!ok) break;
+                    tc::mma_commit(s_full);
+                }
+                if (it >= 1) {  // O(it - 1) += P V
+                    const int c = it - 1, b = c & 1;
+                    if (!(ok = tc::mbar_wait(o_ready, c & 1, a.err))) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; kk++) {
+                            const uint64_t ad = tc::smem_desc_sw128(pb_a + (kk >> 2) * kKbBytes + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::smem_desc_sw128(
+                                rn_a + (b * 4 + 2 * half) * kKbBytes + kk * 2048, kKbBytes, 1024);
+                            tc::mma_f16(tmem + OC + half * 128, ad, bd, id_o, (c | kk) != 0);
+                        }
+                        tc::mma_commit(&kbfree[b * 2 + half]);
+                    }
+                    tc::mma_commit(o_done);
+                    // both CTAs may write the next chunk's P (none after the last)
+                    if (c + 1 < nch) tc::mma_commit_multicast(pb_free, (uint16_t)0x3);
+                }
+            }
+            tc::mma_commit(mma_done);
+            tc::mbar_wait(mma_done, 0, a.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- gathers (TMA)
+        tc::grid_dep_wait();
+        if (nch > 0) {
+            tc::prefetch_tensormap(&map64);
+            tc::prefetch_tensormap(&map64s);
+        }
+        int g = 0;        // ring stage counter
+        int ropes = 0;    // rope loads issued
+        for (int c = 0; c < nch && ok; c++) {
+            // row units of rows 4 lane .. 4 lane + 3 of the chunk (-1: no row, read as zeros)
+            int32_t u[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int k = k0 + c * kRowsPerChunk + 4 * lane + i;
+                int32_t id = k < k1 ? ids[k] : -1;
+                if (id >= a.max_row) {
+                    set_error(a.err, HS_ERR_INDEX_RANGE);
+                    id = -1;
+                }
+                u[i] = id < 0 ? -1 : (int32_t)(((int64_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P);
+            }
+            // the four nope K-blocks of this CTA's half
+            for (int kb = 0; kb < 4; kb++, g++) {
+                const int s = g % kRingStages;
+                if (!(ok = warp_wait(&ring_empty[s], ((g / kRingStages) & 1) ^ 1, a.err))) break;
+                if (lane == 0) tc::mbar_expect_tx(&ring_full[s], kRawKb);
+                __syncwarp();
+                tc::tma_gather4(ring + s * kRawKb + 256 * lane, &map64, &ring_full[s],
+                                256 * (int)rank + 64 * kb, u[0], u[1], u[2], u[3]);
+            }
+            if (!ok) break;
+            // the rope half, straight into its operand tile (S(c-1) has read the last one)
+            if (c >= 1 && !(ok = warp_wait(rr_free, (c - 1) & 1, a.err))) break;
+            if (lane == 0) tc::mbar_expect_tx(rr_full, 8192);
+            __syncwarp();
+            tc::tma_gather4(rr + 256 * lane, &map64s, rr_full, 528 + 64 * (int)rank, u[0], u[1], u[2], u[3]);
+            ropes++;
+        }
+        // never leave with a copy into this CTA's shared memory in flight
+        // (the consumers have waited for every one on the normal path)
+        if (lane == 0) {
+            for (int i = g - kRingStages; i < g; i++)
+                if (i >= 0) tc::mbar_wait(&ring_full[i % kRingStages], (i / kRingStages) & 1, a.err);
+            if (ropes > 0) tc::mbar_wait(rr_full, (ropes - 1) & 1, a.err);
+        }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------ converters
+        tc::grid_dep_wait();
+        const int ct = threadIdx.x - 320;  // 0..127
+        const int part = ct & 3;           // 16-byte slice of a row's 64 K-block bytes
+        int g = 0;
+        for (int c = 0; c < nch && ok; c++) {
+            const int b = c & 1;
+            // this thread's rows ct/4 + 32 i and their two group scales (the
+            // rows' ids are L2-hot; a missing row keeps scale 0)
+            float2 sg[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int k = k0 + c * kRowsPerChunk + (ct >> 2) + 32 * i;
+                const int32_t id = k < k1 ? ids[k] : -1;
+                sg[i] = make_float2(0.f, 0.f);
+                if (id >= 0 && id < a.max_row) {
+                    const size_t unit = ((size_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P;
+                    const uint2 w = tc::ld_nc8(a.pool + unit * 656 + 512 + 8 * rank);
+                    sg[i] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+                }
+            }
+            for (int kb = 0; kb < 4; kb++, g++) {
+                const int s = g % kRingStages;
+                if (c >= 2 && (kb & 1) == 0 &&
+                    !(ok = warp_wait(&kbfree[b * 2 + (kb >> 1)], ((c - 2) >> 1) & 1, a.err)))
+                    break;
+                if (!(ok = warp_wait(&ring_full[s], (g / kRingStages) & 1, a.err))) break;
+                const uint8_t *src = ring + s * kRawKb;
+                uint8_t *dst = rn + (b * 4 + kb) * kKbBytes;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int row = (ct >> 2) + 32 * i;
+                    const uint4 raw = *(const uint4 *)(src + row * 64 + part * 16);
+                    const float scl = (kb >> 1) ? sg[i].y : sg[i].x;
+                    range_bad |= 448.f * fabsf(scl) > kMaxF16P;
+                    const __half s_hi = __float2half_rn(scl);
+                    const __half2 shi2 = __half2half2(s_hi);
+                    const __half2 slo2 = __half2half2(__float2half_rn(scl - __half2float(s_hi)));
+                    const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&raw;
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) h[e] = e4m3x2_scaled(pp[e], shi2, slo2);
+                    *(uint4 *)(dst + tc::sw128_offset(row, 2 * part)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *(uint4 *)(dst + tc::sw128_offset(row, 2 * part + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+                }
+                tc::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&kbf[b * 4 + kb]);
+                    tc::mbar_arrive(&ring_empty[s]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------- exchange, softmax, rescale, output
+        const int sp = warp & 3, ch = (warp - 2) >> 2;
+        const int h = 32 * sp + lane;                  // head = TMEM lane
+        const bool own = (sp >> 1) == (int)rank;       // this CTA normalises heads [64 rank, +64)
+        const int ho = h - 64 * (int)rank;             // index among own heads
+        const int hp = h - 64 * (int)peer;             // index among the peer's heads
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16);
+        // queries: the nope half of head h (dims 256 rank + 128 ch ..) -> TMEM,
+        // fp16 pairs; the rope half of every head -> the 64-byte-swizzled tile
+        const __nv_bfloat16 *qh = a.q + (head0 + h) * kLatent;
+        auto load_q = [&]() {
+            const uint4 *src = (const uint4 *)(qh + 256 * rank + 128 * ch);
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const uint4 w = src[half * 8 + i];
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        range_bad |= bf16x2_beyond_f16(ws[e]);
+                        v[4 * i + e] = bf16x2_to_f16x2(ws[e]);
+                    }
+                }
+                tc::tmem_st32(lane_base + QN + 64 * ch + 32 * half, v);
+            }
+            const int t = threadIdx.x - 64;  // 0..255
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const int unit = t + 256 * i, hh = unit >> 2, part = unit & 3;
+                const uint4 w = *(const uint4 *)(a.q + (head0 + hh) * kLatent + 512 + 32 * rank + 8 * part);
+                *(uint4 *)(qr + tc::sw64_offset(hh, part)) = w;
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(q_full);
+        };
+        if (a.q_ready) load_q();
+        tc::grid_dep_wait();
+        if (!a.q_ready) load_q();
+
+        float mref = -INFINITY, lpart = 0.f;
+        const uint32_t srx_peer = tc::mapa(tc::smem_addr(srx), peer);
+        const uint32_t srx_full_peer = tc::mapa(tc::smem_addr(&srx_full[ch]), peer);
+        const uint32_t srx_free_peer = tc::mapa(tc::smem_addr(srx_free), peer);
+        const uint32_t p_full_peer = tc::mapa(tc::smem_addr(p_full), peer);
+        const uint32_t alpha_peer = tc::mapa(tc::smem_addr(alpha_rx), peer);
+        // the warp that waits for a transfer barrier also arms its next phase
+        const bool p_armer = !own && ch == 0 && sp == 2 * (int)peer && lane == 0;
+        const bool s_armer = own && sp == 2 * (int)rank && lane == 0;
+        for (int c = 0; c < nch && ok; c++) {
+            // validity of this warp's 64 rows (ids are L2-hot)
+            uint32_t vm[2];
+#pragma unroll
+            for (int w2 = 0; w2 < 2; w2++) {
+                const int k = k0 + c * kRowsPerChunk + 64 * ch + 32 * w2 + lane;
+                const int32_t id = k < k1 ? ids[k] : -1;
+                vm[w2] = __ballot_sync(0xffffffffu, id >= 0 && id < a.max_row);
+            }
+            if (!(ok = warp_wait(s_full, c & 1, a.err))) break;
+            tc::fence_after_sync();
+            float v[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) tc::tmem_ld16(lane_base + SC + 64 * ch + 16 * q4, v + 16 * q4);
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(s_free);
+            const int k_round = 2 * c + ch;  // order of the exchange rounds through srx
+            if (!own) {
+                // ---- send the peer's heads' partial sums of this half chunk
+                if (k_round >= 1 && !(ok = warp_wait_cluster(srx_free, (k_round - 1) & 1, a.err))) break;
+#pragma unroll
+                for (int j4 = 0; j4 < 16; j4++) {
+                    const uint4 w = make_uint4(__float_as_uint(v[4 * j4]), __float_as_uint(v[4 * j4 + 1]),
+                                               __float_as_uint(v[4 * j4 + 2]), __float_as_uint(v[4 * j4 + 3]));
+                    tc::st_async_v4(srx_peer + (uint32_t)((j4 * 64 + hp) * 16), w, srx_full_peer);
+                }
+                // ---- the peer's P rows and rescale factors for this chunk
+                if (!(ok = warp_wait_cluster(p_full, c & 1, a.err))) break;
+                if (p_armer && c + 1 < nch) tc::mbar_expect_tx(p_full, kPFullBytes);
+                const float al = alpha_rx[hp];
+                if (al != 1.f && c >= 1) {  // (before chunk 0's P V there is nothing to scale)
+                    if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) break;
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int q = 0; q < 8; q++) {
+                        float o[16];
+                        const uint32_t ta = lane_base + OC + 128 * ch + 16 * q;
+                        tc::tmem_ld16(ta, o);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) o[i] *= al;
+                        tc::tmem_st16(ta, o);
+                    }
+                    tc::tmem_st_wait();
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(o_ready);
+            } else {
+                // ---- receive the peer's partial sums of these heads
+                if (!(ok = warp_wait_cluster(&srx_full[ch], c & 1, a.err))) {
+                    bar_or(2, 128, true);
+                    break;
+                }
+                if (s_armer && c + 1 < nch) tc::mbar_expect_tx(&srx_full[ch], 64 * 64 * 4);
+                float lmax = -INFINITY;
+#pragma unroll
+                for (int j4 = 0; j4 < 16; j4++) {
+                    const float4 pv = srx[j4 * 64 + ho];
+                    const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int j = 4 * j4 + e;
+                        const bool valid = (vm[j >> 5] >> (j & 31)) & 1u;
+                        v[j] = valid ? (v[j] + pp[e]) * a.scale_log2 : -INFINITY;
+                        lmax = fmaxf(lmax, v[j]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_remote(srx_free_peer);  // srx may take the next round
+                mxs[ch * 64 + ho] = lmax;
+                if (bar_or(2, 128, false)) {  // a partner timed out
+                    ok = false;
+                    break;
+                }
+                const float cm = fmaxf(lmax, mxs[(1 - ch) * 64 + ho]);
+                float mnew = mref, al = 1.f;
+                if (cm > -INFINITY && (mref == -INFINITY || cm > mref + kRescaleLog2)) {
+                    mnew = cm;
+                    al = mref == -INFINITY ? 0.f : ex2(mref - mnew);
+                }
+                float psum = 0.f;
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) {
+                    const float p0 = mnew == -INFINITY ? 0.f : ex2(v[j] - mnew);
+                    const float p1 = mnew == -INFINITY ? 0.f : ex2(v[j + 1] - mnew);
+                    psum += p0 + p1;
+                    pk[j >> 1] = pack_h2(p0, p1);
+                }
+                lpart = lpart * al + psum;
+                mref = mnew;
+                // P(c) may overwrite P(c-1) once O(c-1) is done in both CTAs
+                if (c >= 1 && !(ok = warp_wait_cluster(pb_free, (c - 1) & 1, a.err))) {
+                    bar_or(2, 128, true);
+                    break;
+                }
+                uint8_t *prow = pb + ch * kKbBytes;
+#pragma unroll
+                for (int q = 0; q < 8; q++)
+                    *(uint4 *)(prow + tc::sw128_offset(h, q)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                if (ch == 0) tc::st_async_b32(alpha_peer + 4 * ho, __float_as_uint(al), p_full_peer);
+                if (al != 1.f && c >= 1) {  // (before chunk 0's P V there is nothing to scale)
+                    if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) {
+                        bar_or(2, 128, true);
+                        break;
+                    }
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int q = 0; q < 8; q++) {
+                        float o[16];
+                        const uint32_t ta = lane_base + OC + 128 * ch + 16 * q;
+                        tc::tmem_ld16(ta, o);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) o[i] *= al;
+                        tc::tmem_st16(ta, o);
+                    }
+                    tc::tmem_st_wait();
+                }
+                tc::fence_async_smem();  // P is read by the tensor core (async proxy)
+                tc::fence_before_sync();
+                // every own-head P row of this chunk is written: send them to the peer
+                if (bar_or(2, 128, false)) {
+                    ok = false;
+                    break;
+                }
+                if (sp == 2 * (int)rank && ch == 0 && lane == 0) {
+#pragma unroll
+                    for (int kbp = 0; kbp < 2; kbp++) {
+                        const uint32_t off = kbp * kKbBytes + 64 * rank * 128;
+                        tc::bulk_s2s(tc::mapa(tc::smem_addr(pb + off), peer), pb + off, 8192, p_full_peer);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(o_ready);
+            }
+        }
+        // ------------------------------------------------------------ output
+        // own heads: l = the two half-chunk sums, m = the reference maximum;
+        // the peer's heads: (l, m) from the peer
+        if (ok && own) {
+            lss[ch * 64 + ho] = lpart;
+            if (bar_or(2, 128, false)) ok = false;
+        }
+        float l = 0.f, m = -INFINITY;
+        if (own) {
+            if (ok) {
+                l = lss[ho] + lss[64 + ho];
+                m = mref;
+                if (ch == 0) {
+                    const uint32_t lm_peer = tc::mapa(tc::smem_addr(lm_rx), peer);
+                    const uint32_t lm_full_peer = tc::mapa(tc::smem_addr(lm_full), peer);
+                    tc::st_async_b32(lm_peer + 4 * ho, __float_as_uint(l), lm_full_peer);
+                    tc::st_async_b32(lm_peer + 256 + 4 * ho, __float_as_uint(m), lm_full_peer);
+                }
+            }
+        } else {
+            if (ok && nch > 0) {
+                ok = warp_wait_cluster(lm_full, 0, a.err);
+                l = lm_rx[hp];
+                m = lm_rx[64 + hp];
+            }
+        }
+        bool fin = ok && (nch == 0 || warp_wait(o_done, (nch - 1) & 1, a.err));
+        tc::fence_after_sync();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int dbase = 256 * (int)rank + 128 * ch;
+        if (a.splits == 1) {
+            __nv_bfloat16 *dst = a.out + (head0 + h) * kNope + dbase;
+#pragma unroll 1
+            for (int q = 0; q < 8; q++) {
+                float o[16];
+                if (fin && nch > 0) {
+                    tc::tmem_ld16(lane_base + OC + 128 * ch + 16 * q, o);
+                    tc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i++) o[i] = 0.f;
+                }
+                uint4 w0, w1;
+                w0.x = pack_bf2(o[0] * inv, o[1] * inv);
+                w0.y = pack_bf2(o[2] * inv, o[3] * inv);
+                w0.z = pack_bf2(o[4] * inv, o[5] * inv);
+                w0.w = pack_bf2(o[6] * inv, o[7] * inv);
+                w1.x = pack_bf2(o[8] * inv, o[9] * inv);
+                w1.y = pack_bf2(o[10] * inv, o[11] * inv);
+                w1.z = pack_bf2(o[12] * inv, o[13] * inv);
+                w1.w = pack_bf2(o[14] * inv, o[15] * inv);
+                *(uint4 *)(dst + 16 * q) = w0;
+                *(uint4 *)(dst + 16 * q + 8) = w1;
+            }
+            if (own && ch == 0 && a.lse) a.lse[head0 + h] = l > 0.f ? (m + log2f(l)) * kLn2P : -INFINITY;
+        } else {
+            float *rec = a.part + ((head0 + h) * a.splits + split) * (kNope + 2);
+#pragma unroll 1
+            for (int q = 0; q < 8; q++) {
+                float o[16];
+                if (fin && nch > 0) {
+                    tc::tmem_ld16(lane_base + OC + 128 * ch + 16 * q, o);
+                    tc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i++) o[i] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; i += 2)  // records are 514 floats: 8-byte aligned only
+                    *(float2 *)(rec + dbase + 16 * q + i) = make_float2(o[i], o[i + 1]);
+            }
+            if (own && ch == 0) {
+                rec[kNope] = l > 0.f ? m : -INFINITY;
+                rec[kNope + 1] = l;
+            }
+        }
+    }
+    if (range_bad) set_error(a.err, HS_ERR_RANGE);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();  // no transfer into this CTA's shared memory is in flight
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool pair_eligible(const hs_pool *p) {
+    // row units are TMA coordinates (int32)
+    const int64_t units = p->cfg.gpu_blocks * p->cfg.num_mla_layers * p->cfg.page_tokens;
+    return p->cfg.row_fmt == HS_ROW_E4M3_656 && p->cfg.mla_heads % kPairHeads == 0 && p->has_row_maps &&
+           units < ((int64_t)1 << 31);
+}
+
+// Row ranges per query for the pair kernel: one 2-CTA cluster per (query,
+// 128 heads, range), one CTA per SM.  Cost in chunk times: waves x (chunks
+// per range + about three of start-up) + one for the combine pass.
+int pair_splits(const hs_pool_config &c, int rows) {
+    const int chunks = (c.top_k + kRowsPerChunk - 1) / kRowsPerChunk;
+    const int pairs = rows * (c.mla_heads / kPairHeads);
+    const int slots = kNumSMs / 2;
+    int best = 1;
+    long best_cost = -1;
+    for (int s = 1; s <= chunks && s <= kMaxSplits; s++) {
+        const long cps = (chunks + s - 1) / s;
+        const long waves = ((long)pairs * s + slots - 1) / slots;
+        const long cost = waves * (cps + 3) + (s > 1 ? 1 : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    const int kc = ((c.top_k + best - 1) / best + kRowsPerChunk - 1) / kRowsPerChunk * kRowsPerChunk;
+    return (c.top_k + kc - 1) / kc;
+}
+
+cudaError_t pair_setup(const hs_pool *) {
+    return cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::bytes);
+}
+
+cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id, int B,
+                                  int nq, float scale, void *out, float *lse, cudaStream_t st, bool q_ready) {
+    const int rows = B * nq, K = p->cfg.top_k;
+    const int splits = pair_splits(p->cfg, rows);
+    PairArgs a;
+    a.q = (const __nv_bfloat16 *)q;
+    a.row_id = row_id;
+    a.pool = p->d.rows;
+    a.layer = layer;
+    a.L = p->cfg.num_mla_layers;
+    a.P = p->cfg.page_tokens;
+    a.H = p->cfg.mla_heads;
+    a.K = K;
+    a.splits = splits;
+    a.kc = ((K + splits - 1) / splits + kRowsPerChunk - 1) / kRowsPerChunk * kRowsPerChunk;
+    a.max_row = (int)(p->cfg.gpu_blocks * p->cfg.page_tokens);
+    a.scale_log2 = scale * kLog2eP;
+    a.out = (__nv_bfloat16 *)out;
+    a.lse = lse;
+    a.part = p->d.attn_part;
+    a.q_ready = q_ready;
+    a.err = p->d.err;
+    dim3 grid(2 * splits, rows, a.H / kPairHeads);
+    PdlLaunch lc(grid, dim3(kPairThreads), PairSmem::bytes, st, dim3(2, 1, 1));
+    return cudaLaunchKernelEx(&lc.cfg, attn_pair_kernel, p->row_map64, p->row_map64s, a);
+}
+
+}  // namespace hs

@@ -182,6 +182,12 @@ __device__ __forceinline__ void grid_dep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+__device__ __forceinline__ uint2 ld_nc8(const void *ptr) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"((uint64_t)ptr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_nc4(const void *ptr) {
     uint32_t v;
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"((uint64_t)ptr));
@@ -286,6 +292,91 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem desc]^T, 16-bit inputs, A read from tensor
+// memory (lane m = row m of A, K packed two 16-bit values per 32-bit column).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` once every tcgen05 operation issued so far by this thread has
+// completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns per thread (register -> TMEM).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// ------------------------------------------------------ cluster transfers
+// 16 bytes into another CTA's shared memory (cluster address), counted as
+// transaction bytes on that CTA's mbarrier (cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            addr),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(v), "r"(mbar)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// another CTA's (cluster addresses for the destination and its mbarrier).
+__device__ __forceinline__ void bulk_s2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "r"(smem_addr(src)), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
+// Arm an mbarrier of this CTA for `bytes` transaction bytes (with one arrival).
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
+    mbar_expect_tx(bar, bytes);
+}
+
+// Four rows of a 2-D tensor (rows y0..y3, a box of one row) into shared
+// memory, one after another; a row outside the tensor reads zeros.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+        "l"((uint64_t)map), "r"(smem_addr(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor, 128-byte swizzle.  The tile starts on a
 // 1024-byte boundary (plus a K offset inside the 128-byte row for K-major).
@@ -318,6 +409,13 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, uint32_t a_fmt, 
                                                   uint32_t a_mn_major, uint32_t b_mn_major) {
     return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn_major << 15) | (b_mn_major << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk `c` (0..3) of row `r` inside a 64-byte
+// swizzled tile whose rows are 64 bytes apart (8-row atoms of 512 bytes):
+// chunk index XOR ((row / 2) % 4).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t r, uint32_t c) {
+    return (r >> 3) * 512u + (r & 7u) * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
 }
 
 // Byte offset of element chunk (16 bytes) `c` of row `r` inside a 128-byte
