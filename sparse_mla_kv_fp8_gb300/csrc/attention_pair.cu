@@ -305,19 +305,40 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         int g = 0;        // ring stage counter
         int ropes = 0;    // rope loads issued
+        // unit of row r of chunk c (-1: no row, read as zeros)
+        auto unit_of = [&](int c, int r) -> int32_t {
+            const int k = k0 + c * kRowsPerChunk + r;
+            int32_t id = (c < nch && k < k1) ? ids[k] : -1;
+            if (id >= a.max_row) {
+                set_error(a.err, HS_ERR_INDEX_RANGE);
+                id = -1;
+            }
+            return id < 0 ? -1 : (int32_t)(((int64_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P);
+        };
+        // bring the rows of chunks 0 and 1 into L2 (this CTA its 64 of each
+        // chunk's 128 rows, all 656 bytes: the peer reads the other half)
+        auto prefetch = [&](int c) {
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const int32_t un = unit_of(c, 64 * (int)rank + 32 * i + lane);
+                if (un >= 0) tc::prefetch_l2(a.pool + (size_t)un * 656, 656);
+            }
+        };
+        prefetch(0);
+        prefetch(1);
         for (int c = 0; c < nch && ok; c++) {
-            // row units of rows 4 lane .. 4 lane + 3 of the chunk (-1: no row, read as zeros)
+            // rows 4 lane .. 4 lane + 3 of the chunk
             int32_t u[4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int k = k0 + c * kRowsPerChunk + 4 * lane + i;
-                int32_t id = k < k1 ? ids[k] : -1;
-                if (id >= a.max_row) {
-                    set_error(a.err, HS_ERR_INDEX_RANGE);
-                    id = -1;
-                }
-                u[i] = id < 0 ? -1 : (int32_t)(((int64_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P);
-            }
+            for (int i = 0; i < 4; i++) u[i] = unit_of(c, 4 * lane + i);
+            prefetch(c + 2);
+            // the rope half, straight into its operand tile, as soon as S(c-1)
+            // has read the last one (its rope MMAs come first)
+            if (c >= 1 && !(ok = warp_wait(rr_free, (c - 1) & 1, a.err))) break;
+            if (lane == 0) tc::mbar_expect_tx(rr_full, 8192);
+            __syncwarp();
+            tc::tma_gather4(rr + 256 * lane, &map64s, rr_full, 528 + 64 * (int)rank, u[0], u[1], u[2], u[3]);
+            ropes++;
             // the four nope K-blocks of this CTA's half
             for (int kb = 0; kb < 4; kb++, g++) {
                 const int s = g % kRingStages;
@@ -327,13 +348,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 tc::tma_gather4(ring + s * kRawKb + 256 * lane, &map64, &ring_full[s],
                                 256 * (int)rank + 64 * kb, u[0], u[1], u[2], u[3]);
             }
-            if (!ok) break;
-            // the rope half, straight into its operand tile (S(c-1) has read the last one)
-            if (c >= 1 && !(ok = warp_wait(rr_free, (c - 1) & 1, a.err))) break;
-            if (lane == 0) tc::mbar_expect_tx(rr_full, 8192);
-            __syncwarp();
-            tc::tma_gather4(rr + 256 * lane, &map64s, rr_full, 528 + 64 * (int)rank, u[0], u[1], u[2], u[3]);
-            ropes++;
         }
         // never leave with a copy into this CTA's shared memory in flight
         // (the consumers have waited for every one on the normal path)
@@ -459,7 +473,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const int32_t id = k < k1 ? ids[k] : -1;
                 vm[w2] = __ballot_sync(0xffffffffu, id >= 0 && id < a.max_row);
             }
-            if (!(ok = warp_wait(s_full, c & 1, a.err))) break;
+            if (!(ok = warp_wait(s_full, c & 1, a.err))) {
+                if (own) bar_or(2, 128, true);  // the partners leave at their next barrier
+                break;
+            }
             tc::fence_after_sync();
             float v[64];
 #pragma unroll
@@ -482,7 +499,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (!(ok = warp_wait_cluster(p_full, c & 1, a.err))) break;
                 if (p_armer && c + 1 < nch) tc::mbar_expect_tx(p_full, kPFullBytes);
                 const float al = alpha_rx[hp];
-                if (al != 1.f && c >= 1) {  // (before chunk 0's P V there is nothing to scale)
+                // the warp rescales together (TMEM loads and stores are warp-wide);
+                // before chunk 0's P V there is nothing to scale
+                if (__any_sync(0xffffffffu, al != 1.f) && c >= 1) {
                     if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) break;
                     tc::fence_after_sync();
 #pragma unroll 1
@@ -555,7 +574,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     *(uint4 *)(prow + tc::sw128_offset(h, q)) =
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 if (ch == 0) tc::st_async_b32(alpha_peer + 4 * ho, __float_as_uint(al), p_full_peer);
-                if (al != 1.f && c >= 1) {  // (before chunk 0's P V there is nothing to scale)
+                if (__any_sync(0xffffffffu, al != 1.f) && c >= 1) {  // (warp-wide, as above)
                     if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) {
                         bar_or(2, 128, true);
                         break;

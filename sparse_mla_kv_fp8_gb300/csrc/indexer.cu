@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // queries -> 128-byte-swizzled K-major rows; head weights -> smem
     const uint8_t *qb = a.q + (size_t)b * a.ncols * 128;
-    for (int i = threadIdx.x; i < a.ncols * 8; i += kTcThreads) {
+    for (int i = threadIdx.x; i < a.ncols * 8; i += blockDim.x) {
         const int r = i >> 3, c = i & 7;
         *(uint4 *)(qs + tc::sw128_offset(r, c)) = *(const uint4 *)(qb + r * 128 + c * 16);
     }
-    for (int i = threadIdx.x; i < a.ncols; i += kTcThreads) wsm[i] = a.w[(size_t)b * a.ncols + i];
+    for (int i = threadIdx.x; i < a.ncols; i += blockDim.x) wsm[i] = a.w[(size_t)b * a.ncols + i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; s++) {
             tc::mbar_init(&full[s], 1);
