@@ -46,23 +46,21 @@ namespace {
 constexpr int kRowsPerChunk = 128;
 constexpr int kPairHeads = 128;
 constexpr int kPairThreads = 448;  // 14 warps
-constexpr int kRingStages = 3;
 constexpr int kKbBytes = 16384;    // 128 rows x 64 fp16 (128-byte swizzle)
-constexpr int kRawKb = 8192;       // 128 rows x 64 E4M3 bytes
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kLog2eP = 1.4426950408889634f;
 constexpr float kLn2P = 0.6931471805599453f;
 constexpr float kMaxF16P = 65504.f;
 constexpr uint32_t kPFullBytes = 2 * 64 * 128 + 64 * 4;  // the peer's P rows + rescale factors
+constexpr uint32_t kSrxBytes = 64 * 128 * 4;              // the peer's partial scores of 64 heads
 
 struct PairSmem {
     static constexpr int rn = 0;                              // 2 buffers x 4 K-blocks (fp16)
     static constexpr int pb = rn + 2 * 4 * kKbBytes;          // P: 2 K-blocks (fp16)
-    static constexpr int ring = pb + 2 * kKbBytes;            // raw K-block stages
-    static constexpr int qr = ring + kRingStages * kRawKb;    // queries' rope half (bf16, 64-byte swizzle)
-    static constexpr int rr = qr + 8192;                      // rows' rope half (bf16, 64-byte swizzle)
-    static constexpr int srx = rr + 8192;                     // received partial S: [16][64] float4
-    static constexpr int alpha_rx = srx + 16384;              // [64] peer's rescale factors
+    static constexpr int qr = pb + 2 * kKbBytes;              // queries' rope half (bf16, 64-byte swizzle)
+    static constexpr int rr = qr + 8192;                      // rows' rope half, 2 buffers (same layout)
+    static constexpr int srx = rr + 2 * 8192;                 // received partial S: [32][64] float4
+    static constexpr int alpha_rx = srx + 32768;              // [64] peer's rescale factors
     static constexpr int lm_rx = alpha_rx + 256;              // [2][64] peer's l, m
     static constexpr int mx = lm_rx + 512;                    // [2][64] half-chunk maxima
     static constexpr int lsum = mx + 512;                     // [2][64] half-chunk sums
@@ -153,7 +151,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *rn = smem + PairSmem::rn;
     uint8_t *pb = smem + PairSmem::pb;
-    uint8_t *ring = smem + PairSmem::ring;
     uint8_t *qr = smem + PairSmem::qr;
     uint8_t *rr = smem + PairSmem::rr;
     float4 *srx = (float4 *)(smem + PairSmem::srx);
@@ -162,16 +159,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     float *mxs = (float *)(smem + PairSmem::mx);
     float *lss = (float *)(smem + PairSmem::lsum);
     uint64_t *bar = (uint64_t *)(smem + PairSmem::bars);
-    uint64_t *ring_full = bar;            // [3]
-    uint64_t *ring_empty = bar + 3;       // [3]
-    uint64_t *kbf = bar + 10;             // [2][4]
-    uint64_t *kbfree = bar + 18;          // [2][2]
-    uint64_t *rr_full = bar + 22;
-    uint64_t *rr_free = bar + 23;
+    uint64_t *kbf = bar;                  // [2][4]: K-block (and, for 0, the rope tile) converted
+    uint64_t *kbfree = bar + 8;           // [2][2]: K-blocks 0-1 / 2-3 (and the rope tile) read
     uint64_t *s_full = bar + 24;
     uint64_t *s_free = bar + 25;
-    uint64_t *srx_full = bar + 26;        // [2]: one per half chunk
-    uint64_t *srx_free = bar + 28;
+    uint64_t *srx_full = bar + 26;        // the peer's partial scores of a chunk arrived
+    uint64_t *srx_free = bar + 28;        // the peer has read this CTA's last partial scores
     uint64_t *p_full = bar + 29;
     uint64_t *pb_free = bar + 30;
     uint64_t *o_ready = bar + 31;
@@ -192,20 +185,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const size_t head0 = (size_t)qrow * a.H + (size_t)hg * kPairHeads;  // first head row
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 3; i++) {
-            tc::mbar_init(&ring_full[i], 1);
-            tc::mbar_init(&ring_empty[i], 4);
-        }
         for (int i = 0; i < 2; i++) {
-            tc::mbar_init(&srx_full[i], 1);
             for (int k = 0; k < 4; k++) tc::mbar_init(&kbf[i * 4 + k], 4);
             for (int k = 0; k < 2; k++) tc::mbar_init(&kbfree[i * 2 + k], 1);
         }
-        tc::mbar_init(rr_full, 1);
-        tc::mbar_init(rr_free, 1);
+        tc::mbar_init(srx_full, 1);
         tc::mbar_init(s_full, 1);
         tc::mbar_init(s_free, 8);
-        tc::mbar_init(srx_free, 2);
+        tc::mbar_init(srx_free, 4);
         tc::mbar_init(p_full, 1);
         tc::mbar_init(pb_free, 2);
         tc::mbar_init(o_ready, 8);
@@ -218,8 +205,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // bytes is armed now, before the peer can send (each later phase is
         // armed by the thread that waited for the phase before it)
         if (nch > 0) {
-            tc::mbar_expect_tx(&srx_full[0], 64 * 64 * 4);
-            tc::mbar_expect_tx(&srx_full[1], 64 * 64 * 4);
+            tc::mbar_expect_tx(srx_full, kSrxBytes);
             tc::mbar_expect_tx(p_full, kPFullBytes);
             tc::mbar_expect_tx(lm_full, 512);
         }
@@ -252,18 +238,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (it < nch) {  // S(it)
                     const int c = it, b = c & 1;
                     if (c >= 1 && !(ok = tc::mbar_wait(s_free, (c - 1) & 1, a.err))) break;
-                    if (!(ok = tc::mbar_wait(rr_full, c & 1, a.err))) break;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < 2; kk++) {
-                        const uint64_t ad = tc::smem_desc(qr_a + kk * 32, 16, 512, 4);
-                        const uint64_t bd = tc::smem_desc(rr_a + kk * 32, 16, 512, 4);
-                        tc::mma_f16(tmem + SC, ad, bd, id_rope, kk);
-                    }
-                    tc::mma_commit(rr_free);
                     for (int kb = 0; kb < 4 && ok; kb++) {
                         if (!(ok = tc::mbar_wait(&kbf[b * 4 + kb], (c >> 1) & 1, a.err))) break;
                         tc::fence_after_sync();
+                        if (kb == 0) {  // the rope tile is converted with K-block 0
+#pragma unroll
+                            for (int kk = 0; kk < 2; kk++) {
+                                const uint64_t ad = tc::smem_desc(qr_a + kk * 32, 16, 512, 4);
+                                const uint64_t bd = tc::smem_desc(rr_a + b * 8192 + kk * 32, 16, 512, 4);
+                                tc::mma_f16(tmem + SC, ad, bd, id_rope, kk);
+                            }
+                        }
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) {
                             const uint64_t bd = tc::smem_desc_sw128(rn_a + (b * 4 + kb) * kKbBytes + kk * 32, 16, 1024);
@@ -297,118 +282,90 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             tc::mbar_wait(mma_done, 0, a.err);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------- gathers (TMA)
+        // --------------------------------------------------- L2 prefetch
+        // (this CTA 64 of each chunk's 128 rows, all 656 bytes: the peer reads
+        // the other half of every row and prefetches the other 64 rows)
         tc::grid_dep_wait();
-        if (nch > 0) {
-            tc::prefetch_tensormap(&map64);
-            tc::prefetch_tensormap(&map64s);
-        }
-        int g = 0;        // ring stage counter
-        int ropes = 0;    // rope loads issued
-        // unit of row r of chunk c (-1: no row, read as zeros)
-        auto unit_of = [&](int c, int r) -> int32_t {
-            const int k = k0 + c * kRowsPerChunk + r;
-            int32_t id = (c < nch && k < k1) ? ids[k] : -1;
-            if (id >= a.max_row) {
-                set_error(a.err, HS_ERR_INDEX_RANGE);
-                id = -1;
-            }
-            return id < 0 ? -1 : (int32_t)(((int64_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P);
-        };
-        // bring the rows of chunks 0 and 1 into L2 (this CTA its 64 of each
-        // chunk's 128 rows, all 656 bytes: the peer reads the other half)
         auto prefetch = [&](int c) {
 #pragma unroll
             for (int i = 0; i < 2; i++) {
-                const int32_t un = unit_of(c, 64 * (int)rank + 32 * i + lane);
-                if (un >= 0) tc::prefetch_l2(a.pool + (size_t)un * 656, 656);
+                const int k = k0 + c * kRowsPerChunk + 64 * (int)rank + 32 * i + lane;
+                const int32_t id = (c < nch && k < k1) ? ids[k] : -1;
+                if (id >= 0 && id < a.max_row)
+                    tc::prefetch_l2(a.pool + (((size_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P) * 656, 656);
             }
         };
-        prefetch(0);
-        prefetch(1);
-        for (int c = 0; c < nch && ok; c++) {
-            // rows 4 lane .. 4 lane + 3 of the chunk
-            int32_t u[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) u[i] = unit_of(c, 4 * lane + i);
-            prefetch(c + 2);
-            // the rope half, straight into its operand tile, as soon as S(c-1)
-            // has read the last one (its rope MMAs come first)
-            if (c >= 1 && !(ok = warp_wait(rr_free, (c - 1) & 1, a.err))) break;
-            if (lane == 0) tc::mbar_expect_tx(rr_full, 8192);
-            __syncwarp();
-            tc::tma_gather4(rr + 256 * lane, &map64s, rr_full, 528 + 64 * (int)rank, u[0], u[1], u[2], u[3]);
-            ropes++;
-            // the four nope K-blocks of this CTA's half
-            for (int kb = 0; kb < 4; kb++, g++) {
-                const int s = g % kRingStages;
-                if (!(ok = warp_wait(&ring_empty[s], ((g / kRingStages) & 1) ^ 1, a.err))) break;
-                if (lane == 0) tc::mbar_expect_tx(&ring_full[s], kRawKb);
-                __syncwarp();
-                tc::tma_gather4(ring + s * kRawKb + 256 * lane, &map64, &ring_full[s],
-                                256 * (int)rank + 64 * kb, u[0], u[1], u[2], u[3]);
-            }
-        }
-        // never leave with a copy into this CTA's shared memory in flight
-        // (the consumers have waited for every one on the normal path)
-        if (lane == 0) {
-            for (int i = g - kRingStages; i < g; i++)
-                if (i >= 0) tc::mbar_wait(&ring_full[i % kRingStages], (i / kRingStages) & 1, a.err);
-            if (ropes > 0) tc::mbar_wait(rr_full, (ropes - 1) & 1, a.err);
-        }
+        // in chunk order: the first chunks' rows arrive first
+        for (int c = 0; c < nch; c++) prefetch(c);
     } else if (warp >= 10) {
         // ------------------------------------------------------ converters
+        // Thread ct owns rows ct/4 + 32 i (i < 4) and the 16-byte slice ct % 4
+        // of each row's 64 bytes in every nope K-block of this CTA's half and
+        // of its rope half: 16 + 4 loads of 16 bytes and 4 of the rows' two
+        // group scales per chunk, issued a chunk ahead into registers.
         tc::grid_dep_wait();
         const int ct = threadIdx.x - 320;  // 0..127
-        const int part = ct & 3;           // 16-byte slice of a row's 64 K-block bytes
-        int g = 0;
-        for (int c = 0; c < nch && ok; c++) {
-            const int b = c & 1;
-            // this thread's rows ct/4 + 32 i and their two group scales (the
-            // rows' ids are L2-hot; a missing row keeps scale 0)
-            float2 sg[4];
+        const int part = ct & 3;
+        uint4 raw[4][4], rope[4];
+        float2 sg[4];
+        auto load = [&](int c) {
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 const int k = k0 + c * kRowsPerChunk + (ct >> 2) + 32 * i;
-                const int32_t id = k < k1 ? ids[k] : -1;
-                sg[i] = make_float2(0.f, 0.f);
-                if (id >= 0 && id < a.max_row) {
-                    const size_t unit = ((size_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P;
-                    const uint2 w = tc::ld_nc8(a.pool + unit * 656 + 512 + 8 * rank);
-                    sg[i] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+                int32_t id = (c < nch && k < k1) ? ids[k] : -1;
+                if (id >= a.max_row) {
+                    set_error(a.err, HS_ERR_INDEX_RANGE);
+                    id = -1;
                 }
+                if (id < 0) {
+#pragma unroll
+                    for (int kb = 0; kb < 4; kb++) raw[kb][i] = make_uint4(0, 0, 0, 0);
+                    rope[i] = make_uint4(0, 0, 0, 0);
+                    sg[i] = make_float2(0.f, 0.f);
+                    continue;
+                }
+                const uint8_t *row = a.pool + (((size_t)(id / a.P) * a.L + a.layer) * a.P + id % a.P) * 656;
+#pragma unroll
+                for (int kb = 0; kb < 4; kb++) raw[kb][i] = tc::ld_nc16(row + 256 * rank + 64 * kb + 16 * part);
+                rope[i] = tc::ld_nc16(row + 528 + 64 * rank + 16 * part);
+                const uint2 w = tc::ld_nc8(row + 512 + 8 * rank);
+                sg[i] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
             }
-            for (int kb = 0; kb < 4; kb++, g++) {
-                const int s = g % kRingStages;
+        };
+        load(0);
+        for (int c = 0; c < nch && ok; c++) {
+            const int b = c & 1;
+            for (int kb = 0; kb < 4; kb++) {
                 if (c >= 2 && (kb & 1) == 0 &&
                     !(ok = warp_wait(&kbfree[b * 2 + (kb >> 1)], ((c - 2) >> 1) & 1, a.err)))
                     break;
-                if (!(ok = warp_wait(&ring_full[s], (g / kRingStages) & 1, a.err))) break;
-                const uint8_t *src = ring + s * kRawKb;
+                if (kb == 0) {  // the rope half: bf16 as it is, into its 64-byte-swizzled tile
+                    uint8_t *rt = rr + b * 8192;
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        *(uint4 *)(rt + tc::sw64_offset((ct >> 2) + 32 * i, part)) = rope[i];
+                }
                 uint8_t *dst = rn + (b * 4 + kb) * kKbBytes;
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
-                    const int row = (ct >> 2) + 32 * i;
-                    const uint4 raw = *(const uint4 *)(src + row * 64 + part * 16);
+                    const int r = (ct >> 2) + 32 * i;
                     const float scl = (kb >> 1) ? sg[i].y : sg[i].x;
                     range_bad |= 448.f * fabsf(scl) > kMaxF16P;
                     const __half s_hi = __float2half_rn(scl);
                     const __half2 shi2 = __half2half2(s_hi);
                     const __half2 slo2 = __half2half2(__float2half_rn(scl - __half2float(s_hi)));
-                    const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&raw;
+                    const __nv_fp8x2_storage_t *pp = (const __nv_fp8x2_storage_t *)&raw[kb][i];
                     uint32_t h[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++) h[e] = e4m3x2_scaled(pp[e], shi2, slo2);
-                    *(uint4 *)(dst + tc::sw128_offset(row, 2 * part)) = make_uint4(h[0], h[1], h[2], h[3]);
-                    *(uint4 *)(dst + tc::sw128_offset(row, 2 * part + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+                    *(uint4 *)(dst + tc::sw128_offset(r, 2 * part)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *(uint4 *)(dst + tc::sw128_offset(r, 2 * part + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
                 }
                 tc::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(&kbf[b * 4 + kb]);
-                    tc::mbar_arrive(&ring_empty[s]);
-                }
+                if (lane == 0) tc::mbar_arrive(&kbf[b * 4 + kb]);
             }
+            if (ok) load(c + 1);  // the registers are free: the next chunk's rows
         }
     } else {
         // ------------------------------- exchange, softmax, rescale, output
@@ -457,13 +414,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
         float mref = -INFINITY, lpart = 0.f;
         const uint32_t srx_peer = tc::mapa(tc::smem_addr(srx), peer);
-        const uint32_t srx_full_peer = tc::mapa(tc::smem_addr(&srx_full[ch]), peer);
+        const uint32_t srx_full_peer = tc::mapa(tc::smem_addr(srx_full), peer);
         const uint32_t srx_free_peer = tc::mapa(tc::smem_addr(srx_free), peer);
         const uint32_t p_full_peer = tc::mapa(tc::smem_addr(p_full), peer);
         const uint32_t alpha_peer = tc::mapa(tc::smem_addr(alpha_rx), peer);
         // the warp that waits for a transfer barrier also arms its next phase
         const bool p_armer = !own && ch == 0 && sp == 2 * (int)peer && lane == 0;
-        const bool s_armer = own && sp == 2 * (int)rank && lane == 0;
+        const bool s_armer = own && sp == 2 * (int)rank && ch == 0 && lane == 0;
+        // a sender warp's handling of chunk cc's arrival from the peer: its P
+        // rows and rescale factors; rescale this CTA's O rows of the peer's
+        // heads when needed, then let the MMA warp run O(cc)
+        auto sender_finish = [&](int cc) -> bool {
+            if (!warp_wait_cluster(p_full, cc & 1, a.err)) return false;
+            if (p_armer && cc + 1 < nch) tc::mbar_expect_tx(p_full, kPFullBytes);
+            const float al = alpha_rx[hp];
+            // the warp rescales together (TMEM loads and stores are warp-wide);
+            // before chunk 0's P V there is nothing to scale
+            if (__any_sync(0xffffffffu, al != 1.f) && cc >= 1) {
+                if (!warp_wait(o_done, (cc - 1) & 1, a.err)) return false;
+                tc::fence_after_sync();
+#pragma unroll 1
+                for (int q = 0; q < 8; q++) {
+                    float o[16];
+                    const uint32_t ta = lane_base + OC + 128 * ch + 16 * q;
+                    tc::tmem_ld16(ta, o);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) o[i] *= al;
+                    tc::tmem_st16(ta, o);
+                }
+                tc::tmem_st_wait();
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(o_ready);
+            return true;
+        };
         for (int c = 0; c < nch && ok; c++) {
             // validity of this warp's 64 rows (ids are L2-hot)
             uint32_t vm[2];
@@ -478,58 +464,49 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            float v[64];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) tc::tmem_ld16(lane_base + SC + 64 * ch + 16 * q4, v + 16 * q4);
-            tc::tmem_ld_wait();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(s_free);
-            const int k_round = 2 * c + ch;  // order of the exchange rounds through srx
+            const uint32_t sbase = lane_base + SC + 64 * ch;
             if (!own) {
-                // ---- send the peer's heads' partial sums of this half chunk
-                if (k_round >= 1 && !(ok = warp_wait_cluster(srx_free, (k_round - 1) & 1, a.err))) break;
+                // ---- send the peer's heads' partial sums of this half chunk, 16
+                // columns at a time (after the peer has read the last chunk's)
+                if (c >= 1 && !(ok = warp_wait_cluster(srx_free, (c - 1) & 1, a.err))) break;
 #pragma unroll
-                for (int j4 = 0; j4 < 16; j4++) {
-                    const uint4 w = make_uint4(__float_as_uint(v[4 * j4]), __float_as_uint(v[4 * j4 + 1]),
-                                               __float_as_uint(v[4 * j4 + 2]), __float_as_uint(v[4 * j4 + 3]));
-                    tc::st_async_v4(srx_peer + (uint32_t)((j4 * 64 + hp) * 16), w, srx_full_peer);
-                }
-                // ---- the peer's P rows and rescale factors for this chunk
-                if (!(ok = warp_wait_cluster(p_full, c & 1, a.err))) break;
-                if (p_armer && c + 1 < nch) tc::mbar_expect_tx(p_full, kPFullBytes);
-                const float al = alpha_rx[hp];
-                // the warp rescales together (TMEM loads and stores are warp-wide);
-                // before chunk 0's P V there is nothing to scale
-                if (__any_sync(0xffffffffu, al != 1.f) && c >= 1) {
-                    if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) break;
-                    tc::fence_after_sync();
-#pragma unroll 1
-                    for (int q = 0; q < 8; q++) {
-                        float o[16];
-                        const uint32_t ta = lane_base + OC + 128 * ch + 16 * q;
-                        tc::tmem_ld16(ta, o);
-                        tc::tmem_ld_wait();
+                for (int q4 = 0; q4 < 4; q4++) {
+                    float v[16];
+                    tc::tmem_ld16(sbase + 16 * q4, v);
+                    tc::tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; i++) o[i] *= al;
-                        tc::tmem_st16(ta, o);
+                    for (int j4 = 0; j4 < 4; j4++) {
+                        const uint4 w = make_uint4(__float_as_uint(v[4 * j4]), __float_as_uint(v[4 * j4 + 1]),
+                                                   __float_as_uint(v[4 * j4 + 2]), __float_as_uint(v[4 * j4 + 3]));
+                        tc::st_async_v4(srx_peer + (uint32_t)(((16 * ch + 4 * q4 + j4) * 64 + hp) * 16), w,
+                                        srx_full_peer);
                     }
-                    tc::tmem_st_wait();
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(o_ready);
+                if (lane == 0) tc::mbar_arrive(s_free);
+                // ---- then the peer's P rows and rescale factors of the chunk
+                // before (the send of this chunk goes first: it overlaps the
+                // peer's softmax of the last one)
+                if (c >= 1 && !(ok = sender_finish(c - 1))) break;
             } else {
+                float v[64];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) tc::tmem_ld16(sbase + 16 * q4, v + 16 * q4);
+                tc::tmem_ld_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(s_free);
                 // ---- receive the peer's partial sums of these heads
-                if (!(ok = warp_wait_cluster(&srx_full[ch], c & 1, a.err))) {
+                if (!(ok = warp_wait_cluster(srx_full, c & 1, a.err))) {
                     bar_or(2, 128, true);
                     break;
                 }
-                if (s_armer && c + 1 < nch) tc::mbar_expect_tx(&srx_full[ch], 64 * 64 * 4);
+                if (s_armer && c + 1 < nch) tc::mbar_expect_tx(srx_full, kSrxBytes);
                 float lmax = -INFINITY;
 #pragma unroll
                 for (int j4 = 0; j4 < 16; j4++) {
-                    const float4 pv = srx[j4 * 64 + ho];
+                    const float4 pv = srx[(16 * ch + j4) * 64 + ho];
                     const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
@@ -540,7 +517,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive_remote(srx_free_peer);  // srx may take the next round
+                // srx may take the next chunk (relaxed: the values read are already used)
+                if (lane == 0) tc::mbar_arrive_remote_relaxed(srx_free_peer);
                 mxs[ch * 64 + ho] = lmax;
                 if (bar_or(2, 128, false)) {  // a partner timed out
                     ok = false;
@@ -552,27 +530,28 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     mnew = cm;
                     al = mref == -INFINITY ? 0.f : ex2(mref - mnew);
                 }
-                float psum = 0.f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    const float p0 = mnew == -INFINITY ? 0.f : ex2(v[j] - mnew);
-                    const float p1 = mnew == -INFINITY ? 0.f : ex2(v[j + 1] - mnew);
-                    psum += p0 + p1;
-                    pk[j >> 1] = pack_h2(p0, p1);
-                }
-                lpart = lpart * al + psum;
-                mref = mnew;
                 // P(c) may overwrite P(c-1) once O(c-1) is done in both CTAs
                 if (c >= 1 && !(ok = warp_wait_cluster(pb_free, (c - 1) & 1, a.err))) {
                     bar_or(2, 128, true);
                     break;
                 }
+                float psum = 0.f;
                 uint8_t *prow = pb + ch * kKbBytes;
 #pragma unroll
-                for (int q = 0; q < 8; q++)
-                    *(uint4 *)(prow + tc::sw128_offset(h, q)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int q = 0; q < 8; q++) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int j = 8 * q + 2 * e;
+                        const float p0 = mnew == -INFINITY ? 0.f : ex2(v[j] - mnew);
+                        const float p1 = mnew == -INFINITY ? 0.f : ex2(v[j + 1] - mnew);
+                        psum += p0 + p1;
+                        pk[e] = pack_h2(p0, p1);
+                    }
+                    *(uint4 *)(prow + tc::sw128_offset(h, q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                lpart = lpart * al + psum;
+                mref = mnew;
                 if (ch == 0) tc::st_async_b32(alpha_peer + 4 * ho, __float_as_uint(al), p_full_peer);
                 if (__any_sync(0xffffffffu, al != 1.f) && c >= 1) {  // (warp-wide, as above)
                     if (!(ok = warp_wait(o_done, (c - 1) & 1, a.err))) {
@@ -610,6 +589,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (lane == 0) tc::mbar_arrive(o_ready);
             }
         }
+        if (!own && ok && nch > 0) ok = sender_finish(nch - 1);
         // ------------------------------------------------------------ output
         // own heads: l = the two half-chunk sums, m = the reference maximum;
         // the peer's heads: (l, m) from the peer
