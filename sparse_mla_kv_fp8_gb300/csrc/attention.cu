@@ -971,18 +971,28 @@ cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, co
                                   int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
                                   bool q_ready);
 
-static bool pair_cfg(const hs_pool_config &c) {
-    return c.row_fmt == HS_ROW_E4M3_656 && c.mla_heads % 128 == 0;
+// Which tensor-core kernel a batch takes.  The pair kernel (the latent dims
+// split over a 2-CTA cluster, every MMA at M = N = 128, each row converted
+// once) wins when the batch fills the GPU with pairs: measured at 128 heads,
+// K = 2048, 256 queries it takes 348 us per layer against 445 for the
+// 64-head kernel; below about one wave of pairs its longer per-chunk chain
+// (two exchanges between the CTAs per 128 rows) costs more than it saves (32
+// queries: 70 against 62 us; 4 queries: 42 against 30 us).
+constexpr int kPairMinQueryGroups = 64;  // queries x 128-head groups
+
+static bool pair_cfg(const hs_pool_config &c, int rows) {
+    return c.row_fmt == HS_ROW_E4M3_656 && c.mla_heads % 128 == 0 &&
+           rows * (c.mla_heads / 128) >= kPairMinQueryGroups;
 }
 
 static int splits_for(const hs_pool_config &c, int rows) {
-    if (pair_cfg(c)) return pair_splits(c, rows);
+    if (pair_cfg(c, rows)) return pair_splits(c, rows);
     return tc_eligible(c) ? tc_splits(c, rows) : simt_splits(c, rows);
 }
 
 int attention_kernel_count(const hs_pool *p, int B, int nq) {
     const int s = splits_for(p->cfg, B * nq);
-    if (pair_cfg(p->cfg)) return s > 1 ? 2 : 1;
+    if (pair_cfg(p->cfg, B * nq)) return s > 1 ? 2 : 1;
     if (tc_eligible(p->cfg)) return s > 2 ? 2 : 1;
     return s > 1 ? 2 : 1;
 }
@@ -1016,8 +1026,7 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
     const int rows = B * nq;
     const int K = p->cfg.top_k;
     const int splits = splits_for(p->cfg, rows);
-    if (pair_cfg(p->cfg)) {
-        if (!pair_eligible(p)) return cudaErrorInvalidValue;
+    if (pair_cfg(p->cfg, rows) && pair_eligible(p)) {
         cudaError_t e = launch_pair_attention(p, layer, q, row_id, B, nq, scale, out, lse, st, q_ready);
         if (e != cudaSuccess) return e;
         if (splits > 1)

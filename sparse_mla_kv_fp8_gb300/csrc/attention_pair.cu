@@ -21,15 +21,16 @@
 //   O_r += P V_r       (V_r: the CTA's 256 nope dims, two N = 128 MMAs; the
 //                       P rows of the other CTA's heads arrive by a bulk copy)
 // TMEM (512 columns): queries' nope half [0,128) (fp16 pairs), S [128,256),
-// O [256,512).  Rows reach shared memory by TMA: per chunk a gather of the
-// four nope K-blocks of the CTA's half (64 E4M3 bytes per row) into a
-// three-stage ring and of the rope half straight into its 64-byte-swizzled
-// operand tile; four converter warps dequantise each K-block (E4M3 x the
-// row's group scale, read from global memory -> fp16, the scale split into
-// two fp16s) into
-// 128-byte-swizzled operand tiles, double buffered by chunk, so that chunk
-// c+1's K-blocks are converted while chunk c's P V products run.
-// Warp 0 issues the MMAs, warp 1 owns TMEM and issues the gathers, warps 2-9
+// O [256,512).  Four converter warps load each chunk's rows a chunk ahead
+// into registers (16-byte loads of the CTA's half of every row; the rows are
+// brought into L2 in bulk beforehand) and write them K-block by K-block into
+// 128-byte-swizzled fp16 operand tiles (E4M3 x the row's group scale, the
+// scale split into two fp16s) and the rope half, bf16 as it is, into a
+// 64-byte-swizzled tile, double buffered by chunk, so that chunk c+1's
+// K-blocks are converted while chunk c's P V products run.  (Gathering the
+// rows with TMA, four 64-byte row slices per copy, was measured about ten
+// times slower to land per chunk than these loads.)
+// Warp 0 issues the MMAs, warp 1 owns TMEM and prefetches rows, warps 2-9
 // run the exchange, softmax, rescale and epilogue (thread = TMEM lane = head,
 // one warp per (lane quarter, half chunk)), warps 10-13 convert.
 // Every wait is bounded; on a time-out the kernel records HS_ERR_TIMEOUT,
@@ -145,8 +146,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 __global__ void __launch_bounds__(kPairThreads, 1)
-    attn_pair_kernel(const __grid_constant__ CUtensorMap map64, const __grid_constant__ CUtensorMap map64s,
-                     PairArgs a) {
+    attn_pair_kernel(PairArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *rn = smem + PairSmem::rn;
@@ -680,10 +680,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 }  // namespace
 
 bool pair_eligible(const hs_pool *p) {
-    // row units are TMA coordinates (int32)
-    const int64_t units = p->cfg.gpu_blocks * p->cfg.num_mla_layers * p->cfg.page_tokens;
-    return p->cfg.row_fmt == HS_ROW_E4M3_656 && p->cfg.mla_heads % kPairHeads == 0 && p->has_row_maps &&
-           units < ((int64_t)1 << 31);
+    return p->cfg.row_fmt == HS_ROW_E4M3_656 && p->cfg.mla_heads % kPairHeads == 0;
 }
 
 // Row ranges per query for the pair kernel: one 2-CTA cluster per (query,
@@ -736,7 +733,7 @@ cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, co
     a.err = p->d.err;
     dim3 grid(2 * splits, rows, a.H / kPairHeads);
     PdlLaunch lc(grid, dim3(kPairThreads), PairSmem::bytes, st, dim3(2, 1, 1));
-    return cudaLaunchKernelEx(&lc.cfg, attn_pair_kernel, p->row_map64, p->row_map64s, a);
+    return cudaLaunchKernelEx(&lc.cfg, attn_pair_kernel, a);
 }
 
 }  // namespace hs

@@ -100,9 +100,6 @@ struct hs_pool {
     hs::DevPtrs d;
     CUtensorMap key_map;     // TMA map of the indexer key slab (E4M3, dim 128)
     bool has_key_map;
-    CUtensorMap row_map64;   // TMA maps of the block pool's rows (64-byte boxes),
-    CUtensorMap row_map64s;  // plain and with the 64-byte swizzle
-    bool has_row_maps;
     // a second stream and L events, made at creation, on which the miss copy of
     // layer l+1 runs while the attention of layer l runs on the caller's stream
     cudaStream_t side = nullptr;

@@ -43,25 +43,6 @@ bool make_key_map(hs_pool *p) {
     return r == CUDA_SUCCESS;
 }
 
-// 2-D views of the block pool for row gathers: one row per (block, layer,
-// token) unit, 656 bytes each; a box is 64 bytes of one row (TMA gather4
-// takes four rows per copy).  `swz` selects the 64-byte swizzle the tensor
-// core reads (for the rope half, loaded straight into its operand tile).
-bool make_row_map(hs_pool *p, CUtensorMap *m, bool swz) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const uint64_t units = (uint64_t)p->cfg.gpu_blocks * p->cfg.num_mla_layers * p->cfg.page_tokens;
-    cuuint64_t gdim[2] = {656, (cuuint64_t)units};
-    cuuint64_t gstride[1] = {656};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p->d.rows, gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swz ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -302,14 +283,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
             return HS_ERR_CUDA;
         }
         p->has_key_map = true;
-    }
-    p->has_row_maps = false;
-    if (cfg->row_fmt == HS_ROW_E4M3_656) {
-        if (!make_row_map(p, &p->row_map64, false) || !make_row_map(p, &p->row_map64s, true)) {
-            delete p;
-            return HS_ERR_CUDA;
-        }
-        p->has_row_maps = true;
     }
     const size_t maxR = cfg->max_requests;
     p->seq_len.assign(maxR, 0);

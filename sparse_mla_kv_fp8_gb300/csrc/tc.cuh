@@ -361,17 +361,6 @@ __device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes
     mbar_expect_tx(bar, bytes);
 }
 
-// Four rows of a 2-D tensor (rows y0..y3, a box of one row) into shared
-// memory, one after another; a row outside the tensor reads zeros.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
-        "l"((uint64_t)map), "r"(smem_addr(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-        : "memory");
-}
-
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -11,7 +11,9 @@ Every output is compared with the fp64 oracle within 2e-3 + 1e-2 |ref|.
 The shapes pick the kernel routes by themselves: two requests over K = 2048
 split every query's rows over many CTAs (partials + combine kernel); 32
 queries take two row ranges per query (a 2-CTA cluster that merges in
-distributed shared memory); 80 queries take one range per query; 16 heads
+distributed shared memory); 64 or more queries (x 128-head groups) take the
+kernel that splits the latent dims over a 2-CTA cluster (with 80 queries one
+range each; 64 queries with K = 704; 256 heads as two head groups); 16 heads
 (not a multiple of 64) take the CUDA-core kernel.
 
 Sources: "Un contexte d'un million sur huit H200", « Les trois états de
@@ -151,6 +153,8 @@ def _run(B, nq, H, K, N, seed):
     (20, 4, 128, 2048, 2300),   # one range per query (MTP3: 80 queries)
     (3, 1, 128, 704, 1500),     # K not a multiple of the 128-row chunk
     (3, 2, 16, 512, 1400),      # 16 heads: the CUDA-core kernel
+    (64, 1, 128, 704, 1500),    # 64 queries: the 2-CTA latent-split kernel, ragged K
+    (17, 4, 256, 1024, 1800),   # 256 heads: two 128-head groups per query (68 x 2 groups)
 ])
 def test_peaked_softmax_and_rescale(B, nq, H, K, N):
     _run(B, nq, H, K, N, seed=11 + B)

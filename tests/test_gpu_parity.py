@@ -740,6 +740,9 @@ def test_indexer_tensor_core_pipeline_wraps():
     # zero residency, every row arrives through the hot buffer
     ("tc-zero", dict(B=2, N=4000, K=1024, Hi=8, Di=32, L=1, T=0, mode=2, steps=3,
                      source="uniform_zipf")),
+    # 64 queries (MTP3 x 16 requests): the latent-split 2-CTA kernel, misses and hits
+    ("tc-pair", dict(B=16, N=[1500 + 97 * i for i in range(16)], K=512, Hi=8, Di=32, L=2,
+                     T=128, num_spec=3, steps=3, source="recency_zipf", check_attn_every=2)),
 ])
 def test_attention_tensor_core_128_heads(name, kw):
     """128 heads with E4M3 rows: the tcgen05 attention kernel against the oracle."""
