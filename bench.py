@@ -3,8 +3,7 @@
 
 One step = indexer score -> top-K -> fused resolve (plan + miss copies from
 pinned host memory) -> sparse MLA decode of the 4 MLA layers of one
-IndexShare group, captured in a CUDA graph and replayed; the miss copy of
-layer l+1 runs on a second stream while the attention of layer l runs.
+IndexShare group, captured in a CUDA graph and replayed.
 
 Workloads (``--workload``; the headline line is the first, the others are
 reported as secondary lines in the same JSON object):
@@ -272,8 +271,7 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
     def enqueue_step(st):
         if drawn:
             # the indexer and top-K on their own inputs, the resolve and the
-            # attention (hs_resolve_attend: per-layer miss copies overlapping
-            # the attention of the layer before) on the trace's lists
+            # attention (hs_resolve_attend) on the trace's lists
             pool.indexer_topk(q, wt, B, nq, topk, stream=st)
             pool.resolve_attend(trace.buf, B, nq, qm, tau, out, rid, stream=st)
         else:

@@ -350,15 +350,10 @@ hs_status hs_dcp_combine(const void *o_parts, const float *lse_parts, int32_t R,
                          int32_t H, void *out, float *lse, cudaStream_t stream);
 
 /* Resolve + the sparse MLA decode of every layer of the group, for a top-K
- * the caller already has: the second half of hs_step.  topk, row_id: as for
- * hs_resolve; q_mla, out, lse: as in hs_step_args ([L][B][nq]...).  With a
- * host pool the miss copy is split by layer: layer 0's rows are copied on
- * `stream` right after the plan and layers 1..L-1 on a second stream the
- * pool owns (forked and joined with events, so the call can be captured in a
- * CUDA graph), and the attention of layer l waits only for the rows of layer
- * l: the copy of layer l+1 over the host link overlaps the attention of
- * layer l.  The results are those of hs_resolve followed by
- * hs_sparse_mla_decode for each layer. */
+ * the caller already has (the second half of hs_step, e.g. for a selection
+ * made elsewhere): hs_resolve followed by hs_sparse_mla_decode for each of
+ * the L layers, enqueued on `stream`.  topk, row_id: as for hs_resolve;
+ * q_mla, out, lse: as in hs_step_args ([L][B][nq]...). */
 hs_status hs_resolve_attend(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
                             const void *q_mla, float softmax_scale, void *out, float *lse,
                             int32_t *row_id, cudaStream_t stream);
@@ -377,10 +372,8 @@ typedef struct {
 
 /* One decode step of one IndexShare group: indexer score -> top-K ->
  * fused resolve (with miss copies) -> sparse MLA decode for each of the L
- * layers, i.e. the indexer's top-K followed by hs_resolve_attend (the miss
- * copies of layers 1..L-1 run on the pool's second stream, overlapping the
- * attention of the layer before).  Enqueued on `stream`; no host
- * synchronisation. */
+ * layers, i.e. the indexer's top-K followed by hs_resolve_attend.  Enqueued
+ * on `stream`; no host synchronisation. */
 hs_status hs_step(hs_pool *pool, const hs_step_args *args, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */

@@ -71,8 +71,6 @@ struct PairSmem {
     static constexpr int bytes = tslot + 16 + 1024;           // + alignment slack
 };
 static_assert(PairSmem::bytes <= 232448, "pair attention shared memory");
-// leaves room on the SM for a light miss-copy CTA next to it
-static_assert(PairSmem::bytes + 1024 + 1024 <= 233472, "pair attention co-residency");
 
 struct PairArgs {
     const __nv_bfloat16 *q;  // [rows][H][576]

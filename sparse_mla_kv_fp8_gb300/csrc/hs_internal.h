@@ -100,15 +100,6 @@ struct hs_pool {
     hs::DevPtrs d;
     CUtensorMap key_map;     // TMA map of the indexer key slab (E4M3, dim 128)
     bool has_key_map;
-    // a second stream and L events, made at creation, on which the miss copy of
-    // layer l+1 runs while the attention of layer l runs on the caller's stream
-    cudaStream_t side = nullptr;
-    std::vector<cudaEvent_t> layer_ev;
-    ~hs_pool() {
-        for (cudaEvent_t ev : layer_ev)
-            if (ev) cudaEventDestroy(ev);
-        if (side) cudaStreamDestroy(side);
-    }
     // host mirrors
     std::vector<int32_t> seq_len;
     std::vector<int32_t> mode;  // -1 = closed

@@ -312,12 +312,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     ms(p->d.stats, 0, 32);
     ms(p->d.miss_count, 0, maxR * 4);
     if (e == cudaSuccess) e = hs::setup_kernel_attributes(p);
-    if (e == cudaSuccess && cfg->host_blocks > 0) {
-        e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
-        p->layer_ev.assign(cfg->num_mla_layers, nullptr);
-        for (auto &ev : p->layer_ev)
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         delete p;
@@ -588,39 +582,24 @@ hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const i
     return cuda_status(hs::launch_attention(p, layer, q, row_id, B, nq, scale, out, lse, st));
 }
 
-// Resolve, then the attention of every layer.  With a host pool the miss
-// copy runs per layer: layer 0's rows on `st` right after the plan, layers
-// 1..L-1 on the pool's side stream (ordered after the plan by an event), so
-// that the copy of layer l+1 (bound by the host link) runs while the
-// attention of layer l (bound by the tensor cores and HBM) runs on `st`; the
-// attention of layer l waits for its own rows only.  Events make the fork and
-// the join, so the sequence can be captured in a CUDA graph.
+// Resolve (the plan, then one miss copy of every layer's rows), then the
+// attention of every layer, all on `st`.  (Copying layer l+1's rows on a
+// second stream while layer l's attention runs was measured: it gained at a
+// small miss volume but lost at the mixed-residency MTP3 workload, 142,000
+// tokens x 64 requests, about 160,000 misses per step: 5.4-5.7 ms against
+// 5.0 ms per step, the copy's long-latency host loads slowing the attention
+// CTAs they share the SMs with.)
 static cudaError_t resolve_attend(hs_pool *p, const int32_t *topk, int B, int nq,
                                   const void *q_mla, float scale, void *out, float *lse,
                                   int32_t *row_id, cudaStream_t st, bool q_ready) {
     const int H = p->cfg.mla_heads, L = p->cfg.num_mla_layers;
     const size_t qstride = (size_t)B * nq * H * hs::kLatent * 2;
     const size_t ostride = (size_t)B * nq * H * hs::kNope * 2;
-    const bool copies = p->cfg.host_blocks > 0;
-    cudaError_t e = hs::launch_resolve_plan(p, topk, B, nq, row_id, st);
-    if (e == cudaSuccess && copies) {
-        if (L > 1) {
-            e = cudaEventRecord(p->layer_ev[0], st);  // the plan is done: miss lists ready
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->layer_ev[0], 0);
-            for (int l = 1; l < L && e == cudaSuccess; l++) {
-                e = hs::launch_miss_copy(p, B, nq, p->side, l, l + 1);
-                if (e == cudaSuccess) e = cudaEventRecord(p->layer_ev[l], p->side);
-            }
-        }
-        if (e == cudaSuccess) e = hs::launch_miss_copy(p, B, nq, st, 0, 1);
-    }
-    for (int l = 0; l < L && e == cudaSuccess; l++) {
-        if (copies && l > 0) e = cudaStreamWaitEvent(st, p->layer_ev[l], 0);  // layer l's rows
-        if (e == cudaSuccess)
-            e = hs::launch_attention(p, l, (const uint8_t *)q_mla + l * qstride, row_id, B, nq,
-                                     scale, (uint8_t *)out + l * ostride,
-                                     lse ? lse + (size_t)l * B * nq * H : nullptr, st, q_ready);
-    }
+    cudaError_t e = hs::launch_resolve(p, topk, B, nq, row_id, st);
+    for (int l = 0; l < L && e == cudaSuccess; l++)
+        e = hs::launch_attention(p, l, (const uint8_t *)q_mla + l * qstride, row_id, B, nq, scale,
+                                 (uint8_t *)out + l * ostride,
+                                 lse ? lse + (size_t)l * B * nq * H : nullptr, st, q_ready);
     return e;
 }
 
@@ -650,11 +629,9 @@ hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
 
 int32_t hs_step_kernel_count(const hs_pool *p, int32_t B, int32_t nq) {
     if (!p || B <= 0 || B > p->cfg.max_requests || nq <= 0 || nq > p->nq_max) return -1;
-    const int L = p->cfg.num_mla_layers;
-    // the plan, then one miss copy per layer when there is a host pool
-    const int resolve = 1 + (p->cfg.host_blocks > 0 ? L : 0);
-    return hs::indexer_kernel_count(p, B, nq) + hs::topk_kernel_count(p, B, nq) + resolve +
-           L * hs::attention_kernel_count(p, B, nq);
+    return hs::indexer_kernel_count(p, B, nq) + hs::topk_kernel_count(p, B, nq) +
+           hs::resolve_kernel_count(p, B, nq) +
+           p->cfg.num_mla_layers * hs::attention_kernel_count(p, B, nq);
 }
 
 hs_status hs_pool_get_error(hs_pool *p, hs_status *out) {

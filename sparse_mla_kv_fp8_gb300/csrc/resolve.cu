@@ -345,16 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     }
 }
 
-// Rows of layers [l0, l1) of every miss; 16-byte units, four loads in flight
-// per thread.  The grid is small (about two 128-thread CTAs per SM over all
-// requests) and each CTA light (at most 64 registers per thread, no shared
-// memory), so that it runs on the SMs beside the attention CTAs when the copy
-// of one layer overlaps the attention of the previous one: the copy is bound
-// by the host link, and a few MB in flight saturate it.
-constexpr int kCopyThreads = 128;
+// Rows of layers [l0, l1) of every miss: 16-byte units over the host link,
+// four loads in flight per thread, written to the miss's hot-buffer slot.
+constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
-__global__ void __launch_bounds__(kCopyThreads, 8) miss_copy_kernel(
+__global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(
     const int32_t *__restrict__ miss_count, const int32_t *__restrict__ miss_tok,
     const int32_t *__restrict__ miss_slot, int n, const int32_t *__restrict__ host_block_table,
     const int32_t *__restrict__ hot_blocks, const uint8_t *__restrict__ host_rows,
@@ -457,9 +453,8 @@ cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, i
     const int n = nq * p->cfg.top_k;
     if (l1 < 0) l1 = p->cfg.num_mla_layers;
     if (p->cfg.host_blocks > 0) {
-        // about two CTAs per SM in all: enough loads in flight to cover the
-        // host link's latency, few enough to leave the SMs to the attention
-        const int gx = (2 * kNumSMs + B - 1) / B;
+        // enough CTAs in flight to cover the host link's latency, at any B
+        const int gx = (4 * kNumSMs + B - 1) / B;
         dim3 grid(gx, B);
         PdlLaunch lc(grid, dim3(kCopyThreads), 0, st);
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count,

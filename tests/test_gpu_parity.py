@@ -805,11 +805,9 @@ def test_host_read_probe_copies_pinned_host_memory():
 
 
 def test_resolve_attend_overlapped_copies_equal_separate_calls():
-    """hs_resolve_attend (the miss copy split by layer, layers 1..L-1 copied on
-    the pool's second stream while the attention of the layer before runs)
-    gives bit-identical row ids, state and outputs to hs_resolve followed by
-    hs_sparse_mla_decode per layer, eager and replayed from a CUDA graph, on
-    a mixed-residency pool with misses every step."""
+    """hs_resolve_attend gives bit-identical row ids, state and outputs to
+    hs_resolve followed by hs_sparse_mla_decode per layer, eager and replayed
+    from a CUDA graph, on a mixed-residency pool with misses every step."""
     from harness import Case, Runner
     hs = _hs()
     case = Case("overlap", B=3, N=[3000, 2500, 4100], K=256, Hi=8, Di=32, H=128, L=3, T=256,
