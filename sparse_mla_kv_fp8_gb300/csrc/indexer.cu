@@ -11,7 +11,7 @@
 //   B = the request's nq*Hi query rows (same layout), staged once per CTA;
 //   D = 128 TMEM lanes x nq*Hi columns, two accumulators (double buffer).
 // Warp 0 issues TMA, warp 1 issues MMAs, warps 2-9 (one thread per token =
-// one TMEM lane) read D, apply sigma, ReLU and the head weights and write the
+// one TMEM lane) read D, apply ReLU, the head weights and sigma and write the
 // scores (coalesced): with an even nq, warps 2-5 take the even queries and
 // warps 6-9 the odd ones (two warps per TMEM sub-partition, so that each
 // SMSP has a second warp to issue while the other waits); with one query
@@ -233,39 +233,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!__all_sync(0xffffffffu, w)) break;  // the warp leaves together
             tc::fence_after_sync();
             const uint32_t tb = lane_base + acc * a.ncols;
+            // per query: sum_h w[h] * ReLU(d[h]) over 16-column groups, the
+            // next group's TMEM load in flight while this one is reduced,
+            // eight independent partial sums; sigma > 0 comes out of the sum
+            // (sigma * ReLU(d) = ReLU(sigma * d); with the power-of-two key
+            // scales of the workloads both orders are exact)
+            const int ng = a.Hi >> 4;
             for (int j = half; j < a.nq; j += jstep) {
-                // four independent partial sums (the weighted ReLU terms are summed
-                // in a tree rather than one 64-long dependent chain)
-                float part[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int h0 = 0; h0 < a.Hi; h0 += 64) {
-                    // up to four 16-column loads in flight, one wait
-                    const int n16 = min(4, (a.Hi - h0) >> 4);
-                    float v[64];
+                float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float v[2][16];
+                tc::tmem_ld16(tb + j * a.Hi, v[0]);
+                tc::tmem_ld_wait();
+                for (int g = 0; g < ng; g++) {
+                    if (g + 1 < ng) tc::tmem_ld16(tb + j * a.Hi + 16 * (g + 1), v[(g + 1) & 1]);
+                    const float *vg = v[g & 1];
+                    const float4 *wq = (const float4 *)(wsm + j * a.Hi + 16 * g);
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        if (q < n16) tc::tmem_ld16(tb + j * a.Hi + h0 + 16 * q, v + 16 * q);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (q < n16) {
-                            const float4 *wq = (const float4 *)(wsm + j * a.Hi + h0 + 16 * q);
-                            float4 wv[4];
-#pragma unroll
-                            for (int u = 0; u < 4; u++) wv[u] = wq[u];  // smem broadcast
-#pragma unroll
-                            for (int u = 0; u < 4; u++) {
-                                const float *ww = (const float *)&wv[u];
-#pragma unroll
-                                for (int e = 0; e < 4; e++) {
-                                    const float x = sig * v[16 * q + 4 * u + e];
-                                    part[e] = fmaf(ww[e], gate(x), part[e]);
-                                }
-                            }
-                        }
+                    for (int u = 0; u < 4; u++) {
+                        const float4 wv = wq[u];  // shared-memory broadcast
+                        part[2 * (u & 1)] = fmaf(wv.x, gate(vg[4 * u]), part[2 * (u & 1)]);
+                        part[2 * (u & 1) + 1] = fmaf(wv.y, gate(vg[4 * u + 1]), part[2 * (u & 1) + 1]);
+                        part[4 + 2 * (u & 1)] = fmaf(wv.z, gate(vg[4 * u + 2]), part[4 + 2 * (u & 1)]);
+                        part[5 + 2 * (u & 1)] = fmaf(wv.w, gate(vg[4 * u + 3]), part[5 + 2 * (u & 1)]);
                     }
+                    tc::tmem_ld_wait();
                 }
-                const float accs = (part[0] + part[1]) + (part[2] + part[3]);
-                if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = accs;
+                const float accs = ((part[0] + part[1]) + (part[2] + part[3])) +
+                                   ((part[4] + part[5]) + (part[6] + part[7]));
+                if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = sig * accs;
             }
             tc::fence_before_sync();
             tc::mbar_arrive(&tempty[acc]);
