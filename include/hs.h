@@ -184,14 +184,18 @@ hs_status hs_request_open(hs_pool *pool, int32_t req, hs_mode mode);
 
 /* Append n tokens to request `req`.  mla_rows: [n][L][R] bytes; idx_keys:
  * [n][Di] elements of the indexer format; idx_scale: [n] fp32 (NULL = 1.0).
- * Each pointer may be host or device memory.  The rows are written to the GPU
- * pool when their page is resident (full mode: every page; mixed: the tail
- * window) and to the pinned host pool when it exists (a full-residency page
- * thus already has its host copy, which later lets it leave the GPU without a
- * copy: "Les trois états de résidence").  In mixed mode pages that slide out
- * of the tail window give their GPU block back.  Synchronises `stream` before
- * returning (off the decode path).  HS_ERR_CAPACITY: no GPU block;
- * HS_ERR_HOST_POOL_FULL: no host block; HS_ERR_INVALID_ARG: past max_tokens. */
+ * Each pointer may be host or device memory.  Rows of a page that is resident
+ * (full mode: every page; mixed: the tail window) are written to the GPU pool
+ * only; rows of a page that is not are written to the pinned host pool.  The
+ * host copy of a resident page is left to hs_precopy ("Les trois états de
+ * résidence": completed prefix pages are copied to the host ahead of time);
+ * a page that slides out of the tail window (mixed mode) gets it here, on
+ * `stream`, when no pre-copy has made it, and then gives its GPU block back.
+ * With a host pool, every page also reserves its host block here.
+ * Synchronises `stream` before returning (off the decode path); never waits
+ * for pre-copies still in flight unless a page they cover leaves the GPU.
+ * HS_ERR_CAPACITY: no GPU block; HS_ERR_HOST_POOL_FULL: no host block;
+ * HS_ERR_INVALID_ARG: past max_tokens.  Nothing changes on these errors. */
 hs_status hs_append(hs_pool *pool, int32_t req, const void *mla_rows,
                     const void *idx_keys, const float *idx_scale, int32_t n,
                     cudaStream_t stream);
@@ -199,17 +203,62 @@ hs_status hs_append(hs_pool *pool, int32_t req, const void *mla_rows,
 /* Change the residency of a request between steps ("Les trois états de
  * résidence": full, mixed, zero), in any direction.  Pages that the new mode
  * keeps off the GPU (outside the tail window in mixed mode, all of them in
- * zero mode) release their GPU blocks; pages it keeps on the GPU that are not
- * there get a block and their rows copied back from the host pool; a hot
- * buffer is leased when leaving full residency and returned when entering
- * it; the hot buffer starts empty.  Needs a host pool (HS_ERR_INVALID_ARG
- * otherwise); HS_ERR_CAPACITY, with nothing changed, when the pool lacks the
- * blocks.  Synchronises `stream`. */
+ * zero mode) release their GPU blocks, after their host copy is written on
+ * `stream` (or `stream` is ordered after the pre-copy that wrote it); pages it
+ * keeps on the GPU that are not there get a block and their rows copied back
+ * from the host pool; a hot buffer is leased when leaving full residency and
+ * returned when entering it; the hot buffer starts empty.  Needs a host pool
+ * (HS_ERR_INVALID_ARG otherwise); HS_ERR_CAPACITY, with nothing changed, when
+ * the pool lacks the blocks.  The pressure policy below stops managing the
+ * request.  Synchronises `stream`. */
 hs_status hs_request_set_mode(hs_pool *pool, int32_t req, hs_mode mode,
                               cudaStream_t stream);
 
-/* Release every GPU and host block of the request. */
+/* Release every GPU and host block of the request (after any pre-copy still
+ * in flight, which may touch them, has finished). */
 hs_status hs_request_close(hs_pool *pool, int32_t req);
+
+/* Pre-copy of completed pages ("Les trois états de résidence": in full
+ * residency the completed prefix pages are copied to the host ahead of time,
+ * so that they can later give their GPU slot up with no further copy).
+ * Enqueues on `stream`, normally a side stream of the caller's, one
+ * device->host copy per run of neighbouring blocks, covering every completed
+ * page (all P tokens appended) of every open request that is on the GPU and
+ * has no host copy yet.  The copies run on the copy engine, not the SMs, and
+ * the call returns without waiting for them: decode steps go on meanwhile
+ * (they only read those blocks).  Calls that later take one of those blocks
+ * away (hs_append's tail roll-out, hs_request_set_mode, the pressure calls)
+ * order their own stream after these copies on the device; hs_request_close
+ * and hs_pool_destroy wait for them on the host.  Each call also orders
+ * `stream` after the previous batch.  *pages (may be NULL): pages enqueued.
+ * HS_ERR_INVALID_ARG without a host pool. */
+hs_status hs_precopy(hs_pool *pool, cudaStream_t stream, int64_t *pages);
+
+/* Pressure policy ("Ce qui se passe": the cache stays on the GPU while there
+ * is room, and offloading applies only under real memory pressure; the pages
+ * give no policy, so this is a reading).  Append as hs_append; when the
+ * append does not fit in the free GPU blocks, flip to mixed residency the
+ * full-residency request with the most resident pages among those whose flip
+ * frees blocks (lower id on ties), and retry, until the append fits.  The
+ * blocks a flip frees join the shared pool: the flipped request's own hot
+ * buffer and any other request's next pages or hot buffer come out of it.
+ * flipped: host [max_requests] (may be NULL) receives the flipped ids in
+ * order, *n_flipped their number (flips stay done on error).
+ * HS_ERR_CAPACITY when no flip is left that would free a block. */
+hs_status hs_append_pressure(hs_pool *pool, int32_t req, const void *mla_rows,
+                             const void *idx_keys, const float *idx_scale,
+                             int32_t n, cudaStream_t stream, int32_t *flipped,
+                             int32_t *n_flipped);
+
+/* The other half of the pressure policy (reading): return requests that
+ * hs_append_pressure flipped to full residency, the last flipped first, while
+ * the free GPU blocks cover the pages that come back (less the hot buffer
+ * given up) plus one block per open request (room for each one's next page,
+ * so a return is not undone by the next appends).  Stops at the first that
+ * does not fit.  restored: host [max_requests] (may be NULL), *n_restored
+ * their number. */
+hs_status hs_pool_relieve(hs_pool *pool, cudaStream_t stream, int32_t *restored,
+                          int32_t *n_restored);
 
 /* Number of free blocks left in the device pool. */
 int64_t hs_pool_free_gpu_blocks(const hs_pool *pool);

@@ -209,6 +209,86 @@ class HotState:
 
 
 # --------------------------------------------------------------------------
+# pool pressure  ("Ce qui se passe": the cache stays on the GPU while there is
+# room and is offloaded only under real pressure; the pages give no policy,
+# so the rule below is a reading)
+# --------------------------------------------------------------------------
+def gpu_blocks(mode: int, N: int, T: int, P: int, hot_pages: int) -> int:
+    """GPU blocks a request of N tokens holds in `mode`: its resident pages
+    (page_resident), plus its hot buffer of hot_pages blocks unless it is in
+    full residency."""
+    npages = (N + P - 1) // P
+    return int(page_resident(mode, N, T, P)[:npages].sum()) + (0 if mode == FULL else hot_pages)
+
+
+class PressurePolicy:
+    """Block accounting of a device pool of `cap` blocks shared by requests,
+    and the pressure reading.
+
+    An append that would take the blocks in use past `cap` first flips to
+    mixed residency the full-residency request with the most pages among
+    those whose flip lowers its block count (lower id on ties), again and
+    again until the append fits.  relieve() returns flipped requests to full
+    residency, the last flipped first, while the free blocks cover the blocks
+    the return adds plus one block per open request; it stops at the first
+    that does not fit.  A request set by hand or closed leaves the policy."""
+
+    def __init__(self, cap: int, T: int, P: int, hot_pages: int):
+        self.cap, self.T, self.P, self.hot_pages = cap, T, P, hot_pages
+        self.mode: dict[int, int] = {}
+        self.N: dict[int, int] = {}
+        self.flipped: list[int] = []
+
+    def blocks(self, r: int, mode: int | None = None, N: int | None = None) -> int:
+        return gpu_blocks(self.mode[r] if mode is None else mode, self.N[r] if N is None else N,
+                          self.T, self.P, self.hot_pages)
+
+    def used(self) -> int:
+        return sum(self.blocks(r) for r in self.mode)
+
+    def open(self, r: int, mode: int = FULL):
+        self.mode[r], self.N[r] = mode, 0
+
+    def close(self, r: int):
+        del self.mode[r], self.N[r]
+        if r in self.flipped:
+            self.flipped.remove(r)
+
+    def set_mode(self, r: int, mode: int):
+        self.mode[r] = mode
+        if r in self.flipped:
+            self.flipped.remove(r)
+
+    def append(self, r: int, n: int):
+        """Returns (flipped ids in order, status)."""
+        flips = []
+        while self.used() - self.blocks(r) + self.blocks(r, N=self.N[r] + n) > self.cap:
+            cands = [x for x in sorted(self.mode) if self.mode[x] == FULL
+                     and self.blocks(x, MIXED) < self.blocks(x, FULL)]
+            if not cands:
+                return flips, ERR_CAPACITY
+            most = max((self.N[x] + self.P - 1) // self.P for x in cands)
+            x = min(x for x in cands if (self.N[x] + self.P - 1) // self.P == most)
+            self.mode[x] = MIXED
+            self.flipped.append(x)
+            flips.append(x)
+        self.N[r] += n
+        return flips, OK
+
+    def relieve(self) -> list[int]:
+        back = []
+        while self.flipped:
+            x = self.flipped[-1]
+            need = self.blocks(x, FULL) - self.blocks(x)
+            if self.cap - self.used() < need + len(self.mode):
+                break
+            self.mode[x] = FULL
+            self.flipped.pop()
+            back.append(x)
+        return back
+
+
+# --------------------------------------------------------------------------
 # sparse MLA attention  ("Ce qui se passe")
 # --------------------------------------------------------------------------
 def attention(fmt: int, q_bf16: np.ndarray, rows: np.ndarray, tau: float,

@@ -108,6 +108,12 @@ struct hs_pool {
     std::vector<int32_t> hot_blocks;
     std::vector<int32_t> free_gpu;
     std::vector<int32_t> free_host;
+    // host_ok[req * max_pages + page]: the pinned host pool holds every token
+    // appended to the page so far (or a pre-copy of it is enqueued)
+    std::vector<uint8_t> host_ok;
+    cudaEvent_t precopy_ev;  // recorded after the last pre-copy batch
+    bool precopy_pending;    // a pre-copy batch was enqueued and not waited for
+    std::vector<int32_t> policy_flipped;  // requests the pressure policy flipped, in order
 };
 
 namespace hs {

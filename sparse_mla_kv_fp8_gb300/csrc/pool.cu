@@ -182,11 +182,85 @@ int first_tail_page(const hs_pool *p, int mode, int64_t N) {
     return (int)(s / P);
 }
 
+size_t block_bytes(const hs_pool *p) {
+    return (size_t)p->cfg.num_mla_layers * p->cfg.page_tokens * p->R;
+}
+
+// Device->host copies of whole blocks on `st` (the copy engine), given as
+// (GPU block, host block) pairs; runs of neighbouring pairs go as one copy.
+cudaError_t copy_blocks_to_host(hs_pool *p, const std::vector<std::pair<int32_t, int32_t>> &pairs,
+                                cudaStream_t st) {
+    const size_t bb = block_bytes(p);
+    cudaError_t e = cudaSuccess;
+    for (size_t i = 0; i < pairs.size() && e == cudaSuccess;) {
+        size_t j = i + 1;
+        while (j < pairs.size() && pairs[j].first == pairs[j - 1].first + 1 &&
+               pairs[j].second == pairs[j - 1].second + 1)
+            j++;
+        e = cudaMemcpyAsync(p->host_base + (size_t)pairs[i].second * bb,
+                            p->d.rows + (size_t)pairs[i].first * bb, (j - i) * bb,
+                            cudaMemcpyDeviceToHost, st);
+        i = j;
+    }
+    return e;
+}
+
+// The pages of `req` listed in `pages` are about to give their GPU block
+// back: on `st`, write the host copy of those that have none, and order `st`
+// after the pre-copies of the others (a device-side wait, no host wait).
+cudaError_t secure_host_copies(hs_pool *p, int32_t req, const std::vector<int> &pages,
+                               cudaStream_t st) {
+    const size_t mp = p->max_pages;
+    const int32_t *bt = p->block_table.data() + req * mp;
+    const int32_t *hbt = p->host_block_table.data() + req * mp;
+    uint8_t *ok = p->host_ok.data() + req * mp;
+    std::vector<std::pair<int32_t, int32_t>> pairs;
+    bool wait = false;
+    for (int pg : pages) {
+        if (ok[pg]) wait = true;
+        else pairs.push_back({bt[pg], hbt[pg]});
+    }
+    cudaError_t e = cudaSuccess;
+    if (wait && p->precopy_pending) e = cudaStreamWaitEvent(st, p->precopy_ev, 0);
+    if (e == cudaSuccess) e = copy_blocks_to_host(p, pairs, st);
+    if (e == cudaSuccess)
+        for (int pg : pages) ok[pg] = 1;
+    return e;
+}
+
+void forget_policy(hs_pool *p, int32_t req) {
+    auto &v = p->policy_flipped;
+    for (size_t i = 0; i < v.size(); i++)
+        if (v[i] == req) {
+            v.erase(v.begin() + i);
+            return;
+        }
+}
+
+int resident_pages(const hs_pool *p, int32_t req) {
+    const size_t mp = p->max_pages;
+    const int32_t *bt = p->block_table.data() + req * mp;
+    const int npages = (int)((p->seq_len[req] + p->cfg.page_tokens - 1) / p->cfg.page_tokens);
+    int n = 0;
+    for (int pg = 0; pg < npages; pg++) n += bt[pg] >= 0;
+    return n;
+}
+
+// GPU blocks request `req` would hold in `mode` at its current length.
+int64_t blocks_in_mode(const hs_pool *p, int32_t req, int mode) {
+    const int P = p->cfg.page_tokens;
+    const int64_t N = p->seq_len[req];
+    const int npages = (int)((N + P - 1) / P);
+    const int tail0 = first_tail_page(p, mode, N);
+    const int64_t res = std::max(0, npages - std::min(tail0, npages));
+    return res + (mode == HS_FULL ? 0 : p->hot_pages);
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 101; }
+int32_t hs_abi_version(void) { return 102; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -290,6 +364,9 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->block_table.assign(maxR * p->max_pages, -1);
     p->host_block_table.assign(maxR * p->max_pages, -1);
     p->hot_blocks.assign(maxR * p->hot_pages, -1);
+    p->host_ok.assign(maxR * p->max_pages, 0);
+    p->precopy_pending = false;
+    p->precopy_ev = nullptr;
     p->free_gpu.resize(cfg->gpu_blocks);
     for (int64_t i = 0; i < cfg->gpu_blocks; i++) p->free_gpu[i] = (int32_t)(cfg->gpu_blocks - 1 - i);
     p->free_host.resize(cfg->host_blocks);
@@ -312,16 +389,24 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     ms(p->d.stats, 0, 32);
     ms(p->d.miss_count, 0, maxR * 4);
     if (e == cudaSuccess) e = hs::setup_kernel_attributes(p);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->precopy_ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
-        delete p;
+        hs_pool_destroy(p);
         return HS_ERR_CUDA;
     }
     *out = p;
     return HS_OK;
 }
 
-void hs_pool_destroy(hs_pool *pool) { delete pool; }
+void hs_pool_destroy(hs_pool *pool) {
+    if (!pool) return;
+    if (pool->precopy_ev) {
+        if (pool->precopy_pending) cudaEventSynchronize(pool->precopy_ev);  // copies into the host arena
+        cudaEventDestroy(pool->precopy_ev);
+    }
+    delete pool;
+}
 
 hs_status hs_pool_get_layout(const hs_pool *pool, hs_layout *out) {
     if (!pool || !out) return HS_ERR_INVALID_ARG;
@@ -386,35 +471,41 @@ hs_status hs_append(hs_pool *p, int32_t req, const void *mla_rows, const void *i
             p->free_host.pop_back();
         }
     }
-    // release pages that left the tail window (mixed mode) before leasing
-    if (mode == HS_MIXED)
+    cudaError_t e = cudaSuccess;
+    // pages that left the tail window (mixed mode): host copy first (the
+    // page's earlier rows may live on the GPU only), then the block goes back
+    if (mode == HS_MIXED) {
+        std::vector<int> leaving;
         for (int pg = 0; pg < std::min(tail0, p0 + 1); pg++)
-            if (bt[pg] >= 0) {
-                p->free_gpu.push_back(bt[pg]);
-                bt[pg] = -1;
-            }
+            if (bt[pg] >= 0) leaving.push_back(pg);
+        e = secure_host_copies(p, req, leaving, st);
+        for (int pg : leaving) {
+            p->free_gpu.push_back(bt[pg]);
+            bt[pg] = -1;
+        }
+    }
     for (int pg = p0; pg <= p1; pg++)
         if (pg >= tail0 && bt[pg] < 0) {
             bt[pg] = p->free_gpu.back();
             p->free_gpu.pop_back();
         }
-    cudaError_t e = cudaSuccess;
+    // rows of a resident page go to the GPU only (its host copy is left to
+    // hs_precopy, or made when the page leaves); the others to the host pool
+    uint8_t *ok = p->host_ok.data() + req * mp;
     const uint8_t *src = (const uint8_t *)mla_rows;
     for (int pg = p0; pg <= p1 && e == cudaSuccess; pg++) {
         const int64_t t0 = std::max<int64_t>(N0, (int64_t)pg * P);
         const int64_t t1 = std::min<int64_t>(N1, (int64_t)(pg + 1) * P);
         const size_t cnt = (size_t)(t1 - t0);
+        const bool on_gpu = bt[pg] >= 0;
+        uint8_t *base = on_gpu ? p->d.rows + (size_t)bt[pg] * block_bytes(p)
+                               : p->host_base + (size_t)hbt[pg] * block_bytes(p);
         for (int l = 0; l < L && e == cudaSuccess; l++) {
             const uint8_t *s = src + ((size_t)(t0 - N0) * L + l) * R;
-            if (bt[pg] >= 0) {
-                uint8_t *dst = p->d.rows + (((size_t)bt[pg] * L + l) * P + (t0 % P)) * R;
-                e = cudaMemcpy2DAsync(dst, R, s, (size_t)L * R, R, cnt, cudaMemcpyDefault, st);
-            }
-            if (e == cudaSuccess && has_host) {
-                uint8_t *dst = p->host_base + (((size_t)hbt[pg] * L + l) * P + (t0 % P)) * R;
-                e = cudaMemcpy2DAsync(dst, R, s, (size_t)L * R, R, cnt, cudaMemcpyDefault, st);
-            }
+            uint8_t *dst = base + ((size_t)l * P + (t0 % P)) * R;
+            e = cudaMemcpy2DAsync(dst, R, s, (size_t)L * R, R, cnt, cudaMemcpyDefault, st);
         }
+        ok[pg] = on_gpu ? 0 : 1;
     }
     const size_t krow = (size_t)p->cfg.idx_dim * p->idx_esize;
     if (e == cudaSuccess)
@@ -436,7 +527,7 @@ hs_status hs_append(hs_pool *p, int32_t req, const void *mla_rows, const void *i
     return cuda_status(e);
 }
 
-hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_t st) {
+static hs_status set_mode(hs_pool *p, int32_t req, int mode, cudaStream_t st) {
     if (!req_ok(p, req) || p->mode[req] < 0) return HS_ERR_INVALID_ARG;
     if (mode != HS_FULL && mode != HS_MIXED && mode != HS_ZERO) return HS_ERR_INVALID_ARG;
     const int cur = p->mode[req];
@@ -446,7 +537,7 @@ hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_
     int32_t *bt = p->block_table.data() + req * mp;
     int32_t *hbt = p->host_block_table.data() + req * mp;
     int32_t *hot = p->hot_blocks.data() + (size_t)req * p->hot_pages;
-    const int P = p->cfg.page_tokens, L = p->cfg.num_mla_layers, R = p->R;
+    const int P = p->cfg.page_tokens;
     const int64_t N = p->seq_len[req];
     const int npages = (int)((N + P - 1) / P);
     const int tail0 = first_tail_page(p, mode, N);  // pages >= tail0 are resident afterwards
@@ -460,25 +551,27 @@ hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_
     const int hot_in = (cur == HS_FULL) ? p->hot_pages : 0;   // a hot buffer to lease
     const int hot_out = (mode == HS_FULL) ? p->hot_pages : 0;  // a hot buffer to return
     if ((int64_t)p->free_gpu.size() + leave + hot_out < (int64_t)join + hot_in) return HS_ERR_CAPACITY;
+    // pages leaving the GPU: their host copies first, then their blocks
+    std::vector<int> leaving;
     for (int pg = 0; pg < npages; pg++)
-        if (pg < tail0 && bt[pg] >= 0) {
-            p->free_gpu.push_back(bt[pg]);
-            bt[pg] = -1;
-        }
+        if (pg < tail0 && bt[pg] >= 0) leaving.push_back(pg);
+    cudaError_t e = secure_host_copies(p, req, leaving, st);
+    for (int pg : leaving) {
+        p->free_gpu.push_back(bt[pg]);
+        bt[pg] = -1;
+    }
     if (hot_out)
         for (int i = 0; i < p->hot_pages; i++) {
             p->free_gpu.push_back(hot[i]);
             hot[i] = -1;
         }
-    cudaError_t e = cudaSuccess;
-    const size_t block_bytes = (size_t)L * P * R;
+    const size_t bb = block_bytes(p);
     for (int pg = tail0; pg < npages && e == cudaSuccess; pg++)
         if (bt[pg] < 0) {  // back onto the GPU: one block copied from the host pool
             bt[pg] = p->free_gpu.back();
             p->free_gpu.pop_back();
-            e = cudaMemcpyAsync(p->d.rows + (size_t)bt[pg] * block_bytes,
-                                p->host_base + (size_t)hbt[pg] * block_bytes, block_bytes,
-                                cudaMemcpyDefault, st);
+            e = cudaMemcpyAsync(p->d.rows + (size_t)bt[pg] * bb, p->host_base + (size_t)hbt[pg] * bb,
+                                bb, cudaMemcpyHostToDevice, st);
         }
     if (hot_in)
         for (int i = 0; i < p->hot_pages; i++) {
@@ -492,9 +585,20 @@ hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_
     return cuda_status(e);
 }
 
+hs_status hs_request_set_mode(hs_pool *p, int32_t req, hs_mode mode, cudaStream_t st) {
+    hs_status s = set_mode(p, req, mode, st);
+    if (s == HS_OK) forget_policy(p, req);  // the caller now decides this request's residency
+    return s;
+}
+
 hs_status hs_request_close(hs_pool *p, int32_t req) {
     if (!req_ok(p, req) || p->mode[req] < 0) return HS_ERR_INVALID_ARG;
     const size_t mp = p->max_pages;
+    // a pre-copy may still read this request's blocks or write its host blocks
+    if (p->precopy_pending && cudaEventSynchronize(p->precopy_ev) != cudaSuccess) return HS_ERR_CUDA;
+    p->precopy_pending = false;
+    std::fill(p->host_ok.begin() + req * mp, p->host_ok.begin() + (req + 1) * mp, 0);
+    forget_policy(p, req);
     for (size_t pg = 0; pg < mp; pg++) {
         int32_t &g = p->block_table[req * mp + pg];
         if (g >= 0) p->free_gpu.push_back(g);
@@ -514,6 +618,89 @@ hs_status hs_request_close(hs_pool *p, int32_t req) {
     if (e == cudaSuccess) e = upload_tables(p, req, 0);
     if (e == cudaSuccess) e = cudaStreamSynchronize(0);
     return cuda_status(e);
+}
+
+hs_status hs_precopy(hs_pool *p, cudaStream_t st, int64_t *pages) {
+    if (pages) *pages = 0;
+    if (!p || p->cfg.host_blocks == 0) return HS_ERR_INVALID_ARG;
+    const int P = p->cfg.page_tokens;
+    const size_t mp = p->max_pages;
+    std::vector<std::pair<int32_t, int32_t>> pairs;
+    std::vector<size_t> marked;
+    for (int32_t r = 0; r < p->cfg.max_requests; r++) {
+        if (p->mode[r] < 0) continue;
+        const int complete = (int)(p->seq_len[r] / P);
+        for (int pg = 0; pg < complete; pg++) {
+            const size_t i = r * mp + pg;
+            if (p->block_table[i] >= 0 && !p->host_ok[i] && p->host_block_table[i] >= 0) {
+                pairs.push_back({p->block_table[i], p->host_block_table[i]});
+                marked.push_back(i);
+            }
+        }
+    }
+    if (pairs.empty()) return HS_OK;
+    // one event then covers every batch so far, whichever stream each used
+    cudaError_t e = p->precopy_pending ? cudaStreamWaitEvent(st, p->precopy_ev, 0) : cudaSuccess;
+    if (e == cudaSuccess) e = copy_blocks_to_host(p, pairs, st);
+    if (e == cudaSuccess) e = cudaEventRecord(p->precopy_ev, st);
+    if (e != cudaSuccess) return HS_ERR_CUDA;
+    p->precopy_pending = true;
+    for (size_t i : marked) p->host_ok[i] = 1;
+    if (pages) *pages = (int64_t)pairs.size();
+    return HS_OK;
+}
+
+hs_status hs_append_pressure(hs_pool *p, int32_t req, const void *mla_rows, const void *idx_keys,
+                             const float *idx_scale, int32_t n, cudaStream_t st, int32_t *flipped,
+                             int32_t *n_flipped) {
+    if (n_flipped) *n_flipped = 0;
+    if (!req_ok(p, req) || p->mode[req] < 0) return HS_ERR_INVALID_ARG;
+    int nf = 0;
+    for (;;) {
+        hs_status s = hs_append(p, req, mla_rows, idx_keys, idx_scale, n, st);
+        if (s != HS_ERR_CAPACITY || p->cfg.host_blocks == 0) return s;
+        // the full-residency request with the most resident pages whose flip
+        // frees blocks, lower id on ties
+        int32_t x = -1;
+        int best = -1;
+        for (int32_t r = 0; r < p->cfg.max_requests; r++) {
+            if (p->mode[r] != HS_FULL) continue;
+            if (blocks_in_mode(p, r, HS_MIXED) >= blocks_in_mode(p, r, HS_FULL)) continue;
+            const int res = resident_pages(p, r);
+            if (res > best) {
+                best = res;
+                x = r;
+            }
+        }
+        if (x < 0) return HS_ERR_CAPACITY;
+        s = set_mode(p, x, HS_MIXED, st);
+        if (s != HS_OK) return s;
+        p->policy_flipped.push_back(x);
+        if (flipped) flipped[nf] = x;
+        nf++;
+        if (n_flipped) *n_flipped = nf;
+    }
+}
+
+hs_status hs_pool_relieve(hs_pool *p, cudaStream_t st, int32_t *restored, int32_t *n_restored) {
+    if (n_restored) *n_restored = 0;
+    if (!p) return HS_ERR_INVALID_ARG;
+    int64_t open = 0;
+    for (int32_t r = 0; r < p->cfg.max_requests; r++) open += p->mode[r] >= 0;
+    int nr = 0;
+    while (!p->policy_flipped.empty()) {
+        const int32_t x = p->policy_flipped.back();
+        // net blocks the return takes: every page back, the hot buffer given up
+        const int64_t need = blocks_in_mode(p, x, HS_FULL) - blocks_in_mode(p, x, p->mode[x]);
+        if ((int64_t)p->free_gpu.size() < need + open) break;  // keep one page per request free
+        hs_status s = set_mode(p, x, HS_FULL, st);
+        if (s != HS_OK) return s;
+        p->policy_flipped.pop_back();
+        if (restored) restored[nr] = x;
+        nr++;
+        if (n_restored) *n_restored = nr;
+    }
+    return HS_OK;
 }
 
 static bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15) == 0; }

@@ -80,6 +80,9 @@ hs_request_open = _decl("hs_request_open", _i32, [_P, _i32, _i32])
 hs_append = _decl("hs_append", _i32, [_P, _i32, _P, _P, _P, _i32, _P])
 hs_request_set_mode = _decl("hs_request_set_mode", _i32, [_P, _i32, _i32, _P])
 hs_request_close = _decl("hs_request_close", _i32, [_P, _i32])
+hs_precopy = _decl("hs_precopy", _i32, [_P, _P, _P])
+hs_append_pressure = _decl("hs_append_pressure", _i32, [_P, _i32, _P, _P, _P, _i32, _P, _P, _P])
+hs_pool_relieve = _decl("hs_pool_relieve", _i32, [_P, _P, _P, _P])
 hs_indexer_score = _decl("hs_indexer_score", _i32, [_P, _P, _P, _i32, _i32, _P, _i64, _P])
 hs_topk = _decl("hs_topk", _i32, [_P, _P, _i64, _i32, _i32, _P, _P])
 hs_indexer_topk = _decl("hs_indexer_topk", _i32, [_P, _P, _P, _i32, _i32, _P, _P])
@@ -219,6 +222,32 @@ class Pool:
 
     def close_request(self, req: int):
         check(hs_request_close(self.handle, req), "hs_request_close")
+
+    def precopy(self, stream=None) -> int:
+        """Enqueue the host pre-copy of completed resident pages on `stream`;
+        returns the number of pages enqueued (nothing is waited for)."""
+        n = ctypes.c_int64()
+        check(hs_precopy(self.handle, _stream(stream), ctypes.byref(n)), "hs_precopy")
+        return n.value
+
+    def append_pressure(self, req: int, rows, keys, scale=None, stream=None) -> list:
+        """Append under the pressure policy; returns the requests it flipped."""
+        n = rows.shape[0]
+        ids = (_i32 * self.cfg.max_requests)()
+        nf = _i32()
+        check(hs_append_pressure(self.handle, req, _ptr(rows, "rows"), _ptr(keys, "keys"),
+                                 _ptr(scale, "scale"), n, _stream(stream), ids, ctypes.byref(nf)),
+              "hs_append_pressure")
+        return list(ids[:nf.value])
+
+    def relieve(self, stream=None) -> list:
+        """Return policy-flipped requests to full residency while blocks allow;
+        returns the requests restored."""
+        ids = (_i32 * self.cfg.max_requests)()
+        nr = _i32()
+        check(hs_pool_relieve(self.handle, _stream(stream), ids, ctypes.byref(nr)),
+              "hs_pool_relieve")
+        return list(ids[:nr.value])
 
     def free_gpu_blocks(self) -> int:
         return int(hs_pool_free_gpu_blocks(self.handle))

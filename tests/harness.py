@@ -221,6 +221,41 @@ class Runner:
         self.sig[b] = torch.cat([self.sig[b], sg])
         self.N[b] += n
 
+    def append_pressure(self, b, n, policy):
+        """Append the next n tokens of request b through the library's
+        pressure policy.  The requests it flips must be the ones the oracle's
+        reading (oracle.PressurePolicy) flips; they restart with an empty hot
+        buffer on the oracle side too."""
+        c = self.c
+        n0 = self.N[b]
+        r = wl.mla_rows(c.seed, b, n0, n, c.L, c.row_fmt, device=self.dev)
+        k = wl.idx_keys(c.seed, b, n0, n, c.Di, c.idx_fmt, device=self.dev)
+        sg = (wl.idx_sigma(n, self.dev, seed=c.seed, b=b, t0=n0) if c.sigma
+              else wl.idx_sigma(n, self.dev))
+        want, status = policy.append(b, n)
+        assert status == oracle.OK
+        got = self.pool.append_pressure(b, r, k, sg)
+        assert got == want, f"{c.name}: flips {got}, the policy's reading gives {want}"
+        for x in got:
+            self.modes[x] = hs.HS_MIXED
+            self.hot[x] = oracle.HotState(self.C, self.max_tokens)
+        self.rows[b] = torch.cat([self.rows[b], r])
+        self.keys[b] = torch.cat([self.keys[b], k])
+        self.sig[b] = torch.cat([self.sig[b], sg])
+        self.N[b] += n
+        return got
+
+    def relieve(self, policy):
+        """The library's return of flipped requests, checked against the
+        oracle's reading; returned requests read every page in place."""
+        want = policy.relieve()
+        got = self.pool.relieve()
+        assert got == want, f"{self.c.name}: returned {got}, the policy's reading gives {want}"
+        for x in got:
+            self.modes[x] = hs.HS_FULL
+            self.hot[x] = oracle.HotState(self.C, self.max_tokens)
+        return got
+
     def _locate(self, rid, st):
         """Pool row ids -> (kind, value) with the request's own tables:
         1 = resident token, 2 = hot slot, 0 = padding."""

@@ -213,14 +213,21 @@ def test_zero_residency_4x1M_64_steps(hs):
 
 
 def test_agentic_growth_16x13_turns(hs):
-    """The agentic growth trace at full size.  Every step: no device error and
-    every selected row id of every request reads its own token's bytes (all
-    layers, every 8th step; the first and last step of each turn always).  Two
-    requests (the first to flip and one that flips last or never) are
+    """The agentic growth trace at full size.  Every append goes through the
+    library's pressure policy (hs_append_pressure), whose flips must be the
+    oracle's reading of it (oracle.PressurePolicy: when an append does not
+    fit, the full-residency request with the most pages flips first); after
+    every round of appends the completed pages are pre-copied to the host on
+    a side stream (hs_precopy).  Every step: no device error and every
+    selected row id of every request reads its own token's bytes (all
+    layers, every 8th step; the first and last step of each turn always).
+    Two requests (the first to flip and one that flips last or never) are
     followed by the oracle on every step: exact row locations and hot-buffer
     state, and at each turn's first and last step the exact top-K and
-    sampled attention.  Flips follow the trace's policy: when an append does
-    not fit, the full-residency request with the most pages flips first."""
+    sampled attention.  At the end two requests finish (closed) and
+    hs_pool_relieve returns the flipped requests as the reading says; their
+    pages are back on the GPU, byte for byte, and one more step over the
+    remaining requests matches the oracle."""
     from fullsize import locate
     B, K, L, P, T, H, Hi, Di, seed = 16, 2048, 4, 64, 4096, 128, 64, 128, 0
     prompt0, prompt, decode, turns = 74160, 753, 220, 13
@@ -241,31 +248,26 @@ def test_agentic_growth_16x13_turns(hs):
     keys = [wl.idx_keys(seed, b, 0, final, Di, wl.IDX_E4M3, device=dev) for b in range(B)]
     follow = {}   # request -> oracle HotState (from its flip on)
     flips = []
-
-    def flip_largest():
-        full = [b for b in range(B) if modes[b] == hs.HS_FULL]
-        if not full:
-            return False
-        x = full[int(np.argmax([N[b] for b in full]))]  # most pages, lowest id on ties
-        pool.set_mode(x, hs.HS_MIXED)
-        modes[x] = hs.HS_MIXED
-        flips.append(x)
-        if len(flips) == 1:
-            follow[x] = oracle.HotState(C, max_tokens)
-        return True
+    pol = oracle.PressurePolicy(cap=20000, T=T, P=P, hot_pages=C // P)
+    side = torch.cuda.Stream()
 
     def append(b, n):
-        while True:
-            try:
-                pool.append(b, truth[b][N[b]:N[b] + n], keys[b][N[b]:N[b] + n])
-                break
-            except hs.HSError as e:
-                assert e.status == hs.HS_ERR_CAPACITY and flip_largest()
+        want, status = pol.append(b, n)
+        assert status == oracle.OK
+        got = pool.append_pressure(b, truth[b][N[b]:N[b] + n], keys[b][N[b]:N[b] + n])
+        assert got == want, (b, N[b], got, want)
+        for x in got:
+            modes[x] = hs.HS_MIXED
+            flips.append(x)
+            if len(flips) == 1:
+                follow[x] = oracle.HotState(C, max_tokens)
         N[b] += n
 
     for b in range(B):
         pool.open(b, hs.HS_FULL)
+        pol.open(b)
         append(b, prompt0)
+    assert pool.precopy(side) == B * (prompt0 // P)
     torch.cuda.synchronize()
     last = B - 1  # followed from the start; flips (if at all) late, being the highest id
     follow[last] = None
@@ -280,6 +282,7 @@ def test_agentic_growth_16x13_turns(hs):
         if turn:
             for b in range(B):
                 append(b, prompt)
+            pool.precopy(side)
         for d in range(decode):
             step += 1
             edge = d == 0 or d == decode - 1
@@ -328,9 +331,45 @@ def test_agentic_growth_16x13_turns(hs):
                     _check_attention(truth[b], qm, out, lse, tk[b, 0], b, 0, l)
             for b in range(B):
                 append(b, 1)  # the decoded token joins the tail
+            pool.precopy(side)
     torch.cuda.synchronize()
     assert N == [final] * B
     assert flips and flips[0] == 0, flips  # every request is the same size: lowest id first
     assert hs.HS_FULL in modes              # only as many flips as the cap needs
     assert checked_topk >= 2 * turns
+    # two conversations end; the flipped requests come back as blocks free up
+    back = []
+    for x in (B - 1, B - 2):
+        assert modes[x] == hs.HS_FULL
+        pool.close_request(x)
+        pol.close(x)
+        want = pol.relieve()
+        got = pool.relieve()
+        assert got == want, (x, got, want)
+        back += got
+    assert sorted(back) == sorted(flips), (back, flips)
+    prow = pool.rows_view()
+    for x in back:
+        st = pool.dump_state(x)
+        bt = st["block_table"][:pages]
+        assert (bt >= 0).all() and (st["hot_blocks"] < 0).all()
+        tok = torch.arange(final, device=dev)
+        blk = torch.from_numpy(bt.astype(np.int64)).to(dev)[tok // P]
+        assert torch.equal(prow[blk, :, tok % P], truth[x]), f"request {x} after its return"
+    B2 = B - 2
+    step += 1
+    q = torch.stack([wl.idx_query(seed, b, step, 1, Hi, Di, wl.IDX_E4M3, dev) for b in range(B2)])
+    w = torch.stack([wl.idx_weights(seed, b, step, 1, Hi, dev) for b in range(B2)])
+    qm = wl.mla_query(seed, step, B2, 1, H, L, dev).contiguous()
+    out2, lse2 = out[:, :B2].contiguous(), lse[:, :B2].contiguous()
+    topk2, rid2 = topk[:B2].contiguous(), rid[:B2].contiguous()
+    pool.step(B2, 1, q.contiguous(), w.contiguous(), qm, tau, out2, topk2, rid2, lse2)
+    torch.cuda.synchronize()
+    assert pool.get_error() == hs.HS_OK
+    for x in back:
+        kb = keys[x].cpu().numpy()
+        sc = oracle.indexer_scores(oracle.IDX_E4M3, q[x].cpu().numpy(), w[x].cpu().numpy(), kb,
+                                   np.ones(final, np.float32), final)
+        np.testing.assert_array_equal(topk2[x, 0].cpu().numpy(), oracle.topk(sc[0], final, K))
+        _check_attention(truth[x], qm, out2, lse2, topk2[x, 0].cpu().numpy(), x, 0, step % L)
     pool.close()

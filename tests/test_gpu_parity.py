@@ -472,48 +472,97 @@ def test_full_to_mixed_flip_keeps_outputs():
         r.close()
 
 
-def flip_largest_full(r):
-    """Pool-pressure policy of the agentic trace: flip the full-residency
-    request with the most resident pages (lower id on ties) to mixed."""
-    hs = _hs()
-    full = [b for b in range(r.c.B) if r.modes[b] == hs.HS_FULL]
-    if not full:
-        return False
-    pages = [(r.N[b] + r.c.P - 1) // r.c.P for b in full]
-    r.flip_to_mixed(full[int(np.argmax(pages))])  # argmax takes the lowest id on ties
-    return True
-
-
 def test_agentic_growth_flips_under_pool_cap():
     """The agentic growth trace at reduced size: every request starts with a
     long prompt, then each turn appends a prompt and decodes token by token
-    with the real indexer top-K; the GPU pool is capped so that requests flip
-    from full to mixed residency mid-trace (largest first).  Every step is
-    compared with the oracle: indices, row locations, hot-buffer state, row
-    bytes and attention."""
+    with the real indexer top-K.  Appends go through the library's pressure
+    policy (hs_append_pressure) into a GPU pool capped so that requests flip
+    from full to mixed residency mid-trace; completed pages are pre-copied to
+    the host on a side stream after every round of appends, so the flips
+    release pages whose host copies came from there.  Then the caller parks
+    a request in zero residency and hs_pool_relieve returns the flipped one.
+    Flips and returns must be the oracle's reading of the policy; every step
+    is compared with the oracle: indices, row locations, hot-buffer state,
+    row bytes and attention."""
     from harness import Case, Runner
     hs = _hs()
     r = Runner(Case("agentic", B=4, N=1500, K=256, H=128, L=2, T=256, mode=hs.HS_FULL,
                     max_tokens=1792, gpu_blocks=100, host_blocks=4 * 28 + 4, steps=0))
+    pol = oracle.PressurePolicy(cap=100, T=256, P=64, hot_pages=r.C // 64)
+    side = torch.cuda.Stream()
     try:
+        for b in range(r.c.B):
+            pol.open(b)
+            assert pol.append(b, 1500) == ([], oracle.OK)
+        copied = r.pool.precopy(side)
+        assert copied == 4 * (1500 // 64)
         flips = []
         for turn in range(5):
             if turn:
                 for b in range(r.c.B):
-                    before = list(r.modes)
-                    r.append(b, 60, on_capacity=lambda _: flip_largest_full(r))
-                    flips += [x for x in range(r.c.B) if r.modes[x] != before[x]]
+                    flips += r.append_pressure(b, 60, pol)
+                r.pool.precopy(side)
             for _ in range(6):
                 r.run_step()
                 for b in range(r.c.B):
-                    before = list(r.modes)
-                    r.append(b, 1, on_capacity=lambda _: flip_largest_full(r))
-                    flips += [x for x in range(r.c.B) if r.modes[x] != before[x]]
-        assert flips and flips[0] == 0  # the first flip takes the largest, lowest id
-        assert hs.HS_FULL in r.modes    # and only as many as the cap needs
+                    flips += r.append_pressure(b, 1, pol)
+                r.pool.precopy(side)
+        assert flips == [0]             # the largest, lowest id, and only as many as the cap needs
+        assert r.modes.count(hs.HS_FULL) == 3
         st = r.pool.stats()
         assert (st["resident"], st["hits"], st["misses"]) == (
             r.stats["resident"], r.stats["hits"], r.stats["misses"])
+        assert r.stats["misses"] > 0
+        assert r.relieve(pol) == []     # the pool is still under pressure
+        r.set_mode(1, hs.HS_ZERO)       # the caller parks a request: its pages free up
+        pol.set_mode(1, oracle.ZERO)
+        assert r.relieve(pol) == [0]    # the flipped request comes back
+        assert r.pool.free_gpu_blocks() == 100 - pol.used()
+        for _ in range(3):
+            r.run_step()
+            for b in range(r.c.B):
+                assert r.append_pressure(b, 1, pol) == []
+    finally:
+        r.close()
+
+
+def test_precopy_copies_completed_pages_off_the_append_path():
+    """Full residency with a host pool: hs_append writes resident pages to
+    the GPU only; hs_precopy enqueues on a side stream the host copy of each
+    completed page once (the partial page waits until it completes).  Flips
+    right after a pre-copy, which may still be in flight, order themselves
+    after it; the steps then read the pre-copied rows from the host pool and
+    match the oracle."""
+    from harness import Case, Runner
+    hs = _hs()
+    r = Runner(Case("precopy", B=2, N=[1000, 700], K=128, Hi=8, Di=32, H=16, L=2, T=256,
+                    mode=hs.HS_FULL, steps=0, max_tokens=1600))
+    side = torch.cuda.Stream()
+    P = r.c.P
+    try:
+        host = r.pool.host_rows_view()          # [host blocks, L, P, R]
+        host.fill_(0xAB)                        # nothing written there so far
+        r.append(0, 100)
+        r.append(1, 30)
+        assert r.N == [1100, 730]
+        hbt = [r.pool.dump_state(b)["host_block_table"] for b in range(2)]
+        for b in range(2):
+            for pg in range((r.N[b] + P - 1) // P):
+                assert (host[int(hbt[b][pg])] == 0xAB).all(), f"req {b} page {pg} written by append"
+        assert r.pool.precopy(side) == 1100 // P + 730 // P
+        side.synchronize()
+        for b in range(2):
+            for pg in range(r.N[b] // P):
+                want = r.rows[b][pg * P:(pg + 1) * P].transpose(0, 1).cpu()
+                assert torch.equal(host[int(hbt[b][pg])], want), f"req {b} page {pg}"
+            assert (host[int(hbt[b][r.N[b] // P])] == 0xAB).all()   # the partial page
+        assert r.pool.precopy(side) == 0
+        r.append(0, 60)                          # 1160 tokens: page 17 completes
+        assert r.pool.precopy(side) == 1
+        r.set_mode(0, hs.HS_ZERO)                # straight after the pre-copy
+        r.set_mode(1, hs.HS_MIXED)
+        for _ in range(3):
+            r.run_step()
         assert r.stats["misses"] > 0
     finally:
         r.close()

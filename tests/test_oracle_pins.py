@@ -633,3 +633,130 @@ def test_zero_residency_start_gives_full_residency_outputs(nq):
             o, l = oracle.attention(oracle.ROW_E4M3_656, qb, truth[sel], tau)
             np.testing.assert_array_equal(outs[oracle.FULL][j][0], o)
     assert hits > 0
+
+
+# --------------------------------------------------------------------------
+# pool pressure reading ("Ce qui se passe": offload only under real pressure)
+# --------------------------------------------------------------------------
+def test_pressure_policy_hand_worked_example():
+    """Cap 10 blocks, P = 4, T = 4, hot buffer 2 blocks, three requests opened
+    in full residency.  Worked by hand:
+      r0 += 12 -> 3 pages (3 used); r1 += 16 -> 4 pages (7); r2 += 8 -> 2 (9).
+      r2 += 8 would need 3 + 4 + 4 = 11 blocks.  Flips that free blocks: r1
+      (mixed: tail page 3 + 2 hot = 3 < 4); not r0 (page 2 + 2 hot = 3 = 3)
+      nor r2 (page 1 + 2 hot = 3 > 2).  Flip r1: 3 + 3 + 4 = 10 fits.
+      r0 += 4 would need 4 + 3 + 4 = 11; only r2 frees blocks (3 < 4): flip
+      r2, 4 + 3 + 3 = 10 fits.
+      Nothing returns while the pool is full.  Close r0 (6 used, 2 open):
+      r2 (last flipped) needs 1 more block + 2 spare <= 4 free: back; then
+      r1 needs 1 + 2 <= 3 free: back (8 used)."""
+    pol = oracle.PressurePolicy(cap=10, T=4, P=4, hot_pages=2)
+    for r in range(3):
+        pol.open(r)
+    assert pol.append(0, 12) == ([], oracle.OK)
+    assert pol.append(1, 16) == ([], oracle.OK)
+    assert pol.append(2, 8) == ([], oracle.OK)
+    assert pol.used() == 9
+    assert pol.append(2, 8) == ([1], oracle.OK)
+    assert pol.used() == 10
+    assert pol.append(0, 4) == ([2], oracle.OK)
+    assert pol.used() == 10
+    assert pol.mode == {0: oracle.FULL, 1: oracle.MIXED, 2: oracle.MIXED}
+    assert pol.relieve() == []
+    pol.close(0)
+    assert pol.used() == 6
+    assert pol.relieve() == [2, 1]
+    assert pol.used() == 8 and pol.flipped == []
+
+
+def test_pressure_policy_capacity_when_no_flip_frees_blocks():
+    """Short requests hold fewer pages than a hot buffer: no flip lowers the
+    count, so an append past the cap fails and nothing flips."""
+    pol = oracle.PressurePolicy(cap=4, T=4, P=4, hot_pages=2)
+    pol.open(0)
+    pol.open(1)
+    assert pol.append(0, 8) == ([], oracle.OK)    # 2 pages
+    assert pol.append(1, 8) == ([], oracle.OK)    # 2 pages, pool full
+    # a flip of either would hold page 1 + 2 hot = 3 > 2 blocks
+    assert pol.append(1, 1) == ([], oracle.ERR_CAPACITY)
+    assert pol.N == {0: 8, 1: 8} and pol.used() == 4
+
+
+def test_pressure_policy_agentic_trace_first_flip_closed_form():
+    """Sixteen equal requests of the agentic growth trace (74,160 prompt
+    tokens, then 220 decoded and 753 prompt tokens per turn) in a pool of
+    20,000 blocks of 64 tokens: 16 x 1,250 pages = 16 x 80,000 tokens fill it
+    exactly.  Before turn 7 a request holds 74,160 + 220 + 5 x 973 = 79,245
+    tokens, 79,998 after turn 7's prompt; decode appends go request by
+    request, so the first append past 80,000 tokens is request 0's third
+    decoded token of turn 7, and the largest full request (all tie at 1,250
+    pages) is request 0 itself."""
+    P, T, hot = 64, 4096, 4096 // 64
+    pol = oracle.PressurePolicy(cap=20000, T=T, P=P, hot_pages=hot)
+    for b in range(16):
+        pol.open(b)
+        assert pol.append(b, 74160) == ([], oracle.OK)
+    first = None
+    for turn in range(7):
+        if turn:
+            for b in range(16):
+                f, st = pol.append(b, 753)
+                assert st == oracle.OK and not f
+        for d in range(220):
+            for b in range(16):
+                f, st = pol.append(b, 1)
+                assert st == oracle.OK
+                if f:
+                    first = (turn, d, b, f)
+                    break
+            if first:
+                break
+        if first:
+            break
+    assert first == (6, 2, 0, [0])
+    # the flip keeps request 0's tail window (pages 1186..1250) and a hot buffer
+    assert pol.blocks(0) == (1250 - (80001 - T) // P + 1) + hot == 129
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_pressure_policy_flips_only_under_pressure(seed):
+    """Random growth traces: an append that fits flips nothing; one that
+    does not, flips until it fits, each flip lowering the blocks in use; the
+    pool never goes past its cap; a capacity error leaves the request's
+    length unchanged and no flip would free a block."""
+    rng = np.random.default_rng(seed)
+    P, T, hot = 8, 16, 3
+    cap = int(rng.integers(40, 90))
+    pol = oracle.PressurePolicy(cap=cap, T=T, P=P, hot_pages=hot)
+    for r in range(5):
+        pol.open(r)
+    for _ in range(300):
+        r = int(rng.integers(0, 5))
+        n = int(rng.integers(1, 40))
+        used0 = pol.used()
+        fits = used0 - pol.blocks(r) + pol.blocks(r, N=pol.N[r] + n) <= cap
+        before = dict(pol.mode), dict(pol.N)
+        flips, st = pol.append(r, n)
+        assert pol.used() <= cap
+        if fits:
+            assert flips == [] and st == oracle.OK and pol.N[r] == before[1][r] + n
+            continue
+        assert flips or st == oracle.ERR_CAPACITY
+        # replay the flips one by one: each lowers the count
+        mode, used = dict(before[0]), used0
+        for x in flips:
+            assert mode[x] == oracle.FULL
+            gain = (oracle.gpu_blocks(oracle.FULL, before[1][x], T, P, hot)
+                    - oracle.gpu_blocks(oracle.MIXED, before[1][x], T, P, hot))
+            assert gain > 0
+            mode[x] = oracle.MIXED
+            used -= gain
+        if st == oracle.ERR_CAPACITY:
+            assert pol.N[r] == before[1][r]
+            assert all(pol.blocks(x, oracle.MIXED) >= pol.blocks(x, oracle.FULL)
+                       for x in pol.mode if pol.mode[x] == oracle.FULL)
+        else:
+            assert pol.N[r] == before[1][r] + n
+        if rng.random() < 0.1:
+            back = pol.relieve()
+            assert pol.used() + len(pol.mode) <= cap or not back
