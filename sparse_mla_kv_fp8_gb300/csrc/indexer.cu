@@ -10,12 +10,13 @@
 //       request's key slab, kStages-deep ring;
 //   B = the request's nq*Hi query rows (same layout), staged once per CTA;
 //   D = 128 TMEM lanes x nq*Hi columns, two accumulators (double buffer).
-// Warp 0 issues TMA, warp 1 issues MMAs, warps 2-9 (one thread per token =
-// one TMEM lane) read D, apply ReLU, the head weights and sigma and write the
-// scores (coalesced): with an even nq, warps 2-5 take the even queries and
-// warps 6-9 the odd ones (two warps per TMEM sub-partition, so that each
-// SMSP has a second warp to issue while the other waits); with one query
-// only warps 2-5 work.  Every mbarrier wait is bounded.
+// Warp 0 issues TMA, warp 1 issues MMAs, and G = min(nq, 4) groups of four
+// epilogue warps (one thread per token = one TMEM lane) read D, apply ReLU,
+// the head weights and sigma and write the scores (coalesced): group g takes
+// queries g, g + G, ...  The epilogue is bound by instruction issue, so one
+// warp per query and TMEM sub-partition gives each SMSP up to four warps to
+// switch between while TMEM loads are in flight.  Every mbarrier wait is
+// bounded.
 //
 // General kernel (any format / dims): one CTA per 128-token tile of one
 // request; keys and queries decoded to fp32 in shared memory; each thread
@@ -97,7 +98,8 @@ __global__ void __launch_bounds__(kTile) indexer_simt_kernel(
 // tensor-core path
 // ------------------------------------------------------------------------
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 320;
+constexpr int kTcMaxGroups = 4;  // epilogue warp groups (one per query)
+constexpr int kTcThreads = 64 + 128 * kTcMaxGroups;
 constexpr int kTileBytes = kTile * 128;  // 128 tokens x 128 B
 
 struct IdxTcArgs {
@@ -119,6 +121,36 @@ struct IdxTcSmem {
     static constexpr int tslot_off = bar_off + (2 * kTcStages + 5) * 8;
     static constexpr int bytes = tslot_off + 16 + 1024;         // + alignment slack
 };
+
+// sum_h w[h] * ReLU(d[h]) over nh columns of one TMEM lane row starting at
+// taddr (nh a multiple of 32), in 32-column batches (both loads in flight,
+// one wait) and eight independent partial sums.  fmaxf(d, 0) may give -0 for
+// d = -0 where ReLU gives +0; the sums start at +0 and every product with a
+// zero is a zero, so the total is the same.
+template <int kNh>
+__device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *wj, int nh) {
+    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int n = kNh ? kNh : nh;
+#pragma unroll
+    for (int h0 = 0; h0 < (kNh ? kNh : 256); h0 += 32) {
+        if (!kNh && h0 >= n) break;
+        float v[32];
+        tc::tmem_ld16(taddr + h0, v);
+        tc::tmem_ld16(taddr + h0 + 16, v + 16);
+        tc::tmem_ld_wait();
+        const float4 *wq = (const float4 *)(wj + h0);
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const float4 wv = wq[u];  // shared-memory broadcast
+            const int o = 4 * (u & 1);
+            part[o] = fmaf(wv.x, fmaxf(v[4 * u], 0.f), part[o]);
+            part[o + 1] = fmaf(wv.y, fmaxf(v[4 * u + 1], 0.f), part[o + 1]);
+            part[o + 2] = fmaf(wv.z, fmaxf(v[4 * u + 2], 0.f), part[o + 2]);
+            part[o + 3] = fmaf(wv.w, fmaxf(v[4 * u + 3], 0.f), part[o + 3]);
+        }
+    }
+    return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IdxTcArgs a) {
@@ -157,7 +189,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int k = 0; k < 2; k++) {
             tc::mbar_init(&tfull[k], 1);
-            tc::mbar_init(&tempty[k], (a.nq % 2 == 0) ? 256 : 128);
+            tc::mbar_init(&tempty[k], (int)blockDim.x - 64);  // every epilogue thread
         }
         tc::mbar_init(done, 1);
         tc::fence_barrier_init();
@@ -215,10 +247,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, a.err);
         }
-    } else if (warp < 6 || a.nq % 2 == 0) {
+    } else {
         const int sp = warp & 3;  // TMEM sub-partition this warp may read
         const int half = (warp - 2) >> 2;  // queries j = half, half + jstep, ...
-        const int jstep = (a.nq % 2 == 0) ? 2 : 1;
+        const int jstep = ((int)blockDim.x - 64) >> 7;  // the number of groups
         const int row = sp * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(sp * 32) << 16);
         const float *ksc = a.ksc + (size_t)b * a.maxT;
@@ -233,33 +265,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!__all_sync(0xffffffffu, w)) break;  // the warp leaves together
             tc::fence_after_sync();
             const uint32_t tb = lane_base + acc * a.ncols;
-            // per query: sum_h w[h] * ReLU(d[h]) over 16-column groups, the
-            // next group's TMEM load in flight while this one is reduced,
-            // eight independent partial sums; sigma > 0 comes out of the sum
-            // (sigma * ReLU(d) = ReLU(sigma * d); with the power-of-two key
-            // scales of the workloads both orders are exact)
-            const int ng = a.Hi >> 4;
+            // per query (sigma > 0 comes out of the sum: sigma * ReLU(d) =
+            // ReLU(sigma * d); with the power-of-two key scales of the
+            // workloads both orders are exact)
             for (int j = half; j < a.nq; j += jstep) {
-                float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                float v[2][16];
-                tc::tmem_ld16(tb + j * a.Hi, v[0]);
-                tc::tmem_ld_wait();
-                for (int g = 0; g < ng; g++) {
-                    if (g + 1 < ng) tc::tmem_ld16(tb + j * a.Hi + 16 * (g + 1), v[(g + 1) & 1]);
-                    const float *vg = v[g & 1];
-                    const float4 *wq = (const float4 *)(wsm + j * a.Hi + 16 * g);
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const float4 wv = wq[u];  // shared-memory broadcast
-                        part[2 * (u & 1)] = fmaf(wv.x, gate(vg[4 * u]), part[2 * (u & 1)]);
-                        part[2 * (u & 1) + 1] = fmaf(wv.y, gate(vg[4 * u + 1]), part[2 * (u & 1) + 1]);
-                        part[4 + 2 * (u & 1)] = fmaf(wv.z, gate(vg[4 * u + 2]), part[4 + 2 * (u & 1)]);
-                        part[5 + 2 * (u & 1)] = fmaf(wv.w, gate(vg[4 * u + 3]), part[5 + 2 * (u & 1)]);
-                    }
-                    tc::tmem_ld_wait();
-                }
-                const float accs = ((part[0] + part[1]) + (part[2] + part[3])) +
-                                   ((part[4] + part[5]) + (part[6] + part[7]));
+                const float accs = a.Hi == 64
+                    ? weighted_relu_sum<64>(tb + j * a.Hi, wsm + j * a.Hi, 64)
+                    : weighted_relu_sum<0>(tb + j * a.Hi, wsm + j * a.Hi, a.Hi);
                 if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = sig * accs;
             }
             tc::fence_before_sync();
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 bool tc_eligible(const hs_pool *p, int nq) {
     const int ncols = nq * p->cfg.idx_heads;
-    return p->cfg.idx_fmt == HS_IDX_E4M3 && p->cfg.idx_dim == 128 && p->cfg.idx_heads % 16 == 0 &&
+    return p->cfg.idx_fmt == HS_IDX_E4M3 && p->cfg.idx_dim == 128 && p->cfg.idx_heads % 32 == 0 &&
            ncols >= 16 && ncols <= 256 && p->has_key_map;
 }
 
@@ -357,8 +369,8 @@ cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w
         const int ntiles = (maxT + kTile - 1) / kTile;
         a.tiles_per_cta = pick_tiles_per_cta(ntiles, B, per_sm);
         dim3 grid((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta, B);
-        // the second group of epilogue warps works only with an even query count
-        const int threads = (nq % 2 == 0) ? kTcThreads : kTcThreads - 128;
+        // one group of four epilogue warps per query (up to four groups)
+        const int threads = 64 + 128 * (nq < kTcMaxGroups ? nq : kTcMaxGroups);
         indexer_tc_kernel<<<grid, threads, smem, st>>>(p->key_map, a);
         return cudaGetLastError();
     }

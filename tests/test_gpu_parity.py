@@ -140,6 +140,35 @@ def test_indexer_scores_bit_exact():
             r.close()
 
 
+@pytest.mark.parametrize("Hi,num_spec", [(64, 0), (64, 1), (64, 2), (32, 3), (96, 1), (128, 0)])
+def test_indexer_tensor_core_head_and_query_counts(Hi, num_spec):
+    """The tensor-core indexer at every epilogue shape: one to four warp
+    groups (one per query), the unrolled 64-head reduction and the general
+    one (32, 96 and 128 heads), against the oracle's scores bit for bit."""
+    from harness import Case, Runner
+    hs = _hs()
+    case = Case("s-shapes", B=3, N=[1000, 2500, 4097], K=64, Hi=Hi, Di=128, H=16,
+                num_spec=num_spec, sigma=True, mode=hs.HS_FULL)
+    r = Runner(case)
+    try:
+        q, w, _ = r.step_inputs(1)
+        stride = r.max_tokens
+        sc = torch.full((case.B, r.nq, stride), float("nan"), device=r.dev)
+        r.pool.indexer_score(q, w, case.B, r.nq, sc, stride)
+        torch.cuda.synchronize()
+        assert r.pool.get_error() == hs.HS_OK
+        for b in range(case.B):
+            N = r.N[b]
+            ref = oracle.indexer_scores(case.idx_fmt, q[b].cpu().numpy(), w[b].cpu().numpy(),
+                                        r.keys[b].cpu().numpy(), r.sig[b].cpu().numpy(), N)
+            got = sc[b, :, :N].cpu().numpy()
+            for j in range(r.nq):
+                vis = oracle.visible(N, r.nq, j)
+                np.testing.assert_array_equal(got[j, :vis], ref[j, :vis])
+    finally:
+        r.close()
+
+
 @pytest.mark.parametrize("max_tokens", [0, 200064, 300032])
 def test_topk_ties_and_special_scores(max_tokens):
     """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows.
