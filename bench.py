@@ -184,7 +184,7 @@ def algorithmic(w, misses_per_step=0.0):
                                     w["L"], 656)
     return {
         "indexer": dict(bytes=B * N * (Di + 4) + B * nq * Hi * (Di + 4), flops=2 * B * nq * N * Hi * Di),
-        "topk": dict(bytes=B * nq * K * 4, flops=0),
+        "topk": dict(bytes=B * nq * N * 4 + B * nq * K * 4, flops=0),  # every score read once
         "resolve_plan": dict(bytes=B * nq * K * 4 * 3, flops=0),
         "miss_copy": dict(bytes=misses_per_step * L * R, flops=0),
         "attention": dict(bytes=B * nq * K * R + B * nq * H * 576 * 2 + B * nq * H * 512 * 2,
@@ -471,6 +471,52 @@ KERNELS = {"indexer": "indexer_tc_kernel", "topk": "topk_cluster_kernel",
            "attention": "attn_tc_kernel"}
 
 
+def attention_kernel(w):
+    """The tensor-core attention a batch takes: the latent-split pair kernel
+    from 64 (query, 128-head group) pairs up, the 64-head kernel below."""
+    return "attn_pair_kernel" if w["B"] * w["nq"] * (w["H"] // 128) >= 64 else "attn_tc_kernel"
+
+
+# DRAM bytes (read + write) per algorithmic byte of a launch, from the ncu
+# captures summarised under profiles/, with the kernel source they were taken
+# on (sha256 prefix of the .cu file and of the shared device header): a
+# stage's traffic is reported as that ratio x its algorithmic bytes while
+# both sources are unchanged, and as null otherwise.  Each capture is a small
+# case of the same kernel; the ratio carries to the workload's launch because
+# every one of these kernels moves each algorithmic byte once, whatever the
+# batch.
+TC_CUH_SHA = "beffda9b9722625b"
+TRAFFIC = {
+    # keys + sigma read once; scores partly still in L2 at the end (16 x 131,072, 4 queries)
+    "indexer_tc_kernel": ("indexer.cu", "5ba1aa437e69b304", (277.41 + 25.79) / 310.9),
+    # the scores read once, nothing left to write back (16 x 4 rows of 142,000)
+    "topk_cluster_kernel": ("topk.cu", "6797471cd5a693e2", (36.41 + 0.0) / (36.36 + 0.52)),
+    # rows, queries and outputs of one layer (64 x 4 queries x 2048 rows x 128 heads)
+    "attn_pair_kernel": ("attention_pair.cu", "868b39f168560587", (354.26 + 27.07) / 415.2),
+    # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
+    "miss_copy_kernel": ("resolve.cu", "af8aaaeccb960de1", (0.11 + 92.77) / 96.9),
+}
+
+
+def _src_sha(name):
+    import hashlib
+    path = os.path.join(ROOT, "sparse_mla_kv_fp8_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_of(kernel, alg_bytes):
+    t = TRAFFIC.get(kernel)
+    if t is None or alg_bytes <= 0:
+        return None
+    try:
+        if _src_sha(t[0]) != t[1] or _src_sha("tc.cuh") != TC_CUH_SHA:
+            return None
+    except OSError:
+        return None
+    return t[2] * alg_bytes
+
+
 def roofline(stage, alg, peaks, w, ms_per_step, link):
     """Roofline of every stage; the one with the largest share of the step is
     the headline.  Each stage is timed alone between events, so the burst
@@ -489,12 +535,14 @@ def roofline(stage, alg, peaks, w, ms_per_step, link):
         if ms <= 0:
             continue
         a = alg[k]
+        kern = attention_kernel(w) if k == "attention" else KERNELS[k]
+        traffic = traffic_of(kern, a["bytes"])
         gbs = a["bytes"] / (ms / 1e3) / 1e9
         share = ms * n / ms_per_step
         if k == "attention":
             tf = a["flops"] / (ms / 1e3) / 1e12
-            out[k] = {"kernel": KERNELS[k], "bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
-                      "unit": "TFLOP/s", "frac": tf / peaks["bf16"], "traffic": None,
+            out[k] = {"kernel": kern, "bound": "tensor", "achieved": tf, "peak": peaks["bf16"],
+                      "unit": "TFLOP/s", "frac": tf / peaks["bf16"], "traffic": traffic,
                       "peak_source": peaks["src"] + " bf16 burst (the stage is timed alone; fp16 "
                                                     "operands have the same dense rate)",
                       "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm"],
@@ -502,13 +550,15 @@ def roofline(stage, alg, peaks, w, ms_per_step, link):
         elif k == "miss_copy":
             if link is None or a["bytes"] == 0:
                 continue
-            out[k] = {"kernel": KERNELS[k], "bound": "host_link", "achieved": gbs,
+            out[k] = {"kernel": kern, "bound": "host_link", "achieved": gbs,
                       "peak": link["peak_gbs"], "unit": "GB/s", "frac": gbs / link["peak_gbs"],
-                      "traffic": None, "peak_source": link["source"], "share_of_step": share,
+                      "traffic": traffic, "traffic_note": "HBM bytes per launch (the host-link "
+                      "bytes are 1.026x the algorithmic bytes in the capture)",
+                      "peak_source": link["source"], "share_of_step": share,
                       "us_per_launch": ms * 1e3}
         else:
-            out[k] = {"kernel": KERNELS[k], "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": None,
+            out[k] = {"kernel": kern, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
+                      "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": traffic,
                       "peak_source": peaks["src"] + " HBM copy", "share_of_step": share,
                       "us_per_launch": ms * 1e3}
     dom = max(out, key=lambda k: out[k]["share_of_step"])
@@ -763,6 +813,135 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+# ---------------------------------------------------------------------------
+# single-stage cases (small shapes of one kernel, for profiler captures)
+# ---------------------------------------------------------------------------
+CASES = {
+    "indexer_mtp3_16x131072": "the indexer at four queries per request, 16 x 131,072 tokens",
+    "topk_mtp3_16x142000": "top-2048 of 16 x 4 indexer score rows of 142,000 tokens",
+    "attention_mtp3_64x4x2048": "one layer of sparse MLA over 64 x 4 queries x 2048 rows, 128 heads",
+    "miss_copy_mixed_8x142000": "the miss copy of a first step from empty hot buffers, "
+                                "8 requests x 142,000 tokens, mixed residency, MTP3, 4 layers",
+}
+
+
+def _timed(fn, reps, flush):
+    import torch
+    out = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(round(e0.elapsed_time(e1) * 1e3, 1))
+    return out
+
+
+def run_case(name, reps=3):
+    """One kernel of the step on a small shape, L2 flushed before each launch;
+    prints the microseconds per launch."""
+    import numpy as np
+    import torch
+    from sparse_mla_kv_fp8_gb300 import hs
+    from sparse_mla_kv_fp8_gb300 import workload as wl
+    dev = torch.device("cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    P, K = 64, 2048
+
+    def full_pool(B, N, nq, L, rows):
+        cfg = hs.make_config(max_requests=B, max_tokens=(N + P - 1) // P * P, page_tokens=P, top_k=K,
+                             num_spec=nq - 1, tail_tokens=0, num_mla_layers=L, mla_heads=128,
+                             idx_heads=64, idx_dim=128, row_fmt=hs.HS_ROW_E4M3_656,
+                             idx_fmt=hs.HS_IDX_E4M3, gpu_blocks=B * ((N + P - 1) // P))
+        pool = hs.Pool(cfg, device=dev)
+        for b in range(B):
+            pool.open(b, hs.HS_FULL)
+            for t0 in range(0, N, 16384):
+                n = min(16384, N - t0)
+                r = (wl.mla_rows(0, b, t0, n, L, wl.ROW_E4M3_656, device=dev) if rows
+                     else torch.zeros((n, L, 656), dtype=torch.uint8, device=dev))
+                pool.append(b, r, wl.idx_keys(0, b, t0, n, 128, wl.IDX_E4M3, device=dev))
+        return pool
+
+    def idx_inputs(B, nq):
+        q = torch.stack([wl.idx_query(0, b, 1, nq, 64, 128, wl.IDX_E4M3, dev) for b in range(B)])
+        w = torch.stack([wl.idx_weights(0, b, 1, nq, 64, dev) for b in range(B)])
+        return q.contiguous(), w.contiguous()
+
+    if name == "indexer_mtp3_16x131072":
+        B, N, nq = 16, 131072, 4
+        pool = full_pool(B, N, nq, 1, False)
+        q, w = idx_inputs(B, nq)
+        sc = torch.empty((B, nq, N), dtype=torch.float32, device=dev)
+        ts = _timed(lambda i: pool.indexer_score(q, w, B, nq, sc, N), reps, flush)
+    elif name == "topk_mtp3_16x142000":
+        B, N, nq = 16, 142000, 4
+        pool = full_pool(B, N, nq, 1, False)
+        q, w = idx_inputs(B, nq)
+        cap = pool.cfg.max_tokens
+        sc = torch.empty((B, nq, cap), dtype=torch.float32, device=dev)
+        pool.indexer_score(q, w, B, nq, sc, cap)
+        out = torch.empty((B, nq, K), dtype=torch.int32, device=dev)
+        ts = _timed(lambda i: pool.topk(sc, cap, B, nq, out), reps, flush)
+    elif name == "attention_mtp3_64x4x2048":
+        B, N, nq = 64, 16384, 4
+        pool = full_pool(B, N, nq, 1, True)
+        g = torch.Generator(device=dev).manual_seed(1)
+        tk = torch.stack([torch.stack([torch.sort(torch.randperm(N - nq + 1 + j, generator=g, device=dev)[:K])[0]
+                                       for j in range(nq)]) for _ in range(B)]).int()
+        rid = torch.empty_like(tk)
+        pool.resolve(tk, B, nq, rid)
+        qm = wl.mla_query(0, 1, B, nq, 128, 1, dev)[0].contiguous()
+        out = torch.empty((B, nq, 128, 512), dtype=torch.bfloat16, device=dev)
+        ts = _timed(lambda i: pool.sparse_mla_decode(0, qm, rid, B, nq, 1 / math.sqrt(576), out),
+                    reps, flush)
+    elif name == "miss_copy_mixed_8x142000":
+        B, N, nq, L, T = 8, 142000, 4, 4, 4096
+        pages = (N + P - 1) // P
+        C = (nq + 1) * K
+        cfg = hs.make_config(max_requests=B, max_tokens=pages * P, page_tokens=P, top_k=K,
+                             num_spec=nq - 1, tail_tokens=T, num_mla_layers=L, mla_heads=128,
+                             idx_heads=64, idx_dim=128, row_fmt=hs.HS_ROW_E4M3_656,
+                             idx_fmt=hs.HS_IDX_E4M3,
+                             gpu_blocks=B * ((T + P - 1) // P + 1 + C // P) + 8, host_blocks=B * pages)
+        pool = hs.Pool(cfg, device=dev)
+        for b in range(B):
+            pool.open(b, hs.HS_MIXED)
+            for t0 in range(0, N, 16384):
+                n = min(16384, N - t0)
+                pool.append(b, wl.mla_rows(0, b, t0, n, L, wl.ROW_E4M3_656, device=dev),
+                            torch.zeros((n, 128), dtype=torch.uint8, device=dev))
+        tk = np.stack([np.stack([wl.drawn_topk(0, b, 1, j, N - nq + 1 + j, K, P, "recency_zipf", T)
+                                 for j in range(nq)]) for b in range(B)]).astype(np.int32)
+        topk = torch.from_numpy(tk).to(dev)
+        rid = torch.empty_like(topk)
+        w = dict(B=B)
+        per = []
+
+        def one(i):  # the same first step every time: empty hot buffers, then plan, then the copy
+            reset_hot_state(pool, w)
+            pool.reset_stats()
+            pool.resolve_plan(topk, B, nq, rid)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pool.miss_copy(B, nq)
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(round(e0.elapsed_time(e1) * 1e3, 1))
+        _timed(one, reps + 2, flush)  # two more rounds first: they warm the host mapping
+        ts = per
+        mb = pool.stats()["bytes_copied"] / 1e6
+        print(f"miss copy: {mb:.1f} MB per launch", flush=True)
+    else:
+        raise SystemExit(f"unknown case {name}: {sorted(CASES)}")
+    assert pool.get_error() == hs.HS_OK, pool.get_error()
+    print(json.dumps({"case": name, "what": CASES[name], "us_per_launch": ts}), flush=True)
+    pool.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -776,7 +955,13 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-host-link", action="store_true")
+    ap.add_argument("--case", default="", help="run one single-stage case instead: " + ", ".join(CASES))
     args = ap.parse_args()
+    if args.case:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_case(args.case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
