@@ -34,8 +34,11 @@
  *     pointer to caller buffers beyond the call, except the two arenas given
  *     to hs_pool_create.
  *   - Hot-path calls (hs_indexer_score, hs_topk, hs_indexer_topk, hs_resolve,
- *     hs_sparse_mla_decode, hs_step) only enqueue work on `stream`: no host
- *     synchronisation, no allocation, no branch on device data.  They may be
+ *     hs_sparse_mla_decode, hs_resolve_attend, hs_step) only enqueue work on
+ *     `stream` (hs_resolve_attend and hs_step with a host pool also on the
+ *     pool's side stream, joined back into `stream` by events before they
+ *     return): no host synchronisation, no allocation, no branch on device
+ *     data.  They may be
  *     captured in a CUDA graph and replayed.  What they launch depends only
  *     on the pool's configuration and the call's B and nq, so a captured
  *     graph stays valid when requests change residency or grow (hs_append)
@@ -400,9 +403,16 @@ hs_status hs_dcp_combine(const void *o_parts, const float *lse_parts, int32_t R,
 
 /* Resolve + the sparse MLA decode of every layer of the group, for a top-K
  * the caller already has (the second half of hs_step, e.g. for a selection
- * made elsewhere): hs_resolve followed by hs_sparse_mla_decode for each of
- * the L layers, enqueued on `stream`.  topk, row_id: as for hs_resolve;
- * q_mla, out, lse: as in hs_step_args ([L][B][nq]...). */
+ * made elsewhere): the results of hs_resolve followed by hs_sparse_mla_decode
+ * for each of the L layers.  Without a host pool everything is enqueued on
+ * `stream`.  With one, the plan and the attentions go on `stream` and layer
+ * l's missed rows are copied on a side stream the pool owns (about 64 CTAs
+ * at the highest stream priority), so that layer l's copy runs while layer
+ * l-1 attends; `stream` waits for each layer's copy by an event just before
+ * that layer's attention, so when `stream` reaches the end of this call all
+ * of the call's work is done (a CUDA graph captured on `stream` takes the
+ * side stream's work in with it).  topk, row_id: as for hs_resolve; q_mla,
+ * out, lse: as in hs_step_args ([L][B][nq]...). */
 hs_status hs_resolve_attend(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
                             const void *q_mla, float softmax_scale, void *out, float *lse,
                             int32_t *row_id, cudaStream_t stream);
@@ -452,8 +462,9 @@ hs_status hs_pool_load_state(hs_pool *pool, int32_t req, const int32_t *hot_map,
                              const int32_t *slot_token, const uint32_t *stamp,
                              uint32_t step);
 
-/* Number of kernels hs_step enqueues for a batch of B requests x nq queries
- * (host arithmetic, the same decision hs_step makes); -1 on bad arguments. */
+/* Number of kernels hs_step enqueues for a batch of B requests x nq queries,
+ * those on the pool's side stream included (host arithmetic, the same
+ * decision hs_step makes); -1 on bad arguments. */
 int32_t hs_step_kernel_count(const hs_pool *pool, int32_t B, int32_t nq);
 
 /* Failure-path check: enqueue on `stream` one small kernel that waits, with

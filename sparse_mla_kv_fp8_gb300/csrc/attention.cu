@@ -969,7 +969,7 @@ int pair_splits(const hs_pool_config &c, int rows);
 cudaError_t pair_setup(const hs_pool *p);
 cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
                                   int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
-                                  bool q_ready);
+                                  bool q_ready, bool pdl);
 
 // Which tensor-core kernel a batch takes.  The pair kernel (the latent dims
 // split over a 2-CTA cluster, every MMA at M = N = 128, each row converted
@@ -1022,12 +1022,12 @@ cudaError_t attention_setup(const hs_pool *p) {
 
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
                              int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
-                             bool q_ready) {
+                             bool q_ready, bool pdl) {
     const int rows = B * nq;
     const int K = p->cfg.top_k;
     const int splits = splits_for(p->cfg, rows);
     if (pair_cfg(p->cfg, rows) && pair_eligible(p)) {
-        cudaError_t e = launch_pair_attention(p, layer, q, row_id, B, nq, scale, out, lse, st, q_ready);
+        cudaError_t e = launch_pair_attention(p, layer, q, row_id, B, nq, scale, out, lse, st, q_ready, pdl);
         if (e != cudaSuccess) return e;
         if (splits > 1)
             attn_combine_kernel<<<rows * p->cfg.mla_heads, 128, 0, st>>>(p->d.attn_part, splits,
@@ -1057,7 +1057,7 @@ cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const i
         dim3 grid(rows, a.H / kTcHeads, splits);
         // the two splits of a (query, 64 heads) merge through DSMEM as a cluster
         PdlLaunch lc(grid, dim3(kAttnThreads), AttnTcSmem::bytes, st,
-                     a.cluster ? dim3(1, 1, 2) : dim3(1, 1, 1));
+                     a.cluster ? dim3(1, 1, 2) : dim3(1, 1, 1), pdl);
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel, a);
         if (e != cudaSuccess) return e;
     } else {

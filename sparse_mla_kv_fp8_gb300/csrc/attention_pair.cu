@@ -708,7 +708,7 @@ cudaError_t pair_setup(const hs_pool *) {
 }
 
 cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id, int B,
-                                  int nq, float scale, void *out, float *lse, cudaStream_t st, bool q_ready) {
+                                  int nq, float scale, void *out, float *lse, cudaStream_t st, bool q_ready, bool pdl) {
     const int rows = B * nq, K = p->cfg.top_k;
     const int splits = pair_splits(p->cfg, rows);
     PairArgs a;
@@ -730,7 +730,7 @@ cudaError_t launch_pair_attention(const hs_pool *p, int layer, const void *q, co
     a.q_ready = q_ready;
     a.err = p->d.err;
     dim3 grid(2 * splits, rows, a.H / kPairHeads);
-    PdlLaunch lc(grid, dim3(kPairThreads), PairSmem::bytes, st, dim3(2, 1, 1));
+    PdlLaunch lc(grid, dim3(kPairThreads), PairSmem::bytes, st, dim3(2, 1, 1), pdl);
     return cudaLaunchKernelEx(&lc.cfg, attn_pair_kernel, a);
 }
 

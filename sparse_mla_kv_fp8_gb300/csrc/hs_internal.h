@@ -25,22 +25,26 @@ constexpr int kNumSMs = 152;       // GB300
 // cluster_z > 1, a (1, 1, cluster_z) or (cluster_x, 1, 1) cluster.
 struct PdlLaunch {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attrs[2];
-    PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st, dim3 cluster = dim3(1, 1, 1)) {
+    cudaLaunchAttribute attrs[3];  // room for one more attribute set by the caller
+    PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st, dim3 cluster = dim3(1, 1, 1),
+              bool pdl = true) {
         cfg.gridDim = grid;
         cfg.blockDim = block;
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
-        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attrs;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 0;
+        if (pdl) {
+            attrs[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+            cfg.numAttrs++;
+        }
         if (cluster.x * cluster.y * cluster.z > 1) {
-            attrs[1].id = cudaLaunchAttributeClusterDimension;
-            attrs[1].val.clusterDim.x = cluster.x;
-            attrs[1].val.clusterDim.y = cluster.y;
-            attrs[1].val.clusterDim.z = cluster.z;
-            cfg.numAttrs = 2;
+            attrs[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+            attrs[cfg.numAttrs].val.clusterDim.x = cluster.x;
+            attrs[cfg.numAttrs].val.clusterDim.y = cluster.y;
+            attrs[cfg.numAttrs].val.clusterDim.z = cluster.z;
+            cfg.numAttrs++;
         }
     }
 };
@@ -114,6 +118,12 @@ struct hs_pool {
     cudaEvent_t precopy_ev;  // recorded after the last pre-copy batch
     bool precopy_pending;    // a pre-copy batch was enqueued and not waited for
     std::vector<int32_t> policy_flipped;  // requests the pressure policy flipped, in order
+    // with a host pool: the side stream that copies a step's missed rows layer by
+    // layer beside the attention, and the events that order the two
+    cudaStream_t copy_stream;
+    int copy_priority;
+    cudaEvent_t ev_plan;
+    std::vector<cudaEvent_t> ev_copy;  // [L]
 };
 
 namespace hs {
@@ -134,13 +144,13 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
                                 int32_t *row_id, cudaStream_t st);
 // Miss rows of layers [l0, l1) (l1 < 0: through the last layer).
 cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0 = 0,
-                             int l1 = -1);
+                             int l1 = -1, int ctas = 0, int priority = 0);
 // q_ready: the queries were written before the previous kernel on `st`
 // started (true inside hs_step), so the kernel may stage them before it waits
 // for that kernel.
 cudaError_t launch_attention(const hs_pool *p, int layer, const void *q, const int32_t *row_id,
                              int B, int nq, float scale, void *out, float *lse, cudaStream_t st,
-                             bool q_ready = false);
+                             bool q_ready = false, bool pdl = true);
 int indexer_kernel_count(const hs_pool *p, int B, int nq);
 int topk_kernel_count(const hs_pool *p, int B, int nq);
 int resolve_kernel_count(const hs_pool *p, int B, int nq);

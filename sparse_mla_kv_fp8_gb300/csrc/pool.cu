@@ -260,7 +260,7 @@ int64_t blocks_in_mode(const hs_pool *p, int32_t req, int mode) {
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 102; }
+int32_t hs_abi_version(void) { return 103; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -367,6 +367,9 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->host_ok.assign(maxR * p->max_pages, 0);
     p->precopy_pending = false;
     p->precopy_ev = nullptr;
+    p->copy_stream = nullptr;
+    p->copy_priority = 0;
+    p->ev_plan = nullptr;
     p->free_gpu.resize(cfg->gpu_blocks);
     for (int64_t i = 0; i < cfg->gpu_blocks; i++) p->free_gpu[i] = (int32_t)(cfg->gpu_blocks - 1 - i);
     p->free_host.resize(cfg->host_blocks);
@@ -390,6 +393,16 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     ms(p->d.miss_count, 0, maxR * 4);
     if (e == cudaSuccess) e = hs::setup_kernel_attributes(p);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->precopy_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess && cfg->host_blocks > 0) {
+        int lo = 0, hi = 0;  // numerically lower = higher priority
+        e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        p->copy_priority = hi;
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->copy_stream, cudaStreamNonBlocking, hi);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_plan, cudaEventDisableTiming);
+        p->ev_copy.assign(cfg->num_mla_layers, nullptr);
+        for (int l = 0; l < cfg->num_mla_layers && e == cudaSuccess; l++)
+            e = cudaEventCreateWithFlags(&p->ev_copy[l], cudaEventDisableTiming);
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         hs_pool_destroy(p);
@@ -405,6 +418,13 @@ void hs_pool_destroy(hs_pool *pool) {
         if (pool->precopy_pending) cudaEventSynchronize(pool->precopy_ev);  // copies into the host arena
         cudaEventDestroy(pool->precopy_ev);
     }
+    if (pool->copy_stream) {
+        cudaStreamSynchronize(pool->copy_stream);
+        cudaStreamDestroy(pool->copy_stream);
+    }
+    if (pool->ev_plan) cudaEventDestroy(pool->ev_plan);
+    for (cudaEvent_t ev : pool->ev_copy)
+        if (ev) cudaEventDestroy(ev);
     delete pool;
 }
 
@@ -769,24 +789,50 @@ hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const i
     return cuda_status(hs::launch_attention(p, layer, q, row_id, B, nq, scale, out, lse, st));
 }
 
-// Resolve (the plan, then one miss copy of every layer's rows), then the
-// attention of every layer, all on `st`.  (Copying layer l+1's rows on a
-// second stream while layer l's attention runs was measured: it gained at a
-// small miss volume but lost at the mixed-residency MTP3 workload, 142,000
-// tokens x 64 requests, about 160,000 misses per step: 5.4-5.7 ms against
-// 5.0 ms per step, the copy's long-latency host loads slowing the attention
-// CTAs they share the SMs with.)
+// Resolve, then the attention of every layer.  Without a host pool there is
+// nothing to copy: the plan and the attentions run on `st`.  With one, layer
+// l's missed rows are copied on the pool's side stream (about 64 CTAs at a
+// high launch priority) while layer l-1 attends on `st`: `st` waits for
+// layer l's copy, by an event, just before layer l's attention.  (Copying the
+// layers beside the attention with a full-width copy grid was measured
+// slower at the mixed-residency MTP3 workload, 5.4-5.7 against 5.0 ms per
+// step: both kernels' CTAs then shared every SM.)
+// CTAs of a layer's copy that runs beside the attention: the link's rate
+// with about 64 SMs (measured 189 GB/s against 192 for the full-width copy at
+// the MTP3 workload), the other SMs left to the attention.
+constexpr int kCopyCtasBeside = 64;
+
 static cudaError_t resolve_attend(hs_pool *p, const int32_t *topk, int B, int nq,
                                   const void *q_mla, float scale, void *out, float *lse,
                                   int32_t *row_id, cudaStream_t st, bool q_ready) {
     const int H = p->cfg.mla_heads, L = p->cfg.num_mla_layers;
     const size_t qstride = (size_t)B * nq * H * hs::kLatent * 2;
     const size_t ostride = (size_t)B * nq * H * hs::kNope * 2;
-    cudaError_t e = hs::launch_resolve(p, topk, B, nq, row_id, st);
-    for (int l = 0; l < L && e == cudaSuccess; l++)
-        e = hs::launch_attention(p, l, (const uint8_t *)q_mla + l * qstride, row_id, B, nq, scale,
-                                 (uint8_t *)out + l * ostride,
-                                 lse ? lse + (size_t)l * B * nq * H : nullptr, st, q_ready);
+    // beside the copies, an attention launches only once its layer's copy and
+    // the previous layer are done (no early launch: its CTAs would hold SMs
+    // the copy needs while they wait)
+    const bool pdl = p->cfg.host_blocks == 0;
+    auto attend = [&](int l) {
+        return hs::launch_attention(p, l, (const uint8_t *)q_mla + l * qstride, row_id, B, nq, scale,
+                                    (uint8_t *)out + l * ostride,
+                                    lse ? lse + (size_t)l * B * nq * H : nullptr, st, q_ready, pdl);
+    };
+    if (p->cfg.host_blocks == 0) {
+        cudaError_t e = hs::launch_resolve(p, topk, B, nq, row_id, st);
+        for (int l = 0; l < L && e == cudaSuccess; l++) e = attend(l);
+        return e;
+    }
+    cudaError_t e = hs::launch_resolve_plan(p, topk, B, nq, row_id, st);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_plan, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_stream, p->ev_plan, 0);
+    for (int l = 0; l < L && e == cudaSuccess; l++) {
+        e = hs::launch_miss_copy(p, B, nq, p->copy_stream, l, l + 1, kCopyCtasBeside, p->copy_priority);
+        if (e == cudaSuccess) e = cudaEventRecord(p->ev_copy[l], p->copy_stream);
+    }
+    for (int l = 0; l < L && e == cudaSuccess; l++) {
+        e = cudaStreamWaitEvent(st, p->ev_copy[l], 0);
+        if (e == cudaSuccess) e = attend(l);
+    }
     return e;
 }
 
@@ -816,9 +862,10 @@ hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
 
 int32_t hs_step_kernel_count(const hs_pool *p, int32_t B, int32_t nq) {
     if (!p || B <= 0 || B > p->cfg.max_requests || nq <= 0 || nq > p->nq_max) return -1;
-    return hs::indexer_kernel_count(p, B, nq) + hs::topk_kernel_count(p, B, nq) +
-           hs::resolve_kernel_count(p, B, nq) +
-           p->cfg.num_mla_layers * hs::attention_kernel_count(p, B, nq);
+    // the step's resolve is the plan plus, with a host pool, one copy per layer
+    const int L = p->cfg.num_mla_layers;
+    return hs::indexer_kernel_count(p, B, nq) + hs::topk_kernel_count(p, B, nq) + 1 +
+           (p->cfg.host_blocks > 0 ? L : 0) + L * hs::attention_kernel_count(p, B, nq);
 }
 
 hs_status hs_pool_get_error(hs_pool *p, hs_status *out) {

@@ -346,7 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
 }
 
 // Rows of layers [l0, l1) of every miss: 16-byte units over the host link,
-// four loads in flight per thread, written to the miss's hot-buffer slot.
+// four loads in flight per thread, written to the miss's hot-buffer slot; a
+// (gx, B) grid, gx CTAs per request.  Scattered 656-byte rows over the link
+// need many SMs' worth of loads in flight: measured at the mixed-residency
+// MTP3 workload (64 requests, 776 MB), 608 CTAs move 192 GB/s and 64 CTAs
+// (one per request) 189 GB/s, while a flat 24-CTA grid of 512 threads with
+// eight loads in flight per thread managed 94 GB/s.
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
@@ -448,15 +453,26 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
 }
 
 // The miss copy of the last plan (its miss lists stay in the pool's workspace
-// until the next plan).
-cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0, int l1) {
+// until the next plan), layers [l0, l1).  ctas = 0: about four CTAs per SM
+// over the batch (the copy alone); otherwise about that many CTAs in all (a
+// copy beside another kernel, which keeps the other SMs).  priority (0 =
+// none) goes to the launch, so that the copy's CTAs take SMs as they free up
+// before a lower-priority kernel's.
+cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0, int l1,
+                             int ctas, int priority) {
     const int n = nq * p->cfg.top_k;
     if (l1 < 0) l1 = p->cfg.num_mla_layers;
     if (p->cfg.host_blocks > 0) {
-        // enough CTAs in flight to cover the host link's latency, at any B
-        const int gx = (4 * kNumSMs + B - 1) / B;
-        dim3 grid(gx, B);
-        PdlLaunch lc(grid, dim3(kCopyThreads), 0, st);
+        const int want = ctas > 0 ? ctas : 4 * kNumSMs;
+        const int gx = (want + B - 1) / B;
+        PdlLaunch lc(dim3(gx, B), dim3(kCopyThreads), 0, st);
+        if (priority) {
+            // beside another kernel: no early launch behind the previous
+            // copy (its CTAs would hold SMs while they wait), a high priority
+            lc.attrs[0].id = cudaLaunchAttributePriority;
+            lc.attrs[0].val.priority = priority;
+            lc.cfg.numAttrs = 1;
+        }
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count,
                                            (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
                                            n, (const int32_t *)p->d.host_block_table,
