@@ -85,6 +85,33 @@ struct PairArgs {
     int32_t *err;
 };
 
+// Has the phase with this parity completed?  (test_wait: never suspends the
+// thread, so a warp can poll two barriers and take whichever is ready.)
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(ok)
+        : "r"(tc::smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The same, with acquire at cluster scope (for phases completed by the peer).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(ok)
+        : "r"(tc::smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait by every lane of a warp; true when all lanes saw the phase.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
     bool ok = true;
@@ -232,14 +259,23 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const uint32_t rn_a = tc::smem_addr(rn), pb_a = tc::smem_addr(pb);
             const uint32_t qr_a = tc::smem_addr(qr), rr_a = tc::smem_addr(rr);
             ok = tc::mbar_wait(q_full, 0, a.err);
-            for (int it = 0; it <= nch && ok; it++) {
-                if (it < nch) {  // S(it)
-                    const int c = it, b = c & 1;
-                    if (c >= 1 && !(ok = tc::mbar_wait(s_free, (c - 1) & 1, a.err))) break;
-                    for (int kb = 0; kb < 4 && ok; kb++) {
-                        if (!(ok = tc::mbar_wait(&kbf[b * 4 + kb], (c >> 1) & 1, a.err))) break;
+            // Issue S and O in the order their inputs arrive: S(sc) K-block by
+            // K-block as the converters finish them (after the softmax side has
+            // read S(sc-1)), O(oc) as soon as both CTAs' P(oc) is there.  (A
+            // fixed S(c+1)-then-O(c) order made O(c), and the P buffer it frees
+            // for the next softmax, wait for chunk c+1's conversion.)
+            int sc = 0, skb = 0, oc = 0;
+            long long t_last = clock64();
+            while (ok && oc < nch) {
+                bool prog = false;
+                if (sc < nch) {
+                    const int b = sc & 1;
+                    bool go = true;
+                    if (skb == 0 && sc >= 1) go = mbar_test(s_free, (sc - 1) & 1);
+                    if (go) go = mbar_test(&kbf[b * 4 + skb], (sc >> 1) & 1);
+                    if (go) {
                         tc::fence_after_sync();
-                        if (kb == 0) {  // the rope tile is converted with K-block 0
+                        if (skb == 0) {  // the rope tile is converted with K-block 0
 #pragma unroll
                             for (int kk = 0; kk < 2; kk++) {
                                 const uint64_t ad = tc::smem_desc(qr_a + kk * 32, 16, 512, 4);
@@ -249,16 +285,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         }
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) {
-                            const uint64_t bd = tc::smem_desc_sw128(rn_a + (b * 4 + kb) * kKbBytes + kk * 32, 16, 1024);
-                            tc::mma_f16_tmem_a(tmem + SC, tmem + QN + kb * 32 + kk * 8, bd, id_s, 1);
+                            const uint64_t bd = tc::smem_desc_sw128(rn_a + (b * 4 + skb) * kKbBytes + kk * 32, 16, 1024);
+                            tc::mma_f16_tmem_a(tmem + SC, tmem + QN + skb * 32 + kk * 8, bd, id_s, 1);
                         }
+                        if (++skb == 4) {
+                            tc::mma_commit(s_full);
+                            skb = 0;
+                            sc++;
+                        }
+                        prog = true;
                     }
-                    if (!ok) break;
-                    tc::mma_commit(s_full);
                 }
-                if (it >= 1) {  // O(it - 1) += P V
-                    const int c = it - 1, b = c & 1;
-                    if (!(ok = tc::mbar_wait(o_ready, c & 1, a.err))) break;
+                if (oc < sc && mbar_test(o_ready, oc & 1)) {  // O(oc) += P V
+                    const int c = oc, b = c & 1;
                     tc::fence_after_sync();
 #pragma unroll
                     for (int half = 0; half < 2; half++) {
@@ -274,6 +313,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     tc::mma_commit(o_done);
                     // both CTAs may write the next chunk's P (none after the last)
                     if (c + 1 < nch) tc::mma_commit_multicast(pb_free, (uint16_t)0x3);
+                    oc++;
+                    prog = true;
+                }
+                if (prog) {
+                    t_last = clock64();
+                } else if (clock64() - t_last > tc::kWaitCycles) {
+                    set_error(a.err, HS_ERR_TIMEOUT);
+                    ok = false;
+                } else {
+                    __nanosleep(20);  // leave the SMSP's issue slots to the other warps
                 }
             }
             tc::mma_commit(mma_done);
@@ -448,46 +497,81 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             if (lane == 0) tc::mbar_arrive(o_ready);
             return true;
         };
+        int32_t idn[2];  // an own warp's row ids of the chunk it processes next
+#pragma unroll
+        for (int w2 = 0; w2 < 2; w2++) {
+            const int k = k0 + 64 * ch + 32 * w2 + lane;
+            idn[w2] = (own && nch > 0 && k < k1) ? ids[k] : -1;
+        }
         for (int c = 0; c < nch && ok; c++) {
-            // validity of this warp's 64 rows (ids are L2-hot)
+            const uint32_t sbase = lane_base + SC + 64 * ch;
+            if (!own) {
+                // ---- a sender warp has two things to do per chunk, in the
+                // order their inputs arrive: send S(c)'s partial sums of the
+                // peer's heads (once S(c) is done and the peer has read the
+                // last chunk's), and complete chunk c-1 with the peer's P rows
+                // (which lets the MMA warp issue O(c-1); O(c-1) frees the P
+                // buffer that the next softmax writes).  Waiting for either
+                // one first put the other on the chunk's critical path
+                // (measured 9.3-10 K cycles per chunk).
+                bool need_fin = c >= 1, need_send = true;
+                const long long t0 = clock64();
+                while (ok && (need_fin || need_send)) {
+                    int rdy = 0;  // lane 0's view, made the warp's
+                    if (lane == 0) {
+                        if (need_fin && mbar_test_cluster(p_full, (c - 1) & 1)) rdy |= 1;
+                        if (need_send && mbar_test(s_full, c & 1)) rdy |= 2;
+                        if (!rdy && clock64() - t0 > tc::kWaitCycles) rdy = 4;
+                    }
+                    rdy = __shfl_sync(0xffffffffu, rdy, 0);
+                    if (rdy & 1) {
+                        ok = sender_finish(c - 1);
+                        need_fin = false;
+                    } else if (rdy & 2) {
+                        tc::fence_after_sync();
+                        // after the peer has read the last chunk's partial sums
+                        if (c >= 1 && !(ok = warp_wait_cluster(srx_free, (c - 1) & 1, a.err))) break;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) {
+                            float v[16];
+                            tc::tmem_ld16(sbase + 16 * q4, v);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int j4 = 0; j4 < 4; j4++) {
+                                const uint4 w = make_uint4(__float_as_uint(v[4 * j4]), __float_as_uint(v[4 * j4 + 1]),
+                                                           __float_as_uint(v[4 * j4 + 2]), __float_as_uint(v[4 * j4 + 3]));
+                                tc::st_async_v4(srx_peer + (uint32_t)(((16 * ch + 4 * q4 + j4) * 64 + hp) * 16), w,
+                                                srx_full_peer);
+                            }
+                        }
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(s_free);
+                        need_send = false;
+                    } else if (rdy & 4) {
+                        if (lane == 0) set_error(a.err, HS_ERR_TIMEOUT);
+                        ok = false;
+                    } else {
+                        __nanosleep(20);
+                    }
+                }
+                continue;
+            }
+            // validity of this warp's 64 rows; the next chunk's ids load now
+            // and arrive while this chunk runs
             uint32_t vm[2];
 #pragma unroll
             for (int w2 = 0; w2 < 2; w2++) {
-                const int k = k0 + c * kRowsPerChunk + 64 * ch + 32 * w2 + lane;
-                const int32_t id = k < k1 ? ids[k] : -1;
-                vm[w2] = __ballot_sync(0xffffffffu, id >= 0 && id < a.max_row);
+                vm[w2] = __ballot_sync(0xffffffffu, idn[w2] >= 0 && idn[w2] < a.max_row);
+                const int k = k0 + (c + 1) * kRowsPerChunk + 64 * ch + 32 * w2 + lane;
+                idn[w2] = (c + 1 < nch && k < k1) ? ids[k] : -1;
             }
             if (!(ok = warp_wait(s_full, c & 1, a.err))) {
-                if (own) bar_or(2, 128, true);  // the partners leave at their next barrier
+                bar_or(2, 128, true);  // the partners leave at their next barrier
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t sbase = lane_base + SC + 64 * ch;
-            if (!own) {
-                // ---- send the peer's heads' partial sums of this half chunk, 16
-                // columns at a time (after the peer has read the last chunk's)
-                if (c >= 1 && !(ok = warp_wait_cluster(srx_free, (c - 1) & 1, a.err))) break;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) {
-                    float v[16];
-                    tc::tmem_ld16(sbase + 16 * q4, v);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int j4 = 0; j4 < 4; j4++) {
-                        const uint4 w = make_uint4(__float_as_uint(v[4 * j4]), __float_as_uint(v[4 * j4 + 1]),
-                                                   __float_as_uint(v[4 * j4 + 2]), __float_as_uint(v[4 * j4 + 3]));
-                        tc::st_async_v4(srx_peer + (uint32_t)(((16 * ch + 4 * q4 + j4) * 64 + hp) * 16), w,
-                                        srx_full_peer);
-                    }
-                }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(s_free);
-                // ---- then the peer's P rows and rescale factors of the chunk
-                // before (the send of this chunk goes first: it overlaps the
-                // peer's softmax of the last one)
-                if (c >= 1 && !(ok = sender_finish(c - 1))) break;
-            } else {
+            {
                 float v[64];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; q4++) tc::tmem_ld16(sbase + 16 * q4, v + 16 * q4);
