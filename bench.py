@@ -492,9 +492,11 @@ TRAFFIC = {
     # the scores read once, nothing left to write back (16 x 4 rows of 142,000)
     "topk_cluster_kernel": ("topk.cu", "6797471cd5a693e2", (36.41 + 0.0) / (36.36 + 0.52)),
     # rows, queries and outputs of one layer (64 x 4 queries x 2048 rows x 128 heads)
-    "attn_pair_kernel": ("attention_pair.cu", "868b39f168560587", (354.26 + 27.07) / 415.2),
+    "attn_pair_kernel": ("attention_pair.cu", "9bcd4609f6372c9b", (354.27 + 26.66) / 415.2),
+    # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
+    "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
-    "miss_copy_kernel": ("resolve.cu", "af8aaaeccb960de1", (0.11 + 92.77) / 96.9),
+    "miss_copy_kernel": ("resolve.cu", "f4aa9d9de9e5fd21", (0.62 + 93.02) / 96.9),
 }
 
 
@@ -820,6 +822,7 @@ CASES = {
     "indexer_mtp3_16x131072": "the indexer at four queries per request, 16 x 131,072 tokens",
     "topk_mtp3_16x142000": "top-2048 of 16 x 4 indexer score rows of 142,000 tokens",
     "attention_mtp3_64x4x2048": "one layer of sparse MLA over 64 x 4 queries x 2048 rows, 128 heads",
+    "attention_full_32x2048": "one layer of sparse MLA over 32 queries x 2048 rows, 128 heads",
     "miss_copy_mixed_8x142000": "the miss copy of a first step from empty hot buffers, "
                                 "8 requests x 142,000 tokens, mixed residency, MTP3, 4 layers",
 }
@@ -885,8 +888,8 @@ def run_case(name, reps=3):
         pool.indexer_score(q, w, B, nq, sc, cap)
         out = torch.empty((B, nq, K), dtype=torch.int32, device=dev)
         ts = _timed(lambda i: pool.topk(sc, cap, B, nq, out), reps, flush)
-    elif name == "attention_mtp3_64x4x2048":
-        B, N, nq = 64, 16384, 4
+    elif name in ("attention_mtp3_64x4x2048", "attention_full_32x2048"):
+        B, N, nq = (64, 16384, 4) if name == "attention_mtp3_64x4x2048" else (32, 16384, 1)
         pool = full_pool(B, N, nq, 1, True)
         g = torch.Generator(device=dev).manual_seed(1)
         tk = torch.stack([torch.stack([torch.sort(torch.randperm(N - nq + 1 + j, generator=g, device=dev)[:K])[0]
