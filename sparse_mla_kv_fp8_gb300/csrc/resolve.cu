@@ -240,7 +240,24 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         const uint32_t *stp = a.stamp + sc;
         uint32_t prefix = 0, mask = 0;
         int Ms = M, need = M;
-        for (int pass = 0; pass < 4; pass++) {
+        // Digits above the highest bit set in any candidate stamp are 0 for
+        // every candidate and decide nothing: start at the first digit that
+        // can differ (stamps are step numbers, so usually the last one).
+        // Skipping them also skips histograms whose every count lands in
+        // bin 0, where the increments would run one after another.
+        uint32_t orv = 0;
+        for (int s = tid; s < a.C; s += kThreads) {
+            const uint32_t v = stp[s];
+            if (v < step) orv |= v;
+        }
+        orv = __reduce_or_sync(0xffffffffu, orv);
+        if ((tid & 31) == 0) warp_sums[tid >> 5] = (int)orv;
+        __syncthreads();
+        orv = 0;
+        for (int w = 0; w < kThreads / 32; w++) orv |= (uint32_t)warp_sums[w];
+        __syncthreads();
+        const int first = orv == 0 ? 3 : 3 - (31 - __clz(orv)) / 8;
+        for (int pass = first; pass < 4; pass++) {
             const int shift = 24 - 8 * pass;
             if (tid < 256) hist[tid] = 0;
             __syncthreads();
@@ -252,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
             const int c = tid < 256 ? (int)hist[tid] : 0;
             int tot;
             const int ex = block_excl_scan(c, warp_sums, &tot);
-            if (pass == 0 && tot < Ms) {  // uniform: tot is the block's total
+            if (pass == first && tot < Ms) {  // uniform: tot is the block's total
                 if (tid == 0) set_error(a.err, HS_ERR_CAPACITY);
                 Ms = need = tot;
             }
