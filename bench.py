@@ -269,13 +269,10 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
         scrub.max()    # ... then read another, so the write-back of those dirty lines lands here
 
     def enqueue_step(st):
-        if drawn:
-            # the indexer and top-K on their own inputs, the resolve and the
-            # attention (hs_resolve_attend) on the trace's lists
-            pool.indexer_topk(q, wt, B, nq, topk, stream=st)
-            pool.resolve_attend(trace.buf, B, nq, qm, tau, out, rid, stream=st)
-        else:
-            pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=st)
+        # drawn workloads: the indexer and top-K on their own inputs, the
+        # resolve and the attention on the trace's lists (topk_in)
+        pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=st,
+                  topk_in=trace.buf if drawn else None)
 
     def load(i, s):
         a, b_, c = inputs[i % n_inputs]
@@ -648,11 +645,8 @@ def end_to_end(pool, w, inputs, trace, stream, steps, device, first_step):
         stream.wait_event(in_done[i])
         if i >= 2:
             stream.wait_event(out_done[i - 2])  # step i-2's output has left this buffer
-        if drawn:
-            pool.indexer_topk(q, wt, B, nq, topk, stream=stream)
-            pool.resolve_attend(tk_in, B, nq, qm, tau, out, rid, stream=stream)
-        else:
-            pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream)
+        pool.step(B, nq, q, wt, qm, tau, out, topk, rid, stream=stream,
+                  topk_in=tk_in if drawn else None)
         comp_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])

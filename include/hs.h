@@ -427,12 +427,19 @@ typedef struct {
     float *lse;           /* dev [L][B][nq][H] fp32, or NULL                 */
     int32_t *topk;        /* dev [B][nq][K] int32 (output)                   */
     int32_t *row_id;      /* dev [B][nq][K] int32 (output)                   */
+    const int32_t *topk_in; /* dev [B][nq][K] int32, or NULL: lists for the  */
+                            /* resolve in place of the indexer's top-K (which */
+                            /* is still computed and written to topk)         */
 } hs_step_args;
 
 /* One decode step of one IndexShare group: indexer score -> top-K ->
  * fused resolve (with miss copies) -> sparse MLA decode for each of the L
- * layers, i.e. the indexer's top-K followed by hs_resolve_attend.  Enqueued
- * on `stream`; no host synchronisation. */
+ * layers, i.e. the indexer's top-K followed by hs_resolve_attend (of
+ * topk_in when it is given).  Enqueued on `stream`; no host
+ * synchronisation.  With a host pool and B >= 2 the batch runs as two halves
+ * of the requests, so that the first half's miss copies (on the pool's side
+ * stream) run while the second half is scored and selected: the results are
+ * those of the whole batch in one pass. */
 hs_status hs_step(hs_pool *pool, const hs_step_args *args, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */

@@ -58,7 +58,7 @@ class hs_layout(ctypes.Structure):
 class hs_step_args(ctypes.Structure):
     _fields_ = [("B", _i32), ("nq", _i32), ("q_idx", _vp), ("w_idx", _vp), ("q_mla", _vp),
                 ("softmax_scale", _f32), ("out", _vp), ("lse", _vp), ("topk", _vp),
-                ("row_id", _vp)]
+                ("row_id", _vp), ("topk_in", _vp)]
 
 
 def _decl(name, res, args):
@@ -292,10 +292,12 @@ class Pool:
         check(hs_check_wait_timeout(self.handle, limit_cycles, _stream(stream)),
               "hs_check_wait_timeout")
 
-    def step(self, B, nq, q_idx, w_idx, q_mla, scale, out, topk, row_id, lse=None, stream=None):
+    def step(self, B, nq, q_idx, w_idx, q_mla, scale, out, topk, row_id, lse=None, stream=None,
+             topk_in=None):
         a = hs_step_args(B=B, nq=nq, q_idx=_dev(q_idx, "q_idx"), w_idx=_dev(w_idx, "w_idx"),
                          q_mla=_dev(q_mla, "q_mla"), softmax_scale=scale, out=_dev(out, "out"),
-                         lse=_dev(lse, "lse"), topk=_dev(topk, "topk"), row_id=_dev(row_id, "row_id"))
+                         lse=_dev(lse, "lse"), topk=_dev(topk, "topk"), row_id=_dev(row_id, "row_id"),
+                         topk_in=_dev(topk_in, "topk_in"))
         check(hs_step(self.handle, ctypes.byref(a), _stream(stream)), "hs_step")
 
     def resolve_attend(self, topk, B, nq, q_mla, scale, out, row_id, lse=None, stream=None):

@@ -137,6 +137,7 @@ class Runner:
         row_id = torch.full((B, nq, c.K), -7, dtype=torch.int32, device=self.dev)
         out = torch.empty((c.L, B, nq, c.H, 512), dtype=torch.bfloat16, device=self.dev)
         lse = torch.empty((c.L, B, nq, c.H), dtype=torch.float32, device=self.dev)
+        own_topk = None  # a step fed drawn lists still selects with its own indexer
         if c.source == "indexer":
             ref_idx = self.oracle_topk(q, w)
             if c.use_step:
@@ -145,15 +146,21 @@ class Runner:
                 self.pool.indexer_topk(q, w, B, nq, topk)
         else:
             ref_idx = self.drawn(s)
-            topk.copy_(torch.from_numpy(ref_idx).to(self.dev))
-        if not c.use_step or c.source != "indexer":
+            if c.use_step:  # the step's resolve and attention take the drawn lists
+                own_topk = self.oracle_topk(q, w)
+                tk_in = torch.from_numpy(ref_idx).to(self.dev)
+                self.pool.step(B, nq, q, w, qm, self.tau, out, topk, row_id, lse, topk_in=tk_in)
+            else:
+                topk.copy_(torch.from_numpy(ref_idx).to(self.dev))
+        if not c.use_step:
             self.pool.resolve(topk, B, nq, row_id)
             for l in range(c.L):
                 self.pool.sparse_mla_decode(l, qm[l], row_id, B, nq, self.tau, out[l], lse[l])
         torch.cuda.synchronize()
         err = self.pool.get_error()
         got_idx = topk.cpu().numpy()
-        np.testing.assert_array_equal(got_idx, ref_idx, err_msg=f"{c.name} step {s}: top-K")
+        np.testing.assert_array_equal(got_idx, ref_idx if own_topk is None else own_topk,
+                                      err_msg=f"{c.name} step {s}: top-K")
         # oracle resolve
         res = []
         short = False
