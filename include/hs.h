@@ -436,10 +436,7 @@ typedef struct {
  * fused resolve (with miss copies) -> sparse MLA decode for each of the L
  * layers, i.e. the indexer's top-K followed by hs_resolve_attend (of
  * topk_in when it is given).  Enqueued on `stream`; no host
- * synchronisation.  With a host pool and B >= 2 the batch runs as two halves
- * of the requests, so that the first half's miss copies (on the pool's side
- * stream) run while the second half is scored and selected: the results are
- * those of the whole batch in one pass. */
+ * synchronisation. */
 hs_status hs_step(hs_pool *pool, const hs_step_args *args, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */

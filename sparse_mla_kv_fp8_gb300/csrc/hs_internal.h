@@ -123,8 +123,7 @@ struct hs_pool {
     cudaStream_t copy_stream;
     int copy_priority;
     cudaEvent_t ev_plan;
-    cudaEvent_t ev_plan2[2];           // the two halves of a step
-    std::vector<cudaEvent_t> ev_copy;  // [2][L]
+    std::vector<cudaEvent_t> ev_copy;  // [L]
 };
 
 namespace hs {
@@ -135,23 +134,17 @@ __device__ __forceinline__ void set_error(int32_t *err, int code) {
 }
 
 // ---- launchers (each returns cudaGetLastError() after enqueueing) ----
-// b0: the batch is requests [b0, b0 + B) of the pool (batch index b is request
-// b0 + b); the caller's pointers (queries, scores, lists, outputs) start at
-// the batch's first entry.
-// sm_budget > 0: the tensor-core indexer's grid takes at most that many SMs
-// (one wave), leaving the others to a kernel beside it.
 cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w, int B, int nq,
-                                 float *scores, int64_t stride, cudaStream_t st, int b0 = 0,
-                                 int sm_budget = 0);
+                                 float *scores, int64_t stride, cudaStream_t st);
 cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, int B, int nq,
-                        int32_t *topk, cudaStream_t st, int b0 = 0);
+                        int32_t *topk, cudaStream_t st);
 cudaError_t launch_resolve(const hs_pool *p, const int32_t *topk, int B, int nq, int32_t *row_id,
                            cudaStream_t st);
 cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, int nq,
-                                int32_t *row_id, cudaStream_t st, int b0 = 0);
+                                int32_t *row_id, cudaStream_t st);
 // Miss rows of layers [l0, l1) (l1 < 0: through the last layer).
 cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0 = 0,
-                             int l1 = -1, int ctas = 0, int priority = 0, int b0 = 0);
+                             int l1 = -1, int ctas = 0, int priority = 0);
 // q_ready: the queries were written before the previous kernel on `st`
 // started (true inside hs_step), so the kernel may stage them before it waits
 // for that kernel.

@@ -110,7 +110,6 @@ struct IdxTcArgs {
     float *scores;
     int64_t stride;
     int nq, Hi, maxT, tiles_per_cta, ncols, tmem_cols;
-    int b0;  // the batch's first request (its keys' rows in the TMA map)
     int32_t *err;
 };
 
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!tc::mbar_wait(&empty[s], ph ^ 1, a.err)) break;
                 tc::mbar_expect_tx(&full[s], kTileBytes);
                 tc::tma_load_2d(ks + s * kTileBytes, &kmap, &full[s], 0,
-                                (a.b0 + b) * a.maxT + (tile0 + it) * kTile);
+                                b * a.maxT + (tile0 + it) * kTile);
                 issued++;
             }
             // never leave with a copy in flight
@@ -325,17 +324,14 @@ int indexer_kernel_count(const hs_pool *, int, int) { return 1; }
 // Tiles per CTA for a grid of (chunks, B), given how many CTAs fit on one
 // SM: minimise waves x (tiles per CTA + the fixed cost of starting a CTA,
 // about four tiles' worth: TMEM allocation, query staging, pipeline fill).
-// With sm_budget > 0 the grid is one wave on that many SMs, so that the
-// other SMs stay free for a kernel running beside it.
-static int pick_tiles_per_cta(int ntiles, int B, int per_sm, int sm_budget) {
-    const long slots = (long)(sm_budget > 0 ? sm_budget : kNumSMs) * per_sm;
+static int pick_tiles_per_cta(int ntiles, int B, int per_sm) {
+    const long slots = (long)kNumSMs * per_sm;
     int best = ntiles;
     double best_t = 1e30;
     for (int tpc = 1; tpc <= ntiles; tpc++) {
         const long chunks = (ntiles + tpc - 1) / tpc;
         const long ctas = chunks * B;
         const long waves = (ctas + slots - 1) / slots;
-        if (sm_budget > 0 && waves > 1) continue;
         const double t = (double)waves * (tpc + 4.0);
         if (t < best_t) {
             best_t = t;
@@ -346,16 +342,14 @@ static int pick_tiles_per_cta(int ntiles, int B, int per_sm, int sm_budget) {
 }
 
 cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w, int B, int nq,
-                                 float *scores, int64_t stride, cudaStream_t st, int b0,
-                                 int sm_budget) {
+                                 float *scores, int64_t stride, cudaStream_t st) {
     const int maxT = p->cfg.max_tokens;
     if (tc_eligible(p, nq)) {
         IdxTcArgs a;
         a.q = (const uint8_t *)q;
         a.w = w;
-        a.ksc = p->d.idx_scale + (size_t)b0 * maxT;
-        a.seq_len = p->d.seq_len + b0;
-        a.b0 = b0;
+        a.ksc = p->d.idx_scale;
+        a.seq_len = p->d.seq_len;
         a.scores = scores;
         a.stride = stride;
         a.nq = nq;
@@ -373,7 +367,7 @@ cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w
         if (per_sm == 1 && smem < 116 * 1024) smem = 116 * 1024;
         else if (smem < cap && per_sm_tmem < per_sm_smem) smem = cap;
         const int ntiles = (maxT + kTile - 1) / kTile;
-        a.tiles_per_cta = pick_tiles_per_cta(ntiles, B, per_sm, sm_budget);
+        a.tiles_per_cta = pick_tiles_per_cta(ntiles, B, per_sm);
         dim3 grid((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta, B);
         // one group of four epilogue warps per query (up to four groups)
         const int threads = 64 + 128 * (nq < kTcMaxGroups ? nq : kTcMaxGroups);
@@ -382,14 +376,13 @@ cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w
     }
     dim3 grid((maxT + kTile - 1) / kTile, B);
     const size_t sm = simt_smem(p, nq);
-    const size_t kofs = (size_t)b0 * maxT * p->cfg.idx_dim * p->idx_esize;  // bytes
     if (p->cfg.idx_fmt == HS_IDX_E4M3)
-        indexer_simt_kernel<0><<<grid, kTile, sm, st>>>(q, w, p->d.idx_keys + kofs, p->d.idx_scale + (size_t)b0 * maxT,
-                                                         p->d.seq_len + b0, nq, p->cfg.idx_heads,
+        indexer_simt_kernel<0><<<grid, kTile, sm, st>>>(q, w, p->d.idx_keys, p->d.idx_scale,
+                                                         p->d.seq_len, nq, p->cfg.idx_heads,
                                                          p->cfg.idx_dim, maxT, scores, stride);
     else
-        indexer_simt_kernel<1><<<grid, kTile, sm, st>>>(q, w, p->d.idx_keys + kofs, p->d.idx_scale + (size_t)b0 * maxT,
-                                                         p->d.seq_len + b0, nq, p->cfg.idx_heads,
+        indexer_simt_kernel<1><<<grid, kTile, sm, st>>>(q, w, p->d.idx_keys, p->d.idx_scale,
+                                                         p->d.seq_len, nq, p->cfg.idx_heads,
                                                          p->cfg.idx_dim, maxT, scores, stride);
     return cudaGetLastError();
 }

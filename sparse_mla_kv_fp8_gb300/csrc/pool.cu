@@ -260,7 +260,7 @@ int64_t blocks_in_mode(const hs_pool *p, int32_t req, int mode) {
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 103; }
+int32_t hs_abi_version(void) { return 104; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -370,7 +370,6 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->copy_stream = nullptr;
     p->copy_priority = 0;
     p->ev_plan = nullptr;
-    p->ev_plan2[0] = p->ev_plan2[1] = nullptr;
     p->free_gpu.resize(cfg->gpu_blocks);
     for (int64_t i = 0; i < cfg->gpu_blocks; i++) p->free_gpu[i] = (int32_t)(cfg->gpu_blocks - 1 - i);
     p->free_host.resize(cfg->host_blocks);
@@ -400,11 +399,9 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
         p->copy_priority = hi;
         if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->copy_stream, cudaStreamNonBlocking, hi);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_plan, cudaEventDisableTiming);
-        p->ev_copy.assign(2 * cfg->num_mla_layers, nullptr);  // two halves of a step
-        for (int l = 0; l < 2 * cfg->num_mla_layers && e == cudaSuccess; l++)
+        p->ev_copy.assign(cfg->num_mla_layers, nullptr);
+        for (int l = 0; l < cfg->num_mla_layers && e == cudaSuccess; l++)
             e = cudaEventCreateWithFlags(&p->ev_copy[l], cudaEventDisableTiming);
-        for (int h = 0; h < 2 && e == cudaSuccess; h++)
-            e = cudaEventCreateWithFlags(&p->ev_plan2[h], cudaEventDisableTiming);
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -426,8 +423,6 @@ void hs_pool_destroy(hs_pool *pool) {
         cudaStreamDestroy(pool->copy_stream);
     }
     if (pool->ev_plan) cudaEventDestroy(pool->ev_plan);
-    for (cudaEvent_t ev : pool->ev_plan2)
-        if (ev) cudaEventDestroy(ev);
     for (cudaEvent_t ev : pool->ev_copy)
         if (ev) cudaEventDestroy(ev);
     delete pool;
@@ -851,59 +846,11 @@ hs_status hs_resolve_attend(hs_pool *p, const int32_t *topk, int32_t B, int32_t 
                                       false));
 }
 
-// The step in two halves of the requests (with a host pool): half h's
-// indexer, top-K and plan on `st`, then its layer copies on the side stream;
-// half 1 is scored while half 0's rows cross the host link.  Then each
-// half's attention, layer by layer, each after its layer's copy.
-static cudaError_t step_halves(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
-    const int B = a->B, nq = a->nq, L = p->cfg.num_mla_layers, K = p->cfg.top_k;
-    const int H = p->cfg.mla_heads, Hi = p->cfg.idx_heads, Di = p->cfg.idx_dim;
-    const int b0s[2] = {0, B / 2}, nbs[2] = {B / 2, B - B / 2};
-    cudaError_t e = cudaSuccess;
-    for (int h = 0; h < 2 && e == cudaSuccess; h++) {
-        const int b0 = b0s[h], nb = nbs[h];
-        const uint8_t *q = (const uint8_t *)a->q_idx + (size_t)b0 * nq * Hi * Di * p->idx_esize;
-        const float *w = a->w_idx + (size_t)b0 * nq * Hi;
-        int32_t *tk = a->topk + (size_t)b0 * nq * K;
-        const int32_t *lists = a->topk_in ? a->topk_in + (size_t)b0 * nq * K : tk;
-        // the second half is scored while the first half's rows are copied:
-        // its indexer (long-lived CTAs) leaves the copy's SMs free
-        e = hs::launch_indexer_score(p, q, w, nb, nq, p->d.scores, p->score_stride, st, b0,
-                                     h == 1 ? hs::kNumSMs - kCopyCtasBeside : 0);
-        if (e == cudaSuccess) e = hs::launch_topk(p, p->d.scores, p->score_stride, nb, nq, tk, st, b0);
-        if (e == cudaSuccess)
-            e = hs::launch_resolve_plan(p, lists, nb, nq, a->row_id + (size_t)b0 * nq * K, st, b0);
-        if (e == cudaSuccess) e = cudaEventRecord(p->ev_plan2[h], st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_stream, p->ev_plan2[h], 0);
-        for (int l = 0; l < L && e == cudaSuccess; l++) {
-            e = hs::launch_miss_copy(p, nb, nq, p->copy_stream, l, l + 1, kCopyCtasBeside,
-                                     p->copy_priority, b0);
-            if (e == cudaSuccess) e = cudaEventRecord(p->ev_copy[h * L + l], p->copy_stream);
-        }
-    }
-    for (int h = 0; h < 2 && e == cudaSuccess; h++) {
-        const int b0 = b0s[h], nb = nbs[h];
-        for (int l = 0; l < L && e == cudaSuccess; l++) {
-            e = cudaStreamWaitEvent(st, p->ev_copy[h * L + l], 0);
-            const size_t qo = ((size_t)l * B + b0) * nq * H * hs::kLatent * 2;
-            const size_t oo = ((size_t)l * B + b0) * nq * H * hs::kNope * 2;
-            if (e == cudaSuccess)
-                e = hs::launch_attention(p, l, (const uint8_t *)a->q_mla + qo,
-                                         a->row_id + (size_t)b0 * nq * K, nb, nq, a->softmax_scale,
-                                         (uint8_t *)a->out + oo,
-                                         a->lse ? a->lse + ((size_t)l * B + b0) * nq * H : nullptr, st,
-                                         true, false);
-        }
-    }
-    return e;
-}
-
 hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
     if (!a || !step_batch_ok(p, a->B, a->nq) || !a->q_idx || !a->w_idx || !a->q_mla || !a->out ||
         !a->topk || !a->row_id || !aligned16(a->q_mla) || !aligned16(a->out))
         return HS_ERR_INVALID_ARG;
     const int B = a->B, nq = a->nq;
-    if (p->cfg.host_blocks > 0 && B >= 2) return cuda_status(step_halves(p, a, st));
     cudaError_t e = hs::launch_indexer_score(p, a->q_idx, a->w_idx, B, nq, p->d.scores,
                                              p->score_stride, st);
     if (e == cudaSuccess) e = hs::launch_topk(p, p->d.scores, p->score_stride, B, nq, a->topk, st);
@@ -915,15 +862,10 @@ hs_status hs_step(hs_pool *p, const hs_step_args *a, cudaStream_t st) {
 
 int32_t hs_step_kernel_count(const hs_pool *p, int32_t B, int32_t nq) {
     if (!p || B <= 0 || B > p->cfg.max_requests || nq <= 0 || nq > p->nq_max) return -1;
-    // the step's resolve is the plan plus, with a host pool, one copy per
-    // layer; with a host pool and B >= 2, all of it for each half of the batch
+    // the step's resolve is the plan plus, with a host pool, one copy per layer
     const int L = p->cfg.num_mla_layers;
-    auto one = [&](int b) {
-        return hs::indexer_kernel_count(p, b, nq) + hs::topk_kernel_count(p, b, nq) + 1 +
-               (p->cfg.host_blocks > 0 ? L : 0) + L * hs::attention_kernel_count(p, b, nq);
-    };
-    if (p->cfg.host_blocks > 0 && B >= 2) return one(B / 2) + one(B - B / 2);
-    return one(B);
+    return hs::indexer_kernel_count(p, B, nq) + hs::topk_kernel_count(p, B, nq) + 1 +
+           (p->cfg.host_blocks > 0 ? L : 0) + L * hs::attention_kernel_count(p, B, nq);
 }
 
 hs_status hs_pool_get_error(hs_pool *p, hs_status *out) {

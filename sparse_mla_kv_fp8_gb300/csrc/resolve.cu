@@ -435,7 +435,7 @@ cudaError_t resolve_setup(const hs_pool *p) {
 int resolve_kernel_count(const hs_pool *p, int, int) { return p->cfg.host_blocks > 0 ? 2 : 1; }
 
 cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, int nq,
-                                int32_t *row_id, cudaStream_t st, int b0) {
+                                int32_t *row_id, cudaStream_t st) {
     PlanArgs a;
     a.topk = topk;
     a.nq = nq;
@@ -447,16 +447,16 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
     a.max_pages = p->max_pages;
     a.L = p->cfg.num_mla_layers;
     a.R = p->R;
-    a.seq_len = p->d.seq_len + b0;
-    a.block_table = p->d.block_table + (size_t)b0 * p->max_pages;
-    a.hot_map = p->d.hot_map + (size_t)b0 * p->cfg.max_tokens;
-    a.slot_token = p->d.slot_token + (size_t)b0 * p->C;
-    a.stamp = p->d.stamp + (size_t)b0 * p->C;
-    a.hot_blocks = p->d.hot_blocks + (size_t)b0 * p->hot_pages;
-    a.req_step = p->d.req_step + b0;
-    a.miss_count = p->d.miss_count + b0;
-    a.miss_tok = p->d.miss_tok + (size_t)b0 * nq * p->cfg.top_k;
-    a.miss_slot = p->d.miss_slot + (size_t)b0 * nq * p->cfg.top_k;
+    a.seq_len = p->d.seq_len;
+    a.block_table = p->d.block_table;
+    a.hot_map = p->d.hot_map;
+    a.slot_token = p->d.slot_token;
+    a.stamp = p->d.stamp;
+    a.hot_blocks = p->d.hot_blocks;
+    a.req_step = p->d.req_step;
+    a.miss_count = p->d.miss_count;
+    a.miss_tok = p->d.miss_tok;
+    a.miss_slot = p->d.miss_slot;
     a.row_id = row_id;
     a.err = p->d.err;
     a.stats = p->d.stats;
@@ -470,13 +470,13 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
 }
 
 // The miss copy of the last plan (its miss lists stay in the pool's workspace
-// until the next plan), layers [l0, l1), requests [b0, b0 + B).  ctas = 0: about four CTAs per SM
+// until the next plan), layers [l0, l1).  ctas = 0: about four CTAs per SM
 // over the batch (the copy alone); otherwise about that many CTAs in all (a
 // copy beside another kernel, which keeps the other SMs).  priority (0 =
 // none) goes to the launch, so that the copy's CTAs take SMs as they free up
 // before a lower-priority kernel's.
 cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, int l0, int l1,
-                             int ctas, int priority, int b0) {
+                             int ctas, int priority) {
     const int n = nq * p->cfg.top_k;
     if (l1 < 0) l1 = p->cfg.num_mla_layers;
     if (p->cfg.host_blocks > 0) {
@@ -490,12 +490,10 @@ cudaError_t launch_miss_copy(const hs_pool *p, int B, int nq, cudaStream_t st, i
             lc.attrs[0].val.priority = priority;
             lc.cfg.numAttrs = 1;
         }
-        const size_t ml = (size_t)b0 * n;  // the batch's miss lists and tables
-        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count + b0,
-                                           (const int32_t *)p->d.miss_tok + ml, (const int32_t *)p->d.miss_slot + ml,
-                                           n, (const int32_t *)p->d.host_block_table + (size_t)b0 * p->max_pages,
-                                           (const int32_t *)p->d.hot_blocks + (size_t)b0 * p->hot_pages,
-                                           (const uint8_t *)p->host_dev,
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, miss_copy_kernel, (const int32_t *)p->d.miss_count,
+                                           (const int32_t *)p->d.miss_tok, (const int32_t *)p->d.miss_slot,
+                                           n, (const int32_t *)p->d.host_block_table,
+                                           (const int32_t *)p->d.hot_blocks, (const uint8_t *)p->host_dev,
                                            p->d.rows, p->cfg.num_mla_layers, l0, l1, p->cfg.page_tokens,
                                            p->R, p->max_pages, p->hot_pages, p->d.err);
         if (e != cudaSuccess) return e;

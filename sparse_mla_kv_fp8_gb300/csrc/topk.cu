@@ -492,9 +492,8 @@ int topk_kernel_count(const hs_pool *p, int B, int nq) {
 }
 
 cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, int B, int nq,
-                        int32_t *topk, cudaStream_t st, int b0) {
+                        int32_t *topk, cudaStream_t st) {
     const int rows = B * nq, nch = p->topk_nchunks, K = p->cfg.top_k;
-    const int32_t *seq_len = p->d.seq_len + b0;  // the batch's requests
     const int E = cluster_elems(p->cfg.max_tokens, rows);
     if (E) {
         const int G = (p->cfg.max_tokens + kClusterThreads * E - 1) / (kClusterThreads * E);
@@ -503,11 +502,11 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
         const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
         if (E == 16)
             return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<16>, scores, stride, vec4,
-                                      seq_len, nq, K, topk);
+                                      (const int32_t *)p->d.seq_len, nq, K, topk);
         return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<32>, scores, stride, vec4,
-                                  seq_len, nq, K, topk);
+                                  (const int32_t *)p->d.seq_len, nq, K, topk);
     }
-    topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, seq_len, nq, K,
+    topk_init_kernel<<<rows, 256, 0, st>>>(p->d.topk_state, p->d.topk_hist, p->d.seq_len, nq, K,
                                             p->cfg.max_tokens);
     dim3 grid(nch, rows);
     for (int pass = 0; pass < 3; pass++)

@@ -114,17 +114,15 @@ def test_hs_step_matches_separate_calls():
 
 
 @pytest.mark.parametrize("B,nq,mode", [(5, 4, 1), (6, 1, 2), (2, 2, 1)])
-def test_step_in_two_halves_with_given_lists(B, nq, mode):
-    """hs_step with a host pool runs the batch as two halves of the requests
-    (the first half's miss copies beside the second half's indexer and
-    top-K) and takes the lists to resolve from topk_in when given: every
-    step against the oracle, the step's own top-K bit-exact against the
-    oracle's indexer, the resolve, hot-buffer state, rows and attention
-    against the drawn lists; odd and even batches, MTP and one query, mixed
-    and zero residency."""
+def test_step_with_given_lists(B, nq, mode):
+    """hs_step takes the lists to resolve from topk_in when given, while its
+    indexer and top-K still run: every step against the oracle, the step's
+    own top-K bit-exact against the oracle's indexer, the resolve, hot-buffer
+    state, rows and attention against the drawn lists; MTP and one query,
+    mixed and zero residency, with appends between steps."""
     from harness import Case
     hs = _hs()
-    c = Case("step-halves", B=B, N=[1900 + 211 * i for i in range(B)], K=128, Hi=8, Di=32, H=16,
+    c = Case("step-given", B=B, N=[1900 + 211 * i for i in range(B)], K=128, Hi=8, Di=32, H=16,
              L=2, T=128, num_spec=nq - 1, mode=mode, steps=4, source="recency_zipf",
              use_step=True, append=1)
     _run(c)
