@@ -468,6 +468,18 @@ KERNELS = {"indexer": "indexer_tc_kernel", "topk": "topk_cluster_kernel",
            "attention": "attn_tc_kernel"}
 
 
+def topk_kernel(w, max_tokens):
+    """The top-K kernels a batch takes (the library's dispatch): the one-launch
+    cluster kernel while every row's cluster of 1024 x 16 keys fits one wave
+    of the 152 SMs, else the sampled-threshold path (threshold, filter,
+    select), whose filter pass over the scores dominates."""
+    ctas16 = -(-max_tokens // (1024 * 16))
+    rows = w["B"] * w["nq"]
+    if w["K"] > 2048 or (ctas16 <= 8 and rows * ctas16 <= 152):
+        return "topk_cluster_kernel"
+    return "topk_filter_kernel"
+
+
 def attention_kernel(w):
     """The tensor-core attention a batch takes: the latent-split pair kernel
     from 64 (query, 128-head group) pairs up, the 64-head kernel below."""
@@ -534,7 +546,8 @@ def roofline(stage, alg, peaks, w, ms_per_step, link):
         if ms <= 0:
             continue
         a = alg[k]
-        kern = attention_kernel(w) if k == "attention" else KERNELS[k]
+        kern = (attention_kernel(w) if k == "attention"
+                else topk_kernel(w, -(-w["N"] // w["P"]) * w["P"]) if k == "topk" else KERNELS[k])
         traffic = traffic_of(kern, a["bytes"])
         gbs = a["bytes"] / (ms / 1e3) / 1e9
         share = ms * n / ms_per_step

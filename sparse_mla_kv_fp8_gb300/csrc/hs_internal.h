@@ -16,6 +16,8 @@ constexpr int kNope = 512;
 constexpr int kRope = 64;
 constexpr int kTopkChunk = 8192;   // scores per CTA in the top-K passes
 constexpr int kTopkBins = 2048;    // 11-bit digit
+constexpr int kTopkCandCap = 8192;    // candidates a row keeps in the sampled-threshold top-K
+constexpr int kTopkSampledMaxK = 2048;  // largest K that path takes
 constexpr int kMaxSplits = 32;     // split-K partials per attention query
 constexpr int kNumSMs = 152;       // GB300
 
@@ -78,6 +80,7 @@ struct DevPtrs {
     TopkRowState *topk_state;   // [maxR*nq]
     uint32_t *topk_hist;        // [maxR*nq][kTopkBins]
     int32_t *topk_chunk;        // [maxR*nq][nchunks][2]
+    uint2 *topk_cand;           // [maxR*nq][kTopkCandCap] (key, token); null when K > kTopkSampledMaxK
     int32_t *miss_count;        // [maxR]
     int32_t *miss_tok;          // [maxR][nq*K]
     int32_t *miss_slot;         // [maxR][nq*K]

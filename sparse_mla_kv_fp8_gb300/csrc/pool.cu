@@ -131,6 +131,9 @@ hs_layout carve(const hs_pool_config *c, const Derived &d, size_t *extra_offs /*
     extra_offs[7] = cv.take(maxR * (size_t)d.nq * c->top_k * 4);      // miss tok
     extra_offs[8] = cv.take(maxR * (size_t)d.nq * c->top_k * 4);      // miss slot
     extra_offs[9] = cv.take(d.attn_part_floats * 4 + 16);             // attention partials
+    extra_offs[10] = c->top_k <= hs::kTopkSampledMaxK                 // top-K candidates
+                         ? cv.take(rows * (size_t)hs::kTopkCandCap * 8)
+                         : 0;
     L.row_bytes = d.R;
     L.max_pages = d.max_pages;
     L.hot_rows = d.C;
@@ -349,6 +352,7 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
     p->d.miss_tok = (int32_t *)(b + extra[7]);
     p->d.miss_slot = (int32_t *)(b + extra[8]);
     p->d.attn_part = (float *)(b + extra[9]);
+    p->d.topk_cand = cfg->top_k <= hs::kTopkSampledMaxK ? (uint2 *)(b + extra[10]) : nullptr;
 
     p->has_key_map = false;
     if (cfg->idx_fmt == HS_IDX_E4M3 && cfg->idx_dim == 128) {

@@ -11,6 +11,7 @@
 // keys above / equal to T and write the selected indices in ascending token
 // order (keys equal to T are taken lowest index first).  Every count is an
 // integer, so the result is bit-for-bit deterministic.
+#include <algorithm>
 #include <mutex>
 
 #include "hs_internal.h"
@@ -461,6 +462,519 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
     tc::cluster_sync();  // peers may still be reading this CTA's totals
 }
 
+// ---------------------------------------------------------------------------
+// Sampled-threshold top-K (K <= kTopkSampledMaxK, rows of any length).
+//
+// The radix passes above touch every score three times, with an atomic per
+// still-undecided key, and at K / N of a few percent almost every key is
+// decided against the threshold long before the last digit.  This path
+// touches each score once, with a compare:
+//   1. topk_thresh_kernel, one CTA per row: T = the order key of the r-th
+//      largest of S evenly spaced scores of the row, with r chosen so that
+//      about m = max(2.5 K, 2048) tokens are expected at or above T (a
+//      sample quantile: relative spread about 1 / sqrt(r), r >= 80 here).
+//      Rows of at most kTopkCandCap visible tokens take T = 0: all are
+//      candidates.
+//   2. topk_filter_kernel, (chunk, row) CTAs: one coalesced pass; every
+//      visible token with key >= T is appended (key, token) to the row's
+//      candidate list, one atomic per CTA reserving its range.
+//   3. topk_select_kernel, one CTA per row.  When the row kept between K and
+//      kTopkCandCap candidates, they contain every token of the exact top-K:
+//      the K-th largest key of the row is then >= T, and every token at or
+//      above T is a candidate.  A radix select over the candidates (held in
+//      registers) gives the exact threshold key and the number of keys equal
+//      to it to take; bitmaps over windows of the token range then write the
+//      selection in ascending token order, equal keys lowest token first.
+//      When the sample misjudged the row (fewer than K or more than the cap),
+//      the same CTA runs the exact radix select over the whole row instead.
+// Either way the result is the multi-kernel path's, bit for bit.
+// ---------------------------------------------------------------------------
+// Tokens the sampled threshold aims to keep per row: 2.5 K, at least 2048.
+// With the sample sizes below (r >= 80 of the sampled scores at or above
+// the threshold) the kept count stays within +-60 % of this, so between K
+// and the 8192-candidate cap, by more than five times its spread.
+__host__ __device__ constexpr int64_t sampled_target(int K) {
+    return (5 * (int64_t)K) / 2 > 2048 ? (5 * (int64_t)K) / 2 : 2048;
+}
+
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelE = kTopkCandCap / kSelThreads;  // candidates per thread
+constexpr int kFiltThreads = 256;
+constexpr int kFiltE = 16;                         // scores per lane and tile
+constexpr int kFiltTile = 32 * kFiltE;             // tokens per warp tile
+constexpr int kDigitBins = 4096;                   // 12-bit digits
+constexpr int kCoarseBins = kDigitBins / 32;
+constexpr int kWinWords = 4096;                    // bitmap words per window
+constexpr int kWinTokens = kWinWords * 32;
+constexpr int kWordsPer = kWinWords / kSelThreads;  // 16, consecutive per thread
+// Thread t's words sit at t * 17 + q: the 32 lanes reading their q-th words
+// hit 32 different banks.
+constexpr int kWinPadded = kWinWords / kWordsPer * (kWordsPer + 1);
+__device__ __forceinline__ int padded_word(int w) { return w + w / kWordsPer; }
+
+// Shared memory of a selecting CTA: the digit histograms while the
+// threshold is found, then the window bitmaps.  16-byte aligned: the
+// histograms are cleared and read with 16-byte accesses.
+struct __align__(16) SelSmem {
+    union {
+        struct {
+            uint32_t fine[kDigitBins];     // keys in play per digit
+            uint32_t coarse[kCoarseBins];  // per 32 consecutive digits
+        } h;
+        struct {
+            uint32_t gt[kWinPadded], eq[kWinPadded];
+        } w;
+    };
+    uint32_t decided[2];
+    int warp_sums[32];
+    int tot[2];
+};
+// The select kernel's dynamic shared memory: SelSmem, the candidates'
+// tokens, then the selection in output order (copied out coalesced).
+constexpr size_t kSelDynSmem = sizeof(SelSmem) + (size_t)kTopkCandCap * 4 + kTopkSampledMaxK * 4;
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Block-wide smallest and largest of the keys, returned to every thread.
+__device__ __forceinline__ void block_minmax(uint32_t &lo, uint32_t &hi, SelSmem &sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+        sm.h.coarse[warp] = lo;
+        sm.h.coarse[32 + warp] = hi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t a = lane < kSelWarps ? sm.h.coarse[lane] : 0xFFFFFFFFu;
+        uint32_t b = lane < kSelWarps ? sm.h.coarse[32 + lane] : 0u;
+        a = __reduce_min_sync(0xffffffffu, a);
+        b = __reduce_max_sync(0xffffffffu, b);
+        if (lane == 0) {
+            sm.decided[0] = a;
+            sm.decided[1] = b;
+        }
+    }
+    __syncthreads();
+    lo = sm.decided[0];
+    hi = sm.decided[1];
+}
+
+// Digit selection over the key range [lo, hi] of the keys still in play.
+// The digit of a key is (key - lo) >> shift, with shift chosen so that the
+// range spans at most 4096 digits: unlike the key's own high bits, these
+// split the range the keys occupy evenly, also where it straddles a power
+// of two (keys 0x3FF... and 0x400... share no high bits).  The digit that
+// holds the need-th largest key narrows the range for the next pass; a
+// pass with shift 0 ends on the exact key.
+struct DigitRange {
+    uint32_t lo, hi;
+    int shift;  // of the next pass; -1 once lo is the key
+    __device__ __forceinline__ void start(uint32_t l, uint32_t h) {
+        lo = l;
+        hi = h;
+        shift = lo == hi ? -1 : max(0, 32 - __clz(hi - lo) - 12);
+    }
+    __device__ __forceinline__ bool in(uint32_t k) const { return k >= lo && k <= hi; }
+    __device__ __forceinline__ uint32_t digit(uint32_t k) const { return (k - lo) >> shift; }
+};
+
+__device__ __forceinline__ void zero_hist(SelSmem &sm) {
+    uint4 *h = (uint4 *)sm.h.fine;  // fine and coarse are contiguous
+    for (int i = threadIdx.x; i < (kDigitBins + kCoarseBins) / 4; i += kSelThreads)
+        h[i] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void count_key(SelSmem &sm, const DigitRange &r, uint32_t k) {
+    const uint32_t d = r.digit(k);
+    atomicAdd(&sm.h.fine[d], 1u);
+    atomicAdd(&sm.h.coarse[d >> 5], 1u);
+}
+
+// After a counting pass: warp 0 finds the digit holding the need-th largest
+// key, first among the coarse bins (lane l holds coarse bins 127 - 4l - q,
+// top down), then among the 32 digits of that coarse bin; every thread then
+// narrows its range to the digit and takes the rank within it.
+__device__ __forceinline__ void digit_decide(SelSmem &sm, DigitRange &r, uint32_t &need) {
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        const int nd = (int)need;
+        const uint4 c4 = *(const uint4 *)(sm.h.coarse + kCoarseBins - 4 - 4 * lane);
+        const int cs[4] = {(int)c4.w, (int)c4.z, (int)c4.y, (int)c4.x};
+        const int sum = cs[0] + cs[1] + cs[2] + cs[3];
+        const int incl = warp_incl_scan(sum);
+        const int above = incl - sum;
+        const int src = __ffs(__ballot_sync(0xffffffffu, above < nd && nd <= incl)) - 1;
+        int C = 0, base = 0, a = above;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (a < nd && nd <= a + cs[q]) {
+                C = kCoarseBins - 1 - 4 * lane - q;
+                base = a;
+            }
+            a += cs[q];
+        }
+        C = __shfl_sync(0xffffffffu, C, src);
+        base = __shfl_sync(0xffffffffu, base, src);
+        const int f = (int)sm.h.fine[32 * C + 31 - lane];
+        const int fa = base + warp_incl_scan(f) - f;
+        if (fa < nd && nd <= fa + f) {  // exactly one lane
+            sm.decided[0] = (uint32_t)(32 * C + 31 - lane);
+            sm.decided[1] = (uint32_t)(nd - fa);
+        }
+    }
+    __syncthreads();
+    const uint32_t d = sm.decided[0];
+    need = sm.decided[1];
+    const uint32_t lo = r.lo + (d << r.shift);
+    const unsigned long long top = (unsigned long long)lo + ((1ull << r.shift) - 1ull);
+    r.start(lo, top < r.hi ? (uint32_t)top : r.hi);
+}
+
+// Exact selection over keys held in registers: key e of thread t is the
+// (e * 256 + t)-th of n.  Returns the key of the need-th largest (1 <= need
+// <= n) and leaves in `need` how many keys equal to it are among the need
+// largest.
+template <int E>
+__device__ uint32_t block_select(const uint32_t (&key)[E], int n, uint32_t &need, SelSmem &sm) {
+    const int tid = threadIdx.x;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        if (e * kSelThreads + tid < n) {
+            lo = min(lo, key[e]);
+            hi = max(hi, key[e]);
+        }
+    }
+    block_minmax(lo, hi, sm);
+    DigitRange r;
+    r.start(lo, hi);
+#pragma unroll 1
+    while (r.shift >= 0) {  // uniform over the CTA
+        __syncthreads();  // the previous reads of the histograms are done
+        zero_hist(sm);
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            if (e * kSelThreads + tid < n && r.in(key[e])) count_key(sm, r, key[e]);
+        __syncthreads();
+        digit_decide(sm, r, need);
+    }
+    return r.lo;
+}
+
+// Write this thread's share of a selection in ascending token order.  gt /
+// eq hold the thread's tokens above / equal to the threshold as bits of
+// consecutive tokens t0 + [0, 32); g and eb count the tokens above / equal
+// before them; equal keys are taken while fewer than `need` came before.
+__device__ __forceinline__ void emit_ordered(uint32_t gt, uint32_t eq, int64_t t0, int &g, int &eb,
+                                             int need, int32_t *out) {
+    uint32_t bits = gt | eq;
+    while (bits) {
+        const int i = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int32_t t = (int32_t)(t0 + i);
+        if ((gt >> i) & 1u) {
+            out[g + min(eb, need)] = t;
+            g++;
+        } else {
+            if (eb < need) out[g + eb] = t;
+            eb++;
+        }
+    }
+}
+
+// Sampled threshold of one row: the key of the r-th largest of S = E * 256
+// scores, taken as S / 8 runs of 8 consecutive tokens centred at
+// ((2j + 1) * vis) / (2 * S / 8), j < S / 8.
+template <int E>
+__global__ void __launch_bounds__(kSelThreads) topk_thresh_kernel(const float *__restrict__ scores,
+                                                                  int64_t stride,
+                                                                  const int32_t *seq_len, int nq,
+                                                                  int K, int max_tokens,
+                                                                  TopkRowState *st) {
+    __shared__ SelSmem sm;
+    const int row = blockIdx.x, tid = threadIdx.x;
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();
+    const int b = row / nq, j = row - b * nq;
+    const int vis = max(0, min(seq_len[b] - nq + j + 1, max_tokens));
+    const bool take_all = vis <= K;
+    uint32_t T = 0;
+    if (!take_all && vis > kTopkCandCap) {  // uniform over the CTA
+        constexpr int S = E * kSelThreads;
+        const int64_t m = sampled_target(K);
+        const int r = (int)max((int64_t)1, min((int64_t)S, ((int64_t)S * m + vis - 1) / vis));
+        const float *src = scores + (size_t)row * stride;
+        // S / 8 runs of 8 consecutive scores (one 32-byte sector each),
+        // centred at evenly spaced tokens; consecutive threads read a run
+        constexpr int kRuns = S / 8;
+        uint32_t key[E];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int i = e * kSelThreads + tid, run = i >> 3;
+            const int64_t c = ((2 * (int64_t)run + 1) * vis) / (2 * kRuns);
+            const int64_t first = min(max(c - 4, (int64_t)0), (int64_t)vis - 8);  // vis > 8192
+            key[e] = order_key(src[first + (i & 7)]);
+        }
+        uint32_t need = (uint32_t)r;
+        T = block_select<E>(key, S, need, sm);
+    }
+    if (tid == 0) {
+        TopkRowState s;
+        s.prefix = T;
+        s.mask = 0;
+        s.need = K;
+        s.take_all = take_all;
+        s.ticket = 0;  // candidates appended so far
+        s.visible = vis;
+        s.pad[0] = s.pad[1] = 0;
+        st[row] = s;
+    }
+}
+
+// Persistent filter: every warp walks tiles of 512 tokens (16 per lane) with
+// a stride of the grid's warp count, tiles of consecutive rows side by side
+// (so the warps in flight spread their atomics over the rows' counters), and
+// holds the next tile's scores in registers while it handles the current
+// one, so its loads stay in flight across the candidate atomic.  Scores are
+// read up to the row capacity (inside every score row), masked to the
+// visible tokens afterwards.
+__global__ void __launch_bounds__(kFiltThreads, 4) topk_filter_kernel(const float *__restrict__ scores,
+                                                                      int64_t stride, int vec4,
+                                                                      int max_tokens, int rows,
+                                                                      TopkRowState *st, uint2 *cand) {
+    const int lane = threadIdx.x & 31;
+    const int tiles = (max_tokens + kFiltTile - 1) / kFiltTile;
+    const uint32_t wstride = gridDim.x * (kFiltThreads / 32);
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();
+    // element e of this lane is token base + tok_off(e): lane-interleaved
+    // float4s when rows are 16-byte aligned, else lane-interleaved scores
+    auto tok_off = [&](int e) -> int {
+        return vec4 ? 4 * (32 * (e >> 2) + lane) + (e & 3) : 32 * e + lane;
+    };
+    auto load = [&](int row, int tile, float (&v)[kFiltE]) {
+        const int64_t base = (int64_t)tile * kFiltTile;
+        const float *src = scores + (size_t)row * stride + base;
+        const int64_t lim = max_tokens - base;  // tokens of this tile inside the row capacity
+        if (vec4) {
+#pragma unroll
+            for (int k = 0; k < kFiltE / 4; k++) {
+                const int o = tok_off(4 * k);
+                float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (o + 3 < lim) {
+                    f = __ldcs((const float4 *)(src + o));
+                } else {
+                    if (o < lim) f.x = src[o];
+                    if (o + 1 < lim) f.y = src[o + 1];
+                    if (o + 2 < lim) f.z = src[o + 2];
+                }
+                v[4 * k] = f.x;
+                v[4 * k + 1] = f.y;
+                v[4 * k + 2] = f.z;
+                v[4 * k + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kFiltE; e++) {
+                const int o = tok_off(e);
+                v[e] = o < lim ? src[o] : 0.f;
+            }
+        }
+    };
+    float cur[kFiltE], nxt[kFiltE];
+    // tile id = tile * rows + row; the warp's ids advance by wstride, so
+    // (row, tile) advance by (wstride % rows, wstride / rows) with a carry
+    const uint32_t w0 = blockIdx.x * (kFiltThreads / 32) + (threadIdx.x >> 5);
+    const uint32_t drow = (uint32_t)(wstride % rows), dtile = (uint32_t)(wstride / rows);
+    int row = (int)(w0 % (uint32_t)rows), tile = (int)(w0 / (uint32_t)rows);
+    if (tile < tiles) load(row, tile, cur);
+#pragma unroll 1
+    while (tile < tiles) {
+        int nrow = row + (int)drow, ntile = tile + (int)dtile;
+        if (nrow >= rows) {
+            nrow -= rows;
+            ntile++;
+        }
+        if (ntile < tiles) load(nrow, ntile, nxt);
+        const int64_t base = (int64_t)tile * kFiltTile;
+        const int vis = st[row].visible;
+        if (!st[row].take_all && base < vis) {  // uniform over the warp
+            const uint32_t T = st[row].prefix;
+            uint32_t hit = 0;
+#pragma unroll
+            for (int e = 0; e < kFiltE; e++)
+                if (base + tok_off(e) < vis && order_key(cur[e]) >= T) hit |= 1u << e;
+            const int c = __popc(hit);
+            const int incl = warp_incl_scan(c);
+            uint32_t pos = 0;
+            if (lane == 31 && incl) pos = atomicAdd(&st[row].ticket, (uint32_t)incl);
+            pos = __shfl_sync(0xffffffffu, pos, 31) + (uint32_t)(incl - c);
+            uint2 *dst = cand + (size_t)row * kTopkCandCap;
+#pragma unroll
+            for (int e = 0; e < kFiltE; e++) {  // entries past the cap are counted, not stored
+                if ((hit >> e) & 1u) {
+                    if (pos < (uint32_t)kTopkCandCap)
+                        dst[pos] = make_uint2(order_key(cur[e]), (uint32_t)(base + tok_off(e)));
+                    pos++;
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kFiltE; e++) cur[e] = nxt[e];
+        row = nrow;
+        tile = ntile;
+    }
+}
+
+// The exact selection over a whole row from its scores (the select kernel's
+// path for rows whose sampled threshold kept too few or too many tokens).
+__device__ void select_whole_row(const float *__restrict__ src, int vis, int K, int32_t *out,
+                                 SelSmem &sm) {
+    const int tid = threadIdx.x;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0, need = (uint32_t)K;
+    for (int t = tid; t < vis; t += kSelThreads) {
+        const uint32_t key = order_key(src[t]);
+        lo = min(lo, key);
+        hi = max(hi, key);
+    }
+    block_minmax(lo, hi, sm);
+    DigitRange r;
+    r.start(lo, hi);
+#pragma unroll 1
+    while (r.shift >= 0) {  // uniform over the CTA
+        __syncthreads();
+        zero_hist(sm);
+        __syncthreads();
+        for (int t = tid; t < vis; t += kSelThreads) {
+            const uint32_t key = order_key(src[t]);
+            if (r.in(key)) count_key(sm, r, key);
+        }
+        __syncthreads();
+        digit_decide(sm, r, need);
+    }
+    const uint32_t T = r.lo;
+    // ordered write, in tiles of 256 x 32 tokens (32 consecutive per thread)
+    int g0 = 0, e0 = 0;
+#pragma unroll 1
+    for (int64_t tile = 0; tile < vis; tile += 32 * kSelThreads) {
+        const int64_t t0 = tile + 32 * (int64_t)tid;
+        uint32_t gt = 0, eq = 0;
+#pragma unroll 4
+        for (int i = 0; i < 32; i++) {
+            if (t0 + i < vis) {
+                const uint32_t key = order_key(src[t0 + i]);
+                gt |= (uint32_t)(key > T) << i;
+                eq |= (uint32_t)(key == T) << i;
+            }
+        }
+        const int v = (__popc(eq) << 16) | __popc(gt);  // at most 8192 of each per tile
+        const int incl = block_incl_scan(v, sm.warp_sums);
+        if (tid == kSelThreads - 1) {
+            sm.tot[0] = incl & 0xFFFF;
+            sm.tot[1] = incl >> 16;
+        }
+        const int excl = incl - v;
+        int g = g0 + (excl & 0xFFFF), eb = e0 + (excl >> 16);
+        emit_ordered(gt, eq, t0, g, eb, (int)need, out);
+        __syncthreads();
+        g0 += sm.tot[0];
+        e0 += sm.tot[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSelThreads, 2)
+topk_select_kernel(const float *__restrict__ scores, int64_t stride, const TopkRowState *st,
+                   const uint2 *cand, int K, int32_t *topk) {
+    extern __shared__ __align__(16) uint8_t sel_dyn[];
+    SelSmem &sm = *(SelSmem *)sel_dyn;
+    uint32_t *toks = (uint32_t *)(sel_dyn + sizeof(SelSmem));  // [kTopkCandCap]
+    int32_t *obuf = (int32_t *)(toks + kTopkCandCap);           // [K]
+    const int row = blockIdx.x, tid = threadIdx.x;
+    tc::grid_dep_launch();
+    tc::grid_dep_wait();
+    const TopkRowState s = st[row];
+    const int vis = s.visible;
+    int32_t *out = topk + (size_t)row * K;
+    if (s.take_all) {
+        for (int i = tid; i < K; i += kSelThreads) out[i] = i < vis ? i : -1;
+        return;
+    }
+    const uint32_t n = s.ticket;
+    if (n < (uint32_t)K || n > (uint32_t)kTopkCandCap) {  // uniform over the CTA
+        select_whole_row(scores + (size_t)row * stride, vis, K, out, sm);
+        return;
+    }
+    const uint2 *src = cand + (size_t)row * kTopkCandCap;
+    uint32_t key[kSelE];
+#pragma unroll
+    for (int e = 0; e < kSelE; e++) {
+        const uint32_t i = (uint32_t)(e * kSelThreads + tid);
+        const uint2 v = i < n ? __ldcg(src + i) : make_uint2(0u, 0u);
+        key[e] = v.x;
+        toks[i] = v.y;
+    }
+    uint32_t need = (uint32_t)K;
+    const uint32_t T = block_select<kSelE>(key, (int)n, need, sm);
+    // windows of the token range: mark the candidates at or above T in two
+    // bitmaps, then each thread emits its consecutive words in order
+    int g0 = 0, e0 = 0;
+#pragma unroll 1
+    for (int64_t w0 = 0; w0 < vis; w0 += kWinTokens) {
+        __syncthreads();  // the histograms / the previous window are read
+        for (int i = tid; i < 2 * kWinPadded; i += kSelThreads)
+            sm.w.gt[i] = 0;  // gt and eq are contiguous
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kSelE; e++) {
+            const int i = e * kSelThreads + tid;
+            if (i < (int)n && key[e] >= T) {
+                const int64_t off = (int64_t)toks[i] - w0;
+                if (off >= 0 && off < kWinTokens) {
+                    uint32_t *w = key[e] > T ? sm.w.gt : sm.w.eq;
+                    atomicOr(w + padded_word((int)(off >> 5)), 1u << (off & 31));
+                }
+            }
+        }
+        __syncthreads();
+        uint32_t gw[kWordsPer], ew[kWordsPer];
+        int cg = 0, ce = 0;
+#pragma unroll
+        for (int q = 0; q < kWordsPer; q++) {
+            gw[q] = sm.w.gt[tid * (kWordsPer + 1) + q];
+            ew[q] = sm.w.eq[tid * (kWordsPer + 1) + q];
+            cg += __popc(gw[q]);
+            ce += __popc(ew[q]);
+        }
+        const int v = (ce << 16) | cg;  // at most kTopkCandCap of each per window
+        const int incl = block_incl_scan(v, sm.warp_sums);
+        if (tid == kSelThreads - 1) {
+            sm.tot[0] = incl & 0xFFFF;
+            sm.tot[1] = incl >> 16;
+        }
+        const int excl = incl - v;
+        int g = g0 + (excl & 0xFFFF), eb = e0 + (excl >> 16);
+#pragma unroll
+        for (int q = 0; q < kWordsPer; q++)
+            emit_ordered(gw[q], ew[q], w0 + 32 * (int64_t)(tid * kWordsPer + q), g, eb, (int)need,
+                         obuf);
+        __syncthreads();
+        g0 += sm.tot[0];
+        e0 += sm.tot[1];
+    }
+    for (int i = tid; i < K; i += kSelThreads) out[i] = obuf[i];  // exactly K were written
+}
+
 // Elements per thread for the one-launch path, or 0 when rows are too long.
 // Measured on GB300 with rows of 65,536 tokens: 16 keys per thread (4-CTA
 // clusters) beat 8 keys (8-CTA clusters: 38.9 against 21.6 us at 16 rows)
@@ -484,22 +998,57 @@ cudaError_t topk_setup(const hs_pool *) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(topk_cluster_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kClusterSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSelDynSmem);
     return e;
 }
 
+// The sampled-threshold path, unless every row's cluster of the one-launch
+// kernel fits one wave with 16 keys per thread: there that kernel's single
+// launch measured faster (22.5 against about 30 us at 32 rows of 65,536).
+bool use_sampled(const hs_pool *p, int rows) {
+    return p->d.topk_cand && cluster_elems(p->cfg.max_tokens, rows) != 16;
+}
+
 int topk_kernel_count(const hs_pool *p, int B, int nq) {
+    if (use_sampled(p, B * nq)) return 3;
     return cluster_elems(p->cfg.max_tokens, B * nq) ? 1 : 6;
 }
 
 cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, int B, int nq,
                         int32_t *topk, cudaStream_t st) {
     const int rows = B * nq, nch = p->topk_nchunks, K = p->cfg.top_k;
+    const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
+    if (use_sampled(p, rows)) {  // K <= kTopkSampledMaxK
+        const int maxT = p->cfg.max_tokens;
+        // 4096 samples while they put r >= 128 at the longest row, else 16384
+        const int64_t m = sampled_target(K);
+        const bool wide = 128 * (int64_t)maxT > 4096 * m;
+        PdlLaunch lt(dim3((unsigned)rows), dim3(kSelThreads), 0, st);
+        cudaError_t e = wide ? cudaLaunchKernelEx(&lt.cfg, topk_thresh_kernel<64>, scores, stride,
+                                                  (const int32_t *)p->d.seq_len, nq, K, maxT,
+                                                  p->d.topk_state)
+                             : cudaLaunchKernelEx(&lt.cfg, topk_thresh_kernel<16>, scores, stride,
+                                                  (const int32_t *)p->d.seq_len, nq, K, maxT,
+                                                  p->d.topk_state);
+        if (e != cudaSuccess) return e;
+        const int64_t warps = (int64_t)rows * ((maxT + kFiltTile - 1) / kFiltTile);
+        const int fgrid = (int)std::min<int64_t>((warps + 7) / 8, 4 * kNumSMs);
+        PdlLaunch lf(dim3((unsigned)fgrid), dim3(kFiltThreads), 0, st);
+        e = cudaLaunchKernelEx(&lf.cfg, topk_filter_kernel, scores, stride, vec4, maxT, rows,
+                               p->d.topk_state, p->d.topk_cand);
+        if (e != cudaSuccess) return e;
+        PdlLaunch ls(dim3((unsigned)rows), dim3(kSelThreads), kSelDynSmem, st);
+        return cudaLaunchKernelEx(&ls.cfg, topk_select_kernel, scores, stride,
+                                  (const TopkRowState *)p->d.topk_state,
+                                  (const uint2 *)p->d.topk_cand, K, topk);
+    }
     const int E = cluster_elems(p->cfg.max_tokens, rows);
     if (E) {
         const int G = (p->cfg.max_tokens + kClusterThreads * E - 1) / (kClusterThreads * E);
         PdlLaunch lc(dim3((unsigned)G, (unsigned)rows), dim3(kClusterThreads), kClusterSmem, st,
                      dim3((unsigned)G, 1, 1));
-        const int vec4 = ((uintptr_t)scores % 16 == 0) && (stride % 4 == 0);
         if (E == 16)
             return cudaLaunchKernelEx(&lc.cfg, topk_cluster_kernel<16>, scores, stride, vec4,
                                       (const int32_t *)p->d.seq_len, nq, K, topk);

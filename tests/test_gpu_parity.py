@@ -184,15 +184,21 @@ def test_indexer_tensor_core_head_and_query_counts(Hi, num_spec):
         r.close()
 
 
+@pytest.mark.parametrize("K", [512, 2560])
 @pytest.mark.parametrize("max_tokens", [0, 200064, 300032])
-def test_topk_ties_and_special_scores(max_tokens):
+def test_topk_ties_and_special_scores(max_tokens, K):
     """hs_topk on crafted scores: heavy ties, +0, negatives, all-equal rows.
-    The row capacity picks the kernel: one cluster launch with 16 keys per
-    thread (up to 20,032 tokens per row here) or 32 (200,064), and the
-    multi-kernel radix select beyond 262,144."""
+    K = 512 takes the one-launch cluster kernel at the smallest capacity
+    (20,032 tokens: every row's 2-CTA cluster fits one wave) and the
+    sampled-threshold path at the others (rows of at most 8,192 visible
+    tokens all candidates, longer rows sampled; the all-equal rows overflow
+    the candidate list and take the whole-row select).  K = 2560 takes the
+    radix paths, picked by the row capacity: one cluster launch with 16
+    keys per thread (20,032) or 32 (200,064), and the multi-kernel radix
+    select beyond 262,144."""
     from harness import Case, Runner
     hs = _hs()
-    case = Case("topk", B=4, N=[20000, 9000, 300, 16385], K=512, Hi=8, Di=32, H=16,
+    case = Case("topk", B=4, N=[20000, 9000, 300, 16385], K=K, Hi=8, Di=32, H=16,
                 num_spec=1, mode=hs.HS_FULL, max_tokens=max_tokens)
     r = Runner(case)
     try:
@@ -224,6 +230,56 @@ def test_topk_ties_and_special_scores(max_tokens):
                 vis = oracle.visible(r.N[b], 2, j)
                 ref = oracle.topk(s_np[b, j], vis, case.K)
                 np.testing.assert_array_equal(out[b, j].cpu().numpy(), ref)
+    finally:
+        r.close()
+
+
+def test_topk_sampled_threshold_edges():
+    """The sampled-threshold top-K where its sample misleads it, against the
+    oracle.  With 200,064-token rows and K = 512 the threshold step samples
+    16,384 scores of a 131,072-token row, as 2,048 runs of 8 tokens
+    [64j + 28, 64j + 36), and aims at 2,048 tokens at or above the 256th
+    largest sample; a row keeps at most 8,192 candidates.
+      row 0: the samples are distinct and above every other score, so only
+             256 tokens reach the threshold (fewer than K): whole-row select;
+      row 1: every other sample is 1.0 and every other score 0.0, so exactly
+             8,192 tokens reach it (the candidate cap, inclusive): the
+             candidate path, with the K-th score tied 8,192 ways;
+      row 2: as row 1 with one more 1.0 (8,193 tokens, past the cap): the
+             whole-row select, with the same ties;
+      row 3: 40,000 equal scores, all candidates: past the cap, whole row;
+      row 4: 200,000 normal scores: the candidate path over two bitmap
+             windows of 131,072 tokens."""
+    from harness import Case, Runner
+    hs = _hs()
+    N = [131072, 131072, 131072, 40000, 200000]
+    case = Case("topk", B=5, N=N, K=512, Hi=8, Di=32, H=16, L=1, num_spec=0,
+                mode=hs.HS_FULL, max_tokens=200064)
+    r = Runner(case)
+    try:
+        stride = r.max_tokens
+        g = torch.Generator().manual_seed(11)
+        sc = torch.full((case.B, 1, stride), -7.0)
+        samples = (torch.arange(2048) * 64 + 28).repeat_interleave(8) + torch.arange(8).repeat(2048)
+        sc[0, 0, :N[0]] = torch.rand(N[0], generator=g)
+        sc[0, 0, samples] = 2.0 + torch.randperm(16384, generator=g).float()
+        sc[1, 0, :N[1]] = 0.0
+        sc[1, 0, samples[::2]] = 1.0
+        sc[2, 0, :N[2]] = 0.0
+        sc[2, 0, samples[::2]] = 1.0
+        sc[2, 0, 1] = 1.0
+        sc[3, 0, :N[3]] = -3.5
+        sc[4, 0, :N[4]] = torch.randn(N[4], generator=g)
+        sc = sc.to(r.dev)
+        out = torch.full((case.B, 1, case.K), -9, dtype=torch.int32, device=r.dev)
+        r.pool.topk(sc, stride, case.B, 1, out)
+        torch.cuda.synchronize()
+        s_np = sc.cpu().numpy()
+        for b in range(case.B):
+            ref = oracle.topk(s_np[b, 0], N[b], case.K)
+            np.testing.assert_array_equal(out[b, 0].cpu().numpy(), ref, err_msg=f"row {b}")
+        np.testing.assert_array_equal(out[1, 0].cpu().numpy(), samples[::2][:512].numpy())
+        np.testing.assert_array_equal(out[3, 0].cpu().numpy(), np.arange(512))
     finally:
         r.close()
 
