@@ -526,13 +526,19 @@ struct __align__(16) SelSmem {
             uint32_t gt[kWinPadded], eq[kWinPadded];
         } w;
     };
-    uint32_t decided[2];
+    uint32_t decided[3];
     int warp_sums[32];
     int tot[2];
+    uint32_t few[32];  // the keys of a digit small enough for one warp
+    int nfew;
 };
-// The select kernel's dynamic shared memory: SelSmem, the candidates'
-// tokens, then the selection in output order (copied out coalesced).
-constexpr size_t kSelDynSmem = sizeof(SelSmem) + (size_t)kTopkCandCap * 4 + kTopkSampledMaxK * 4;
+// The select kernel's dynamic shared memory: SelSmem, the packed counts of
+// the selected tokens before each bitmap word, the candidates' tokens, then
+// the selection in output order (copied out coalesced).
+constexpr size_t kSelPreOff = sizeof(SelSmem);
+constexpr size_t kSelTokOff = kSelPreOff + (size_t)kWinPadded * 4;
+constexpr size_t kSelOutOff = kSelTokOff + (size_t)kTopkCandCap * 4;
+constexpr size_t kSelDynSmem = kSelOutOff + (size_t)kTopkSampledMaxK * 4;
 
 __device__ __forceinline__ int warp_incl_scan(int v) {
     const int lane = threadIdx.x & 31;
@@ -630,6 +636,7 @@ __device__ __forceinline__ void digit_decide(SelSmem &sm, DigitRange &r, uint32_
         if (fa < nd && nd <= fa + f) {  // exactly one lane
             sm.decided[0] = (uint32_t)(32 * C + 31 - lane);
             sm.decided[1] = (uint32_t)(nd - fa);
+            sm.decided[2] = (uint32_t)f;
         }
     }
     __syncthreads();
@@ -662,12 +669,38 @@ __device__ uint32_t block_select(const uint32_t (&key)[E], int n, uint32_t &need
     while (r.shift >= 0) {  // uniform over the CTA
         __syncthreads();  // the previous reads of the histograms are done
         zero_hist(sm);
+        if (tid == 0) sm.nfew = 0;
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; e++)
             if (e * kSelThreads + tid < n && r.in(key[e])) count_key(sm, r, key[e]);
         __syncthreads();
         digit_decide(sm, r, need);
+        if (r.shift >= 0 && sm.decided[2] <= 32u) {
+            // at most 32 keys left in the range: gather them and let one
+            // warp rank them against each other
+            const int cnt = (int)sm.decided[2];
+#pragma unroll
+            for (int e = 0; e < E; e++)
+                if (e * kSelThreads + tid < n && r.in(key[e])) sm.few[atomicAdd(&sm.nfew, 1)] = key[e];
+            __syncthreads();
+            if (tid < 32) {
+                const uint32_t k = tid < cnt ? sm.few[tid] : 0u;
+                int gt = 0, eq = 0;
+                for (int j = 0; j < cnt; j++) {
+                    const uint32_t o = sm.few[j];
+                    gt += o > k;
+                    eq += o == k;
+                }
+                if (tid < cnt && gt < (int)need && (int)need <= gt + eq) {  // same values
+                    sm.decided[0] = k;
+                    sm.decided[1] = need - (uint32_t)gt;
+                }
+            }
+            __syncthreads();
+            need = sm.decided[1];
+            return sm.decided[0];
+        }
     }
     return r.lo;
 }
@@ -748,26 +781,26 @@ __global__ void __launch_bounds__(kSelThreads) topk_thresh_kernel(const float *_
 // holds the next tile's scores in registers while it handles the current
 // one, so its loads stay in flight across the candidate atomic.  Scores are
 // read up to the row capacity (inside every score row), masked to the
-// visible tokens afterwards.
+// visible tokens only in the tile that holds the end of the row.  V4: rows
+// are 16-byte aligned, a lane reads float4s.
+template <bool V4>
 __global__ void __launch_bounds__(kFiltThreads, 4) topk_filter_kernel(const float *__restrict__ scores,
-                                                                      int64_t stride, int vec4,
-                                                                      int max_tokens, int rows,
-                                                                      TopkRowState *st, uint2 *cand) {
+                                                                      int64_t stride, int max_tokens,
+                                                                      int rows, TopkRowState *st,
+                                                                      uint2 *cand) {
     const int lane = threadIdx.x & 31;
     const int tiles = (max_tokens + kFiltTile - 1) / kFiltTile;
     const uint32_t wstride = gridDim.x * (kFiltThreads / 32);
     tc::grid_dep_launch();
     tc::grid_dep_wait();
     // element e of this lane is token base + tok_off(e): lane-interleaved
-    // float4s when rows are 16-byte aligned, else lane-interleaved scores
-    auto tok_off = [&](int e) -> int {
-        return vec4 ? 4 * (32 * (e >> 2) + lane) + (e & 3) : 32 * e + lane;
-    };
+    // float4s (V4) or lane-interleaved scores
+    auto tok_off = [&](int e) -> int { return V4 ? 4 * (32 * (e >> 2) + lane) + (e & 3) : 32 * e + lane; };
     auto load = [&](int row, int tile, float (&v)[kFiltE]) {
-        const int64_t base = (int64_t)tile * kFiltTile;
+        const int base = tile * kFiltTile;
         const float *src = scores + (size_t)row * stride + base;
-        const int64_t lim = max_tokens - base;  // tokens of this tile inside the row capacity
-        if (vec4) {
+        const int lim = max_tokens - base;  // tokens of this tile inside the row capacity
+        if (V4) {
 #pragma unroll
             for (int k = 0; k < kFiltE / 4; k++) {
                 const int o = tok_off(4 * k);
@@ -792,46 +825,63 @@ __global__ void __launch_bounds__(kFiltThreads, 4) topk_filter_kernel(const floa
             }
         }
     };
-    float cur[kFiltE], nxt[kFiltE];
+    auto handle = [&](int row, int tile, const float (&v)[kFiltE]) {
+        const int base = tile * kFiltTile;
+        const int vis = __ldg(&st[row].visible);
+        if (__ldg(&st[row].take_all) || base >= vis) return;  // uniform over the warp
+        const uint32_t T = __ldg(&st[row].prefix);
+        uint32_t hit = 0;
+        if (base + kFiltTile <= vis) {
+#pragma unroll
+            for (int e = 0; e < kFiltE; e++) hit |= (uint32_t)(order_key(v[e]) >= T) << e;
+        } else {
+#pragma unroll
+            for (int e = 0; e < kFiltE; e++)
+                hit |= (uint32_t)(base + tok_off(e) < vis && order_key(v[e]) >= T) << e;
+        }
+        if (!__any_sync(0xffffffffu, hit)) return;
+        const int c = __popc(hit);
+        const int incl = warp_incl_scan(c);
+        uint32_t pos = 0;
+        if (lane == 31) pos = atomicAdd(&st[row].ticket, (uint32_t)incl);
+        pos = __shfl_sync(0xffffffffu, pos, 31) + (uint32_t)(incl - c);
+        uint2 *dst = cand + (size_t)row * kTopkCandCap;
+#pragma unroll
+        for (int e = 0; e < kFiltE; e++) {  // entries past the cap are counted, not stored
+            if ((hit >> e) & 1u) {
+                if (pos < (uint32_t)kTopkCandCap)
+                    dst[pos] = make_uint2(order_key(v[e]), (uint32_t)(base + tok_off(e)));
+                pos++;
+            }
+        }
+    };
     // tile id = tile * rows + row; the warp's ids advance by wstride, so
     // (row, tile) advance by (wstride % rows, wstride / rows) with a carry
     const uint32_t w0 = blockIdx.x * (kFiltThreads / 32) + (threadIdx.x >> 5);
-    const uint32_t drow = (uint32_t)(wstride % rows), dtile = (uint32_t)(wstride / rows);
+    const int drow = (int)(wstride % (uint32_t)rows), dtile = (int)(wstride / (uint32_t)rows);
     int row = (int)(w0 % (uint32_t)rows), tile = (int)(w0 / (uint32_t)rows);
-    if (tile < tiles) load(row, tile, cur);
+    auto advance = [&](int &r, int &t) {
+        r += drow;
+        t += dtile;
+        if (r >= rows) {
+            r -= rows;
+            t++;
+        }
+    };
+    float a[kFiltE], b[kFiltE];  // two tiles in turn: one in flight, one handled
+    if (tile < tiles) load(row, tile, a);
 #pragma unroll 1
     while (tile < tiles) {
-        int nrow = row + (int)drow, ntile = tile + (int)dtile;
-        if (nrow >= rows) {
-            nrow -= rows;
-            ntile++;
-        }
-        if (ntile < tiles) load(nrow, ntile, nxt);
-        const int64_t base = (int64_t)tile * kFiltTile;
-        const int vis = st[row].visible;
-        if (!st[row].take_all && base < vis) {  // uniform over the warp
-            const uint32_t T = st[row].prefix;
-            uint32_t hit = 0;
-#pragma unroll
-            for (int e = 0; e < kFiltE; e++)
-                if (base + tok_off(e) < vis && order_key(cur[e]) >= T) hit |= 1u << e;
-            const int c = __popc(hit);
-            const int incl = warp_incl_scan(c);
-            uint32_t pos = 0;
-            if (lane == 31 && incl) pos = atomicAdd(&st[row].ticket, (uint32_t)incl);
-            pos = __shfl_sync(0xffffffffu, pos, 31) + (uint32_t)(incl - c);
-            uint2 *dst = cand + (size_t)row * kTopkCandCap;
-#pragma unroll
-            for (int e = 0; e < kFiltE; e++) {  // entries past the cap are counted, not stored
-                if ((hit >> e) & 1u) {
-                    if (pos < (uint32_t)kTopkCandCap)
-                        dst[pos] = make_uint2(order_key(cur[e]), (uint32_t)(base + tok_off(e)));
-                    pos++;
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < kFiltE; e++) cur[e] = nxt[e];
+        int nrow = row, ntile = tile;
+        advance(nrow, ntile);
+        if (ntile < tiles) load(nrow, ntile, b);
+        handle(row, tile, a);
+        row = nrow;
+        tile = ntile;
+        if (tile >= tiles) break;
+        advance(nrow, ntile);
+        if (ntile < tiles) load(nrow, ntile, a);
+        handle(row, tile, b);
         row = nrow;
         tile = ntile;
     }
@@ -898,8 +948,9 @@ topk_select_kernel(const float *__restrict__ scores, int64_t stride, const TopkR
                    const uint2 *cand, int K, int32_t *topk) {
     extern __shared__ __align__(16) uint8_t sel_dyn[];
     SelSmem &sm = *(SelSmem *)sel_dyn;
-    uint32_t *toks = (uint32_t *)(sel_dyn + sizeof(SelSmem));  // [kTopkCandCap]
-    int32_t *obuf = (int32_t *)(toks + kTopkCandCap);           // [K]
+    uint32_t *pre = (uint32_t *)(sel_dyn + kSelPreOff);  // [kWinPadded]
+    uint32_t *toks = (uint32_t *)(sel_dyn + kSelTokOff);  // [kTopkCandCap]
+    int32_t *obuf = (int32_t *)(sel_dyn + kSelOutOff);    // [K]
     const int row = blockIdx.x, tid = threadIdx.x;
     tc::grid_dep_launch();
     tc::grid_dep_wait();
@@ -927,51 +978,63 @@ topk_select_kernel(const float *__restrict__ scores, int64_t stride, const TopkR
     uint32_t need = (uint32_t)K;
     const uint32_t T = block_select<kSelE>(key, (int)n, need, sm);
     // windows of the token range: mark the candidates at or above T in two
-    // bitmaps, then each thread emits its consecutive words in order
+    // bitmaps, count the marks before every word (block scan over threads
+    // holding 16 consecutive words each), then every marked candidate takes
+    // its output position from those counts
     int g0 = 0, e0 = 0;
 #pragma unroll 1
-    for (int64_t w0 = 0; w0 < vis; w0 += kWinTokens) {
+    for (int w0 = 0; w0 < vis; w0 += kWinTokens) {
         __syncthreads();  // the histograms / the previous window are read
         for (int i = tid; i < 2 * kWinPadded; i += kSelThreads)
             sm.w.gt[i] = 0;  // gt and eq are contiguous
         __syncthreads();
+        uint32_t mine = 0;  // bit e: candidate e of this thread is marked in this window
 #pragma unroll
         for (int e = 0; e < kSelE; e++) {
             const int i = e * kSelThreads + tid;
-            if (i < (int)n && key[e] >= T) {
-                const int64_t off = (int64_t)toks[i] - w0;
-                if (off >= 0 && off < kWinTokens) {
-                    uint32_t *w = key[e] > T ? sm.w.gt : sm.w.eq;
-                    atomicOr(w + padded_word((int)(off >> 5)), 1u << (off & 31));
-                }
+            const int off = (int)toks[i] - w0;
+            if (i < (int)n && key[e] >= T && off >= 0 && off < kWinTokens) {
+                atomicOr((key[e] > T ? sm.w.gt : sm.w.eq) + padded_word(off >> 5), 1u << (off & 31));
+                mine |= 1u << e;
             }
         }
         __syncthreads();
-        uint32_t gw[kWordsPer], ew[kWordsPer];
-        int cg = 0, ce = 0;
+        int v = 0;  // packed (equal << 16) | above of this thread's words
 #pragma unroll
         for (int q = 0; q < kWordsPer; q++) {
-            gw[q] = sm.w.gt[tid * (kWordsPer + 1) + q];
-            ew[q] = sm.w.eq[tid * (kWordsPer + 1) + q];
-            cg += __popc(gw[q]);
-            ce += __popc(ew[q]);
+            const int pw = tid * (kWordsPer + 1) + q;
+            v += (__popc(sm.w.eq[pw]) << 16) | __popc(sm.w.gt[pw]);
         }
-        const int v = (ce << 16) | cg;  // at most kTopkCandCap of each per window
-        const int incl = block_incl_scan(v, sm.warp_sums);
+        const int incl = block_incl_scan(v, sm.warp_sums);  // at most kTopkCandCap of each
         if (tid == kSelThreads - 1) {
             sm.tot[0] = incl & 0xFFFF;
             sm.tot[1] = incl >> 16;
         }
-        const int excl = incl - v;
-        int g = g0 + (excl & 0xFFFF), eb = e0 + (excl >> 16);
+        int run = incl - v;
 #pragma unroll
-        for (int q = 0; q < kWordsPer; q++)
-            emit_ordered(gw[q], ew[q], w0 + 32 * (int64_t)(tid * kWordsPer + q), g, eb, (int)need,
-                         obuf);
+        for (int q = 0; q < kWordsPer; q++) {
+            const int pw = tid * (kWordsPer + 1) + q;
+            pre[pw] = (uint32_t)run;
+            run += (__popc(sm.w.eq[pw]) << 16) | __popc(sm.w.gt[pw]);
+        }
         __syncthreads();
+        const int nd = (int)need;
+#pragma unroll
+        for (int e = 0; e < kSelE; e++) {
+            if ((mine >> e) & 1u) {
+                const int i = e * kSelThreads + tid, off = (int)toks[i] - w0;
+                const int pw = padded_word(off >> 5);
+                const uint32_t below = (1u << (off & 31)) - 1u, pk = pre[pw];
+                const int g = g0 + (int)(pk & 0xFFFFu) + __popc(sm.w.gt[pw] & below);
+                const int eb = e0 + (int)(pk >> 16) + __popc(sm.w.eq[pw] & below);
+                if (key[e] > T) obuf[g + min(eb, nd)] = (int32_t)toks[i];
+                else if (eb < nd) obuf[g + eb] = (int32_t)toks[i];
+            }
+        }
         g0 += sm.tot[0];
         e0 += sm.tot[1];
     }
+    __syncthreads();
     for (int i = tid; i < K; i += kSelThreads) out[i] = obuf[i];  // exactly K were written
 }
 
@@ -1036,8 +1099,10 @@ cudaError_t launch_topk(const hs_pool *p, const float *scores, int64_t stride, i
         const int64_t warps = (int64_t)rows * ((maxT + kFiltTile - 1) / kFiltTile);
         const int fgrid = (int)std::min<int64_t>((warps + 7) / 8, 4 * kNumSMs);
         PdlLaunch lf(dim3((unsigned)fgrid), dim3(kFiltThreads), 0, st);
-        e = cudaLaunchKernelEx(&lf.cfg, topk_filter_kernel, scores, stride, vec4, maxT, rows,
-                               p->d.topk_state, p->d.topk_cand);
+        e = vec4 ? cudaLaunchKernelEx(&lf.cfg, topk_filter_kernel<true>, scores, stride, maxT, rows,
+                                      p->d.topk_state, p->d.topk_cand)
+                 : cudaLaunchKernelEx(&lf.cfg, topk_filter_kernel<false>, scores, stride, maxT, rows,
+                                      p->d.topk_state, p->d.topk_cand);
         if (e != cudaSuccess) return e;
         PdlLaunch ls(dim3((unsigned)rows), dim3(kSelThreads), kSelDynSmem, st);
         return cudaLaunchKernelEx(&ls.cfg, topk_select_kernel, scores, stride,
