@@ -497,15 +497,16 @@ def attention_kernel(w):
 TC_CUH_SHA = "beffda9b9722625b"
 TRAFFIC = {
     # keys + sigma read once; scores partly still in L2 at the end (16 x 131,072, 4 queries)
-    "indexer_tc_kernel": ("indexer.cu", "5ba1aa437e69b304", (277.41 + 25.79) / 310.9),
-    # the scores read once, nothing left to write back (16 x 4 rows of 142,000)
-    "topk_cluster_kernel": ("topk.cu", "6797471cd5a693e2", (36.41 + 0.0) / (36.36 + 0.52)),
+    "indexer_tc_kernel": ("indexer.cu", "77e081fbcc938a4a", (277.41 + 25.65) / 310.9),
+    # the sampled-threshold filter: the scores read once, the few candidates
+    # still in L2 at the end (16 x 4 rows of 142,000)
+    "topk_filter_kernel": ("topk.cu", "6698f043a64ba116", (36.39 + 0.003) / (36.36 + 0.52)),
     # rows, queries and outputs of one layer (64 x 4 queries x 2048 rows x 128 heads)
     "attn_pair_kernel": ("attention_pair.cu", "9bcd4609f6372c9b", (354.27 + 26.66) / 415.2),
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
-    "miss_copy_kernel": ("resolve.cu", "f4aa9d9de9e5fd21", (0.62 + 93.02) / 96.9),
+    "miss_copy_kernel": ("resolve.cu", "4f3dbaec407d11e4", (0.95 + 91.43) / 96.9),
 }
 
 

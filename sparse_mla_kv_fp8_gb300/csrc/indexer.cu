@@ -152,6 +152,53 @@ __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *
     return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
 }
 
+// Two fp32 lanes as one 64-bit operand of the packed f32x2 instructions.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// d = a * b + c in each of the two fp32 lanes (rounded like fmaf).
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+
+// The 64-head sum of one query in 32-column batches (both loads of a batch
+// in flight, one wait), the products through packed f32x2 FMAs (two heads
+// per instruction) into eight partial sums.
+__device__ __forceinline__ float weighted_relu_sum64(uint32_t taddr, const float *wj) {
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // +0 in every lane
+#pragma unroll
+    for (int h0 = 0; h0 < 64; h0 += 32) {
+        float v[32];
+        tc::tmem_ld16(taddr + h0, v);
+        tc::tmem_ld16(taddr + h0 + 16, v + 16);
+        tc::tmem_ld_wait();
+        const float4 *wq = (const float4 *)(wj + h0);
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const float4 wv = wq[u];  // shared-memory broadcast
+            const unsigned long long r0 = pack2(fmaxf(v[4 * u], 0.f), fmaxf(v[4 * u + 1], 0.f));
+            const unsigned long long r1 = pack2(fmaxf(v[4 * u + 2], 0.f), fmaxf(v[4 * u + 3], 0.f));
+            acc[(2 * u) & 3] = fma2(r0, pack2(wv.x, wv.y), acc[(2 * u) & 3]);
+            acc[(2 * u + 1) & 3] = fma2(r1, pack2(wv.z, wv.w), acc[(2 * u + 1) & 3]);
+        }
+    }
+    const float2 p0 = unpack2(acc[0]), p1 = unpack2(acc[1]), p2 = unpack2(acc[2]),
+                 p3 = unpack2(acc[3]);
+    return ((p0.x + p0.y) + (p1.x + p1.y)) + ((p2.x + p2.y) + (p3.x + p3.y));
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IdxTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -270,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // workloads both orders are exact)
             for (int j = half; j < a.nq; j += jstep) {
                 const float accs = a.Hi == 64
-                    ? weighted_relu_sum<64>(tb + j * a.Hi, wsm + j * a.Hi, 64)
+                    ? weighted_relu_sum64(tb + j * a.Hi, wsm + j * a.Hi)
                     : weighted_relu_sum<0>(tb + j * a.Hi, wsm + j * a.Hi, a.Hi);
                 if (t < N) a.scores[((size_t)b * a.nq + j) * a.stride + t] = sig * accs;
             }
