@@ -379,8 +379,14 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
             "miss_bytes_per_step": nbytes, "us_miss_copy": ms_copy * 1e3, "achieved_gbs": ach,
             "peak_gbs": link["peak_gbs"], "peak_source": link["source"], "frac": ach / link["peak_gbs"],
             "peak_candidates": link["candidates"],
-            "timed": "miss-copy kernel span (hs_miss_copy, events on its stream) over the misses of "
-                     "the stage-timing steps; bytes = the timed steps' mean misses x L x 656"}
+            "full_grid": {"us": stage["miss_copy_full"] * 1e3,
+                          "achieved_gbs": nbytes / (stage["miss_copy_full"] / 1e3) / 1e9
+                          if stage["miss_copy_full"] > 0 else 0.0,
+                          "what": "the same copy in one hs_miss_copy launch of about four CTAs per SM"},
+            "timed": "miss-copy kernel spans as the step launches them (hs_miss_copy_layers, one "
+                     "launch per layer on a 64-CTA grid, back to back, events on their stream) "
+                     "over the misses of the stage-timing steps; bytes = the timed steps' mean "
+                     "misses x L x 656"}
     if rank == 0 and headline and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     pool.close()
@@ -417,6 +423,7 @@ def config_of(w, steps):
 
 
 HOLD_CYCLES = 1_000_000  # ~0.5 ms of SM clock: longer than enqueueing one step's stages
+STEP_COPY_CTAS = 64      # the grid of the step's per-layer miss copies (hs_step with a host pool)
 
 
 def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, stream, steps,
@@ -428,7 +435,7 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, str
     B, nq, L = w["B"], w["nq"], w["L"]
     tau = 1.0 / math.sqrt(576)
     names = ["indexer", "topk", "resolve_plan", "miss_copy", "attention"]
-    acc = {k: 0.0 for k in names}
+    acc = {k: 0.0 for k in names + ["miss_copy_full"]}
     stride = pool.cfg.max_tokens
     scores = torch.empty((B, nq, stride), dtype=torch.float32, device=q.device)
     for i in range(steps):
@@ -437,7 +444,7 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, str
         wt.copy_(b_)
         qm.copy_(c)
         trace.load(first_step + i)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5 + L)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6 + L)]
         with torch.cuda.stream(stream):
             flush_l2()
             # hold the stream while the host enqueues every stage, so that the
@@ -450,15 +457,23 @@ def stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, str
             ev[2].record(stream)
             pool.resolve_plan(trace.buf if trace.drawn else topk, B, nq, rid, stream=stream)
             ev[3].record(stream)
-            pool.miss_copy(B, nq, stream=stream)
+            # the copy as the step launches it: layer by layer on the
+            # step's 64-CTA grid (here without the attention beside it)
+            for l in range(L):
+                pool.miss_copy_layers(B, nq, l, l + 1, ctas=STEP_COPY_CTAS, stream=stream)
             ev[4].record(stream)
             for l in range(L):
                 pool.sparse_mla_decode(l, qm[l], rid, B, nq, tau, out[l], None, stream=stream)
                 ev[5 + l].record(stream)
+            # and once more in one launch on the full-width grid (hs_miss_copy;
+            # the same rows into the same slots), for comparison
+            pool.miss_copy(B, nq, stream=stream)
+            ev[5 + L].record(stream)
         torch.cuda.synchronize()
         for k in range(4):
             acc[names[k]] += ev[k].elapsed_time(ev[k + 1])
         acc["attention"] += ev[4].elapsed_time(ev[4 + L]) / L
+        acc["miss_copy_full"] += ev[4 + L].elapsed_time(ev[5 + L])
     del scores
     return {k: v / steps for k, v in acc.items()}
 

@@ -349,6 +349,19 @@ hs_status hs_resolve_plan(hs_pool *pool, const int32_t *topk, int32_t B, int32_t
                           int32_t *row_id, cudaStream_t stream);
 hs_status hs_miss_copy(hs_pool *pool, int32_t B, int32_t nq, cudaStream_t stream);
 
+/* The copy of hs_miss_copy for layers [layer_begin, layer_end) only, on a
+ * grid of about `ctas` CTAs in all (0: about four per SM over the batch, as
+ * hs_miss_copy).  For callers that overlap each layer's copy with another
+ * layer's attention on a second stream, as hs_resolve_attend does with
+ * about 64 CTAs: the copy of layer l must complete before layer l's
+ * hs_sparse_mla_decode reads the rows.  The same ordering rule as
+ * hs_miss_copy holds: after the plan it copies for, before the next plan.
+ * HS_ERR_INVALID_ARG for an empty or out-of-range layer range, ctas < 0
+ * or a batch the pool cannot hold; without a host pool there is nothing to
+ * copy and the call returns HS_OK. */
+hs_status hs_miss_copy_layers(hs_pool *pool, int32_t B, int32_t nq, int32_t layer_begin,
+                              int32_t layer_end, int32_t ctas, cudaStream_t stream);
+
 /* Sparse MLA decode of one layer over the resolved rows ("Ce qui se passe"):
  *   z[b][j][h][k] = softmax_scale * q[b][j][h][:576] . row(row_id[b][j][k])[:576]
  *   out[b][j][h][:512] = sum_k softmax_k(z) * row[:512]   (rows with id -1 skipped)

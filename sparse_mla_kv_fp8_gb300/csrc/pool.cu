@@ -263,7 +263,7 @@ int64_t blocks_in_mode(const hs_pool *p, int32_t req, int mode) {
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 104; }
+int32_t hs_abi_version(void) { return 105; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -782,6 +782,13 @@ hs_status hs_resolve_plan(hs_pool *p, const int32_t *topk, int32_t B, int32_t nq
 hs_status hs_miss_copy(hs_pool *p, int32_t B, int32_t nq, cudaStream_t st) {
     if (!step_batch_ok(p, B, nq)) return HS_ERR_INVALID_ARG;
     return cuda_status(hs::launch_miss_copy(p, B, nq, st));
+}
+
+hs_status hs_miss_copy_layers(hs_pool *p, int32_t B, int32_t nq, int32_t l0, int32_t l1,
+                              int32_t ctas, cudaStream_t st) {
+    if (!step_batch_ok(p, B, nq) || l0 < 0 || l1 <= l0 || l1 > p->cfg.num_mla_layers || ctas < 0)
+        return HS_ERR_INVALID_ARG;
+    return cuda_status(hs::launch_miss_copy(p, B, nq, st, l0, l1, ctas));
 }
 
 hs_status hs_sparse_mla_decode(hs_pool *p, int32_t layer, const void *q, const int32_t *row_id,

@@ -89,6 +89,7 @@ hs_indexer_topk = _decl("hs_indexer_topk", _i32, [_P, _P, _P, _i32, _i32, _P, _P
 hs_resolve = _decl("hs_resolve", _i32, [_P, _P, _i32, _i32, _P, _P])
 hs_resolve_plan = _decl("hs_resolve_plan", _i32, [_P, _P, _i32, _i32, _P, _P])
 hs_miss_copy = _decl("hs_miss_copy", _i32, [_P, _i32, _i32, _P])
+hs_miss_copy_layers = _decl("hs_miss_copy_layers", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P])
 hs_host_read_probe = _decl("hs_host_read_probe", _i32, [_P, _P, _sz, _i32, _P])
 hs_sparse_mla_decode = _decl("hs_sparse_mla_decode", _i32,
                              [_P, _i32, _P, _P, _i32, _i32, _f32, _P, _P, _P])
@@ -275,6 +276,10 @@ class Pool:
 
     def miss_copy(self, B, nq, stream=None):
         check(hs_miss_copy(self.handle, B, nq, _stream(stream)), "hs_miss_copy")
+
+    def miss_copy_layers(self, B, nq, layer_begin, layer_end, ctas=0, stream=None):
+        check(hs_miss_copy_layers(self.handle, B, nq, layer_begin, layer_end, ctas, _stream(stream)),
+              "hs_miss_copy_layers")
 
     def sparse_mla_decode(self, layer, q, row_id, B, nq, scale, out, lse=None, stream=None):
         check(hs_sparse_mla_decode(self.handle, layer, _dev(q, "q"), _dev(row_id, "row_id"), B, nq,

@@ -907,7 +907,9 @@ def test_resolve_plan_then_miss_copy_equals_resolve():
     """hs_resolve_plan followed by hs_miss_copy (the two halves, here with the
     copy on a second stream ordered by an event) leaves the same row ids,
     hot-buffer state and row bytes as hs_resolve, step after step, against
-    the oracle."""
+    the oracle.  Every other step copies layer by layer through
+    hs_miss_copy_layers, on a 7-CTA grid for layer 0 and the default one for
+    layer 1; empty or out-of-range layer ranges are refused."""
     from harness import Case, Runner
     hs = _hs()
     case = Case("split", B=3, N=[3000, 2500, 4100], K=256, Hi=8, Di=32, H=16, L=2, T=256,
@@ -924,7 +926,11 @@ def test_resolve_plan_then_miss_copy_equals_resolve():
             ev = torch.cuda.Event()
             ev.record()
             side.wait_event(ev)
-            b.pool.miss_copy(case.B, 2, stream=side)
+            if s % 2:
+                b.pool.miss_copy(case.B, 2, stream=side)
+            else:
+                b.pool.miss_copy_layers(case.B, 2, 0, 1, ctas=7, stream=side)
+                b.pool.miss_copy_layers(case.B, 2, 1, 2, stream=side)
             torch.cuda.synchronize()
             assert a.pool.get_error() == hs.HS_OK and b.pool.get_error() == hs.HS_OK
             assert torch.equal(ra, rb)
@@ -934,6 +940,9 @@ def test_resolve_plan_then_miss_copy_equals_resolve():
                     np.testing.assert_array_equal(sa[k], sb[k])
                 b._check_rows(r, np.where(idx[r] >= 0, idx[r], -1), rb[r])
         assert a.pool.stats() == b.pool.stats() and b.pool.stats()["misses"] > 0
+        for l0, l1, ctas in ((1, 1, 0), (0, 3, 0), (-1, 1, 0), (0, 1, -1)):
+            with pytest.raises(hs.HSError):
+                b.pool.miss_copy_layers(case.B, 2, l0, l1, ctas=ctas)
     finally:
         a.close()
         b.close()
