@@ -32,7 +32,9 @@
 // times slower to land per chunk than these loads.)
 // Warp 0 issues the MMAs, warp 1 owns TMEM and prefetches rows, warps 2-9
 // run the exchange, softmax, rescale and epilogue (thread = TMEM lane = head,
-// one warp per (lane quarter, half chunk)), warps 10-13 convert.
+// one warp per (lane quarter, half chunk)), warps 10, 11, 14 and 15 convert
+// (12 and 13 stay idle, keeping the conversion off the softmax's SM
+// sub-partitions).
 // Every wait is bounded; on a time-out the kernel records HS_ERR_TIMEOUT,
 // skips the remaining work and returns.
 #include <cuda_bf16.h>
@@ -46,7 +48,7 @@ namespace {
 
 constexpr int kRowsPerChunk = 128;
 constexpr int kPairHeads = 128;
-constexpr int kPairThreads = 448;  // 14 warps
+constexpr int kPairThreads = 512;  // 16 warps (12 and 13 idle, see below)
 constexpr int kKbBytes = 16384;    // 128 rows x 64 fp16 (128-byte swizzle)
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kLog2eP = 1.4426950408889634f;
@@ -344,6 +346,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         };
         // in chunk order: the first chunks' rows arrive first
         for (int c = 0; c < nch; c++) prefetch(c);
+    } else if (warp == 12 || warp == 13) {
+        // idle: a warp's SM sub-partition is warp % 4, and sub-partitions 0
+        // and 1 run the softmax of this CTA's heads (TMEM lanes 0-63 or
+        // 64-127 are read from two sub-partitions only), so the converters
+        // are warps 10, 11, 14 and 15, on sub-partitions 2 and 3 (measured
+        // 354.9 -> 344.7 us at 64 x 4 queries against warps 10-13)
     } else if (warp >= 10) {
         // ------------------------------------------------------ converters
         // Thread ct owns rows ct/4 + 32 i (i < 4) and the 16-byte slice ct % 4
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // of its rope half: 16 + 4 loads of 16 bytes and 4 of the rows' two
         // group scales per chunk, issued a chunk ahead into registers.
         tc::grid_dep_wait();
-        const int ct = threadIdx.x - 320;  // 0..127
+        const int ct = warp < 14 ? threadIdx.x - 320 : threadIdx.x - 384;  // 0..127
         const int part = ct & 3;
         uint4 raw[4][4], rope[4];
         float2 sg[4];
