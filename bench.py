@@ -517,7 +517,7 @@ TRAFFIC = {
     # still in L2 at the end (16 x 4 rows of 142,000)
     "topk_filter_kernel": ("topk.cu", "6698f043a64ba116", (36.39 + 0.003) / (36.36 + 0.52)),
     # rows, queries and outputs of one layer (64 x 4 queries x 2048 rows x 128 heads)
-    "attn_pair_kernel": ("attention_pair.cu", "9bcd4609f6372c9b", (354.27 + 26.66) / 415.2),
+    "attn_pair_kernel": ("attention_pair.cu", "c6333d74be841dc2", (353.06 + 23.18) / 415.2),
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
