@@ -106,6 +106,7 @@ struct PlanArgs {
     int32_t *row_id;
     int32_t *err;
     unsigned long long *stats;
+    int words;  // > 0: union of several lists by a bitmap of this many words over the tokens
 };
 
 __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
@@ -165,6 +166,38 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         miss = merged;
         missidx = U;
         U = lst;
+    } else if (a.words > 0) {
+        // Each list is ascending without repeats (validated above), so the
+        // union is the set bits of a bitmap over the request's tokens, in
+        // order; each word's count of the bits before it then gives a
+        // token's index in U without a search (step 6).  Thread t owns
+        // words [t * wpt, (t + 1) * wpt).
+        uint32_t *bm = (uint32_t *)(victim + n);
+        int32_t *wpre = (int32_t *)(bm + a.words);
+        const int words = (N + 31) >> 5;  // N <= max_tokens: words <= a.words
+        for (int w = tid; w < words; w += kThreads) bm[w] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+            const int32_t x = lst[i];
+            if (x >= 0) atomicOr(&bm[x >> 5], 1u << (x & 31));
+        }
+        __syncthreads();
+        const int wpt = (words + kThreads - 1) / kThreads;
+        const int w0 = min(words, tid * wpt), w1 = min(words, w0 + wpt);
+        int cnt = 0;
+        for (int w = w0; w < w1; w++) cnt += __popc(bm[w]);
+        int run = block_excl_scan(cnt, warp_sums, &nu);
+        for (int w = w0; w < w1; w++) {
+            wpre[w] = run;
+            uint32_t bits = bm[w];
+            while (bits) {
+                U[run++] = (w << 5) + __ffs(bits) - 1;
+                bits &= bits - 1;
+            }
+        }
+        __syncthreads();
+        miss = merged;  // merged is unused on this path
+        missidx = lst;  // lists are dead now
     } else {
         int total = 0;
         for (int j = 0; j < a.nq; j++) total += lens[j];
@@ -188,18 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
         missidx = lst;  // lists are dead now
     }
 
-    // 3. classify; hits refresh their stamp
+    // 3. classify; hits refresh their stamp.  Entries in groups of four per
+    // thread, so that their block-table and then hot-map loads are in
+    // flight together.
     int nres = 0, nhit = 0, nmiss = 0;
-    for (int i = tid; i < nu; i += kThreads) {
-        const int32_t u = U[i];
-        const int32_t blk = bt[u / a.P];
-        if (blk >= 0) {
-            uslot[i] = -1;
-            if (single) rid[i] = blk * a.P + u % a.P;  // one list: U[i] is entry i
-            nres++;
-        } else {
-            const int32_t s = a.hot_map[hm + u];
-            if (s >= 0) {
+    constexpr int kG = 4;
+    for (int i0 = tid; i0 < nu; i0 += kG * kThreads) {
+        int32_t u[kG], blk[kG], hs_[kG];
+#pragma unroll
+        for (int g = 0; g < kG; g++) {
+            const int i = i0 + g * kThreads;
+            u[g] = i < nu ? U[i] : -1;
+            blk[g] = u[g] >= 0 ? bt[u[g] / a.P] : 0;
+        }
+#pragma unroll
+        for (int g = 0; g < kG; g++) hs_[g] = (u[g] >= 0 && blk[g] < 0) ? a.hot_map[hm + u[g]] : -1;
+#pragma unroll
+        for (int g = 0; g < kG; g++) {
+            const int i = i0 + g * kThreads;
+            if (i >= nu) continue;
+            if (blk[g] >= 0) {
+                uslot[i] = -1;
+                if (single) rid[i] = blk[g] * a.P + u[g] % a.P;  // one list: U[i] is entry i
+                nres++;
+            } else if (hs_[g] >= 0) {
+                const int32_t s = hs_[g];
                 uslot[i] = s;
                 a.stamp[sc + s] = step;
                 if (single) rid[i] = hb[s / a.P] * a.P + s % a.P;
@@ -347,18 +393,39 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     if (single) return;  // every entry's row id is written above
     __syncthreads();
 
-    // 6. row ids
-    for (int i = tid; i < n; i += kThreads) {
-        const int32_t u = tk[i];
-        int32_t r = -1;
-        if (u >= 0) {
-            const int32_t s = uslot[single ? i : lower_bound(U, nu, u)];
-            if (s == -1)
-                r = bt[u / a.P] * a.P + u % a.P;
-            else if (s >= 0)
-                r = hb[s / a.P] * a.P + s % a.P;
+    // 6. row ids: each entry's index in U (from the bitmap's word counts,
+    // else a search), its slot, then the row (groups of four per thread,
+    // their loads in flight together)
+    const uint32_t *bm = (const uint32_t *)(victim + n);
+    const int32_t *wpre = (const int32_t *)(bm + a.words);
+    for (int i0 = tid; i0 < n; i0 += kG * kThreads) {
+        int32_t u[kG], sl[kG], r[kG];
+#pragma unroll
+        for (int g = 0; g < kG; g++) {
+            const int i = i0 + g * kThreads;
+            u[g] = i < n ? tk[i] : -1;
         }
-        rid[i] = r;
+#pragma unroll
+        for (int g = 0; g < kG; g++) {
+            sl[g] = -3;
+            if (u[g] >= 0) {
+                const int x = u[g];
+                const int ui = a.words > 0 ? wpre[x >> 5] + __popc(bm[x >> 5] & ((1u << (x & 31)) - 1u))
+                                           : lower_bound(U, nu, x);
+                sl[g] = uslot[ui];
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kG; g++) {
+            r[g] = -1;
+            if (sl[g] == -1)
+                r[g] = bt[u[g] / a.P] * a.P + u[g] % a.P;
+            else if (sl[g] >= 0)
+                r[g] = hb[sl[g] / a.P] * a.P + sl[g] % a.P;
+        }
+#pragma unroll
+        for (int g = 0; g < kG; g++)
+            if (i0 + g * kThreads < n) rid[i0 + g * kThreads] = r[g];
     }
 }
 
@@ -421,13 +488,20 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(
     }
 }
 
-size_t plan_smem(int n) { return (size_t)5 * n * 4; }
+// Bitmap words for the union of several lists: while the bitmap and its
+// word counts fit beside the five arrays (rows of up to 262,144 tokens).
+int plan_words(const hs_pool *p, int nq) {
+    const int words = (p->cfg.max_tokens + 31) / 32;
+    return nq > 1 && words <= 8192 ? words : 0;
+}
+
+size_t plan_smem(int n, int words) { return (size_t)5 * n * 4 + (size_t)words * 8; }
 
 }  // namespace
 
 cudaError_t resolve_setup(const hs_pool *p) {
-    const size_t sm = plan_smem(p->nq_max * p->cfg.top_k);
-    if (sm > 200 * 1024) return cudaErrorInvalidValue;
+    const size_t sm = plan_smem(p->nq_max * p->cfg.top_k, plan_words(p, p->nq_max));
+    if (sm > 227 * 1024) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(resolve_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sm);
 }
@@ -460,9 +534,10 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
     a.row_id = row_id;
     a.err = p->d.err;
     a.stats = p->d.stats;
+    a.words = plan_words(p, nq);
     const int n = nq * a.K;
     {
-        PdlLaunch lc(dim3(B), dim3(kThreads), plan_smem(n), st);
+        PdlLaunch lc(dim3(B), dim3(kThreads), plan_smem(n, a.words), st);
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, resolve_plan_kernel, a);
         if (e != cudaSuccess) return e;
     }
