@@ -247,9 +247,10 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
     n_warm = max(warmup, w["warm"]) if not w["restart"] else warmup
     stage_steps = min(steps, 20)
     e2e_steps = min(steps, 50)
-    # steps of the trace: warm-up, timed, stage timing, end to end
+    copy_steps = min(steps, 10) if w["mode"] != "full" else 0
+    # steps of the trace: warm-up, timed, copy timing, stage timing, end to end
     first_timed = 1 if w["restart"] else n_warm + 1
-    total_trace = (first_timed - 1) + steps + stage_steps + e2e_steps
+    total_trace = (first_timed - 1) + steps + copy_steps + stage_steps + e2e_steps
     trace = Trace(w, device, 1, max(total_trace, n_warm))
     pool = setup_pool(w, device)
     tau = 1.0 / math.sqrt(576)
@@ -336,12 +337,38 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
     value = whole_job_rows_per_s(world, rows_per_step, ms_per_step)
     misses_per_step = timed_stats["misses"] / steps
 
+    # ---- the miss copies as the step runs them: the same graph replayed for
+    # the next steps of the trace, the per-layer copy spans read from the
+    # pool's timing events on its copy stream after each step ----
+    in_step_copy_ms, in_step_copy_bytes = 0.0, 0.0
+    if copy_steps:
+        # a second capture of the same step with the timing records on (the
+        # timed graph above carries none)
+        pool.time_copies(True)
+        timed_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(timed_graph, stream=stream):
+                enqueue_step(stream)
+        pool.time_copies(False)
+        torch.cuda.synchronize()
+        s0 = pool.stats()
+        with torch.cuda.stream(stream):
+            for i in range(copy_steps):
+                load(steps + i, first_timed + steps + i)
+                flush_l2()
+                timed_graph.replay()
+                stream.synchronize()
+                in_step_copy_ms += sum(pool.copy_times())
+        in_step_copy_bytes = (pool.stats()["misses"] - s0["misses"]) * L * 656
     # ---- per-stage timing (the next steps of the trace, eager, events between stages) ----
     stage = stage_times(pool, w, inputs, q, wt, qm, out, topk, rid, trace, flush_l2, stream,
-                        stage_steps, first_timed + steps)
+                        stage_steps, first_timed + steps + copy_steps)
+    if copy_steps:
+        stage["miss_copy_in_step"] = in_step_copy_ms / copy_steps  # ms per step, L launches
+        stage["miss_copy_in_step_bytes"] = in_step_copy_bytes / copy_steps
     # ---- end to end: host inputs in, result out, through the public API ----
     e2e = end_to_end(pool, w, inputs, trace, stream, e2e_steps, device,
-                     first_timed + steps + stage_steps)
+                     first_timed + steps + copy_steps + stage_steps)
     if pool.get_error() != hs.HS_OK:
         raise RuntimeError("device error after the timed region")
 
@@ -355,7 +382,7 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
         "ms_per_step": ms_per_step,
         "us_per_layer": ms_per_step * 1e3 / L,
         "value": value,
-        "stage_us": {k: v * 1e3 for k, v in stage.items()},
+        "stage_us": {k: v * 1e3 for k, v in stage.items() if not k.endswith("_bytes")},
         "hbm_frac_step": (step_bytes / (ms_per_step / 1e3)) / (peaks["hbm"] * 1e9),
         "hbm_frac_step_note": "algorithmic HBM bytes of the step (indexer keys, top-K, resolve, "
                               "the L layers' rows, queries and outputs) / step time / measured "
@@ -372,44 +399,41 @@ def run_workload(w, args, rank, world, local_rank, steps, warmup, headline):
         "config": config_of(w, steps),
     }
     if link is not None:
-        ms_copy = stage["miss_copy"]
+        ms_alone = stage["miss_copy"]
         nbytes = misses_per_step * L * 656
-        ach = nbytes / (ms_copy / 1e3) / 1e9 if ms_copy > 0 else 0.0
         res["host_link"] = {
-            "miss_bytes_per_step": nbytes, "us_miss_copy": ms_copy * 1e3, "achieved_gbs": ach,
-            "peak_gbs": link["peak_gbs"], "peak_source": link["source"], "frac": ach / link["peak_gbs"],
+            "miss_bytes_per_step": nbytes, "peak_gbs": link["peak_gbs"], "peak_source": link["source"],
             "peak_candidates": link["candidates"],
-            # the copies' share of the step itself: with a host pool the step
-            # runs prefix -> four per-layer copies (each layer's attention
-            # beside the next copy) -> the last layer's attention, so the copies
-            # take about the step less the prefix stages and one attention
-            "in_step_estimate": in_step_copy(stage, ms_per_step, nbytes),
+            "alone": {"us": ms_alone * 1e3,
+                      "achieved_gbs": nbytes / (ms_alone / 1e3) / 1e9 if ms_alone > 0 else 0.0,
+                      "what": "the copy as the step launches it (one 64-CTA launch per layer, back "
+                              "to back) but alone, between events on its stream, over the misses of "
+                              "the stage-timing steps"},
             "full_grid": {"us": stage["miss_copy_full"] * 1e3,
                           "achieved_gbs": nbytes / (stage["miss_copy_full"] / 1e3) / 1e9
                           if stage["miss_copy_full"] > 0 else 0.0,
-                          "what": "the same copy in one hs_miss_copy launch of about four CTAs per SM"},
-            "timed": "miss-copy kernel spans as the step launches them (hs_miss_copy_layers, one "
-                     "launch per layer on a 64-CTA grid, back to back, events on their stream) "
-                     "over the misses of the stage-timing steps; bytes = the timed steps' mean "
-                     "misses x L x 656"}
+                          "what": "the same copy in one hs_miss_copy launch of about four CTAs per SM"}}
+        if "miss_copy_in_step" in stage:
+            ms_in, b_in = stage["miss_copy_in_step"], stage["miss_copy_in_step_bytes"]
+            ach = b_in / (ms_in / 1e3) / 1e9 if ms_in > 0 else 0.0
+            res["host_link"].update({
+                "us_miss_copy": ms_in * 1e3, "bytes": b_in, "achieved_gbs": ach,
+                "frac": ach / link["peak_gbs"],
+                "timed": "in the step: the per-layer copies on the pool's side stream, beside the "
+                         "attention, spans read from the pool's timing events on that stream "
+                         "(hs_pool_time_copies, in a second capture of the step) over %d graph "
+                         "replays after the timed region; "
+                         "bytes = those steps' misses x L x 656" % copy_steps})
+        else:
+            ach = res["host_link"]["alone"]["achieved_gbs"]
+            res["host_link"].update({"us_miss_copy": ms_alone * 1e3, "achieved_gbs": ach,
+                                     "frac": ach / link["peak_gbs"], "timed": "alone (see above)"})
     if rank == 0 and headline and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     pool.close()
     del pool
     torch.cuda.empty_cache()
     return res
-
-
-def in_step_copy(stage, ms_per_step, nbytes):
-    """Derived, not measured: the step time less the separately timed
-    indexer, top-K, plan and one layer's attention, taken as the span of the
-    step's four back-to-back copies (valid while they are the step's critical
-    path, as they are with a host pool at the mixed-residency workload)."""
-    ms = ms_per_step - (stage["indexer"] + stage["topk"] + stage["resolve_plan"] + stage["attention"])
-    if ms <= 0:
-        return None
-    return {"us": ms * 1e3, "achieved_gbs": nbytes / (ms / 1e3) / 1e9,
-            "what": "step time - (indexer + top-K + plan + one attention), all event-timed"}
 
 
 def reset_hot_state(pool, w):
@@ -595,12 +619,21 @@ def roofline(stage, alg, peaks, w, ms_per_step, link):
         elif k == "miss_copy":
             if link is None or a["bytes"] == 0:
                 continue
+            where = "alone, four 64-CTA launches back to back"
+            if "miss_copy_in_step" in stage:  # measured inside the step itself
+                ms, nb = stage["miss_copy_in_step"], stage["miss_copy_in_step_bytes"]
+                gbs = nb / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+                share = ms / ms_per_step
+                traffic = traffic_of(kern, nb / L)
+                where = "in the step (pool timing events on its copy stream)"
+            else:
+                traffic = traffic_of(kern, a["bytes"] / L)
             out[k] = {"kernel": kern, "bound": "host_link", "achieved": gbs,
                       "peak": link["peak_gbs"], "unit": "GB/s", "frac": gbs / link["peak_gbs"],
-                      "traffic": traffic, "traffic_note": "HBM bytes per launch (the host-link "
-                      "bytes are 1.026x the algorithmic bytes in the capture)",
+                      "traffic": traffic, "traffic_note": "HBM bytes per launch (one layer; the "
+                      "host-link bytes are 1.026x the algorithmic bytes in the capture)",
                       "peak_source": link["source"], "share_of_step": share,
-                      "us_per_launch": ms * 1e3}
+                      "us_per_launch": ms * 1e3 / L, "timed": where}
         else:
             out[k] = {"kernel": kern, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
                       "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": traffic,

@@ -362,6 +362,19 @@ hs_status hs_miss_copy(hs_pool *pool, int32_t B, int32_t nq, cudaStream_t stream
 hs_status hs_miss_copy_layers(hs_pool *pool, int32_t B, int32_t nq, int32_t layer_begin,
                               int32_t layer_end, int32_t ctas, cudaStream_t stream);
 
+/* Timing of the per-layer miss copies that hs_resolve_attend and hs_step run
+ * on the pool's side stream.  With enable != 0, every later such call
+ * records a pair of pool-owned timing events around each layer's copy on
+ * that stream (recorded as external events, so that a CUDA graph captured
+ * after enabling keeps them and records them at every replay).
+ * hs_pool_copy_times writes the durations, in ms, of layers [0, n) of the
+ * last recorded step; call it once that step has completed (after a
+ * stream or device synchronisation).  HS_ERR_INVALID_ARG without a host
+ * pool or for n outside [0, L]; HS_ERR_CUDA when the events have not been
+ * recorded or have not completed. */
+hs_status hs_pool_time_copies(hs_pool *pool, int32_t enable);
+hs_status hs_pool_copy_times(hs_pool *pool, float *ms, int32_t n);
+
 /* Sparse MLA decode of one layer over the resolved rows ("Ce qui se passe"):
  *   z[b][j][h][k] = softmax_scale * q[b][j][h][:576] . row(row_id[b][j][k])[:576]
  *   out[b][j][h][:512] = sum_k softmax_k(z) * row[:512]   (rows with id -1 skipped)

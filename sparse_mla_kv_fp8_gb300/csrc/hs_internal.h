@@ -127,6 +127,9 @@ struct hs_pool {
     int copy_priority;
     cudaEvent_t ev_plan;
     std::vector<cudaEvent_t> ev_copy;  // [L]
+    // timing of the side stream's per-layer copies (hs_pool_time_copies)
+    bool time_copies;
+    std::vector<cudaEvent_t> tc_begin, tc_end;  // [L]
 };
 
 namespace hs {

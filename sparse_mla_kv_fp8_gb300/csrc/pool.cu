@@ -263,7 +263,7 @@ int64_t blocks_in_mode(const hs_pool *p, int32_t req, int mode) {
 
 extern "C" {
 
-int32_t hs_abi_version(void) { return 105; }
+int32_t hs_abi_version(void) { return 106; }
 
 const char *hs_status_string(hs_status s) {
     switch (s) {
@@ -404,8 +404,13 @@ hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena, size_t dev_
         if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->copy_stream, cudaStreamNonBlocking, hi);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_plan, cudaEventDisableTiming);
         p->ev_copy.assign(cfg->num_mla_layers, nullptr);
-        for (int l = 0; l < cfg->num_mla_layers && e == cudaSuccess; l++)
+        p->tc_begin.assign(cfg->num_mla_layers, nullptr);
+        p->tc_end.assign(cfg->num_mla_layers, nullptr);
+        for (int l = 0; l < cfg->num_mla_layers && e == cudaSuccess; l++) {
             e = cudaEventCreateWithFlags(&p->ev_copy[l], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreate(&p->tc_begin[l]);
+            if (e == cudaSuccess) e = cudaEventCreate(&p->tc_end[l]);
+        }
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -428,6 +433,10 @@ void hs_pool_destroy(hs_pool *pool) {
     }
     if (pool->ev_plan) cudaEventDestroy(pool->ev_plan);
     for (cudaEvent_t ev : pool->ev_copy)
+        if (ev) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : pool->tc_begin)
+        if (ev) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : pool->tc_end)
         if (ev) cudaEventDestroy(ev);
     delete pool;
 }
@@ -784,6 +793,25 @@ hs_status hs_miss_copy(hs_pool *p, int32_t B, int32_t nq, cudaStream_t st) {
     return cuda_status(hs::launch_miss_copy(p, B, nq, st));
 }
 
+hs_status hs_pool_time_copies(hs_pool *p, int32_t enable) {
+    if (!p || p->cfg.host_blocks == 0) return HS_ERR_INVALID_ARG;
+    p->time_copies = enable != 0;
+    return HS_OK;
+}
+
+hs_status hs_pool_copy_times(hs_pool *p, float *ms, int32_t n) {
+    if (!p || !ms || p->cfg.host_blocks == 0 || n < 0 || n > p->cfg.num_mla_layers)
+        return HS_ERR_INVALID_ARG;
+    for (int l = 0; l < n; l++) {
+        const cudaError_t e = cudaEventElapsedTime(&ms[l], p->tc_begin[l], p->tc_end[l]);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return HS_ERR_CUDA;
+        }
+    }
+    return HS_OK;
+}
+
 hs_status hs_miss_copy_layers(hs_pool *p, int32_t B, int32_t nq, int32_t l0, int32_t l1,
                               int32_t ctas, cudaStream_t st) {
     if (!step_batch_ok(p, B, nq) || l0 < 0 || l1 <= l0 || l1 > p->cfg.num_mla_layers || ctas < 0)
@@ -836,8 +864,20 @@ static cudaError_t resolve_attend(hs_pool *p, const int32_t *topk, int B, int nq
     cudaError_t e = hs::launch_resolve_plan(p, topk, B, nq, row_id, st);
     if (e == cudaSuccess) e = cudaEventRecord(p->ev_plan, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_stream, p->ev_plan, 0);
+    // timing records: external ones while the stream is being captured, so
+    // that the graph records them at every replay; plain ones otherwise
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (e == cudaSuccess && p->time_copies) e = cudaStreamIsCapturing(p->copy_stream, &cap);
+    auto stamp = [&](cudaEvent_t ev) {
+        return cap == cudaStreamCaptureStatusActive
+                   ? cudaEventRecordWithFlags(ev, p->copy_stream, cudaEventRecordExternal)
+                   : cudaEventRecord(ev, p->copy_stream);
+    };
     for (int l = 0; l < L && e == cudaSuccess; l++) {
-        e = hs::launch_miss_copy(p, B, nq, p->copy_stream, l, l + 1, kCopyCtasBeside, p->copy_priority);
+        if (p->time_copies) e = stamp(p->tc_begin[l]);
+        if (e == cudaSuccess)
+            e = hs::launch_miss_copy(p, B, nq, p->copy_stream, l, l + 1, kCopyCtasBeside, p->copy_priority);
+        if (e == cudaSuccess && p->time_copies) e = stamp(p->tc_end[l]);
         if (e == cudaSuccess) e = cudaEventRecord(p->ev_copy[l], p->copy_stream);
     }
     for (int l = 0; l < L && e == cudaSuccess; l++) {

@@ -90,6 +90,8 @@ hs_resolve = _decl("hs_resolve", _i32, [_P, _P, _i32, _i32, _P, _P])
 hs_resolve_plan = _decl("hs_resolve_plan", _i32, [_P, _P, _i32, _i32, _P, _P])
 hs_miss_copy = _decl("hs_miss_copy", _i32, [_P, _i32, _i32, _P])
 hs_miss_copy_layers = _decl("hs_miss_copy_layers", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P])
+hs_pool_time_copies = _decl("hs_pool_time_copies", _i32, [_P, _i32])
+hs_pool_copy_times = _decl("hs_pool_copy_times", _i32, [_P, ctypes.POINTER(ctypes.c_float), _i32])
 hs_host_read_probe = _decl("hs_host_read_probe", _i32, [_P, _P, _sz, _i32, _P])
 hs_sparse_mla_decode = _decl("hs_sparse_mla_decode", _i32,
                              [_P, _i32, _P, _P, _i32, _i32, _f32, _P, _P, _P])
@@ -276,6 +278,16 @@ class Pool:
 
     def miss_copy(self, B, nq, stream=None):
         check(hs_miss_copy(self.handle, B, nq, _stream(stream)), "hs_miss_copy")
+
+    def time_copies(self, enable=True):
+        check(hs_pool_time_copies(self.handle, 1 if enable else 0), "hs_pool_time_copies")
+
+    def copy_times(self, n=None):
+        """Per-layer durations (ms) of the last recorded step's side-stream copies."""
+        n = self.cfg.num_mla_layers if n is None else n
+        buf = (ctypes.c_float * max(n, 1))()
+        check(hs_pool_copy_times(self.handle, buf, n), "hs_pool_copy_times")
+        return [buf[i] for i in range(n)]
 
     def miss_copy_layers(self, B, nq, layer_begin, layer_end, ctas=0, stream=None):
         check(hs_miss_copy_layers(self.handle, B, nq, layer_begin, layer_end, ctas, _stream(stream)),

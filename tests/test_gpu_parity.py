@@ -965,7 +965,9 @@ def test_host_read_probe_copies_pinned_host_memory():
 def test_resolve_attend_overlapped_copies_equal_separate_calls():
     """hs_resolve_attend gives bit-identical row ids, state and outputs to
     hs_resolve followed by hs_sparse_mla_decode per layer, eager and replayed
-    from a CUDA graph, on a mixed-residency pool with misses every step."""
+    from a CUDA graph, on a mixed-residency pool with misses every step.  With
+    copy timing on (before the capture), every step, eager or replayed,
+    leaves one completed span per layer's copy."""
     from harness import Case, Runner
     hs = _hs()
     case = Case("overlap", B=3, N=[3000, 2500, 4100], K=256, Hi=8, Di=32, H=128, L=3, T=256,
@@ -981,6 +983,7 @@ def test_resolve_attend_overlapped_copies_equal_separate_calls():
         qm = torch.empty((L, B, nq, H, 576), dtype=torch.bfloat16, device=a.dev)
         st = torch.cuda.Stream()
         graph = None
+        b.pool.time_copies(True)
         for s in range(1, 9):
             tk.copy_(torch.from_numpy(a.drawn(s)))
             qm.copy_(a.step_inputs(s)[2])
@@ -1001,6 +1004,8 @@ def test_resolve_attend_overlapped_copies_equal_separate_calls():
             assert torch.equal(ra, rb), f"step {s}: row ids"
             assert torch.equal(oa, ob), f"step {s}: outputs"
             assert torch.equal(la, lb), f"step {s}: lse"
+            spans = b.pool.copy_times()
+            assert len(spans) == L and all(0.0 < t < 1000.0 for t in spans), spans
             for r in range(B):
                 sa, sb = a.pool.dump_state(r), b.pool.dump_state(r)
                 for k in ("hot_map", "slot_token", "stamp", "step"):
