@@ -562,7 +562,7 @@ TRAFFIC = {
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
-    "miss_copy_kernel": ("resolve.cu", "4f3dbaec407d11e4", (0.95 + 91.43) / 96.9),
+    "miss_copy_kernel": ("resolve.cu", "c057ddbba3b0b05a", (0.33 + 91.43) / 96.9),
 }
 
 
