@@ -351,7 +351,9 @@ hs_status hs_miss_copy(hs_pool *pool, int32_t B, int32_t nq, cudaStream_t stream
 
 /* The copy of hs_miss_copy for layers [layer_begin, layer_end) only, on a
  * grid of about `ctas` CTAs in all (0: about four per SM over the batch, as
- * hs_miss_copy).  For callers that overlap each layer's copy with another
+ * hs_miss_copy).  The copy itself is the one "Un contexte d'un million sur
+ * huit H200", « Les trois états de résidence », defines: exactly one row
+ * per miss and layer from pinned host memory into the request's hot buffer.  For callers that overlap each layer's copy with another
  * layer's attention on a second stream, as hs_resolve_attend does with
  * about 64 CTAs: the copy of layer l must complete before layer l's
  * hs_sparse_mla_decode reads the rows.  The same ordering rule as
@@ -362,8 +364,9 @@ hs_status hs_miss_copy(hs_pool *pool, int32_t B, int32_t nq, cudaStream_t stream
 hs_status hs_miss_copy_layers(hs_pool *pool, int32_t B, int32_t nq, int32_t layer_begin,
                               int32_t layer_end, int32_t ctas, cudaStream_t stream);
 
-/* Timing of the per-layer miss copies that hs_resolve_attend and hs_step run
- * on the pool's side stream.  With enable != 0, every later such call
+/* Timing of the per-layer miss copies (« Les trois états de résidence »)
+ * that hs_resolve_attend and hs_step run on the pool's side stream: an
+ * instrument for the step's host-link rate, no part of the method.  With enable != 0, every later such call
  * records a pair of pool-owned timing events around each layer's copy on
  * that stream (recorded as external events, so that a CUDA graph captured
  * after enabling keeps them and records them at every replay).
