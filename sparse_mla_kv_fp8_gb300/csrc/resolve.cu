@@ -7,8 +7,10 @@
 //
 // resolve_plan_kernel: one 1024-thread CTA per request.
 //   1. validate the nq lists (ascending, -1 padded, inside the request);
-//   2. merge them into U, their sorted union without duplicates (merge-path
-//      ranks by binary search, then a compaction of first occurrences);
+//   2. merge them into U, their sorted union without duplicates (the set
+//      bits of a bitmap over the request's tokens, whose per-word counts also
+//      index U in step 6; beyond 262,144 tokens merge-path ranks by binary
+//      search, then a compaction of first occurrences);
 //   3. classify each u in U: resident page -> in place; hot_map[u] >= 0 -> hit
 //      (stamp = step); else miss; misses are compacted in ascending order;
 //   4. choose victims: among slots with stamp < step, the M smallest keys

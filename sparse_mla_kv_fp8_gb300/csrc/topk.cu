@@ -470,23 +470,25 @@ topk_cluster_kernel(const float *__restrict__ scores, int64_t stride, int vec4,
 // decided against the threshold long before the last digit.  This path
 // touches each score once, with a compare:
 //   1. topk_thresh_kernel, one CTA per row: T = the order key of the r-th
-//      largest of S evenly spaced scores of the row, with r chosen so that
-//      about m = max(2.5 K, 2048) tokens are expected at or above T (a
-//      sample quantile: relative spread about 1 / sqrt(r), r >= 80 here).
-//      Rows of at most kTopkCandCap visible tokens take T = 0: all are
-//      candidates.
-//   2. topk_filter_kernel, (chunk, row) CTAs: one coalesced pass; every
-//      visible token with key >= T is appended (key, token) to the row's
-//      candidate list, one atomic per CTA reserving its range.
-//   3. topk_select_kernel, one CTA per row.  When the row kept between K and
-//      kTopkCandCap candidates, they contain every token of the exact top-K:
-//      the K-th largest key of the row is then >= T, and every token at or
-//      above T is a candidate.  A radix select over the candidates (held in
-//      registers) gives the exact threshold key and the number of keys equal
-//      to it to take; bitmaps over windows of the token range then write the
-//      selection in ascending token order, equal keys lowest token first.
-//      When the sample misjudged the row (fewer than K or more than the cap),
-//      the same CTA runs the exact radix select over the whole row instead.
+//      largest of S scores of the row (S / 8 runs of 8 consecutive tokens
+//      at evenly spaced positions), with r chosen so that about
+//      m = max(2.5 K, 2048) tokens are expected at or above T (a sample
+//      quantile: relative spread about 1 / sqrt(r), r >= 80 here).  Rows of
+//      at most kTopkCandCap visible tokens take T = 0: all are candidates.
+//   2. topk_filter_kernel, persistent warps over 512-token tiles: one
+//      coalesced pass; every visible token with key >= T is appended (key,
+//      token) to the row's candidate list, one atomic per warp and tile
+//      reserving its range.
+//   3. topk_select_kernel, per row one CTA or a cluster of one CTA per
+//      131,072-token window.  When the row kept between K and kTopkCandCap
+//      candidates, they contain every token of the exact top-K: the K-th
+//      largest key of the row is then >= T, and every token at or above T
+//      is a candidate.  An exact selection over the candidates (held in
+//      registers; 12-bit digits of key - min) gives the threshold key and
+//      the number of keys equal to it to take; bitmaps over the windows then
+//      place the selection in ascending token order, equal keys lowest token
+//      first.  When the sample misjudged the row (fewer than K or more than
+//      the cap), one CTA runs the exact selection over the whole row instead.
 // Either way the result is the multi-kernel path's, bit for bit.
 // ---------------------------------------------------------------------------
 // Tokens the sampled threshold aims to keep per row: 2.5 K, at least 2048.
