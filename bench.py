@@ -556,13 +556,13 @@ TRAFFIC = {
     "indexer_tc_kernel": ("indexer.cu", "77e081fbcc938a4a", (277.41 + 25.65) / 310.9),
     # the sampled-threshold filter: the scores read once, the few candidates
     # still in L2 at the end (16 x 4 rows of 142,000)
-    "topk_filter_kernel": ("topk.cu", "e84fd6732f724895", (36.389 + 0.002) / (36.36 + 0.52)),
+    "topk_filter_kernel": ("topk.cu", "b43a3cee7e2b2d50", (36.389 + 0.001) / (36.36 + 0.52)),
     # rows, queries and outputs of one layer (64 x 4 queries x 2048 rows x 128 heads)
     "attn_pair_kernel": ("attention_pair.cu", "c6333d74be841dc2", (353.06 + 23.18) / 415.2),
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
-    "miss_copy_kernel": ("resolve.cu", "c057ddbba3b0b05a", (0.33 + 91.43) / 96.9),
+    "miss_copy_kernel": ("resolve.cu", "762e35e383c7a949", (0.11 + 92.95) / 96.9),
 }
 
 
