@@ -552,8 +552,10 @@ def attention_kernel(w):
 # batch.
 TC_CUH_SHA = "beffda9b9722625b"
 TRAFFIC = {
-    # keys + sigma read once; scores partly still in L2 at the end (16 x 131,072, 4 queries)
-    "indexer_tc_kernel": ("indexer.cu", "77e081fbcc938a4a", (277.41 + 25.65) / 310.9),
+    # keys + sigma read once; scores partly still in L2 at the end, by queries
+    # per request (32 x 65,536 at one query, 16 x 131,072 at four)
+    "indexer_tc_kernel": ("indexer.cu", "594beef5a28364ce",
+                          {1: (277.13 + 7.94) / 285.5, 4: (277.42 + 25.56) / 310.9}),
     # the sampled-threshold filter: the scores read once, the few candidates
     # still in L2 at the end (16 x 4 rows of 142,000)
     "topk_filter_kernel": ("topk.cu", "b43a3cee7e2b2d50", (36.389 + 0.001) / (36.36 + 0.52)),
@@ -573,7 +575,7 @@ def _src_sha(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def traffic_of(kernel, alg_bytes):
+def traffic_of(kernel, alg_bytes, nq=1):
     t = TRAFFIC.get(kernel)
     if t is None or alg_bytes <= 0:
         return None
@@ -582,7 +584,10 @@ def traffic_of(kernel, alg_bytes):
             return None
     except OSError:
         return None
-    return t[2] * alg_bytes
+    ratio = t[2]
+    if isinstance(ratio, dict):  # captured per query count: the nearest one
+        ratio = ratio[min(ratio, key=lambda k: (abs(k - nq), k))]
+    return ratio * alg_bytes
 
 
 def roofline(stage, alg, peaks, w, ms_per_step, link):
@@ -605,7 +610,7 @@ def roofline(stage, alg, peaks, w, ms_per_step, link):
         a = alg[k]
         kern = (attention_kernel(w) if k == "attention"
                 else topk_kernel(w, -(-w["N"] // w["P"]) * w["P"]) if k == "topk" else KERNELS[k])
-        traffic = traffic_of(kern, a["bytes"])
+        traffic = traffic_of(kern, a["bytes"], w["nq"])
         gbs = a["bytes"] / (ms / 1e3) / 1e9
         share = ms * n / ms_per_step
         if k == "attention":
@@ -893,6 +898,7 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 CASES = {
     "indexer_mtp3_16x131072": "the indexer at four queries per request, 16 x 131,072 tokens",
+    "indexer_full_32x65536": "the indexer at one query per request, 32 x 65,536 tokens",
     "topk_mtp3_16x142000": "top-2048 of 16 x 4 indexer score rows of 142,000 tokens",
     "attention_mtp3_64x4x2048": "one layer of sparse MLA over 64 x 4 queries x 2048 rows, 128 heads",
     "attention_full_32x2048": "one layer of sparse MLA over 32 queries x 2048 rows, 128 heads",
@@ -946,8 +952,8 @@ def run_case(name, reps=3):
         w = torch.stack([wl.idx_weights(0, b, 1, nq, 64, dev) for b in range(B)])
         return q.contiguous(), w.contiguous()
 
-    if name == "indexer_mtp3_16x131072":
-        B, N, nq = 16, 131072, 4
+    if name in ("indexer_mtp3_16x131072", "indexer_full_32x65536"):
+        B, N, nq = (16, 131072, 4) if name == "indexer_mtp3_16x131072" else (32, 65536, 1)
         pool = full_pool(B, N, nq, 1, False)
         q, w = idx_inputs(B, nq)
         sc = torch.empty((B, nq, N), dtype=torch.float32, device=dev)

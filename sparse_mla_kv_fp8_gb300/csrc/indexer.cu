@@ -113,13 +113,17 @@ struct IdxTcArgs {
     int32_t *err;
 };
 
+// Shared memory of one CTA for ncols = nq * Hi query rows: the rows take
+// ncols x 128 B (a multiple of 4 KB, since Hi % 32 == 0), so the key stages
+// behind them stay 1024-aligned for the 128-byte swizzle.  Sizing the rows
+// by ncols rather than the 256 maximum lets three CTAs share an SM at one
+// query (three epilogue warps per TMEM sub-partition instead of two).
 struct IdxTcSmem {
-    static constexpr int q_off = 0;                             // 32 KB, 1024-aligned
-    static constexpr int k_off = 256 * 128;                     // stages, 1024-aligned
-    static constexpr int w_off = k_off + kTcStages * kTileBytes;
-    static constexpr int bar_off = w_off + 256 * 4;
-    static constexpr int tslot_off = bar_off + (2 * kTcStages + 5) * 8;
-    static constexpr int bytes = tslot_off + 16 + 1024;         // + alignment slack
+    __host__ __device__ static int k_off(int ncols) { return ncols * 128; }
+    __host__ __device__ static int w_off(int ncols) { return k_off(ncols) + kTcStages * kTileBytes; }
+    __host__ __device__ static int bar_off(int ncols) { return w_off(ncols) + 256 * 4; }
+    __host__ __device__ static int tslot_off(int ncols) { return bar_off(ncols) + (2 * kTcStages + 5) * 8; }
+    __host__ __device__ static int bytes(int ncols) { return tslot_off(ncols) + 16 + 1024; }  // + alignment slack
 };
 
 // sum_h w[h] * ReLU(d[h]) over nh columns of one TMEM lane row starting at
@@ -203,15 +207,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IdxTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *qs = smem + IdxTcSmem::q_off;
-    uint8_t *ks = smem + IdxTcSmem::k_off;
-    float *wsm = (float *)(smem + IdxTcSmem::w_off);
-    uint64_t *full = (uint64_t *)(smem + IdxTcSmem::bar_off);
+    uint8_t *qs = smem;
+    uint8_t *ks = smem + IdxTcSmem::k_off(a.ncols);
+    float *wsm = (float *)(smem + IdxTcSmem::w_off(a.ncols));
+    uint64_t *full = (uint64_t *)(smem + IdxTcSmem::bar_off(a.ncols));
     uint64_t *empty = full + kTcStages;
     uint64_t *tfull = empty + kTcStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
-    uint32_t *tslot = (uint32_t *)(smem + IdxTcSmem::tslot_off);
+    uint32_t *tslot = (uint32_t *)(smem + IdxTcSmem::tslot_off(a.ncols));
 
     const int b = blockIdx.y;
     const int N = a.seq_len[b];
@@ -406,10 +410,10 @@ cudaError_t launch_indexer_score(const hs_pool *p, const void *q, const float *w
         a.tmem_cols = tmem_cols_for(a.ncols);
         a.err = p->d.err;
         const int per_sm_tmem = 512 / a.tmem_cols;
-        const int per_sm_smem = (228 * 1024) / (IdxTcSmem::bytes + 1024);
+        const int per_sm_smem = (228 * 1024) / (IdxTcSmem::bytes(a.ncols) + 1024);
         const int per_sm = per_sm_tmem < per_sm_smem ? per_sm_tmem : per_sm_smem;
         // never co-schedule more CTAs than TMEM holds: pad the smem request
-        int smem = IdxTcSmem::bytes;
+        int smem = IdxTcSmem::bytes(a.ncols);
         const int cap = (228 * 1024) / per_sm - 1024;
         if (per_sm == 1 && smem < 116 * 1024) smem = 116 * 1024;
         else if (smem < cap && per_sm_tmem < per_sm_smem) smem = cap;
