@@ -109,6 +109,7 @@ struct PlanArgs {
     int32_t *err;
     unsigned long long *stats;
     int words;  // > 0: union of several lists by a bitmap of this many words over the tokens
+    int stage_pages;  // > 0: the request's block table is staged in shared memory
 };
 
 __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
@@ -119,19 +120,29 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_plan_kernel(PlanArgs a) {
     __shared__ int sel[4];
     const int b = blockIdx.x, tid = threadIdx.x;
     tc::grid_dep_launch();
-    tc::grid_dep_wait();  // the lists come from the previous kernel
     const int n = a.nq * a.K;
     int32_t *lst = sm;            // [n] the lists; later: index into U of each miss
     int32_t *merged = lst + n;    // [n] merged lists; later: miss tokens
     int32_t *U = merged + n;      // [n] sorted unique union
     int32_t *uslot = U + n;       // [n] -1 resident, >= 0 slot, -2 miss, -3 unserved
     int32_t *victim = uslot + n;  // [n] victim slots, ascending
+    // The request's length and block table change only through copies from
+    // the host, ordered on the stream before every kernel of the step: the
+    // table's used pages are staged while the previous kernel still runs
+    // (behind the bitmap and its word counts, [stage_pages]).
     const int N = a.seq_len[b];
+    const int32_t *bt = a.block_table + (size_t)b * a.max_pages;
+    if (a.stage_pages > 0) {
+        int32_t *bts = victim + n + 2 * a.words;
+        const int np = min(a.stage_pages, (N + a.P - 1) / a.P);
+        for (int i = tid; i < np; i += kThreads) bts[i] = bt[i];
+        bt = bts;  // read after the __syncthreads below
+    }
+    tc::grid_dep_wait();  // the lists (and the previous plan's step count) come from earlier kernels
     const uint32_t step = a.req_step[b] + 1;
     const int32_t *tk = a.topk + (size_t)b * n;
     int32_t *rid = a.row_id + (size_t)b * n;
     const size_t hm = (size_t)b * a.maxT, sc = (size_t)b * a.C;
-    const int32_t *bt = a.block_table + (size_t)b * a.max_pages;
     const int32_t *hb = a.hot_blocks + (size_t)b * a.hot_pages;
 
     // 1. load and validate
@@ -499,13 +510,21 @@ int plan_words(const hs_pool *p, int nq) {
 
 size_t plan_smem(int n, int words) { return (size_t)5 * n * 4 + (size_t)words * 8; }
 
+constexpr size_t kPlanSmemMax = 225 * 1024;  // 227 KB per CTA less the kernel's static arrays
+
+// The block table is staged while it fits beside the rest.
+int plan_stage_pages(const hs_pool *p, int n, int words) {
+    return plan_smem(n, words) + (size_t)p->max_pages * 4 <= kPlanSmemMax ? p->max_pages : 0;
+}
+
 }  // namespace
 
 cudaError_t resolve_setup(const hs_pool *p) {
     const size_t sm = plan_smem(p->nq_max * p->cfg.top_k, plan_words(p, p->nq_max));
-    if (sm > 227 * 1024) return cudaErrorInvalidValue;
+    if (sm > kPlanSmemMax) return cudaErrorInvalidValue;
+    // each launch asks for what its batch needs, the staged table included
     return cudaFuncSetAttribute(resolve_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)sm);
+                                (int)kPlanSmemMax);
 }
 
 int resolve_kernel_count(const hs_pool *p, int, int) { return p->cfg.host_blocks > 0 ? 2 : 1; }
@@ -538,8 +557,9 @@ cudaError_t launch_resolve_plan(const hs_pool *p, const int32_t *topk, int B, in
     a.stats = p->d.stats;
     a.words = plan_words(p, nq);
     const int n = nq * a.K;
+    a.stage_pages = plan_stage_pages(p, n, a.words);
     {
-        PdlLaunch lc(dim3(B), dim3(kThreads), plan_smem(n, a.words), st);
+        PdlLaunch lc(dim3(B), dim3(kThreads), plan_smem(n, a.words) + (size_t)a.stage_pages * 4, st);
         cudaError_t e = cudaLaunchKernelEx(&lc.cfg, resolve_plan_kernel, a);
         if (e != cudaSuccess) return e;
     }
