@@ -564,7 +564,7 @@ TRAFFIC = {
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
     # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
-    "miss_copy_kernel": ("resolve.cu", "762e35e383c7a949", (0.11 + 92.95) / 96.9),
+    "miss_copy_kernel": ("resolve.cu", "3ab01ede87a6d55b", (0.80 + 91.63) / 96.9),
 }
 
 
