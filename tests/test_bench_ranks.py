@@ -1,6 +1,8 @@
-"""The benchmark's multi-rank logic on CPU (gloo, two ranks): the step time is
-the slowest rank's, the value counts every rank's rows (weak scaling), and
-the reference arm runs on rank 0 only.  No GPU is involved."""
+"""The benchmark's host logic on CPU.  Multi-rank (gloo, two ranks): the step
+time is the slowest rank's, the value counts every rank's rows (weak
+scaling), and the reference arm runs on rank 0 only.  The traffic lookup:
+the captured ratio for the nearest query count, none for a changed source.
+No GPU is involved."""
 import os
 import socket
 import types
@@ -50,3 +52,21 @@ def test_two_gloo_ranks_max_time_and_whole_job_rows():
         assert t == 20.0                                     # the slowest rank's time
         assert v == pytest.approx(2 * 32 * 2048 * 4 / (2.0 / 1e3))  # both ranks' rows
     assert by_rank[1][2] is None                             # the reference arm: rank 0 only
+
+
+def test_traffic_ratio_by_query_count_and_stale_source(monkeypatch):
+    """A stage's DRAM traffic is its captured ratio x its algorithmic bytes:
+    the ratio of the nearest captured query count, and none once the
+    kernel's source no longer matches the captured one."""
+    import bench
+    monkeypatch.setitem(bench.TRAFFIC, "indexer_tc_kernel",
+                        ("indexer.cu", bench._src_sha("indexer.cu"), {1: 0.5, 4: 2.0}))
+    assert bench.traffic_of("indexer_tc_kernel", 100.0, 1) == 50.0
+    assert bench.traffic_of("indexer_tc_kernel", 100.0, 4) == 200.0
+    assert bench.traffic_of("indexer_tc_kernel", 100.0, 2) == 50.0   # nearer to 1
+    assert bench.traffic_of("indexer_tc_kernel", 100.0, 3) == 200.0  # nearer to 4
+    assert bench.traffic_of("indexer_tc_kernel", 100.0, 8) == 200.0
+    assert bench.traffic_of("indexer_tc_kernel", 0.0, 1) is None
+    monkeypatch.setitem(bench.TRAFFIC, "indexer_tc_kernel", ("indexer.cu", "0" * 16, 1.0))
+    assert bench.traffic_of("indexer_tc_kernel", 100.0) is None
+    assert bench.traffic_of("no_such_kernel", 100.0) is None
