@@ -542,9 +542,9 @@ def attention_kernel(w):
     return "attn_pair_kernel" if w["B"] * w["nq"] * (w["H"] // 128) >= 64 else "attn_tc_kernel"
 
 
-# DRAM bytes (read + write) per algorithmic byte of a launch, from the ncu
-# captures summarised under profiles/, with the kernel source they were taken
-# on (sha256 prefix of the .cu file and of the shared device header): a
+# DRAM bytes (read + write) per algorithmic byte of a launch, from ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch of a
+# bench --case run), with the kernel source they were taken on (sha256 prefix of the .cu file and of the shared device header): a
 # stage's traffic is reported as that ratio x its algorithmic bytes while
 # both sources are unchanged, and as null otherwise.  Each capture is a small
 # case of the same kernel; the ratio carries to the workload's launch because
@@ -563,7 +563,8 @@ TRAFFIC = {
     "attn_pair_kernel": ("attention_pair.cu", "c6333d74be841dc2", (353.06 + 23.18) / 415.2),
     # the same for the 64-head kernel (32 queries x 2048 rows x 128 heads; its output stays in L2)
     "attn_tc_kernel": ("attention.cu", "c50a20464a4d96f7", (54.50 + 0.58) / 51.9),
-    # HBM writes of the copied rows (their 1.026x host-link reads are in profiles/)
+    # HBM writes of the copied rows (their host-link reads, L2 sectors filled
+    # from system memory, come to 1.026x the algorithmic bytes)
     "miss_copy_kernel": ("resolve.cu", "3ab01ede87a6d55b", (0.80 + 91.63) / 96.9),
 }
 
