@@ -554,8 +554,8 @@ TC_CUH_SHA = "beffda9b9722625b"
 TRAFFIC = {
     # keys + sigma read once; scores partly still in L2 at the end, by queries
     # per request (32 x 65,536 at one query, 16 x 131,072 at four)
-    "indexer_tc_kernel": ("indexer.cu", "594beef5a28364ce",
-                          {1: (277.13 + 7.94) / 285.5, 4: (277.42 + 25.56) / 310.9}),
+    "indexer_tc_kernel": ("indexer.cu", "79922739c3459ee5",
+                          {1: (277.16 + 7.35) / 285.5, 4: (277.42 + 25.87) / 310.9}),
     # the sampled-threshold filter: the scores read once, the few candidates
     # still in L2 at the end (16 x 4 rows of 142,000)
     "topk_filter_kernel": ("topk.cu", "b43a3cee7e2b2d50", (36.389 + 0.001) / (36.36 + 0.52)),

@@ -156,6 +156,39 @@ __device__ __forceinline__ float weighted_relu_sum(uint32_t taddr, const float *
     return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
 }
 
+// The waits of the producer and MMA threads.  Each try_wait may suspend the
+// thread for up to kCtlSuspendNs and resumes it as soon as the phase
+// completes, so a waiting control thread takes no issue slots from the
+// epilogue warps that share its SM sub-partition (warps 0 and 1 sit on
+// sub-partitions 0 and 1; with a plain retry loop there, a clock64 trace
+// showed those epilogue warps about 15 % slower per tile than the others and
+// the MMA of each tile waiting for them).  Bounded like tc::mbar_wait.
+constexpr uint32_t kCtlSuspendNs = 1000000;  // at most 1 ms per look
+
+__device__ __forceinline__ bool ctl_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(ok)
+        : "r"(tc::smem_addr(bar)), "r"(parity), "r"(kCtlSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool ctl_wait(uint64_t *bar, uint32_t parity, int32_t *err) {
+    if (ctl_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!ctl_try_wait(bar, parity)) {
+        if (clock64() - t0 > tc::kWaitCycles) {
+            set_error(err, HS_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Two fp32 lanes as one 64-bit operand of the packed f32x2 instructions.
 __device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
     unsigned long long r;
@@ -262,7 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int it = 0; it < nt; it++) {
                 const int s = it % kTcStages;
                 const uint32_t ph = (it / kTcStages) & 1;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1, a.err)) break;
+                if (!ctl_wait(&empty[s], ph ^ 1, a.err)) break;
                 tc::mbar_expect_tx(&full[s], kTileBytes);
                 tc::tma_load_2d(ks + s * kTileBytes, &kmap, &full[s], 0,
                                 b * a.maxT + (tile0 + it) * kTile);
@@ -270,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // never leave with a copy in flight
             for (int it = max(0, issued - kTcStages); it < issued; it++)
-                tc::mbar_wait(&full[it % kTcStages], (it / kTcStages) & 1, a.err);
+                ctl_wait(&full[it % kTcStages], (it / kTcStages) & 1, a.err);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -281,8 +314,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t ph = (it / kTcStages) & 1;
                 const int acc = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
-                if (!tc::mbar_wait(&tempty[acc], aph ^ 1, a.err)) break;
-                if (!tc::mbar_wait(&full[s], ph, a.err)) break;
+                if (!ctl_wait(&tempty[acc], aph ^ 1, a.err)) break;
+                if (!ctl_wait(&full[s], ph, a.err)) break;
                 tc::fence_after_sync();
                 const uint32_t kaddr = tc::smem_addr(ks + s * kTileBytes);
 #pragma unroll
@@ -296,7 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // every MMA this thread issued has completed before TMEM is freed
             tc::mma_commit(done);
-            tc::mbar_wait(done, 0, a.err);
+            ctl_wait(done, 0, a.err);
         }
     } else {
         const int sp = warp & 3;  // TMEM sub-partition this warp may read
