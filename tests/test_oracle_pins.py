@@ -418,6 +418,40 @@ def test_resolve_capacity_error_when_buffer_too_small():
     assert st.slot_token.tolist() == [1, 13, 9] and st.hot_map[5] == -1
 
 
+def test_resolve_shortfall_never_evicts_rows_of_this_step():
+    """Under a hot-buffer shortfall (fewer free-able slots than misses; the
+    capacity error of our reading), a slot that this step already uses is
+    never a victim ("Les trois états de résidence": a hit refreshes its LRU
+    entry, so it is the most recent use), and every entry that the step
+    locates in the hot buffer still holds its token when the step ends.
+    Hand-worked, then as an invariant over random shortfalls."""
+    P, N = 4, 64
+    res = oracle.page_resident(oracle.ZERO, N, 0, P)
+    st = oracle.HotState(2, N)
+    r = st.resolve(res, P, N, np.array([[1, 5, -1]], np.int32))
+    assert r["status"] == 0 and st.slot_token.tolist() == [1, 5]
+    # step 2: 1 hits slot 0 (stamp 2); the misses 9 and 13 find one slot of
+    # an earlier step (slot 1): 9 takes it, 13 reads nothing, slot 0 keeps 1
+    r = st.resolve(res, P, N, np.array([[1, 9, 13]], np.int32))
+    assert r["status"] == oracle.ERR_CAPACITY
+    assert r["loc_kind"].tolist() == [[2, 2, 0]]
+    assert r["loc_val"].tolist() == [[0, 1, -1]]
+    assert st.slot_token.tolist() == [1, 9]
+    assert (st.hot_map[1], st.hot_map[9], st.hot_map[5], st.hot_map[13]) == (0, 1, -1, -1)
+    rng = np.random.default_rng(21)
+    shortfalls = 0
+    for C in (3, 5, 8):
+        st = oracle.HotState(C, N)
+        for _ in range(40):
+            idx = np.stack([np.sort(rng.choice(16, 4, replace=False)) for _ in range(2)]).astype(np.int32)
+            r = st.resolve(res, P, N, idx)
+            assert r["status"] in (0, oracle.ERR_CAPACITY)
+            shortfalls += r["status"] == oracle.ERR_CAPACITY
+            for j, k in zip(*np.nonzero(r["loc_kind"] == 2)):
+                assert st.slot_token[r["loc_val"][j, k]] == idx[j, k]
+    assert shortfalls > 0
+
+
 def test_resolve_capacity_rule_always_has_victims():
     """With C = (num_spec+2)*K the victims always exist (union <= nq*K = C-K)."""
     rng = np.random.default_rng(9)
