@@ -141,6 +141,22 @@ def test_indexer_scores_exact_int64(fmt, Hi, Di, bound, nq, N, sig):
     np.testing.assert_array_equal(got.astype(np.float64), want)
 
 
+def test_visibility_reading_matches_the_scored_tokens():
+    """oracle.visible (the reading the harnesses use: query j of nq sees
+    [0, N - nq + j + 1)) names exactly the tokens the indexer scores, which
+    the integer recomputation above pins; the last query sees every token."""
+    rng = np.random.default_rng(3)
+    for nq, N in ((1, 9), (2, 12), (4, 11)):
+        q = rng.standard_normal((nq, 2, 8)).astype(np.float32)
+        k = rng.standard_normal((N, 8)).astype(np.float32)
+        w = np.ones((nq, 2), np.float32)
+        s = oracle.indexer_scores(oracle.IDX_F32, q, w, k, np.ones(N, np.float32), N)
+        for j in range(nq):
+            v = oracle.visible(N, nq, j)
+            assert np.isfinite(s[j, :v]).all() and np.isneginf(s[j, v:]).all()
+        assert oracle.visible(N, nq, nq - 1) == N
+
+
 def test_indexer_identity_gate_build(tmp_path):
     """The oracle built with -DHSO_IDENTITY_GATE (the other plain reading of the
     gate) against the same integer closed form without the max; the default
@@ -701,6 +717,39 @@ def test_pressure_policy_hand_worked_example():
     assert pol.used() == 6
     assert pol.relieve() == [2, 1]
     assert pol.used() == 8 and pol.flipped == []
+
+
+def test_pressure_policy_flips_the_most_pages_and_keeps_a_margin():
+    """Cap 23 blocks, P = 4, T = 8, hot buffer 2 blocks.  Worked by hand:
+      r0 += 20 -> 5 pages; r1 += 40 -> 10; r2 += 28 -> 7 (22 used).
+      r0 += 8 would need 22 - 5 + 7 = 24.  Every request's flip frees blocks
+      (mixed: its last two pages + 2 hot = 4, against 5, 10 and 7): the one
+      with the most pages, r1, flips: 5 + 4 + 7 = 16, and the append fits
+      (18 used, 5 free).
+      r1's return adds 10 - 4 = 6 blocks.  With 5 free, nothing returns.
+      Close r2 and reopen it with 20 tokens (16 used, 7 free, 3 open): 7
+      covers the 6 blocks but not the margin of one block per open request
+      (6 + 3 = 9), so nothing returns.  Close r2 again (11 used, 12 free, 2
+      open): 6 + 2 <= 12, r1 returns (17 used)."""
+    pol = oracle.PressurePolicy(cap=23, T=8, P=4, hot_pages=2)
+    for r in range(3):
+        pol.open(r)
+    assert pol.append(0, 20) == ([], oracle.OK)
+    assert pol.append(1, 40) == ([], oracle.OK)
+    assert pol.append(2, 28) == ([], oracle.OK)
+    assert pol.used() == 22
+    assert pol.append(0, 8) == ([1], oracle.OK)
+    assert pol.used() == 18
+    assert pol.relieve() == []
+    pol.close(2)
+    pol.open(2)
+    assert pol.append(2, 20) == ([], oracle.OK)
+    assert pol.used() == 16
+    assert pol.relieve() == []
+    pol.close(2)
+    assert pol.used() == 11
+    assert pol.relieve() == [1]
+    assert pol.used() == 17 and pol.flipped == []
 
 
 def test_pressure_policy_capacity_when_no_flip_frees_blocks():
