@@ -11,6 +11,7 @@ Nothing here runs on a GPU and the oracle's own files are never modified.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -122,21 +123,45 @@ def _run_pins(files, workdir, selection):
         "sys.exit(pytest.main(['-x', '-q', '-p', 'no:cacheprovider', '-m', 'not gpu', "
         f"{PINS!r}, '-k', {selection!r}]))\n"
     )
+    env = dict(os.environ, OMP_NUM_THREADS="1")  # the children run side by side
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
-                       timeout=300)
+                       timeout=600, env=env)
     return r.returncode, (r.stdout + r.stderr)[-1500:]
 
 
-def test_unchanged_copy_passes_every_selection(tmp_path):
-    selection = " or ".join(f"({s})" for s in sorted({m[4] for m in MUTANTS}))
-    rc, tail = _run_pins(_sources(), str(tmp_path), selection)
+CONTROL = "unchanged copy"
+
+
+@pytest.fixture(scope="module")
+def runs(tmp_path_factory):
+    """Every child run at once (they are independent): name -> (exit code,
+    output tail), the unchanged copy under CONTROL; None for a mutant whose
+    text is missing or not unique."""
+    base = tmp_path_factory.mktemp("oracle_mutants")
+    jobs = {CONTROL: (_sources(), " or ".join(f"({s})" for s in sorted({m[4] for m in MUTANTS})))}
+    out = {}
+    for i, (name, fname, old, new, selection) in enumerate(MUTANTS):
+        files = _sources()
+        if files[fname].count(old) != 1:
+            out[name] = None
+            continue
+        files[fname] = files[fname].replace(old, new)
+        jobs[name] = (files, selection)
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        futs = {name: ex.submit(_run_pins, files, str(base / f"run{i}"), sel)
+                for i, (name, (files, sel)) in enumerate(jobs.items())}
+        out.update({name: f.result() for name, f in futs.items()})
+    return out
+
+
+def test_unchanged_copy_passes_every_selection(runs):
+    rc, tail = runs[CONTROL]
     assert rc == 0, tail
 
 
 @pytest.mark.parametrize("name,fname,old,new,selection", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_planted_mistake_fails_a_pin(tmp_path, name, fname, old, new, selection):
-    files = _sources()
-    assert files[fname].count(old) == 1, f"the text to mutate is not unique in {fname}: {old!r}"
-    files[fname] = files[fname].replace(old, new)
-    rc, tail = _run_pins(files, str(tmp_path), selection)
+def test_planted_mistake_fails_a_pin(runs, name, fname, old, new, selection):
+    assert runs[name] is not None, f"the text to mutate is not unique in {fname}: {old!r}"
+    rc, tail = runs[name]
     assert rc == 1, f"no pin caught '{name}' (pytest exit {rc}):\n{tail}"
