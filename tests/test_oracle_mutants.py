@@ -74,6 +74,22 @@ MUTANTS = [
      "            for (i = 0; i < HSO_NOPE; i++)\n                dot += qh[i]", ATTENTION),
     ("attention: log-sum-exp in base 2", C_SRC,
      "lse[h] = mx + log(l);", "lse[h] = mx + log2(l);", ATTENTION),
+    ("f32 rows read with swapped neighbours", C_SRC,
+     "memcpy(&f, row + 4 * i, 4);", "memcpy(&f, row + 4 * (i ^ 1), 4);", FORMATS),
+    ("bf16 shifted by 15 bits", C_SRC,
+     "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;", FORMATS),
+    ("e4m3 NaN for the whole top binade", C_SRC,
+     "if (e == 15 && m == 7)", "if (e == 15)", FORMATS),
+    ("top-K indices left in score order", C_SRC,
+     "    qsort(out, (size_t)m, sizeof(int32_t), cmp_i32);\n", "", TOPK),
+    ("resolve: the evicted token stays in the hot map", C_SRC,
+     "            hot_map[slot_token[c]] = -1;\n", "", RESOLVE),
+    ("resolve: a copied row keeps its slot's old stamp", C_SRC,
+     "        stamp[c] = step;\n", "", RESOLVE),
+    ("attention: the mask ignored", C_SRC,
+     "if (mask && !mask[rr]) {", "if (0) {", ATTENTION),
+    ("attention: softmax not normalised", C_SRC,
+     "            o[(size_t)h * HSO_NOPE + i] /= l;\n", "", ATTENTION),
     ("visibility one token short (Python reading)", PY_SRC,
      "    return N - nq + j + 1\n", "    return N - nq + j\n", INDEXER + " or visibility"),
     ("tail window drops its partial first page", PY_SRC,
