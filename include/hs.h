@@ -162,13 +162,21 @@ typedef struct {
 hs_status hs_pool_required_bytes(const hs_pool_config *cfg, size_t *dev_bytes,
                                  size_t *host_bytes);
 
-/* Carve a pool out of caller-owned memory.  dev_arena: device memory of at
+/* Carve a pool out of caller-owned memory: the shared block pool that holds
+ * resident pages, tails and hot buffers alike, and the pinned host pool
+ * ("Un contexte d'un million sur huit H200", « Les trois états de
+ * résidence »; hot buffers of (num_spec + 2) * K rows: « Ce qu'il faut en
+ * retenir »).  dev_arena: device memory of at
  * least *dev_bytes (16-byte aligned, 256 recommended).  host_arena: pinned
  * host memory (cudaHostAlloc / torch pin_memory) of at least *host_bytes, or
  * NULL when cfg->host_blocks == 0; it must be reachable from the device
  * (unified addressing).  Both must outlive the pool; the pool never allocates
  * device or pinned memory after this call.  Initialises the arena's tables
- * (synchronously on the default stream). */
+ * (synchronously on the default stream).  Errors: HS_ERR_INVALID_ARG (a bad
+ * config, a NULL or unaligned arena, a host arena that is not pinned or not
+ * reachable from the device), HS_ERR_ARENA_TOO_SMALL, HS_ERR_CUDA; *out is
+ * then NULL and nothing the call made stays allocated (the arenas remain
+ * the caller's). */
 hs_status hs_pool_create(const hs_pool_config *cfg, void *dev_arena,
                          size_t dev_bytes, void *host_arena, size_t host_bytes,
                          hs_pool **out);
@@ -281,7 +289,10 @@ hs_status hs_indexer_score(hs_pool *pool, const void *q, const float *w,
                            int32_t B, int32_t nq, float *scores,
                            int64_t score_stride, cudaStream_t stream);
 
-/* Top-K: for each (b, j) the K largest scores[(b*nq+j)*score_stride + t] over
+/* Top-K ("Un contexte d'un million sur huit H200", « Ce qui se passe »: the
+ * indexer picks the top-K tokens; K = 2048 selected tokens: "vLLM sert
+ * GLM-5.3 en contexte 1M sur 16 H200", « Comment s'y prendre »): for each
+ * (b, j) the K largest scores[(b*nq+j)*score_stride + t] over
  * t < seq_len[b] - nq + j + 1 (query j sees up to its own position); equal
  * scores go to the lower t; written ascending to topk[(b*nq+j)*K ..] and
  * padded with -1 when fewer than K tokens are visible.  Deterministic. */
@@ -314,7 +325,9 @@ hs_status hs_topk_noalloc(const float *scores, int64_t score_stride,
                           int32_t K, int32_t max_tokens, int32_t *topk,
                           cudaStream_t stream);
 
-/* hs_indexer_score + hs_topk with the scores kept in the pool's workspace. */
+/* hs_indexer_score + hs_topk with the scores kept in the pool's workspace
+ * (« Ce qui se passe »: the indexer scores every cached token and picks the
+ * top-K).  Errors as for those two calls. */
 hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
                           int32_t B, int32_t nq, int32_t *topk,
                           cudaStream_t stream);
@@ -337,7 +350,8 @@ hs_status hs_indexer_topk(hs_pool *pool, const void *q, const float *w,
 hs_status hs_resolve(hs_pool *pool, const int32_t *topk, int32_t B, int32_t nq,
                      int32_t *row_id, cudaStream_t stream);
 
-/* The two halves of hs_resolve, for callers that time them apart or run the
+/* The two halves of hs_resolve (« Les trois états de résidence »), for
+ * callers that time them apart or run the
  * copy on another stream (ordered after the plan by an event):
  * hs_resolve_plan does the union, classification, LRU update and row ids,
  * and leaves the step's miss lists in the pool's workspace; hs_miss_copy then
@@ -422,7 +436,9 @@ hs_status hs_dcp_topk_merge(hs_pool *pool, const float *scores, int64_t score_st
                             int32_t rows, int32_t *topk, int32_t *part_topk,
                             cudaStream_t stream);
 
-/* Merge the shards' attention outputs: o_parts dev [R][rows][H][512] bf16 and
+/* Merge the shards' attention outputs (decode context parallelism: "vLLM
+ * sert GLM-5.3 en contexte 1M sur 16 H200", « Le mécanisme »): o_parts dev
+ * [R][rows][H][512] bf16 and
  * lse_parts dev [R][rows][H] fp32 (hs_sparse_mla_decode of each shard over
  * its part_topk rows) -> out dev [rows][H][512] bf16 = sum_r w_r o_r with
  * w_r = exp(lse_r - lse), lse = ln sum_r exp(lse_r) (written if lse != NULL).
@@ -430,7 +446,9 @@ hs_status hs_dcp_topk_merge(hs_pool *pool, const float *scores, int64_t score_st
 hs_status hs_dcp_combine(const void *o_parts, const float *lse_parts, int32_t R, int32_t rows,
                          int32_t H, void *out, float *lse, cudaStream_t stream);
 
-/* Resolve + the sparse MLA decode of every layer of the group, for a top-K
+/* Resolve + the sparse MLA decode of every layer of the group (« Les trois
+ * états de résidence »; attention over the selected rows only: « Ce qui se
+ * passe »), for a top-K
  * the caller already has (the second half of hs_step, e.g. for a selection
  * made elsewhere): the results of hs_resolve followed by hs_sparse_mla_decode
  * for each of the L layers.  Without a host pool everything is enqueued on
@@ -461,7 +479,9 @@ typedef struct {
                             /* is still computed and written to topk)         */
 } hs_step_args;
 
-/* One decode step of one IndexShare group: indexer score -> top-K ->
+/* One decode step of one IndexShare group ("Un contexte d'un million sur
+ * huit H200", « Ce qui se passe »: one indexer layer serves four sparse-MLA
+ * layers): indexer score -> top-K ->
  * fused resolve (with miss copies) -> sparse MLA decode for each of the L
  * layers, i.e. the indexer's top-K followed by hs_resolve_attend (of
  * topk_in when it is given).  Enqueued on `stream`; no host
